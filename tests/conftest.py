@@ -1,0 +1,29 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a B300 GPU and the built CUDA library")
+    config.addinivalue_line("markers", "slow: long CPU-only test")
+
+
+def pytest_collection_modifyitems(config, items):
+    # tests marked gpu are skipped when no CUDA device is present, so that
+    # `-m "not gpu"` and plain runs both stay green on a CPU-only host
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:
+        has_gpu = False
+    if has_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for it in items:
+        if "gpu" in it.keywords:
+            it.add_marker(skip)
