@@ -1,0 +1,88 @@
+// Launchers of every kernel on the training step, shared by the model driver
+// and the per-operation C ABI.  All launchers enqueue on `st` and return the
+// launch status; none allocates memory — scratch comes from the caller.
+#pragma once
+#include "common.cuh"
+
+#define GPT2_MAX_SEGS 16
+
+// ---- GEMM ------------------------------------------------------------------
+// D(m, n) = sum_k A(m, k) * B(n, k) followed by an epilogue.
+//   A(m,k) = a_kmajor ? A[m*lda + k] : A[k*lda + m]
+//   B(n,k) = b_kmajor ? B[n*ldb + k] : B[k*ldb + n]
+enum GemmEpi : int {
+  EPI_STORE = 0,     // D[m,n] = acc (+ bias[n])                       (type T)
+  EPI_GELU = 1,      // aux[m,n] = acc + bias[n]; D[m,n] = GELU(aux)   (type T)
+  EPI_GELU_BWD = 2,  // D[m,n] = acc * GELU'(aux[m,n])                 (type T)
+  EPI_ACC_F32 = 3,   // D[m,n] += acc                                  (float)
+};
+struct GemmArgs {
+  const void* A; long long lda; int a_kmajor;
+  const void* B; long long ldb; int b_kmajor;
+  int M, N, K;
+  void* D; long long ldd;
+  const void* bias;          // [N] of type T or nullptr
+  void* aux; long long ldaux;
+  int epi;
+};
+template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
+// tcgen05/TMA tensor-core path (bf16 operands); returns cudaErrorNotSupported
+// when the shape or layout is outside what the kernel handles.
+cudaError_t gemm_tc(const GemmArgs& a, int* flags, cudaStream_t st);
+bool gemm_tc_supported(const GemmArgs& a);
+
+// ---- bandwidth kernels ---------------------------------------------------
+template <typename T>
+cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, int B, int T_, int C,
+                            int V, int* flags, cudaStream_t st);
+// dwte/dwpe += scatter of dres (fp32 [B*T][C]); keys: 2*pow2(B*T) uint32 scratch
+cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
+                             int C, uint32_t* keys, cudaStream_t st);
+size_t encoder_backward_scratch_bytes(int BT);
+
+template <typename T>
+cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* rstd, const T* a,
+                                       const T* b, const T* w, const T* bias, int rows, int C,
+                                       cudaStream_t st);
+// dres = (accumulate ? dres : 0) + LN backward(dy); dres_c (optional) = T copy
+template <typename T>
+cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
+                               const float* rstd, const T* w, int rows, int C, int accumulate,
+                               cudaStream_t st);
+// dw += sum_rows dy*xhat, db += sum_rows dy ; partial: [nchunks][2][C] floats
+template <typename T>
+cudaError_t ln_param_grad(float* dw, float* db, const T* dy, const T* x, const float* mean,
+                          const float* rstd, int rows, int C, float* partial, int nchunks,
+                          cudaStream_t st);
+// out[c] += sum_rows X[r*ldx + c] ; partial: [nchunks][cols] floats
+template <typename T>
+cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial,
+                   int nchunks, cudaStream_t st);
+int reduce_chunks(int rows);  // number of row chunks the reductions use
+
+template <typename T>
+cudaError_t attention_forward_simt(T* out, float* lse, const T* qkv, int B, int T_, int C, int H,
+                                   cudaStream_t st);
+template <typename T>
+cudaError_t attention_backward_simt(T* dqkv, float* Dbuf, const T* dout, const T* qkv, const T* out,
+                                    const float* lse, int B, int T_, int C, int H, cudaStream_t st);
+
+template <typename T>
+cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,
+                       float dloss, int write_grad, int* flags, cudaStream_t st);
+cudaError_t mean_loss(float* loss, const float* losses, int n, cudaStream_t st);
+
+struct AdamSegments {
+  int n;
+  long long off[GPT2_MAX_SEGS + 1];
+  float wd[GPT2_MAX_SEGS];
+};
+cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* pc, long long n, float lr,
+                  float b1, float b2, float eps, float bc1, float bc2, const AdamSegments& seg,
+                  cudaStream_t st);
+cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream_t st);
+
+template <typename T>
+cudaError_t gelu_forward(T* out, const T* in, long long n, cudaStream_t st);
+template <typename T>
+cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cudaStream_t st);

@@ -1,0 +1,935 @@
+// Bandwidth-bound kernels of the training step plus the SIMT GEMM and SIMT
+// attention used by the fp32 exact-check mode.
+//
+// Layer semantics follow "llm.c: GPT-2 training in plain C, with every
+// gradient written by hand", §2 How the code works (encoder, layernorm,
+// matmul, attention, gelu, residual, softmax + crossentropy, each with a
+// hand-written backward), and the talk "llm.c's Origin and the Future of LLM
+// Compilers", [13:50] Avengers Assemble (fused residual+LayerNorm, fused
+// classifier, full determinism: no floating-point atomics anywhere here).
+#include "kernels.cuh"
+#include <math.h>
+
+#define LN_EPS 1e-5f
+#define GELU_SCALE 0.7978845608028654f   // sqrt(2/pi)
+#define GELU_CUBIC 0.044715f
+
+#include <atomic>
+static std::atomic<unsigned long long> g_launches{0};
+void gpt2_count_launches(int n) { g_launches += (unsigned long long)n; }
+unsigned long long gpt2_total_launches() { return g_launches.load(); }
+// status of the kernels just enqueued; n = how many were launched
+static inline cudaError_t launch_status(int n) {
+  gpt2_count_launches(n);
+  return cudaGetLastError();
+}
+
+// ============================================================================
+// encoder: out[b,t,:] = wte[tok[b,t]] + wpe[t]
+// ============================================================================
+template <typename T>
+__global__ void encoder_forward_kernel(T* __restrict__ out, const int* __restrict__ tok,
+                                       const T* __restrict__ wte, const T* __restrict__ wpe, int BT,
+                                       int T_, int C, int V, int* flags) {
+  constexpr int N = VecN<T>::n;
+  const int nvec = C / N;
+  long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)BT * nvec) return;
+  int bt = (int)(idx / nvec), cv = (int)(idx % nvec);
+  int t = bt % T_;
+  int v = tok[bt];
+  if (v < 0 || v >= V) {  // out-of-range token: flag it, read row 0 instead
+    if (cv == 0) atomicOr(flags, FLAG_TOKEN_RANGE);
+    v = 0;
+  }
+  float a[N], b[N];
+  ld16(wte + (size_t)v * C + cv * N, a);
+  ld16(wpe + (size_t)t * C + cv * N, b);
+#pragma unroll
+  for (int i = 0; i < N; i++) a[i] += b[i];
+  st16(out + (size_t)bt * C + cv * N, a);
+}
+
+template <typename T>
+cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, int B, int T_, int C,
+                            int V, int* flags, cudaStream_t st) {
+  long long n = (long long)B * T_ * (C / VecN<T>::n);
+  encoder_forward_kernel<T><<<(unsigned)cdiv(n, 256), 256, 0, st>>>(out, tok, wte, wpe, B * T_, T_, C, V, flags);
+  return launch_status(1);
+}
+
+// ----------------------------------------------------------------------------
+// encoder backward, deterministic (no atomics):
+//   dwpe[t] += sum_b dres[b,t]
+//   dwte[v] += sum over positions with token v, in increasing position order.
+// Positions are bucketed by a single-CTA bitonic sort of (token << 16 | pos).
+// ----------------------------------------------------------------------------
+__global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dres, int B, int T_, int C) {
+  int nvec = C / 4;
+  long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)T_ * nvec) return;
+  int t = (int)(idx / nvec), cv = (int)(idx % nvec);
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int b = 0; b < B; b++) {
+    float x[4];
+    ld16(dres + ((size_t)b * T_ + t) * C + cv * 4, x);
+#pragma unroll
+    for (int i = 0; i < 4; i++) s[i] += x[i];
+  }
+  float* dst = dwpe + (size_t)t * C + cv * 4;
+  float o[4];
+  ld16(dst, o);
+#pragma unroll
+  for (int i = 0; i < 4; i++) o[i] += s[i];
+  st16(dst, o);
+}
+
+static inline int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+size_t encoder_backward_scratch_bytes(int BT) { return (size_t)pow2_at_least(BT) * sizeof(uint32_t); }
+
+// one CTA sorts n (power of two, <= 32768) keys in shared memory
+__global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restrict__ tok, int BT, int n) {
+  extern __shared__ uint32_t sk[];
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    sk[i] = i < BT ? (((uint32_t)tok[i] & 0xFFFFu) << 16) | (uint32_t)i : 0xFFFFFFFFu;
+  __syncthreads();
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int ixj = i ^ j;
+        if (ixj > i) {
+          uint32_t a = sk[i], b = sk[ixj];
+          bool up = (i & k) == 0;
+          if ((a > b) == up) { sk[i] = b; sk[ixj] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) keys_out[i] = sk[i];
+}
+
+// block i: if sorted key i starts a token run, sum that run's rows in order
+__global__ void wte_grad_runs_kernel(float* __restrict__ dwte, const float* __restrict__ dres,
+                                     const uint32_t* __restrict__ keys, int BT, int C) {
+  int i = blockIdx.x;
+  uint32_t tk = keys[i] >> 16;
+  if (i > 0 && (keys[i - 1] >> 16) == tk) return;
+  int end = i + 1;
+  while (end < BT && (keys[end] >> 16) == tk) end++;
+  for (int cv = threadIdx.x; cv < C / 4; cv += blockDim.x) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = i; j < end; j++) {
+      int pos = (int)(keys[j] & 0xFFFFu);
+      float x[4];
+      ld16(dres + (size_t)pos * C + cv * 4, x);
+#pragma unroll
+      for (int q = 0; q < 4; q++) s[q] += x[q];
+    }
+    float* dst = dwte + (size_t)tk * C + cv * 4;
+    float o[4];
+    ld16(dst, o);
+#pragma unroll
+    for (int q = 0; q < 4; q++) o[q] += s[q];
+    st16(dst, o);
+  }
+}
+
+cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
+                             int C, uint32_t* keys, cudaStream_t st) {
+  int BT = B * T_;
+  int n = pow2_at_least(BT);
+  if (n > 32768) return cudaErrorInvalidValue;
+  long long nv = (long long)T_ * (C / 4);
+  wpe_grad_kernel<<<(unsigned)cdiv(nv, 256), 256, 0, st>>>(dwpe, dres, B, T_, C);
+  size_t smem = (size_t)n * sizeof(uint32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(bitonic_sort_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768 * 4);
+    attr_set = true;
+  }
+  bitonic_sort_keys_kernel<<<1, 1024, smem, st>>>(keys, tok, BT, n);
+  wte_grad_runs_kernel<<<BT, 192, 0, st>>>(dwte, dres, keys, BT, C);
+  return launch_status(3);
+}
+
+// ============================================================================
+// fused residual + LayerNorm forward: r = a (+ b); y = (r - mean) * rstd * w + bias
+// one warp per row; the row lives in registers.  In bf16 the stored residual
+// is rounded first and the statistics are taken from the rounded values.
+// ============================================================================
+template <typename T, int NV>
+__global__ void residual_layernorm_forward_kernel(T* __restrict__ resid_out, T* __restrict__ y,
+                                                  float* __restrict__ mean, float* __restrict__ rstd,
+                                                  const T* __restrict__ a, const T* __restrict__ b,
+                                                  const T* __restrict__ w, const T* __restrict__ bias,
+                                                  int rows, int C) {
+  constexpr int N = VecN<T>::n;
+  int lane = threadIdx.x & 31;
+  int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int nvec = C / N;
+  float x[NV][N];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; i++) {
+    int vi = lane + i * 32;
+    if (vi < nvec) {
+      ld16_cs(a + (size_t)row * C + vi * N, x[i]);
+      if (b) {
+        float xb[N];
+        ld16_cs(b + (size_t)row * C + vi * N, xb);
+#pragma unroll
+        for (int k = 0; k < N; k++) x[i][k] = round_to<T>(x[i][k] + xb[k]);
+        st16(resid_out + (size_t)row * C + vi * N, x[i]);
+      }
+#pragma unroll
+      for (int k = 0; k < N; k++) sum += x[i][k];
+    }
+  }
+  float mu = warp_sum(sum) / (float)C;
+  float var = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; i++) {
+    if (lane + i * 32 < nvec) {
+#pragma unroll
+      for (int k = 0; k < N; k++) {
+        float d = x[i][k] - mu;
+        var += d * d;
+      }
+    }
+  }
+  var = warp_sum(var) / (float)C;
+  float rs = 1.0f / sqrtf(var + LN_EPS);
+#pragma unroll
+  for (int i = 0; i < NV; i++) {
+    int vi = lane + i * 32;
+    if (vi < nvec) {
+      float wv[N], bv[N], o[N];
+      ld16(w + vi * N, wv);
+      ld16(bias + vi * N, bv);
+#pragma unroll
+      for (int k = 0; k < N; k++) o[k] = (x[i][k] - mu) * rs * wv[k] + bv[k];
+      st16(y + (size_t)row * C + vi * N, o);
+    }
+  }
+  if (lane == 0) {
+    mean[row] = mu;
+    rstd[row] = rs;
+  }
+}
+
+template <typename T>
+cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* rstd, const T* a,
+                                       const T* b, const T* w, const T* bias, int rows, int C,
+                                       cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  int nvec = C / N;
+  unsigned grid = (unsigned)cdiv(rows, 8);
+  if (nvec <= 32 * 2)
+    residual_layernorm_forward_kernel<T, 2><<<grid, 256, 0, st>>>(resid_out, y, mean, rstd, a, b, w, bias, rows, C);
+  else if (nvec <= 32 * 4)
+    residual_layernorm_forward_kernel<T, 4><<<grid, 256, 0, st>>>(resid_out, y, mean, rstd, a, b, w, bias, rows, C);
+  else if (nvec <= 32 * 8)
+    residual_layernorm_forward_kernel<T, 8><<<grid, 256, 0, st>>>(resid_out, y, mean, rstd, a, b, w, bias, rows, C);
+  else if (nvec <= 32 * 16)
+    residual_layernorm_forward_kernel<T, 16><<<grid, 256, 0, st>>>(resid_out, y, mean, rstd, a, b, w, bias, rows, C);
+  else
+    return cudaErrorInvalidValue;
+  return launch_status(1);
+}
+
+// ============================================================================
+// LayerNorm backward (input gradient), one warp per row:
+//   dnorm = dy * w; dx = rstd * (dnorm - mean(dnorm) - xhat * mean(dnorm * xhat))
+//   dres = (accumulate ? dres : 0) + dx   (fp32; optional copy in T)
+// ============================================================================
+template <typename T, int NV>
+__global__ void layernorm_backward_kernel(float* __restrict__ dres, T* __restrict__ dres_c,
+                                          const T* __restrict__ dy, const T* __restrict__ x,
+                                          const float* __restrict__ mean, const float* __restrict__ rstd,
+                                          const T* __restrict__ w, int rows, int C, int accumulate) {
+  constexpr int N = VecN<T>::n;
+  int lane = threadIdx.x & 31;
+  int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int nvec = C / N;
+  float mu = mean[row], rs = rstd[row];
+  float dn[NV][N], xh[NV][N];
+  float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; i++) {
+    int vi = lane + i * 32;
+    if (vi < nvec) {
+      float d[N], xv[N], wv[N];
+      ld16(dy + (size_t)row * C + vi * N, d);
+      ld16(x + (size_t)row * C + vi * N, xv);
+      ld16(w + vi * N, wv);
+#pragma unroll
+      for (int k = 0; k < N; k++) {
+        xh[i][k] = (xv[k] - mu) * rs;
+        dn[i][k] = d[k] * wv[k];
+        s1 += dn[i][k];
+        s2 += dn[i][k] * xh[i][k];
+      }
+    }
+  }
+  s1 = warp_sum(s1) / (float)C;
+  s2 = warp_sum(s2) / (float)C;
+#pragma unroll
+  for (int i = 0; i < NV; i++) {
+    int vi = lane + i * 32;
+    if (vi < nvec) {
+      float o[N];
+#pragma unroll
+      for (int k = 0; k < N; k++) o[k] = (dn[i][k] - s1 - xh[i][k] * s2) * rs;
+      float* dst = dres + (size_t)row * C + vi * N;
+#pragma unroll
+      for (int k = 0; k < N; k += 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (accumulate) ld16(dst + k, acc);
+        float r4[4] = {acc[0] + o[k], acc[1] + o[k + 1], acc[2] + o[k + 2], acc[3] + o[k + 3]};
+        st16(dst + k, r4);
+        o[k] = r4[0]; o[k + 1] = r4[1]; o[k + 2] = r4[2]; o[k + 3] = r4[3];
+      }
+      if (dres_c) st16(dres_c + (size_t)row * C + vi * N, o);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
+                               const float* rstd, const T* w, int rows, int C, int accumulate,
+                               cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  int nvec = C / N;
+  unsigned grid = (unsigned)cdiv(rows, 8);
+  if (nvec <= 32 * 2)
+    layernorm_backward_kernel<T, 2><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
+  else if (nvec <= 32 * 4)
+    layernorm_backward_kernel<T, 4><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
+  else if (nvec <= 32 * 8)
+    layernorm_backward_kernel<T, 8><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
+  else if (nvec <= 32 * 16)
+    layernorm_backward_kernel<T, 16><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
+  else
+    return cudaErrorInvalidValue;
+  return launch_status(1);
+}
+
+// ============================================================================
+// deterministic column reductions: per-chunk partials, then an ordered sum
+// ============================================================================
+int reduce_chunks(int rows) {
+  int c = (int)cdiv(rows, 128);
+  return c < 1 ? 1 : c;
+}
+
+template <typename T>
+__global__ void ln_param_grad_partial_kernel(float* __restrict__ partial, const T* __restrict__ dy,
+                                             const T* __restrict__ x, const float* __restrict__ mean,
+                                             const float* __restrict__ rstd, int rows, int C, int rows_per) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  int chunk = blockIdx.y;
+  if (c >= C) return;
+  int r0 = chunk * rows_per, r1 = min(rows, r0 + rows_per);
+  float sw = 0.f, sb = 0.f;
+  for (int r = r0; r < r1; r++) {
+    float d = to_f(dy[(size_t)r * C + c]);
+    float xh = (to_f(x[(size_t)r * C + c]) - mean[r]) * rstd[r];
+    sw += d * xh;
+    sb += d;
+  }
+  partial[((size_t)chunk * 2 + 0) * C + c] = sw;
+  partial[((size_t)chunk * 2 + 1) * C + c] = sb;
+}
+
+__global__ void sum_chunks_kernel(float* __restrict__ out, const float* __restrict__ partial, int nchunks,
+                                  int cols, long long chunk_stride) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  float s = 0.f;
+  for (int k = 0; k < nchunks; k++) s += partial[(size_t)k * chunk_stride + c];
+  out[c] += s;
+}
+
+template <typename T>
+cudaError_t ln_param_grad(float* dw, float* db, const T* dy, const T* x, const float* mean,
+                          const float* rstd, int rows, int C, float* partial, int nchunks,
+                          cudaStream_t st) {
+  int rows_per = (int)cdiv(rows, nchunks);
+  dim3 grid((unsigned)cdiv(C, 128), nchunks);
+  ln_param_grad_partial_kernel<T><<<grid, 128, 0, st>>>(partial, dy, x, mean, rstd, rows, C, rows_per);
+  sum_chunks_kernel<<<(unsigned)cdiv(C, 256), 256, 0, st>>>(dw, partial, nchunks, C, 2LL * C);
+  sum_chunks_kernel<<<(unsigned)cdiv(C, 256), 256, 0, st>>>(db, partial + C, nchunks, C, 2LL * C);
+  return launch_status(3);
+}
+
+template <typename T>
+__global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ X, int rows,
+                                      int cols, long long ldx, int rows_per) {
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  int chunk = blockIdx.y;
+  if (c >= cols) return;
+  int r0 = chunk * rows_per, r1 = min(rows, r0 + rows_per);
+  float s = 0.f;
+  for (int r = r0; r < r1; r++) s += to_f(X[(size_t)r * ldx + c]);
+  partial[(size_t)chunk * cols + c] = s;
+}
+
+template <typename T>
+cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial,
+                   int nchunks, cudaStream_t st) {
+  int rows_per = (int)cdiv(rows, nchunks);
+  dim3 grid((unsigned)cdiv(cols, 128), nchunks);
+  colsum_partial_kernel<T><<<grid, 128, 0, st>>>(partial, X, rows, cols, ldx, rows_per);
+  sum_chunks_kernel<<<(unsigned)cdiv(cols, 256), 256, 0, st>>>(out, partial, nchunks, cols, cols);
+  return launch_status(2);
+}
+
+// ============================================================================
+// SIMT GEMM (fp32 mode, and any shape the tensor-core path does not take)
+// 64x64 tile, BK 16, 256 threads, 4x4 per thread, fp32 accumulate.
+// ============================================================================
+__device__ __forceinline__ float gelu_f(float x) {
+  float u = GELU_SCALE * (x + GELU_CUBIC * x * x * x);
+  return 0.5f * x * (1.f + tanhf(u));
+}
+__device__ __forceinline__ float gelu_grad_f(float x) {
+  float u = GELU_SCALE * (x + GELU_CUBIC * x * x * x);
+  float th = tanhf(u);
+  float du = GELU_SCALE * (1.f + 3.f * GELU_CUBIC * x * x);
+  return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * du;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const T* A = (const T*)g.A;
+  const T* B = (const T*)g.B;
+  int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; i++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < g.K; k0 += 16) {
+    // 64x16 tiles of A and B: 1024 elements each, 4 per thread
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+      int e = threadIdx.x + r * 256;
+      int mm, kk;
+      if (g.a_kmajor) { mm = e / 16; kk = e % 16; } else { kk = e / 64; mm = e % 64; }
+      int gm = m0 + mm, gk = k0 + kk;
+      float v = 0.f;
+      if (gm < g.M && gk < g.K)
+        v = to_f(g.a_kmajor ? A[(size_t)gm * g.lda + gk] : A[(size_t)gk * g.lda + gm]);
+      As[kk][mm] = v;
+      int nn;
+      if (g.b_kmajor) { nn = e / 16; kk = e % 16; } else { kk = e / 64; nn = e % 64; }
+      int gn = n0 + nn;
+      gk = k0 + kk;
+      v = 0.f;
+      if (gn < g.N && gk < g.K)
+        v = to_f(g.b_kmajor ? B[(size_t)gn * g.ldb + gk] : B[(size_t)gk * g.ldb + gn]);
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; kk++) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; j++) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    int m = m0 + ty * 4 + i;
+    if (m >= g.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      int n = n0 + tx * 4 + j;
+      if (n >= g.N) continue;
+      float v = acc[i][j];
+      if (g.epi == EPI_ACC_F32) {
+        float* D = (float*)g.D;
+        D[(size_t)m * g.ldd + n] += v;
+      } else if (g.epi == EPI_GELU_BWD) {
+        float h = to_f(((const T*)g.aux)[(size_t)m * g.ldaux + n]);
+        ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v * gelu_grad_f(h));
+      } else {
+        if (g.bias) v += to_f(((const T*)g.bias)[n]);
+        if (g.epi == EPI_GELU) {
+          ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
+          v = gelu_f(v);
+        }
+        ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
+      }
+    }
+  }
+}
+
+template <typename T>
+cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st) {
+  if (a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)cdiv(a.N, 64), (unsigned)cdiv(a.M, 64));
+  gemm_simt_kernel<T><<<grid, 256, 0, st>>>(a);
+  return launch_status(1);
+}
+
+// ============================================================================
+// SIMT causal attention (any head size <= 128).  Forward: one warp per query
+// row, keys in chunks of 32 (one key per lane), online max/sum, LSE saved.
+// Backward: D = rowsum(dO*O); a dQ pass per query row and a dK/dV pass per
+// key row recompute P from the LSE (no atomics).
+// ============================================================================
+#define ATT_WARPS 8
+template <typename T>
+__global__ void __launch_bounds__(256) attention_forward_simt_kernel(T* __restrict__ out, float* __restrict__ lse,
+                                                                     const T* __restrict__ qkv, int B, int T_, int C,
+                                                                     int H, float scale) {
+  __shared__ float qs[ATT_WARPS][128];
+  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long gq = (long long)blockIdx.x * ATT_WARPS + warp;
+  if (gq >= (long long)B * H * T_) return;
+  int hd = C / H;
+  int t = (int)(gq % T_);
+  int h = (int)((gq / T_) % H);
+  int b = (int)(gq / ((long long)T_ * H));
+  const size_t rs = 3 * (size_t)C;
+  const T* base = qkv + (size_t)b * T_ * rs;
+  for (int d = lane; d < hd; d += 32) qs[warp][d] = to_f(base[(size_t)t * rs + h * hd + d]) * scale;
+  __syncwarp();
+  float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 <= t; k0 += 32) {
+    int t2 = k0 + lane;
+    float s = -INFINITY;
+    if (t2 <= t) {
+      const T* kr = base + (size_t)t2 * rs + C + h * hd;
+      s = 0.f;
+      for (int d = 0; d < hd; d++) s = fmaf(qs[warp][d], to_f(kr[d]), s);
+    }
+    float mn = fmaxf(m, warp_max(s));
+    float p = t2 <= t ? expf(s - mn) : 0.f;
+    float alpha = expf(m - mn);
+    l = l * alpha + warp_sum(p);
+#pragma unroll
+    for (int i = 0; i < 4; i++) o[i] *= alpha;
+    int jn = min(32, t - k0 + 1);
+    for (int j = 0; j < jn; j++) {
+      float pj = __shfl_sync(0xffffffffu, p, j);
+      const T* vr = base + (size_t)(k0 + j) * rs + 2 * C + h * hd;
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        int d = lane + 32 * i;
+        if (d < hd) o[i] = fmaf(pj, to_f(vr[d]), o[i]);
+      }
+    }
+    m = mn;
+  }
+  float inv = 1.f / l;
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    int d = lane + 32 * i;
+    if (d < hd) out[((size_t)b * T_ + t) * C + h * hd + d] = from_f<T>(o[i] * inv);
+  }
+  if (lane == 0) lse[((size_t)b * H + h) * T_ + t] = m + logf(l);
+}
+
+template <typename T>
+cudaError_t attention_forward_simt(T* out, float* lse, const T* qkv, int B, int T_, int C, int H,
+                                   cudaStream_t st) {
+  int hd = C / H;
+  if (hd > 128 || C % H) return cudaErrorInvalidValue;
+  long long rows = (long long)B * H * T_;
+  attention_forward_simt_kernel<T><<<(unsigned)cdiv(rows, ATT_WARPS), 32 * ATT_WARPS, 0, st>>>(
+      out, lse, qkv, B, T_, C, H, 1.0f / sqrtf((float)hd));
+  return launch_status(1);
+}
+
+// D[b,h,t] = sum_d dO[b,t,h,d] * O[b,t,h,d]
+template <typename T>
+__global__ void attention_bwd_dot_kernel(float* __restrict__ Dbuf, const T* __restrict__ dout,
+                                         const T* __restrict__ out, int B, int T_, int C, int H) {
+  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long gq = (long long)blockIdx.x * ATT_WARPS + warp;
+  if (gq >= (long long)B * H * T_) return;
+  int hd = C / H;
+  int t = (int)(gq % T_), h = (int)((gq / T_) % H), b = (int)(gq / ((long long)T_ * H));
+  size_t o = ((size_t)b * T_ + t) * C + h * hd;
+  float s = 0.f;
+  for (int d = lane; d < hd; d += 32) s += to_f(dout[o + d]) * to_f(out[o + d]);
+  s = warp_sum(s);
+  if (lane == 0) Dbuf[((size_t)b * H + h) * T_ + t] = s;
+}
+
+// dQ[t] = scale * sum_{t2<=t} dS[t,t2] K[t2],  dS = P (dP - D), dP = dO . V
+template <typename T>
+__global__ void __launch_bounds__(256) attention_bwd_dq_kernel(T* __restrict__ dqkv, const T* __restrict__ dout,
+                                                               const T* __restrict__ qkv, const float* __restrict__ lse,
+                                                               const float* __restrict__ Dbuf, int B, int T_, int C,
+                                                               int H, float scale) {
+  __shared__ float qs[ATT_WARPS][128];
+  __shared__ float dos[ATT_WARPS][128];
+  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long gq = (long long)blockIdx.x * ATT_WARPS + warp;
+  if (gq >= (long long)B * H * T_) return;
+  int hd = C / H;
+  int t = (int)(gq % T_), h = (int)((gq / T_) % H), b = (int)(gq / ((long long)T_ * H));
+  const size_t rs = 3 * (size_t)C;
+  const T* base = qkv + (size_t)b * T_ * rs;
+  for (int d = lane; d < hd; d += 32) {
+    qs[warp][d] = to_f(base[(size_t)t * rs + h * hd + d]) * scale;
+    dos[warp][d] = to_f(dout[((size_t)b * T_ + t) * C + h * hd + d]);
+  }
+  __syncwarp();
+  float L = lse[((size_t)b * H + h) * T_ + t];
+  float Dv = Dbuf[((size_t)b * H + h) * T_ + t];
+  float dq[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 <= t; k0 += 32) {
+    int t2 = k0 + lane;
+    float ds = 0.f;
+    if (t2 <= t) {
+      const T* kr = base + (size_t)t2 * rs + C + h * hd;
+      const T* vr = base + (size_t)t2 * rs + 2 * C + h * hd;
+      float s = 0.f, dp = 0.f;
+      for (int d = 0; d < hd; d++) {
+        s = fmaf(qs[warp][d], to_f(kr[d]), s);
+        dp = fmaf(dos[warp][d], to_f(vr[d]), dp);
+      }
+      float p = expf(s - L);
+      ds = p * (dp - Dv);
+    }
+    int jn = min(32, t - k0 + 1);
+    for (int j = 0; j < jn; j++) {
+      float dsj = __shfl_sync(0xffffffffu, ds, j);
+      const T* kr = base + (size_t)(k0 + j) * rs + C + h * hd;
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        int d = lane + 32 * i;
+        if (d < hd) dq[i] = fmaf(dsj, to_f(kr[d]), dq[i]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    int d = lane + 32 * i;
+    if (d < hd) dqkv[((size_t)b * T_ + t) * rs + h * hd + d] = from_f<T>(dq[i] * scale);
+  }
+}
+
+// dV[t2] = sum_{t>=t2} P[t,t2] dO[t];  dK[t2] = scale * sum_{t>=t2} dS[t,t2] Q[t]
+template <typename T>
+__global__ void __launch_bounds__(256) attention_bwd_dkv_kernel(T* __restrict__ dqkv, const T* __restrict__ dout,
+                                                                const T* __restrict__ qkv, const float* __restrict__ lse,
+                                                                const float* __restrict__ Dbuf, int B, int T_, int C,
+                                                                int H, float scale) {
+  __shared__ float ks[ATT_WARPS][128];
+  __shared__ float vs[ATT_WARPS][128];
+  int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long long gk = (long long)blockIdx.x * ATT_WARPS + warp;
+  if (gk >= (long long)B * H * T_) return;
+  int hd = C / H;
+  int t2 = (int)(gk % T_), h = (int)((gk / T_) % H), b = (int)(gk / ((long long)T_ * H));
+  const size_t rs = 3 * (size_t)C;
+  const T* base = qkv + (size_t)b * T_ * rs;
+  for (int d = lane; d < hd; d += 32) {
+    ks[warp][d] = to_f(base[(size_t)t2 * rs + C + h * hd + d]) * scale;
+    vs[warp][d] = to_f(base[(size_t)t2 * rs + 2 * C + h * hd + d]);
+  }
+  __syncwarp();
+  const float* L = lse + ((size_t)b * H + h) * T_;
+  const float* Dv = Dbuf + ((size_t)b * H + h) * T_;
+  float dk[4] = {0.f, 0.f, 0.f, 0.f}, dv[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int q0 = t2; q0 < T_; q0 += 32) {
+    int t = q0 + lane;
+    float p = 0.f, ds = 0.f;
+    if (t < T_) {
+      const T* qr = base + (size_t)t * rs + h * hd;
+      const T* dor = dout + ((size_t)b * T_ + t) * C + h * hd;
+      float s = 0.f, dp = 0.f;
+      for (int d = 0; d < hd; d++) {
+        s = fmaf(ks[warp][d], to_f(qr[d]), s);
+        dp = fmaf(vs[warp][d], to_f(dor[d]), dp);
+      }
+      p = expf(s - L[t]);
+      ds = p * (dp - Dv[t]);
+    }
+    int jn = min(32, T_ - q0);
+    for (int j = 0; j < jn; j++) {
+      float pj = __shfl_sync(0xffffffffu, p, j);
+      float dsj = __shfl_sync(0xffffffffu, ds, j);
+      const T* qr = base + (size_t)(q0 + j) * rs + h * hd;
+      const T* dor = dout + ((size_t)b * T_ + q0 + j) * C + h * hd;
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        int d = lane + 32 * i;
+        if (d < hd) {
+          dv[i] = fmaf(pj, to_f(dor[d]), dv[i]);
+          dk[i] = fmaf(dsj, to_f(qr[d]), dk[i]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    int d = lane + 32 * i;
+    if (d < hd) {
+      dqkv[((size_t)b * T_ + t2) * rs + C + h * hd + d] = from_f<T>(dk[i] * scale);
+      dqkv[((size_t)b * T_ + t2) * rs + 2 * C + h * hd + d] = from_f<T>(dv[i]);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t attention_backward_simt(T* dqkv, float* Dbuf, const T* dout, const T* qkv, const T* out,
+                                    const float* lse, int B, int T_, int C, int H, cudaStream_t st) {
+  int hd = C / H;
+  if (hd > 128 || C % H) return cudaErrorInvalidValue;
+  long long rows = (long long)B * H * T_;
+  unsigned grid = (unsigned)cdiv(rows, ATT_WARPS);
+  float scale = 1.0f / sqrtf((float)hd);
+  attention_bwd_dot_kernel<T><<<grid, 32 * ATT_WARPS, 0, st>>>(Dbuf, dout, out, B, T_, C, H);
+  attention_bwd_dq_kernel<T><<<grid, 32 * ATT_WARPS, 0, st>>>(dqkv, dout, qkv, lse, Dbuf, B, T_, C, H, scale);
+  attention_bwd_dkv_kernel<T><<<grid, 32 * ATT_WARPS, 0, st>>>(dqkv, dout, qkv, lse, Dbuf, B, T_, C, H, scale);
+  return launch_status(3);
+}
+
+// ============================================================================
+// fused softmax + cross-entropy over the first V of Vp columns, one CTA per
+// row.  Pass 1: online (max, sum) with 128-bit loads; loss = lse - z[target].
+// Pass 2 (write_grad): dlogits = (softmax - onehot) * dloss written in place,
+// pad columns 0.  The row (<= 100 KB in bf16) is re-read from L2.
+// ============================================================================
+template <typename T>
+__global__ void __launch_bounds__(1024) softmax_ce_kernel(T* __restrict__ logits, float* __restrict__ losses,
+                                                          const int* __restrict__ targets, int V, int Vp,
+                                                          float dloss, int write_grad, int* flags) {
+  constexpr int N = VecN<T>::n;
+  __shared__ float sm[32], ss[32];
+  __shared__ float s_lse;
+  __shared__ int s_tg;
+  int row = blockIdx.x;
+  T* z = logits + (size_t)row * Vp;
+  const int nvec = Vp / N;
+  float m = -INFINITY, s = 0.f;
+  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    float f[N];
+    ld16(z + (size_t)vi * N, f);
+#pragma unroll
+    for (int k = 0; k < N; k++) {
+      if (vi * N + k < V) {
+        float x = f[k];
+        if (x > m) { s = s * expf(m - x) + 1.f; m = x; }
+        else s += expf(x - m);
+      }
+    }
+  }
+  // combine (m, s) across the warp, then across warps
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    float mm = fmaxf(m, m2);
+    s = (m == -INFINITY ? 0.f : s * expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * expf(m2 - mm));
+    m = mm;
+  }
+  int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) { sm[w] = m; ss[w] = s; }
+  __syncthreads();
+  if (w == 0) {
+    m = lane < nw ? sm[lane] : -INFINITY;
+    s = lane < nw ? ss[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      float mm = fmaxf(m, m2);
+      s = (m == -INFINITY ? 0.f : s * expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * expf(m2 - mm));
+      m = mm;
+    }
+    if (lane == 0) {
+      int tg = targets[row];
+      if (tg < 0 || tg >= V) {
+        atomicOr(flags, FLAG_TARGET_RANGE);
+        tg = 0;
+      }
+      float lse = m + logf(s);
+      s_lse = lse;
+      s_tg = tg;
+      losses[row] = lse - to_f(z[tg]);
+    }
+  }
+  __syncthreads();
+  if (!write_grad) return;
+  float lse = s_lse;
+  int tg = s_tg;
+  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    float f[N];
+    ld16(z + (size_t)vi * N, f);
+#pragma unroll
+    for (int k = 0; k < N; k++) {
+      int idx = vi * N + k;
+      f[k] = idx < V ? (expf(f[k] - lse) - (idx == tg ? 1.f : 0.f)) * dloss : 0.f;
+    }
+    st16(z + (size_t)vi * N, f);
+  }
+}
+
+template <typename T>
+cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,
+                       float dloss, int write_grad, int* flags, cudaStream_t st) {
+  if (Vp % VecN<T>::n) return cudaErrorInvalidValue;
+  softmax_ce_kernel<T><<<rows, 1024, 0, st>>>(logits, losses, targets, V, Vp, dloss, write_grad, flags);
+  return launch_status(1);
+}
+
+// mean of n per-position losses, one CTA, fixed summation order
+__global__ void mean_loss_kernel(float* loss, const float* __restrict__ losses, int n) {
+  __shared__ float sh[32];
+  float s = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) s += losses[i];
+  s = block_sum(s, sh);
+  if (threadIdx.x == 0) *loss = s / (float)n;
+}
+cudaError_t mean_loss(float* loss, const float* losses, int n, cudaStream_t st) {
+  mean_loss_kernel<<<1, 1024, 0, st>>>(loss, losses, n);
+  return launch_status(1);
+}
+
+// ============================================================================
+// AdamW over the whole buffer, 4 params per thread, per-tensor weight decay
+// from a segment table; also writes the bf16 compute copy when pc != nullptr.
+// ============================================================================
+__global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
+                             float* __restrict__ v, bf16* __restrict__ pc, long long nvec, float lr, float b1,
+                             float b2, float eps, float bc1, float bc2, AdamSegments seg) {
+  long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    long long e = i * 4;
+    int s = 0;
+    while (s + 1 < seg.n && e >= seg.off[s + 1]) s++;
+    float wd = seg.wd[s];
+    float pv[4], gv[4], mv[4], vv[4];
+    ld16_cs(p + e, pv);
+    ld16_cs(g + e, gv);
+    ld16_cs(m + e, mv);
+    ld16_cs(v + e, vv);
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      mv[k] = b1 * mv[k] + (1.f - b1) * gv[k];
+      vv[k] = b2 * vv[k] + (1.f - b2) * gv[k] * gv[k];
+      float mh = mv[k] / bc1, vh = vv[k] / bc2;
+      pv[k] -= lr * (mh / (sqrtf(vh) + eps) + wd * pv[k]);
+    }
+    st16_cs(p + e, pv);
+    st16_cs(m + e, mv);
+    st16_cs(v + e, vv);
+    if (pc) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(pv[0], pv[1]), hi = __floats2bfloat162_rn(pv[2], pv[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo);
+      u.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(pc + e) = u;
+    }
+  }
+}
+
+cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* pc, long long n, float lr,
+                  float b1, float b2, float eps, float bc1, float bc2, const AdamSegments& seg,
+                  cudaStream_t st) {
+  if (n % 4) return cudaErrorInvalidValue;
+  long long nvec = n / 4;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = cdiv(nvec, 256);
+  if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+  adamw_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, g, m, v, pc, nvec, lr, b1, b2, eps, bc1, bc2, seg);
+  return launch_status(1);
+}
+
+__global__ void convert_f32_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ in, long long n) {
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = __float2bfloat16_rn(in[i]);
+}
+cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  convert_f32_bf16_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(out, in, n);
+  return launch_status(1);
+}
+
+// ============================================================================
+// standalone GELU forward/backward (128-bit streaming)
+// ============================================================================
+template <typename T>
+__global__ void gelu_forward_kernel(T* __restrict__ out, const T* __restrict__ in, long long nvec) {
+  constexpr int N = VecN<T>::n;
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nvec) return;
+  float f[N];
+  ld16_cs(in + i * N, f);
+#pragma unroll
+  for (int k = 0; k < N; k++) f[k] = gelu_f(f[k]);
+  st16_cs(out + i * N, f);
+}
+template <typename T>
+__global__ void gelu_backward_kernel(T* __restrict__ dinp, const T* __restrict__ inp, const T* __restrict__ dout,
+                                     long long nvec) {
+  constexpr int N = VecN<T>::n;
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nvec) return;
+  float x[N], d[N];
+  ld16_cs(inp + i * N, x);
+  ld16_cs(dout + i * N, d);
+#pragma unroll
+  for (int k = 0; k < N; k++) d[k] *= gelu_grad_f(x[k]);
+  st16_cs(dinp + i * N, d);
+}
+template <typename T>
+cudaError_t gelu_forward(T* out, const T* in, long long n, cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  if (n % N) return cudaErrorInvalidValue;
+  gelu_forward_kernel<T><<<(unsigned)cdiv(n / N, 256), 256, 0, st>>>(out, in, n / N);
+  return launch_status(1);
+}
+template <typename T>
+cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  if (n % N) return cudaErrorInvalidValue;
+  gelu_backward_kernel<T><<<(unsigned)cdiv(n / N, 256), 256, 0, st>>>(dinp, inp, dout, n / N);
+  return launch_status(1);
+}
+
+// ---- explicit instantiations ----------------------------------------------
+#define INST(T)                                                                                           \
+  template cudaError_t encoder_forward<T>(T*, const int*, const T*, const T*, int, int, int, int, int*,  \
+                                          cudaStream_t);                                                  \
+  template cudaError_t residual_layernorm_forward<T>(T*, T*, float*, float*, const T*, const T*, const T*, \
+                                                     const T*, int, int, cudaStream_t);                  \
+  template cudaError_t layernorm_backward<T>(float*, T*, const T*, const T*, const float*, const float*,  \
+                                             const T*, int, int, int, cudaStream_t);                     \
+  template cudaError_t ln_param_grad<T>(float*, float*, const T*, const T*, const float*, const float*,   \
+                                        int, int, float*, int, cudaStream_t);                            \
+  template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, int, cudaStream_t);       \
+  template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \
+  template cudaError_t attention_forward_simt<T>(T*, float*, const T*, int, int, int, int, cudaStream_t); \
+  template cudaError_t attention_backward_simt<T>(T*, float*, const T*, const T*, const T*, const float*, \
+                                                  int, int, int, int, cudaStream_t);                     \
+  template cudaError_t softmax_ce<T>(T*, float*, const int*, int, int, int, float, int, int*,             \
+                                     cudaStream_t);                                                       \
+  template cudaError_t gelu_forward<T>(T*, const T*, long long, cudaStream_t);                            \
+  template cudaError_t gelu_backward<T>(T*, const T*, const T*, long long, cudaStream_t);
+INST(float)
+INST(bf16)

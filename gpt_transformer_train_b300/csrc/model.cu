@@ -1,0 +1,543 @@
+// The GPT-2 training step behind the C ABI of include/gpt2.h.
+//
+// gpt2_forward / gpt2_backward / gpt2_adamw_step enqueue the layer kernels in
+// the order of "llm.c: GPT-2 training in plain C, with every gradient written
+// by hand", §2 How the code works: encoder, then per block
+// layernorm -> qkv matmul -> attention -> attention projection -> residual ->
+// layernorm -> fc matmul -> GELU -> fc projection -> residual, final
+// layernorm, tied classifier, softmax + cross-entropy; the backward runs the
+// same list in reverse.  Every residual add is fused into the next LayerNorm
+// and the classifier's softmax/cross-entropy backward is fused into its
+// forward ("llm.c's Origin and the Future of LLM Compilers", [13:50]).
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.cuh"
+#include "model_layout.h"
+
+extern void gpt2_count_launches(int n);
+extern unsigned long long gpt2_total_launches();
+
+struct gpt2 {
+  gpt2_config cfg;
+  ParamLayout pl;
+  BufferLayout bl;
+  char* base = nullptr;
+  cudaStream_t st = nullptr;
+  int BT = 0;
+  bool have_targets = false;   // last forward computed loss + dlogits
+  bool logits_valid = false;   // last forward kept the logits
+  bool loss_valid = false;
+  const int32_t* fwd_tokens = nullptr;
+  std::string err;
+  // GEMM event trace (roofline measurement)
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_ev;  // pairs
+  std::vector<double> prof_flops;
+  size_t prof_n = 0;
+  template <typename P> P* at(size_t off) const { return reinterpret_cast<P*>(base + off); }
+};
+
+static std::string g_create_err;
+
+#define FAIL(m, code, ...)                                          \
+  do {                                                              \
+    char _b[512];                                                   \
+    snprintf(_b, sizeof _b, __VA_ARGS__);                           \
+    if (m) (m)->err = _b; else g_create_err = _b;                   \
+    return code;                                                    \
+  } while (0)
+#define CK(m, call)                                                                       \
+  do {                                                                                    \
+    cudaError_t _e = (call);                                                              \
+    if (_e != cudaSuccess)                                                                \
+      FAIL(m, GPT2_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(_e), __FILE__, __LINE__); \
+  } while (0)
+
+// --------------------------------------------------------------------------
+// config validation and the planner
+// --------------------------------------------------------------------------
+int validate_config(const gpt2_config& c, const char** why) {
+  *why = "";
+  if (c.L <= 0 || c.C <= 0 || c.H <= 0 || c.max_T <= 0 || c.V <= 0 || c.Vp <= 0 || c.B <= 0 || c.T <= 0)
+    return *why = "all sizes must be positive", GPT2_ERR_INVALID_CONFIG;
+  if (c.C % c.H) return *why = "C must be a multiple of H", GPT2_ERR_INVALID_CONFIG;
+  if (c.Vp < c.V) return *why = "Vp must be >= V", GPT2_ERR_INVALID_CONFIG;
+  if (c.T > c.max_T) return *why = "T must be <= max_T", GPT2_ERR_INVALID_CONFIG;
+  if (c.C > 2048) return *why = "C must be <= 2048", GPT2_ERR_INVALID_CONFIG;
+  if (c.V > 65535) return *why = "V must be <= 65535", GPT2_ERR_INVALID_CONFIG;
+  if ((long long)c.B * c.T > 32768) return *why = "B*T must be <= 32768", GPT2_ERR_INVALID_CONFIG;
+  int hd = c.C / c.H;
+  if (c.precision == GPT2_PRECISION_FP32) {
+    if (c.C % 4 || c.Vp % 4) return *why = "fp32 mode needs C % 4 == 0 and Vp % 4 == 0", GPT2_ERR_INVALID_CONFIG;
+    if (hd > 128) return *why = "head size must be <= 128", GPT2_ERR_INVALID_CONFIG;
+  } else if (c.precision == GPT2_PRECISION_BF16) {
+    if (c.C % 64) return *why = "bf16 mode needs C % 64 == 0", GPT2_ERR_INVALID_CONFIG;
+    if (hd != 64) return *why = "bf16 mode needs head size 64", GPT2_ERR_INVALID_CONFIG;
+    if (c.T % 128) return *why = "bf16 mode needs T % 128 == 0", GPT2_ERR_INVALID_CONFIG;
+    if (((long long)c.B * c.T) % 128) return *why = "bf16 mode needs B*T % 128 == 0", GPT2_ERR_INVALID_CONFIG;
+    if (c.Vp % 128) return *why = "bf16 mode needs Vp % 128 == 0", GPT2_ERR_INVALID_CONFIG;
+  } else {
+    return *why = "precision must be GPT2_PRECISION_FP32 or GPT2_PRECISION_BF16", GPT2_ERR_INVALID_CONFIG;
+  }
+  return GPT2_OK;
+}
+
+BufferLayout buffer_layout(const gpt2_config& c) {
+  BufferLayout b{};
+  ParamLayout pl = param_layout(c);
+  size_t es = c.precision == GPT2_PRECISION_BF16 ? 2 : 4;  // activation element size
+  size_t L = c.L, C = c.C, BT = (size_t)c.B * c.T;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o += (bytes + 255) & ~(size_t)255;
+    return r;
+  };
+  b.params = take(pl.total * 4);
+  b.grads = take(pl.total * 4);
+  b.m = take(pl.total * 4);
+  b.v = take(pl.total * 4);
+  b.pbf = c.precision == GPT2_PRECISION_BF16 ? take(pl.total * 2) : 0;
+  b.resid = take((2 * L + 1) * BT * C * es);
+  b.ln = take((2 * L + 1) * BT * C * es);
+  b.ln_mean = take((2 * L + 1) * BT * 4);
+  b.ln_rstd = take((2 * L + 1) * BT * 4);
+  b.qkv = take(L * BT * 3 * C * es);
+  b.atty = take(L * BT * C * es);
+  b.lse = take(L * BT * c.H * 4);
+  b.fch = take(L * BT * 4 * C * es);
+  b.fchg = take(L * BT * 4 * C * es);
+  b.proj = take(BT * C * es);
+  b.logits = take(BT * (size_t)c.Vp * es);
+  b.losses = take(BT * 4);
+  b.loss = take(256);
+  b.dres = take(BT * C * 4);
+  b.dres_c = c.precision == GPT2_PRECISION_BF16 ? take(BT * C * es) : b.dres;
+  b.dbig = take(BT * 4 * C * es);
+  b.dsmall = take(BT * C * es);
+  b.attD = take(BT * c.H * 4);
+  size_t nch = (size_t)reduce_chunks((int)BT);
+  b.partial = take(nch * 4 * C * 4);
+  b.keys = take(encoder_backward_scratch_bytes((int)BT));
+  b.flags = take(256);
+  b.tok = take(BT * 4);
+  b.tgt = take(BT * 4);
+  b.total = o;
+  return b;
+}
+
+// --------------------------------------------------------------------------
+// typed views and the step
+// --------------------------------------------------------------------------
+template <typename T>
+struct Step {
+  gpt2* m;
+  const gpt2_config& c;
+  size_t BT, C, L;
+  explicit Step(gpt2* mm) : m(mm), c(mm->cfg), BT((size_t)mm->BT), C(mm->cfg.C), L(mm->cfg.L) {}
+
+  // compute copy of a parameter tensor (bf16 copy in bf16 mode, master fp32 otherwise)
+  const T* W(int t, size_t layer = 0, size_t per_layer = 0) const {
+    size_t e = m->pl.off[t] + layer * per_layer;
+    if (c.precision == GPT2_PRECISION_BF16) return m->at<T>(m->bl.pbf) + e;
+    return m->at<T>(m->bl.params) + e;
+  }
+  float* G(int t, size_t layer = 0, size_t per_layer = 0) const {
+    return m->at<float>(m->bl.grads) + m->pl.off[t] + layer * per_layer;
+  }
+  T* resid(size_t i) const { return m->at<T>(m->bl.resid) + i * BT * C; }
+  T* ln(size_t i) const { return m->at<T>(m->bl.ln) + i * BT * C; }
+  float* mean(size_t i) const { return m->at<float>(m->bl.ln_mean) + i * BT; }
+  float* rstd(size_t i) const { return m->at<float>(m->bl.ln_rstd) + i * BT; }
+  T* qkv(size_t l) const { return m->at<T>(m->bl.qkv) + l * BT * 3 * C; }
+  T* atty(size_t l) const { return m->at<T>(m->bl.atty) + l * BT * C; }
+  float* lse(size_t l) const { return m->at<float>(m->bl.lse) + l * BT * c.H; }
+  T* fch(size_t l) const { return m->at<T>(m->bl.fch) + l * BT * 4 * C; }
+  T* fchg(size_t l) const { return m->at<T>(m->bl.fchg) + l * BT * 4 * C; }
+  T* proj() const { return m->at<T>(m->bl.proj); }
+  T* logits() const { return m->at<T>(m->bl.logits); }
+  float* losses() const { return m->at<float>(m->bl.losses); }
+  float* dres() const { return m->at<float>(m->bl.dres); }
+  // operand copy of dres for the GEMMs (== dres in fp32 mode)
+  T* dres_c() const { return m->at<T>(m->bl.dres_c); }
+  T* dres_c_or_null() const { return c.precision == GPT2_PRECISION_BF16 ? dres_c() : nullptr; }
+  T* dbig() const { return m->at<T>(m->bl.dbig); }
+  T* dsmall() const { return m->at<T>(m->bl.dsmall); }
+  int* flags() const { return m->at<int>(m->bl.flags); }
+
+  cudaError_t gemm(GemmArgs a) {
+    bool rec = m->prof_on && m->prof_n < m->prof_flops.size();
+    if (rec) cudaEventRecord(m->prof_ev[2 * m->prof_n], m->st);
+    cudaError_t e;
+    if (c.precision == GPT2_PRECISION_BF16 && gemm_tc_supported(a)) e = gemm_tc(a, flags(), m->st);
+    else e = gemm_simt<T>(a, m->st);
+    if (rec) {
+      cudaEventRecord(m->prof_ev[2 * m->prof_n + 1], m->st);
+      m->prof_flops[m->prof_n++] = 2.0 * a.M * a.N * (double)a.K;
+    }
+    return e;
+  }
+  // out[M][N] = X[M][K] . W[N][K]^T (+ bias), optionally with GELU (aux = pre-activation)
+  cudaError_t linear_fwd(T* out, const T* X, const T* Wt, const T* bias, int M, int N, int K, T* aux = nullptr) {
+    GemmArgs a{X, K, 1, Wt, K, 1, M, N, K, out, N, bias, aux, N, aux ? EPI_GELU : EPI_STORE};
+    return gemm(a);
+  }
+  // dX[M][K] = dY[M][N] . W[N][K]  (optionally times GELU'(aux))
+  cudaError_t linear_dgrad(T* dX, const T* dY, const T* Wt, int M, int N, int K, const T* aux = nullptr) {
+    GemmArgs a{dY, N, 1, Wt, K, 0, M, K, N, dX, K, nullptr, (void*)aux, K, aux ? EPI_GELU_BWD : EPI_STORE};
+    return gemm(a);
+  }
+  // dW[N][K] += dY[M][N]^T . X[M][K]
+  cudaError_t linear_wgrad(float* dW, const T* dY, const T* X, int M, int N, int K) {
+    GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32};
+    return gemm(a);
+  }
+
+  int forward(const int32_t* tok, const int32_t* tgt) {
+    cudaStream_t st = m->st;
+    int B = c.B, T_ = c.T, Ci = c.C, Li = c.L, BTi = m->BT;
+    size_t CC = C * C;
+    CK(m, encoder_forward<T>(resid(0), tok, W(GPT2_WTE), W(GPT2_WPE), B, T_, Ci, c.V, flags(), st));
+    for (int l = 0; l < Li; l++) {
+      if (l == 0)
+        CK(m, residual_layernorm_forward<T>(nullptr, ln(0), mean(0), rstd(0), resid(0), nullptr,
+                                            W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C), BTi, Ci, st));
+      else
+        CK(m, residual_layernorm_forward<T>(resid(2 * l), ln(2 * l), mean(2 * l), rstd(2 * l), resid(2 * l - 1),
+                                            proj(), W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C), BTi, Ci, st));
+      CK(m, linear_fwd(qkv(l), ln(2 * l), W(GPT2_QKVW, l, 3 * CC), W(GPT2_QKVB, l, 3 * C), BTi, 3 * Ci, Ci));
+      CK(m, attention_forward_simt<T>(atty(l), lse(l), qkv(l), B, T_, Ci, c.H, st));
+      CK(m, linear_fwd(proj(), atty(l), W(GPT2_ATTPROJW, l, CC), W(GPT2_ATTPROJB, l, C), BTi, Ci, Ci));
+      CK(m, residual_layernorm_forward<T>(resid(2 * l + 1), ln(2 * l + 1), mean(2 * l + 1), rstd(2 * l + 1),
+                                          resid(2 * l), proj(), W(GPT2_LN2W, l, C), W(GPT2_LN2B, l, C), BTi, Ci, st));
+      CK(m, linear_fwd(fchg(l), ln(2 * l + 1), W(GPT2_FCW, l, 4 * CC), W(GPT2_FCB, l, 4 * C), BTi, 4 * Ci, Ci, fch(l)));
+      CK(m, linear_fwd(proj(), fchg(l), W(GPT2_FCPROJW, l, 4 * CC), W(GPT2_FCPROJB, l, C), BTi, Ci, 4 * Ci));
+    }
+    size_t f = 2 * L;
+    CK(m, residual_layernorm_forward<T>(resid(f), ln(f), mean(f), rstd(f), resid(f - 1), proj(), W(GPT2_LNFW),
+                                        W(GPT2_LNFB), BTi, Ci, st));
+    CK(m, linear_fwd(logits(), ln(f), W(GPT2_WTE), nullptr, BTi, c.Vp, Ci));
+    if (tgt) {
+      CK(m, softmax_ce<T>(logits(), losses(), tgt, BTi, c.V, c.Vp, 1.0f / (float)BTi, 1, flags(), st));
+      CK(m, mean_loss(m->at<float>(m->bl.loss), losses(), BTi, st));
+    }
+    return GPT2_OK;
+  }
+
+  int backward(const int32_t* tok) {
+    cudaStream_t st = m->st;
+    int Ci = c.C, Li = c.L, BTi = m->BT;
+    size_t CC = C * C;
+    int nch = reduce_chunks(BTi);
+    float* part = m->at<float>(m->bl.partial);
+    size_t f = 2 * L;
+    // classifier (tied wte): dlnf = dlogits . wte ; dwte += dlogits^T . lnf
+    CK(m, linear_dgrad(dsmall(), logits(), W(GPT2_WTE), BTi, c.Vp, Ci));
+    CK(m, linear_wgrad(G(GPT2_WTE), logits(), ln(f), BTi, c.Vp, Ci));
+    CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
+                                Ci, 0, st));
+    CK(m, ln_param_grad<T>(G(GPT2_LNFW), G(GPT2_LNFB), dsmall(), resid(f), mean(f), rstd(f), BTi, Ci, part, nch, st));
+    for (int l = Li - 1; l >= 0; l--) {
+      // fc projection (+ GELU backward fused into its input-gradient GEMM)
+      CK(m, linear_dgrad(dbig(), dres_c(), W(GPT2_FCPROJW, l, 4 * CC), BTi, Ci, 4 * Ci, fch(l)));
+      CK(m, linear_wgrad(G(GPT2_FCPROJW, l, 4 * CC), dres_c(), fchg(l), BTi, Ci, 4 * Ci));
+      CK(m, colsum<float>(G(GPT2_FCPROJB, l, C), dres(), BTi, Ci, Ci, part, nch, st));
+      // fc
+      CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_FCW, l, 4 * CC), BTi, 4 * Ci, Ci));
+      CK(m, linear_wgrad(G(GPT2_FCW, l, 4 * CC), dbig(), ln(2 * l + 1), BTi, 4 * Ci, Ci));
+      CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dbig(), BTi, 4 * Ci, 4 * Ci, part, nch, st));
+      // LN2 (+ residual gradient)
+      CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
+                                  rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, st));
+      CK(m, ln_param_grad<T>(G(GPT2_LN2W, l, C), G(GPT2_LN2B, l, C), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
+                             rstd(2 * l + 1), BTi, Ci, part, nch, st));
+      // attention projection
+      CK(m, linear_dgrad(dsmall(), dres_c(), W(GPT2_ATTPROJW, l, CC), BTi, Ci, Ci));
+      CK(m, linear_wgrad(G(GPT2_ATTPROJW, l, CC), dres_c(), atty(l), BTi, Ci, Ci));
+      CK(m, colsum<float>(G(GPT2_ATTPROJB, l, C), dres(), BTi, Ci, Ci, part, nch, st));
+      // attention
+      CK(m, attention_backward_simt<T>(dbig(), m->at<float>(m->bl.attD), dsmall(), qkv(l), atty(l), lse(l), c.B,
+                                       c.T, Ci, c.H, st));
+      // qkv
+      CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
+      CK(m, linear_wgrad(G(GPT2_QKVW, l, 3 * CC), dbig(), ln(2 * l), BTi, 3 * Ci, Ci));
+      CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dbig(), BTi, 3 * Ci, 3 * Ci, part, nch, st));
+      // LN1 (+ residual gradient)
+      CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(2 * l), mean(2 * l), rstd(2 * l),
+                                  W(GPT2_LN1W, l, C), BTi, Ci, 1, st));
+      CK(m, ln_param_grad<T>(G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C), dsmall(), resid(2 * l), mean(2 * l),
+                             rstd(2 * l), BTi, Ci, part, nch, st));
+    }
+    CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
+    return GPT2_OK;
+  }
+};
+
+static int check_flags(gpt2* m) {
+  int h[4] = {0, 0, 0, 0};
+  CK(m, cudaMemcpyAsync(h, m->at<int>(m->bl.flags), sizeof h, cudaMemcpyDeviceToHost, m->st));
+  CK(m, cudaStreamSynchronize(m->st));
+  if (h[0]) {
+    CK(m, cudaMemsetAsync(m->at<int>(m->bl.flags), 0, sizeof h, m->st));
+    CK(m, cudaStreamSynchronize(m->st));
+    if (h[0] & FLAG_TIMEOUT) FAIL(m, GPT2_ERR_TIMEOUT, "a kernel's bounded wait ran out (flags=0x%x)", h[0]);
+    if (h[0] & FLAG_TOKEN_RANGE) FAIL(m, GPT2_ERR_TOKEN_RANGE, "a token id is outside [0, V)");
+    if (h[0] & FLAG_TARGET_RANGE) FAIL(m, GPT2_ERR_TOKEN_RANGE, "a target id is outside [0, V)");
+  }
+  return GPT2_OK;
+}
+
+// --------------------------------------------------------------------------
+// C ABI
+// --------------------------------------------------------------------------
+extern "C" {
+
+size_t gpt2_num_parameters(const gpt2_config* cfg) {
+  const char* why;
+  if (!cfg || validate_config(*cfg, &why) != GPT2_OK) return 0;
+  return param_layout(*cfg).total;
+}
+
+size_t gpt2_tensor_numel(const gpt2_config* cfg, int tensor) {
+  const char* why;
+  if (!cfg || tensor < 0 || tensor >= GPT2_NUM_TENSORS || validate_config(*cfg, &why) != GPT2_OK) return 0;
+  return param_layout(*cfg).numel[tensor];
+}
+
+size_t gpt2_required_bytes(const gpt2_config* cfg) {
+  const char* why;
+  if (!cfg || validate_config(*cfg, &why) != GPT2_OK) return 0;
+  return buffer_layout(*cfg).total;
+}
+
+int gpt2_init_params_host(const gpt2_config* cfg, uint64_t seed, float* host_out) {
+  const char* why;
+  if (!cfg || !host_out) FAIL((gpt2*)nullptr, GPT2_ERR_INVALID_ARG, "NULL argument");
+  int rc = validate_config(*cfg, &why);
+  if (rc) FAIL((gpt2*)nullptr, rc, "invalid config: %s", why);
+  init_params_host(*cfg, seed, host_out);
+  return GPT2_OK;
+}
+
+int gpt2_create(const gpt2_config* cfg, uint64_t seed, void* dev_buf, size_t bytes, void* cuda_stream, gpt2** out) {
+  const char* why;
+  if (out) *out = nullptr;
+  if (!cfg || !dev_buf || !out) FAIL((gpt2*)nullptr, GPT2_ERR_INVALID_ARG, "NULL argument");
+  int rc = validate_config(*cfg, &why);
+  if (rc) FAIL((gpt2*)nullptr, rc, "invalid config: %s", why);
+  BufferLayout bl = buffer_layout(*cfg);
+  if (bytes < bl.total)
+    FAIL((gpt2*)nullptr, GPT2_ERR_BUFFER_TOO_SMALL, "buffer has %zu bytes, the model needs %zu", bytes, bl.total);
+  if ((uintptr_t)dev_buf % 256) FAIL((gpt2*)nullptr, GPT2_ERR_INVALID_ARG, "dev_buf must be 256-byte aligned");
+  gpt2* m = new gpt2();
+  m->cfg = *cfg;
+  m->pl = param_layout(*cfg);
+  m->bl = bl;
+  m->base = (char*)dev_buf;
+  m->st = (cudaStream_t)cuda_stream;
+  m->BT = cfg->B * cfg->T;
+  std::vector<float> host(m->pl.total);
+  init_params_host(*cfg, seed, host.data());
+  cudaError_t e = cudaMemsetAsync(m->base, 0, bl.total, m->st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(m->at<float>(bl.params), host.data(), m->pl.total * 4, cudaMemcpyHostToDevice, m->st);
+  if (e == cudaSuccess && cfg->precision == GPT2_PRECISION_BF16)
+    e = convert_f32_bf16(m->at<bf16>(bl.pbf), m->at<float>(bl.params), (long long)m->pl.total, m->st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->st);
+  if (e != cudaSuccess) {
+    g_create_err = std::string("gpt2_create: ") + cudaGetErrorString(e);
+    delete m;
+    return GPT2_ERR_CUDA;
+  }
+  gpt2_count_launches(cfg->precision == GPT2_PRECISION_BF16 ? 1 : 0);
+  *out = m;
+  return GPT2_OK;
+}
+
+int gpt2_forward(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_dev, float* loss_host) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!tokens_dev) FAIL(m, GPT2_ERR_INVALID_ARG, "tokens_dev is NULL");
+  if (loss_host && !targets_dev) FAIL(m, GPT2_ERR_INVALID_ARG, "loss_host needs targets_dev");
+  int rc = m->cfg.precision == GPT2_PRECISION_BF16 ? Step<bf16>(m).forward(tokens_dev, targets_dev)
+                                                   : Step<float>(m).forward(tokens_dev, targets_dev);
+  m->have_targets = rc == GPT2_OK && targets_dev != nullptr;
+  m->logits_valid = rc == GPT2_OK && targets_dev == nullptr;
+  m->loss_valid = m->have_targets;
+  m->fwd_tokens = tokens_dev;
+  if (rc) return rc;
+  if (loss_host) return gpt2_get_loss(m, loss_host);
+  return GPT2_OK;
+}
+
+int gpt2_backward(gpt2* m) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!m->have_targets) FAIL(m, GPT2_ERR_BAD_ORDER, "gpt2_backward needs a gpt2_forward with targets first");
+  int rc = m->cfg.precision == GPT2_PRECISION_BF16 ? Step<bf16>(m).backward(m->fwd_tokens)
+                                                   : Step<float>(m).backward(m->fwd_tokens);
+  m->have_targets = false;  // dlogits consumed
+  return rc;
+}
+
+int gpt2_zero_grad(gpt2* m) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  CK(m, cudaMemsetAsync(m->at<float>(m->bl.grads), 0, m->pl.total * 4, m->st));
+  return GPT2_OK;
+}
+
+int gpt2_adamw_step(gpt2* m, float lr, float b1, float b2, float eps, float wd, int t) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (t < 1) FAIL(m, GPT2_ERR_INVALID_ARG, "AdamW step t must be >= 1");
+  AdamSegments seg{};
+  seg.n = GPT2_NUM_TENSORS;
+  for (int i = 0; i <= GPT2_NUM_TENSORS; i++) seg.off[i] = (long long)m->pl.off[i];
+  for (int i = 0; i < GPT2_NUM_TENSORS; i++) {
+    bool decay = i == GPT2_WTE || i == GPT2_WPE || i == GPT2_QKVW || i == GPT2_ATTPROJW || i == GPT2_FCW ||
+                 i == GPT2_FCPROJW;
+    seg.wd[i] = decay ? wd : 0.f;
+  }
+  float bc1 = (float)(1.0 - std::pow((double)b1, (double)t));
+  float bc2 = (float)(1.0 - std::pow((double)b2, (double)t));
+  bf16* pc = m->cfg.precision == GPT2_PRECISION_BF16 ? m->at<bf16>(m->bl.pbf) : nullptr;
+  CK(m, adamw(m->at<float>(m->bl.params), m->at<float>(m->bl.grads), m->at<float>(m->bl.m), m->at<float>(m->bl.v),
+              pc, (long long)m->pl.total, lr, b1, b2, eps, bc1, bc2, seg, m->st));
+  return GPT2_OK;
+}
+
+int gpt2_step_host(gpt2* m, const int32_t* tokens_host, const int32_t* targets_host, float lr, float b1, float b2,
+                   float eps, float wd, int t, float* loss_host) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!tokens_host || !targets_host || !loss_host) FAIL(m, GPT2_ERR_INVALID_ARG, "NULL host pointer");
+  size_t nb = (size_t)m->BT * 4;
+  int32_t* tok = m->at<int32_t>(m->bl.tok);
+  int32_t* tgt = m->at<int32_t>(m->bl.tgt);
+  CK(m, cudaMemcpyAsync(tok, tokens_host, nb, cudaMemcpyHostToDevice, m->st));
+  CK(m, cudaMemcpyAsync(tgt, targets_host, nb, cudaMemcpyHostToDevice, m->st));
+  int rc = gpt2_zero_grad(m);
+  if (!rc) rc = gpt2_forward(m, tok, tgt, nullptr);
+  if (!rc) rc = gpt2_backward(m);
+  if (!rc) rc = gpt2_adamw_step(m, lr, b1, b2, eps, wd, t);
+  if (!rc) rc = gpt2_get_loss(m, loss_host);
+  return rc;
+}
+
+int gpt2_get_loss(gpt2* m, float* loss_host) {
+  if (!m || !loss_host) return GPT2_ERR_INVALID_ARG;
+  if (!m->loss_valid) FAIL(m, GPT2_ERR_BAD_ORDER, "no forward with targets has run");
+  CK(m, cudaMemcpyAsync(loss_host, m->at<float>(m->bl.loss), 4, cudaMemcpyDeviceToHost, m->st));
+  int rc = check_flags(m);
+  if (rc) return rc;
+  if (!std::isfinite(*loss_host)) FAIL(m, GPT2_ERR_NAN, "loss is not finite (%f)", *loss_host);
+  return GPT2_OK;
+}
+
+int gpt2_get_params(gpt2* m, int tensor, float* host) {
+  if (!m || !host || tensor < 0 || tensor >= GPT2_NUM_TENSORS) return GPT2_ERR_INVALID_ARG;
+  CK(m, cudaMemcpyAsync(host, m->at<float>(m->bl.params) + m->pl.off[tensor], m->pl.numel[tensor] * 4,
+                        cudaMemcpyDeviceToHost, m->st));
+  CK(m, cudaStreamSynchronize(m->st));
+  return GPT2_OK;
+}
+
+int gpt2_set_params(gpt2* m, int tensor, const float* host) {
+  if (!m || !host || tensor < 0 || tensor >= GPT2_NUM_TENSORS) return GPT2_ERR_INVALID_ARG;
+  float* dst = m->at<float>(m->bl.params) + m->pl.off[tensor];
+  CK(m, cudaMemcpyAsync(dst, host, m->pl.numel[tensor] * 4, cudaMemcpyHostToDevice, m->st));
+  if (m->cfg.precision == GPT2_PRECISION_BF16) {
+    CK(m, convert_f32_bf16(m->at<bf16>(m->bl.pbf) + m->pl.off[tensor], dst, (long long)m->pl.numel[tensor], m->st));
+    gpt2_count_launches(1);
+  }
+  CK(m, cudaStreamSynchronize(m->st));
+  return GPT2_OK;
+}
+
+int gpt2_get_grads(gpt2* m, int tensor, float* host) {
+  if (!m || !host || tensor < 0 || tensor >= GPT2_NUM_TENSORS) return GPT2_ERR_INVALID_ARG;
+  CK(m, cudaMemcpyAsync(host, m->at<float>(m->bl.grads) + m->pl.off[tensor], m->pl.numel[tensor] * 4,
+                        cudaMemcpyDeviceToHost, m->st));
+  CK(m, cudaStreamSynchronize(m->st));
+  return GPT2_OK;
+}
+
+static int copy_act_to_host(gpt2* m, size_t off, size_t n, float* host) {
+  if (m->cfg.precision == GPT2_PRECISION_BF16) {
+    std::vector<uint16_t> tmp(n);
+    CK(m, cudaMemcpyAsync(tmp.data(), m->base + off, n * 2, cudaMemcpyDeviceToHost, m->st));
+    CK(m, cudaStreamSynchronize(m->st));
+    for (size_t i = 0; i < n; i++) {
+      uint32_t u = (uint32_t)tmp[i] << 16;
+      memcpy(&host[i], &u, 4);
+    }
+  } else {
+    CK(m, cudaMemcpyAsync(host, m->base + off, n * 4, cudaMemcpyDeviceToHost, m->st));
+    CK(m, cudaStreamSynchronize(m->st));
+  }
+  return GPT2_OK;
+}
+
+int gpt2_get_logits(gpt2* m, float* host) {
+  if (!m || !host) return GPT2_ERR_INVALID_ARG;
+  if (!m->logits_valid) FAIL(m, GPT2_ERR_BAD_ORDER, "logits are kept only by a forward without targets");
+  int rc = copy_act_to_host(m, m->bl.logits, (size_t)m->BT * m->cfg.Vp, host);
+  return rc ? rc : check_flags(m);
+}
+
+int gpt2_get_losses(gpt2* m, float* host) {
+  if (!m || !host) return GPT2_ERR_INVALID_ARG;
+  if (!m->loss_valid) FAIL(m, GPT2_ERR_BAD_ORDER, "no forward with targets has run");
+  CK(m, cudaMemcpyAsync(host, m->at<float>(m->bl.losses), (size_t)m->BT * 4, cudaMemcpyDeviceToHost, m->st));
+  return check_flags(m);
+}
+
+int gpt2_sync(gpt2* m) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  return check_flags(m);
+}
+
+uint64_t gpt2_launch_count(gpt2* m) {
+  (void)m;
+  return (uint64_t)gpt2_total_launches();
+}
+
+const char* gpt2_last_error(gpt2* m) { return m ? m->err.c_str() : g_create_err.c_str(); }
+
+int gpt2_profile_gemm(gpt2* m, int enable) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (enable && m->prof_ev.empty()) {
+    const size_t n = 8192;
+    m->prof_ev.resize(2 * n);
+    for (auto& e : m->prof_ev) CK(m, cudaEventCreate(&e));
+    m->prof_flops.assign(n, 0.0);
+  }
+  m->prof_on = enable != 0;
+  return GPT2_OK;
+}
+
+int gpt2_profile_read(gpt2* m, double* ms_total, uint64_t* launches, double* flops_total) {
+  if (!m || !ms_total || !launches || !flops_total) return GPT2_ERR_INVALID_ARG;
+  CK(m, cudaStreamSynchronize(m->st));
+  double ms = 0, fl = 0;
+  for (size_t i = 0; i < m->prof_n; i++) {
+    float t = 0.f;
+    CK(m, cudaEventElapsedTime(&t, m->prof_ev[2 * i], m->prof_ev[2 * i + 1]));
+    ms += t;
+    fl += m->prof_flops[i];
+  }
+  *ms_total = ms;
+  *launches = m->prof_n;
+  *flops_total = fl;
+  m->prof_n = 0;
+  return GPT2_OK;
+}
+
+void gpt2_destroy(gpt2* m) {
+  if (!m) return;
+  for (auto& e : m->prof_ev) cudaEventDestroy(e);
+  delete m;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+/*
+ * gpt2_ops.h — kernel-level C ABI: each step of the GPT-2 training step as
+ * its own call, for per-kernel parity tests and roofline measurement.
+ *
+ * The layers and their backward formulas are those of "llm.c: GPT-2 training
+ * in plain C, with every gradient written by hand", §2 How the code works
+ * (encoder, layernorm, matmul, attention, gelu, residual, softmax and
+ * crossentropy, each with a hand-written backward; attention's causal loop
+ * t2 <= t), with the fusions of "llm.c's Origin and the Future of LLM
+ * Compilers", [13:50] Avengers Assemble (residual add fused into LayerNorm,
+ * softmax and cross-entropy fused in the classifier, AdamW as one fused
+ * update, deterministic encoder backward without atomics).
+ *
+ * Conventions
+ *   - dtype selects the activation element type: GPT2_PRECISION_FP32 (float)
+ *     or GPT2_PRECISION_BF16 (__nv_bfloat16).  Statistics (mean, rstd, LSE,
+ *     losses) and parameter gradients are always float.
+ *   - Every pointer except `*_host` is a device pointer owned by the caller;
+ *     rows are contiguous and row-major unless a leading dimension is given.
+ *     Vector kernels need 16-byte aligned rows (C multiple of 4 floats or 8
+ *     bf16 values).
+ *   - `scratch` is caller-owned device memory of at least the size the
+ *     matching *_scratch_bytes() call returns; it is overwritten.
+ *   - `stream` is a cudaStream_t; calls only enqueue work.
+ *   - Returns GPT2_OK or GPT2_ERR_INVALID_ARG (bad shape/dtype/scratch) or
+ *     GPT2_ERR_CUDA (launch failure).  Kernels that check ranges OR a bit into
+ *     *flags_dev (1 token, 2 target, 4 timeout) instead of faulting.
+ */
+#ifndef GPT2_B300_OPS_H
+#define GPT2_B300_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gpt2.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* out[b,t,:] = wte[tok[b,t]] + wpe[t]   (out: [B*T][C], wte: [V..][C], wpe: [>=T][C]) */
+int gpt2_op_encoder_forward(int dtype, void* out, const int32_t* tokens, const void* wte, const void* wpe,
+                            int B, int T, int C, int V, int* flags_dev, void* stream);
+
+/* dwpe[t] += sum_b dres[b,t];  dwte[v] += sum of dres rows with token v, summed in
+ * increasing position order (deterministic).  dres: float [B*T][C]. */
+size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T);
+int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B, int T,
+                             int C, void* scratch, size_t scratch_bytes, void* stream);
+
+/* r = a + b (b may be NULL: r = a, resid_out unused); y = (r - mean)*rstd*w + bias,
+ * rstd = 1/sqrt(biased var + 1e-5); rows x C. */
+int gpt2_op_residual_layernorm_forward(int dtype, void* resid_out, void* y, float* mean, float* rstd,
+                                       const void* a, const void* b, const void* w, const void* bias, int rows,
+                                       int C, void* stream);
+
+/* dres = (accumulate ? dres : 0) + dx with dx = rstd*(dnorm - mean(dnorm) - xhat*mean(dnorm*xhat)),
+ * dnorm = dy*w; dres_c (optional) receives dres in dtype; dw += sum dy*xhat, db += sum dy (if non-NULL). */
+size_t gpt2_op_layernorm_backward_scratch_bytes(int rows, int C);
+int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void* dy, const void* x,
+                               const float* mean, const float* rstd, const void* w, float* dw, float* db,
+                               int rows, int C, int accumulate, void* scratch, size_t scratch_bytes, void* stream);
+
+/* D(m,n) = sum_k A(m,k) B(n,k) then an epilogue:
+ *   A(m,k) = a_kmajor ? A[m*lda+k] : A[k*lda+m];  B(n,k) = b_kmajor ? B[n*ldb+k] : B[k*ldb+n]
+ *   epilogue 0: D = acc (+bias[n])          1: aux = acc + bias[n], D = GELU_tanh(aux)
+ *            2: D = acc * GELU_tanh'(aux)   3: D (float) += acc
+ * path: 0 = best available, 1 = SIMT kernel, 2 = tensor-core (tcgen05) kernel only
+ * (GPT2_ERR_INVALID_ARG if the shape/layout is outside what it handles). */
+int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const void* B, long long ldb,
+                   int b_kmajor, int M, int N, int K, void* D, long long ldd, const void* bias, void* aux,
+                   long long ldaux, int epilogue, int path, int* flags_dev, void* stream);
+
+/* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
+ * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of
+ * the scaled scores q.k/sqrt(hd) over t2 <= t. */
+int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H,
+                              void* stream);
+/* dqkv [B*T][3C] from dout [B*T][C] with P recomputed from lse. */
+size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H);
+int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* out,
+                               const float* lse, int B, int T, int C, int H, void* scratch, size_t scratch_bytes,
+                               void* stream);
+
+/* Per row of logits [rows][Vp]: losses[r] = logsumexp(z[0:V]) - z[target];
+ * write_grad: z[v] = (softmax(z[0:V])[v] - [v == target]) * dloss in place, pads 0. */
+int gpt2_op_softmax_crossentropy(int dtype, void* logits, float* losses, const int32_t* targets, int rows, int V,
+                                 int Vp, float dloss, int write_grad, int* flags_dev, void* stream);
+
+/* AdamW on n floats (n % 4 == 0), bias-corrected at step t >= 1, decay wd;
+ * p_bf16 (optional) receives the updated parameters rounded to bf16. */
+int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* p_bf16, long long n, float lr, float b1,
+                  float b2, float eps, float wd, int t, void* stream);
+
+/* tanh-form GELU forward / backward (dinp = dout * GELU'(inp)) over n elements. */
+int gpt2_op_gelu_forward(int dtype, void* out, const void* in, long long n, void* stream);
+int gpt2_op_gelu_backward(int dtype, void* dinp, const void* inp, const void* dout, long long n, void* stream);
+
+/* out[c] += sum_r X[r*ldx + c] (deterministic order). */
+size_t gpt2_op_colsum_scratch_bytes(int rows, int cols);
+int gpt2_op_colsum(int dtype, float* out, const void* X, int rows, int cols, long long ldx, void* scratch,
+                   size_t scratch_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_B300_OPS_H */

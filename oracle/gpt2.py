@@ -366,9 +366,11 @@ def softmax_forward(logits, V):
     """Max-subtracted softmax over the first V columns; pad columns get 0."""
     z = logits[..., :V]
     m = z.max(axis=-1, keepdims=True)
-    e = np.exp(z - m)
     probs = np.zeros_like(logits)
-    probs[..., :V] = e / e.sum(axis=-1, keepdims=True)
+    e = probs[..., :V]
+    np.subtract(z, m, out=e)
+    np.exp(e, out=e)
+    e /= e.sum(axis=-1, keepdims=True)
     return probs
 
 
@@ -387,7 +389,8 @@ def crossentropy_softmax_backward(probs, targets, dloss):
     B, T = targets.shape
     bi, ti = np.meshgrid(np.arange(B), np.arange(T), indexing="ij")
     d[bi, ti, targets] -= 1.0
-    return d * dloss[..., None]
+    d *= dloss[..., None]
+    return d
 
 
 # ----------------------------------------------------------------------------

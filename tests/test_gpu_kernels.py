@@ -1,0 +1,301 @@
+"""Per-kernel parity: each CUDA kernel, called through the kernel-level C ABI,
+against the oracle's function for the same layer, on seeded inputs with
+ragged sizes (rows not multiples of the tile, odd channel counts).
+
+Tolerances: fp32 kernels against the float64 oracle at 1e-5 relative (sum
+order only); bf16 kernels at the bf16 rounding scale, 2^-8 relative per
+stored element, with reductions done in fp32.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synthetic import normal_array, zipf_tokens
+
+pytestmark = pytest.mark.gpu
+
+DT = {"fp32": torch.float32, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from gpt_transformer_train_b300 import build
+    build.build()
+    import gpt_transformer_train_b300.ops as ops
+    return ops
+
+
+def dev(a, dt=torch.float32):
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda").to(dt)
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def as_stored(a, dt):
+    """The values a kernel actually sees after the input is stored in dt."""
+    return host(dev(a, dt))
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+# ---------------------------------------------------------------------------
+def test_encoder_forward_fp32_bit_exact(ops):
+    B, T, C, V = 3, 37, 64, 500
+    tok, _ = zipf_tokens(B, T, V, 1)
+    wte, wpe = normal_array((V, C), 2, 0.02), normal_array((T, C), 3, 0.02)
+    out = torch.empty(B * T, C, device="cuda")
+    fl = ops.flags()
+    ops.gpt2_op_encoder_forward(out, dev(tok, torch.int32), dev(wte), dev(wpe), B, T, C, V, fl)
+    ref = O.encoder_forward(wte, wpe, tok).reshape(B * T, C)
+    assert ref.dtype == np.float32
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert fl.sum().item() == 0
+
+
+def test_encoder_forward_bf16_gather_exact(ops):
+    B, T, C, V = 2, 50, 128, 300
+    tok, _ = zipf_tokens(B, T, V, 4)
+    wte = dev(normal_array((V, C), 5, 0.02), torch.bfloat16)
+    wpe = dev(normal_array((T, C), 6, 0.02), torch.bfloat16)
+    out = torch.empty(B * T, C, device="cuda", dtype=torch.bfloat16)
+    ops.gpt2_op_encoder_forward(out, dev(tok, torch.int32), wte, wpe, B, T, C, V, ops.flags())
+    ref32 = O.encoder_forward(wte.float().cpu().numpy(), wpe.float().cpu().numpy(), tok).reshape(B * T, C)
+    ref = torch.from_numpy(ref32).to(torch.bfloat16)          # one rounding of the fp32 sum
+    assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_encoder_forward_flags_bad_tokens(ops):
+    B, T, C, V = 1, 8, 64, 16
+    tok = np.arange(8, dtype=np.int32).reshape(1, 8)
+    tok[0, 3] = 16
+    tok[0, 5] = -2
+    fl = ops.flags()
+    out = torch.empty(8, C, device="cuda")
+    ops.gpt2_op_encoder_forward(out, dev(tok, torch.int32), dev(np.ones((V, C), np.float32)),
+                                dev(np.ones((T, C), np.float32)), B, T, C, V, fl)
+    assert fl[0].item() & 1
+
+
+@pytest.mark.parametrize("B,T,C", [(2, 7, 64), (4, 64, 192), (1, 300, 768)])
+def test_encoder_backward_deterministic_scatter(ops, B, T, C):
+    V = 97
+    tok, _ = zipf_tokens(B, T, V, B * T)
+    dres = normal_array((B, T, C), 8)
+    dwte = torch.zeros(V, C, device="cuda")
+    dwpe = torch.zeros(T + 3, C, device="cuda")
+    ops.gpt2_op_encoder_backward(dwte, dwpe, dev(dres), dev(tok, torch.int32), B, T, C)
+    rw, rp = O.encoder_backward(dres, tok, V, T + 3)
+    # same summation order as the definition (positions in increasing order)
+    assert np.array_equal(dwte.cpu().numpy(), rw)
+    assert np.array_equal(dwpe.cpu().numpy(), rp)
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("rows,C", [(1, 64), (37, 768), (130, 1600), (5, 2048)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_residual_layernorm_forward(ops, dt, rows, C, fused):
+    a, b = normal_array((rows, C), 10, 1.0), normal_array((rows, C), 11, 0.5)
+    w, bias = normal_array((C,), 12, 0.3) + 1, normal_array((C,), 13, 0.1)
+    ta, tb, tw, tbias = dev(a, DT[dt]), dev(b, DT[dt]), dev(w, DT[dt]), dev(bias, DT[dt])
+    y = torch.empty(rows, C, device="cuda", dtype=DT[dt])
+    r = torch.empty_like(y)
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    ops.gpt2_op_residual_layernorm_forward(r if fused else None, y, mean, rstd, ta, tb if fused else None, tw,
+                                           tbias, rows, C)
+    x = host(ta) + host(tb) if fused else host(ta)
+    if fused and dt == "bf16":
+        x = as_stored(x, torch.bfloat16)          # the stored residual is rounded first
+    ry, rm, rr = O.layernorm_forward(x, host(tw), host(tbias))
+    if fused:
+        tol = 0 if dt == "fp32" else 0
+        assert np.max(np.abs(host(r) - as_stored(x, DT[dt]))) <= tol
+    assert np.allclose(host(mean), rm, rtol=1e-5, atol=1e-5)
+    assert np.allclose(host(rstd), rr, rtol=1e-5)
+    if dt == "fp32":
+        assert np.max(np.abs(host(y) - ry)) < 2e-5
+    else:
+        assert np.max(np.abs(host(y) - ry) / (np.abs(ry) + 1e-2)) < 2 ** -7
+
+
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("rows,C", [(3, 64), (129, 768), (64, 1600)])
+def test_layernorm_backward(ops, dt, rows, C):
+    x = normal_array((rows, C), 20, 1.5)
+    w = normal_array((C,), 21, 0.2) + 1
+    dy = normal_array((rows, C), 22)
+    dres0 = normal_array((rows, C), 23)
+    tx, tw, tdy = dev(x, DT[dt]), dev(w, DT[dt]), dev(dy, DT[dt])
+    xs, ws, dys = host(tx), host(tw), host(tdy)
+    _, mean, rstd = O.layernorm_forward(xs, ws, np.zeros(C))
+    dres = dev(dres0)
+    dres_c = torch.empty(rows, C, device="cuda", dtype=DT[dt])
+    dw = torch.zeros(C, device="cuda")
+    db = torch.full((C,), 0.5, device="cuda")
+    ops.gpt2_op_layernorm_backward(dres, dres_c, tdy, tx, dev(mean.astype(np.float32)), dev(rstd.astype(np.float32)),
+                                   tw, dw, db, rows, C, 1)
+    rdx, rdw, rdb = O.layernorm_backward(dys, xs, mean, rstd, ws)
+    assert rel_l2(host(dres), dres0 + rdx) < 1e-5
+    assert rel_l2(host(dw), rdw) < 1e-5
+    assert rel_l2(host(db), rdb + 0.5) < 1e-5
+    assert np.max(np.abs(host(dres_c) - as_stored(host(dres), DT[dt]))) == 0
+
+
+# ---------------------------------------------------------------------------
+def _gemm_ref(A, B, akm, bkm, M, N, K):
+    Am = A.reshape(M, K) if akm else A.reshape(K, M).T
+    Bn = B.reshape(N, K) if bkm else B.reshape(K, N).T
+    return Am @ Bn.T
+
+
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("akm,bkm", [(1, 1), (1, 0), (0, 0), (0, 1)])
+@pytest.mark.parametrize("M,N,K", [(65, 33, 17), (128, 192, 64), (200, 70, 300)])
+def test_matmul_simt_layouts(ops, dt, akm, bkm, M, N, K):
+    A = normal_array((M * K,), 30)
+    B = normal_array((N * K,), 31)
+    tA, tB = dev(A, DT[dt]), dev(B, DT[dt])
+    D = torch.empty(M, N, device="cuda", dtype=DT[dt])
+    ops.gpt2_op_matmul(tA, K if akm else M, akm, tB, K if bkm else N, bkm, M, N, K, D, N, path=ops.PATH_SIMT)
+    ref = _gemm_ref(host(tA), host(tB), akm, bkm, M, N, K)
+    tol = 1e-5 if dt == "fp32" else 2 ** -7
+    assert rel_l2(host(D), ref) < tol
+
+
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_matmul_simt_epilogues(ops, dt):
+    M, N, K = 96, 80, 48
+    A, B, bias = normal_array((M, K), 40), normal_array((N, K), 41), normal_array((N,), 42)
+    tA, tB, tbias = dev(A, DT[dt]), dev(B, DT[dt]), dev(bias, DT[dt])
+    acc = host(tA) @ host(tB).T
+    pre = torch.empty(M, N, device="cuda", dtype=DT[dt])
+    D = torch.empty(M, N, device="cuda", dtype=DT[dt])
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias, aux=pre, ldaux=N, epilogue=ops.EPI_GELU,
+                       path=ops.PATH_SIMT)
+    tol = 1e-5 if dt == "fp32" else 2 ** -7
+    assert rel_l2(host(pre), acc + host(tbias)) < tol
+    assert rel_l2(host(D), O.gelu_forward(acc + host(tbias))) < tol
+    D2 = torch.empty_like(D)
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D2, N, aux=pre, ldaux=N, epilogue=ops.EPI_GELU_BWD,
+                       path=ops.PATH_SIMT)
+    assert rel_l2(host(D2), O.gelu_backward(host(pre), acc)) < tol
+    F = dev(np.ones((M, N), np.float32))
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, F, N, epilogue=ops.EPI_ACC_F32, path=ops.PATH_SIMT)
+    assert rel_l2(host(F), acc + 1) < 1e-5
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("B,T,C,H", [(2, 13, 64, 4), (1, 70, 128, 2), (2, 129, 192, 3)])
+def test_attention_forward_backward(ops, dt, B, T, C, H):
+    qkv = normal_array((B, T, 3 * C), 50)
+    dout = normal_array((B, T, C), 51)
+    tq, tdo = dev(qkv, DT[dt]), dev(dout, DT[dt])
+    qs, dos = host(tq), host(tdo)
+    out = torch.empty(B * T, C, device="cuda", dtype=DT[dt])
+    lse = torch.empty(B * H * T, device="cuda")
+    ops.gpt2_op_attention_forward(out, lse, tq, B, T, C, H)
+    ro, att = O.attention_forward(qs, H)
+    tol = 1e-5 if dt == "fp32" else 2 ** -7
+    assert rel_l2(host(out).reshape(B, T, C), ro) < tol
+    # LSE: log of the softmax normaliser of the scaled scores
+    hd = C // H
+    q = qs[..., :C].reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    k = qs[..., C:2 * C].reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    s = q @ k.transpose(0, 1, 3, 2) / math.sqrt(hd)
+    s[..., np.triu(np.ones((T, T), bool), 1)] = -np.inf
+    mx = s.max(-1)
+    rlse = mx + np.log(np.exp(s - mx[..., None]).sum(-1))
+    assert np.max(np.abs(host(lse).reshape(B, H, T) - rlse)) < (1e-5 if dt == "fp32" else 1e-3)
+    dq = torch.empty(B * T, 3 * C, device="cuda", dtype=DT[dt])
+    ops.gpt2_op_attention_backward(dq, tdo, tq, out, lse, B, T, C, H)
+    # the oracle's backward from the kernel's stored output's inputs
+    rd = O.attention_backward(dos, qs, att, H)
+    tolb = 1e-4 if dt == "fp32" else 2e-2
+    for part in range(3):
+        a = host(dq).reshape(B, T, 3 * C)[..., part * C:(part + 1) * C]
+        r = rd[..., part * C:(part + 1) * C]
+        assert rel_l2(a, r) < tolb, part
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("rows,V,Vp", [(3, 512, 512), (17, 1000, 1024), (4, 50257, 50304)])
+def test_softmax_crossentropy(ops, dt, rows, V, Vp):
+    z = normal_array((rows, Vp), 60, 3.0)
+    z[:, V:] = 1e4 if dt == "fp32" else 100.0  # pads must not count
+    tgt = np.random.default_rng(61).integers(0, V, size=rows).astype(np.int32)
+    tz = dev(z, DT[dt])
+    zs = host(tz)
+    losses = torch.empty(rows, device="cuda")
+    fl = ops.flags()
+    dloss = 1.0 / rows
+    ops.gpt2_op_softmax_crossentropy(tz, losses, dev(tgt, torch.int32), rows, V, Vp, dloss, 1, fl)
+    rl = O.crossentropy_forward(zs[None], tgt[None], V)[0]
+    assert np.max(np.abs(host(losses) - rl)) < 1e-4
+    rd = O.crossentropy_softmax_backward(O.softmax_forward(zs[None], V), tgt[None], np.full((1, rows), dloss))[0]
+    got = host(tz)
+    assert np.all(got[:, V:] == 0)
+    if dt == "fp32":
+        assert np.max(np.abs(got - rd)) < 1e-7
+    else:
+        assert np.max(np.abs(got - rd)) < 2 ** -8 * dloss
+    assert fl.sum().item() == 0
+
+
+def test_softmax_crossentropy_flags_bad_target(ops):
+    z = dev(normal_array((2, 64), 62))
+    fl = ops.flags()
+    ops.gpt2_op_softmax_crossentropy(z, torch.empty(2, device="cuda"), dev(np.array([1, 64], np.int32), torch.int32),
+                                     2, 64, 64, 0.5, 0, fl)
+    assert fl[0].item() & 2
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("t", [1, 2, 7])
+def test_adamw(ops, t):
+    n = 4 * 1001
+    p, g = normal_array((n,), 70), normal_array((n,), 71, 1e-2)
+    m, v = normal_array((n,), 72, 1e-3), np.abs(normal_array((n,), 73, 1e-4))
+    tp, tg, tm, tv = dev(p), dev(g), dev(m), dev(v)
+    pb = torch.empty(n, device="cuda", dtype=torch.bfloat16)
+    ops.gpt2_op_adamw(tp, tg, tm, tv, pb, 6e-4, 0.9, 0.95, 1e-8, 0.1, t)
+    rp, rm, rv = p.astype(np.float64), m.astype(np.float64), v.astype(np.float64)
+    O.adamw_update(rp, g.astype(np.float64), rm, rv, 6e-4, 0.9, 0.95, 1e-8, 0.1, t)
+    assert rel_l2(host(tm), rm) < 1e-6 and rel_l2(host(tv), rv) < 1e-6
+    assert np.max(np.abs(host(tp) - rp)) < 1e-6
+    assert torch.equal(pb, tp.to(torch.bfloat16))
+
+
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_gelu_standalone(ops, dt):
+    x = normal_array((4096 + 8,), 80, 2.0)
+    d = normal_array((4096 + 8,), 81)
+    tx, td = dev(x, DT[dt]), dev(d, DT[dt])
+    out = torch.empty_like(tx)
+    ops.gpt2_op_gelu_forward(out, tx)
+    tol = 1e-6 if dt == "fp32" else 2 ** -8
+    assert np.max(np.abs(host(out) - O.gelu_forward(host(tx))) / (np.abs(O.gelu_forward(host(tx))) + 1e-3)) < tol * 4
+    dinp = torch.empty_like(tx)
+    ops.gpt2_op_gelu_backward(dinp, tx, td)
+    ref = O.gelu_backward(host(tx), host(td))
+    assert np.max(np.abs(host(dinp) - ref) / (np.abs(ref) + 1e-3)) < tol * 4
+
+
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+def test_colsum(ops, dt):
+    rows, cols, ldx = 300, 200, 208
+    X = normal_array((rows, ldx), 90)
+    tX = dev(X, DT[dt])
+    out = dev(np.ones(cols, np.float32))
+    ops.gpt2_op_colsum(out, tX, rows, cols, ldx)
+    assert rel_l2(host(out), host(tX)[:, :cols].sum(0) + 1) < 1e-5

@@ -1,0 +1,187 @@
+"""Whole-step parity: the library's forward, backward and AdamW through the
+model C ABI against the oracle on the same seeded tokens and the same seeded
+initial weights (bit-equal, see test_abi_host).
+
+fp32 mode (tiny config: L=2 C=64 H=4 T=64 B=4 V=512): loss rel err <= 1e-5,
+logits max abs err <= 1e-3, per-tensor grad rel-L2 <= 1e-3, parameters
+after AdamW rel-L2 <= 1e-5 over the whole parameter vector (per tensor, the
+key slice of qkvb has an analytically zero gradient, so its post-update
+value is set by rounding noise on both sides), 5 steps on one fixed batch.
+bf16 mode: loss abs err <= 2e-2, per-tensor grad rel-L2 <= 5e-2, 20-step loss
+curve within 2% of the oracle's.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synthetic import zipf_tokens
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "oracle_124m.npz")
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gpt_transformer_train_b300 import build
+    build.build()
+    import gpt_transformer_train_b300 as mod
+    return mod
+
+
+def rel_l2(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _setup(g, L, C, H, V, Vp, maxT, B, T, prec, seed=1234, dtype=np.float64):
+    cfg = g.make_config(L, C, H, V, Vp, maxT, B, T, prec)
+    m = g.GPT2(cfg, seed)
+    ocfg = O.Config(L, C, H, V, Vp, maxT)
+    ref = O.GPT2(ocfg, seed, dtype)
+    tok, tgt = zipf_tokens(B, T, V, seed)
+    ttok = torch.from_numpy(tok).cuda()
+    ttgt = torch.from_numpy(tgt).cuda()
+    return cfg, m, ref, tok, tgt, ttok, ttgt
+
+
+TINY = dict(L=2, C=64, H=4, V=512, Vp=512, maxT=64, B=4, T=64)
+
+
+def test_fp32_tiny_forward_backward_adamw(g):
+    cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
+    # logits (forward without targets keeps them)
+    m.gpt2_forward(ttok)
+    ref.forward(tok)
+    assert np.max(np.abs(m.gpt2_get_logits() - ref.cache["logits"])) <= 1e-3
+    for step in range(1, 6):
+        m.gpt2_zero_grad()
+        ref.zero_grad()
+        loss = m.gpt2_forward(ttok, ttgt)
+        rloss = ref.forward(tok, tgt)
+        assert abs(loss - rloss) / rloss <= 1e-5, (step, loss, rloss)
+        losses = m.gpt2_get_losses()
+        assert np.max(np.abs(losses - ref.cache["losses"])) < 1e-4
+        m.gpt2_backward()
+        ref.backward()
+        if step == 1:
+            for n in g.TENSORS:
+                e = rel_l2(m.gpt2_get_grads(n), ref.grads[n].reshape(-1))
+                assert e <= 1e-3, (n, e)
+        m.gpt2_adamw_step(1e-3, 0.9, 0.999, 1e-8, 0.0, step)
+        ref.adamw_step(1e-3, 0.9, 0.999, 1e-8, 0.0, step)
+        mine = np.concatenate([m.gpt2_get_params(n) for n in g.TENSORS])
+        theirs = O.flatten(ref.params, ref.cfg)
+        assert rel_l2(mine, theirs) <= 1e-5, step
+
+
+def test_fp32_deterministic(g):
+    outs = []
+    for _ in range(2):
+        cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
+        m.gpt2_zero_grad()
+        m.gpt2_forward(ttok, ttgt)
+        m.gpt2_backward()
+        outs.append(np.concatenate([m.gpt2_get_grads(n) for n in g.TENSORS]))
+        m.close()
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+SMALL_BF16 = dict(L=2, C=128, H=2, V=1000, Vp=1024, maxT=256, B=4, T=256)
+
+
+def test_bf16_small_forward_backward_and_curve(g):
+    cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **SMALL_BF16, prec=1, dtype=np.float32)
+    curve, rcurve = [], []
+    for step in range(1, 21):
+        m.gpt2_zero_grad()
+        ref.zero_grad()
+        loss = m.gpt2_forward(ttok, ttgt)
+        rloss = ref.forward(tok, tgt)
+        m.gpt2_backward()
+        ref.backward()
+        if step == 1:
+            assert abs(loss - rloss) <= 2e-2
+            for n in g.TENSORS:
+                e = rel_l2(m.gpt2_get_grads(n), ref.grads[n].reshape(-1))
+                assert e <= 5e-2, (n, e)
+        m.gpt2_adamw_step(6e-4, 0.9, 0.95, 1e-8, 0.1, step)
+        ref.adamw_step(6e-4, 0.9, 0.95, 1e-8, 0.1, step)
+        curve.append(loss)
+        rcurve.append(rloss)
+    curve, rcurve = np.array(curve), np.array(rcurve)
+    assert np.all(np.abs(curve - rcurve) / rcurve <= 0.02), (curve, rcurve)
+    assert rcurve[-1] < rcurve[0]
+
+
+def test_bf16_step_host_matches_device_calls(g):
+    cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **SMALL_BF16, prec=1)
+    cfg2, m2, _, _, _, _, _ = _setup(g, **SMALL_BF16, prec=1)
+    th = torch.from_numpy(tok).pin_memory()
+    gh = torch.from_numpy(tgt).pin_memory()
+    for step in (1, 2):
+        a = m.gpt2_step_host(th, gh, 6e-4, 0.9, 0.95, 1e-8, 0.1, step)
+        m2.gpt2_zero_grad()
+        b = m2.gpt2_forward(ttok, ttgt)
+        m2.gpt2_backward()
+        m2.gpt2_adamw_step(6e-4, 0.9, 0.95, 1e-8, 0.1, step)
+        assert a == b
+    assert np.array_equal(m.gpt2_get_params("fcw"), m2.gpt2_get_params("fcw"))
+
+
+def test_error_paths_on_device(g):
+    cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
+    with pytest.raises(g.GPT2Error) as e:
+        m.gpt2_backward()
+    assert e.value.code == -3
+    bad = ttok.clone()
+    bad[1, 5] = 512
+    with pytest.raises(g.GPT2Error) as e:
+        m.gpt2_forward(bad, ttgt)
+    assert e.value.code == -4
+    badt = ttgt.clone()
+    badt[0, 0] = -1
+    with pytest.raises(g.GPT2Error) as e:
+        m.gpt2_forward(ttok, badt)
+    assert e.value.code == -4
+    # the handle stays usable after a flagged batch
+    loss = m.gpt2_forward(ttok, ttgt)
+    assert math.isfinite(loss)
+    with pytest.raises(g.GPT2Error) as e:
+        m.gpt2_get_logits()
+    assert e.value.code == -3
+
+
+M124 = dict(L=12, C=768, H=12, V=50257, Vp=50304, maxT=1024, B=16, T=1024)
+
+
+@pytest.mark.skipif(not os.path.exists(GOLDEN), reason="stored oracle values for 124M not generated")
+def test_bf16_124m_against_stored_oracle(g):
+    """GPT-2 124M, B=16, T=1024, bf16 — the benchmarked workload — against
+    the oracle's stored fp32 run on the same seeded batch and weights."""
+    gold = np.load(GOLDEN)
+    cfg = g.make_config(*(M124[k] for k in ("L", "C", "H", "V", "Vp", "maxT", "B", "T")), 1)
+    m = g.GPT2(cfg, 1234)
+    tok, tgt = zipf_tokens(16, 1024, 50257, 1234)
+    ttok, ttgt = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+    rl = gold["losses"]
+    for step in range(1, len(rl) + 1):
+        m.gpt2_zero_grad()
+        loss = m.gpt2_forward(ttok, ttgt)
+        if step == 1:
+            assert abs(loss - rl[0]) <= 2e-2
+            pl = m.gpt2_get_losses().reshape(-1)
+            assert np.mean(np.abs(pl - gold["pos_losses0"])) < 2e-2
+        m.gpt2_backward()
+        if step == 1:
+            for n in g.TENSORS:
+                gm = m.gpt2_get_grads(n)
+                idx = gold["grad_idx_" + n]
+                e = rel_l2(gm[idx], gold["grad_val_" + n])
+                assert e <= 5e-2, (n, e)
+                assert abs(np.linalg.norm(gm.astype(np.float64)) / float(gold["grad_norm_" + n]) - 1) <= 5e-2, n
+        m.gpt2_adamw_step(6e-4, 0.9, 0.95, 1e-8, 0.1, step)
+        assert abs(loss - rl[step - 1]) / rl[step - 1] <= 0.02, (step, loss, rl[step - 1])
