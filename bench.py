@@ -137,20 +137,33 @@ def kernel_traffic(kernel_key):
     return d["dram_bytes_per_launch"]
 
 
+def blas_threads():
+    """Threads numpy's BLAS runs the oracle's matmuls on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return min(64, len(os.sched_getaffinity(0)))  # OpenBLAS default: all cores, at most its build limit
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (bench's reference arm and cpu_baseline leg)
 # ---------------------------------------------------------------------------
 def oracle_sample(w):
     import oracle as O
     from synthetic import normal_array, zipf_tokens
-    from threadpoolctl import threadpool_info
     cfg = O.Config(w["L"], w["C"], w["H"], w["V"], w["Vp"], w["maxT"])
     # synthetic weights of the right shapes (timing does not depend on values)
     params = {n: normal_array(s, 100 + i, 0.02) for i, (n, s) in enumerate(O.param_shapes(cfg))}
     ref = O.GPT2(cfg, params=params, dtype=np.float32)
     tok, tgt = zipf_tokens(1, CPU_SAMPLE_T, w["V"], SEED)
-    info = threadpool_info()
-    cores = max([i.get("num_threads", 1) for i in info] or [1])
+    cores = blas_threads()
     state = {"t": 0}
 
     def step():
@@ -301,6 +314,8 @@ def run_ours(args, w):
                "gpu_launches": launches, "clocks": clk}
     if ws > 1:
         torch.distributed.barrier()
+    if rank == 0:
+        print("gpu leg: " + json.dumps(out), file=sys.stderr, flush=True)
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         del m
         torch.cuda.empty_cache()

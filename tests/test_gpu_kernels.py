@@ -192,6 +192,67 @@ def test_matmul_simt_epilogues(ops, dt):
     assert rel_l2(host(F), acc + 1) < 1e-5
 
 
+# ---- tensor-core (tcgen05/TMA) GEMM --------------------------------------
+# Row strides must be multiples of 8 bf16 (16 bytes) for TMA; M, N, K need
+# not be tile multiples (K=104, M=136, N=136/264 exercise the ragged edges).
+TC_SHAPES = [(128, 256, 64), (256, 512, 192), (200, 136, 104), (384, 128, 320), (1024, 768, 768), (136, 264, 72)]
+
+
+@pytest.mark.parametrize("akm,bkm", [(1, 1), (1, 0), (0, 0), (0, 1)])
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+def test_matmul_tc_layouts(ops, akm, bkm, M, N, K):
+    A = normal_array((M * K,), 130 + M)
+    B = normal_array((N * K,), 131 + N)
+    tA, tB = dev(A, torch.bfloat16), dev(B, torch.bfloat16)
+    D = torch.full((M, N), float("nan"), device="cuda", dtype=torch.bfloat16)
+    fl = ops.flags()
+    ops.gpt2_op_matmul(tA, K if akm else M, akm, tB, K if bkm else N, bkm, M, N, K, D, N, path=ops.PATH_TC,
+                       flags_dev=fl)
+    ref = _gemm_ref(host(tA), host(tB), akm, bkm, M, N, K)
+    assert fl.sum().item() == 0
+    assert rel_l2(host(D), ref) < 2 ** -7
+
+
+@pytest.mark.parametrize("N", [256, 384])
+def test_matmul_tc_epilogues(ops, N):
+    M, K = 256, 320
+    A, B, bias = normal_array((M, K), 140), normal_array((N, K), 141), normal_array((N,), 142)
+    tA, tB, tbias = dev(A, torch.bfloat16), dev(B, torch.bfloat16), dev(bias, torch.bfloat16)
+    acc = host(tA) @ host(tB).T
+    fl = ops.flags()
+    D = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias, path=ops.PATH_TC, flags_dev=fl)
+    assert rel_l2(host(D), acc + host(tbias)) < 2 ** -7
+    pre = torch.empty_like(D)
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias, aux=pre, ldaux=N, epilogue=ops.EPI_GELU,
+                       path=ops.PATH_TC, flags_dev=fl)
+    assert rel_l2(host(pre), acc + host(tbias)) < 2 ** -7
+    assert rel_l2(host(D), O.gelu_forward(acc + host(tbias))) < 2 ** -7
+    D2 = torch.empty_like(D)
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D2, N, aux=pre, ldaux=N, epilogue=ops.EPI_GELU_BWD,
+                       path=ops.PATH_TC, flags_dev=fl)
+    assert rel_l2(host(D2), O.gelu_backward(host(pre), acc)) < 2 ** -7
+    F = dev(np.full((M, N), 0.25, np.float32))
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, F, N, epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC, flags_dev=fl)
+    assert rel_l2(host(F), acc + 0.25) < 2e-5
+    assert fl.sum().item() == 0
+
+
+def test_matmul_tc_weight_gradient_pattern(ops):
+    """dW[N][K] += dY[BT][N]^T . X[BT][K]: both operands MN-major, long K."""
+    BT, N, K = 4096, 384, 256
+    dY, X = normal_array((BT, N), 150), normal_array((BT, K), 151)
+    tdy, tx = dev(dY, torch.bfloat16), dev(X, torch.bfloat16)
+    W0 = normal_array((N, K), 152)
+    dW = dev(W0)
+    fl = ops.flags()
+    ops.gpt2_op_matmul(tdy, N, 0, tx, K, 0, N, K, BT, dW, K, epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC,
+                       flags_dev=fl)
+    ref = W0 + host(tdy).T @ host(tx)
+    assert rel_l2(host(dW), ref) < 2e-5
+    assert fl.sum().item() == 0
+
+
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 @pytest.mark.parametrize("B,T,C,H", [(2, 13, 64, 4), (1, 70, 128, 2), (2, 129, 192, 3)])
@@ -278,17 +339,22 @@ def test_adamw(ops, t):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 def test_gelu_standalone(ops, dt):
+    # fp32: 1 + tanh(u) cancels for negative x, so the bound is absolute
+    # (a few ulp of |x|); bf16: one rounding of the stored output.
     x = normal_array((4096 + 8,), 80, 2.0)
     d = normal_array((4096 + 8,), 81)
     tx, td = dev(x, DT[dt]), dev(d, DT[dt])
     out = torch.empty_like(tx)
     ops.gpt2_op_gelu_forward(out, tx)
-    tol = 1e-6 if dt == "fp32" else 2 ** -8
-    assert np.max(np.abs(host(out) - O.gelu_forward(host(tx))) / (np.abs(O.gelu_forward(host(tx))) + 1e-3)) < tol * 4
+    ref = O.gelu_forward(host(tx))
+    bound = 2e-6 * np.maximum(1, np.abs(host(tx))) if dt == "fp32" else 2 ** -8 * np.abs(ref) + 1e-6
+    assert np.all(np.abs(host(out) - ref) <= bound)
     dinp = torch.empty_like(tx)
     ops.gpt2_op_gelu_backward(dinp, tx, td)
     ref = O.gelu_backward(host(tx), host(td))
-    assert np.max(np.abs(host(dinp) - ref) / (np.abs(ref) + 1e-3)) < tol * 4
+    bound = 4e-6 * np.maximum(1, np.abs(host(tx))) * np.abs(host(td)) + 1e-7 if dt == "fp32" \
+        else 2 ** -8 * np.abs(ref) + 1e-5 * np.abs(host(td))
+    assert np.all(np.abs(host(dinp) - ref) <= bound)
 
 
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
