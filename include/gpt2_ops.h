@@ -48,6 +48,25 @@ size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T);
 int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B, int T,
                              int C, void* scratch, size_t scratch_bytes, void* stream);
 
+/* The same encoder backward without a scratch argument, for callers that
+ * cannot allocate device memory: code running inside a host program that owns
+ * all device memory (a framework's caching allocator or a fixed, pre-planned
+ * budget) and code on latency-critical paths where cudaMalloc's implicit
+ * synchronisation is not acceptable.  (The llm.c pages have no counterpart of
+ * this call.)  Its scratch is a library-owned device array of
+ * GPT2_NOALLOC_MAX_TOKENS 32-bit keys (128 KiB), held on every GPU that loads
+ * the library until the process exits; the call itself allocates nothing.
+ * The first call on a device looks up the array's device address on that
+ * device, so make that first call before capturing any stream on it.  Calls
+ * share the array: calls that overlap on the GPU race, and each call rewrites
+ * every key slot it reads, so no state carries over between calls.
+ * Returns GPT2_ERR_BUFFER_TOO_SMALL when B*T exceeds GPT2_NOALLOC_MAX_TOKENS,
+ * GPT2_ERR_INVALID_ARG for bad pointers or C % 4 != 0, GPT2_ERR_CUDA if the
+ * array's address cannot be obtained or a launch fails. */
+#define GPT2_NOALLOC_MAX_TOKENS 32768
+int gpt2_op_encoder_backward_noalloc(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B,
+                                     int T, int C, void* stream);
+
 /* r = a + b (b may be NULL: r = a, resid_out unused); y = (r - mean)*rstd*w + bias,
  * rstd = 1/sqrt(biased var + 1e-5); rows x C. */
 int gpt2_op_residual_layernorm_forward(int dtype, void* resid_out, void* y, float* mean, float* rstd,
