@@ -198,6 +198,23 @@ struct Step {
     return gemm(a);
   }
 
+  // causal attention: tcgen05 flash kernels in bf16 mode, SIMT kernels in fp32 mode
+  bool attention_on_tc() const {
+    return c.precision == GPT2_PRECISION_BF16 && attention_tc_supported(c.B, c.T, c.C, c.H);
+  }
+  cudaError_t attention_fwd(T* out, float* lse_, const T* qkv_) {
+    if (attention_on_tc())
+      return attention_forward_tc((bf16*)out, lse_, (const bf16*)qkv_, c.B, c.T, c.C, c.H, flags(), m->st);
+    return attention_forward_simt<T>(out, lse_, qkv_, c.B, c.T, c.C, c.H, m->st);
+  }
+  cudaError_t attention_bwd(T* dqkv, const T* dout, const T* qkv_, const T* out, const float* lse_) {
+    float* Dbuf = m->at<float>(m->bl.attD);
+    if (attention_on_tc())
+      return attention_backward_tc((bf16*)dqkv, Dbuf, (const bf16*)dout, (const bf16*)qkv_, (const bf16*)out, lse_,
+                                   c.B, c.T, c.C, c.H, flags(), m->st);
+    return attention_backward_simt<T>(dqkv, Dbuf, dout, qkv_, out, lse_, c.B, c.T, c.C, c.H, m->st);
+  }
+
   int forward(const int32_t* tok, const int32_t* tgt) {
     cudaStream_t st = m->st;
     int B = c.B, T_ = c.T, Ci = c.C, Li = c.L, BTi = m->BT;
@@ -211,7 +228,7 @@ struct Step {
         CK(m, residual_layernorm_forward<T>(resid(2 * l), ln(2 * l), mean(2 * l), rstd(2 * l), resid(2 * l - 1),
                                             proj(), W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C), BTi, Ci, st));
       CK(m, linear_fwd(qkv(l), ln(2 * l), W(GPT2_QKVW, l, 3 * CC), W(GPT2_QKVB, l, 3 * C), BTi, 3 * Ci, Ci));
-      CK(m, attention_forward_simt<T>(atty(l), lse(l), qkv(l), B, T_, Ci, c.H, st));
+      CK(m, attention_fwd(atty(l), lse(l), qkv(l)));
       CK(m, linear_fwd(proj(), atty(l), W(GPT2_ATTPROJW, l, CC), W(GPT2_ATTPROJB, l, C), BTi, Ci, Ci));
       CK(m, residual_layernorm_forward<T>(resid(2 * l + 1), ln(2 * l + 1), mean(2 * l + 1), rstd(2 * l + 1),
                                           resid(2 * l), proj(), W(GPT2_LN2W, l, C), W(GPT2_LN2B, l, C), BTi, Ci, st));
@@ -261,8 +278,7 @@ struct Step {
       CK(m, linear_wgrad(G(GPT2_ATTPROJW, l, CC), dres_c(), atty(l), BTi, Ci, Ci));
       CK(m, colsum<float>(G(GPT2_ATTPROJB, l, C), dres(), BTi, Ci, Ci, part, nch, st));
       // attention
-      CK(m, attention_backward_simt<T>(dbig(), m->at<float>(m->bl.attD), dsmall(), qkv(l), atty(l), lse(l), c.B,
-                                       c.T, Ci, c.H, st));
+      CK(m, attention_bwd(dbig(), dsmall(), qkv(l), atty(l), lse(l)));
       // qkv
       CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
       CK(m, linear_wgrad(G(GPT2_QKVW, l, 3 * CC), dbig(), ln(2 * l), BTi, 3 * Ci, Ci));

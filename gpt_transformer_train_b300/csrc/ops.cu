@@ -90,9 +90,14 @@ int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const 
   return rc_of(gemm_simt<float>(a, ST(stream)));
 }
 
-int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H,
-                              void* stream) {
+int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H, int path,
+                              int* flags_dev, void* stream) {
   if (bad_dtype(dtype) || !out || !lse || !qkv || B <= 0 || T <= 0 || C <= 0 || H <= 0 || C % H) return GPT2_ERR_INVALID_ARG;
+  if (path < 0 || path > 2) return GPT2_ERR_INVALID_ARG;
+  const bool tc = dtype == GPT2_PRECISION_BF16 && flags_dev && attention_tc_supported(B, T, C, H);
+  if (path == 2 && !tc) return GPT2_ERR_INVALID_ARG;
+  if (tc && path != 1)
+    return rc_of(attention_forward_tc((bf16*)out, lse, (const bf16*)qkv, B, T, C, H, flags_dev, ST(stream)));
   if (dtype == GPT2_PRECISION_BF16)
     return rc_of(attention_forward_simt<bf16>((bf16*)out, lse, (const bf16*)qkv, B, T, C, H, ST(stream)));
   return rc_of(attention_forward_simt<float>((float*)out, lse, (const float*)qkv, B, T, C, H, ST(stream)));
@@ -104,12 +109,18 @@ size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
 }
 
 int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* out,
-                               const float* lse, int B, int T, int C, int H, void* scratch, size_t scratch_bytes,
-                               void* stream) {
+                               const float* lse, int B, int T, int C, int H, int path, int* flags_dev, void* scratch,
+                               size_t scratch_bytes, void* stream) {
   if (bad_dtype(dtype) || !dqkv || !dout || !qkv || !out || !lse || !scratch || B <= 0 || T <= 0 || C <= 0 || H <= 0 ||
       C % H)
     return GPT2_ERR_INVALID_ARG;
+  if (path < 0 || path > 2) return GPT2_ERR_INVALID_ARG;
   if (scratch_bytes < gpt2_op_attention_backward_scratch_bytes(B, T, H)) return GPT2_ERR_INVALID_ARG;
+  const bool tc = dtype == GPT2_PRECISION_BF16 && flags_dev && attention_tc_supported(B, T, C, H);
+  if (path == 2 && !tc) return GPT2_ERR_INVALID_ARG;
+  if (tc && path != 1)
+    return rc_of(attention_backward_tc((bf16*)dqkv, (float*)scratch, (const bf16*)dout, (const bf16*)qkv,
+                                       (const bf16*)out, lse, B, T, C, H, flags_dev, ST(stream)));
   if (dtype == GPT2_PRECISION_BF16)
     return rc_of(attention_backward_simt<bf16>((bf16*)dqkv, (float*)scratch, (const bf16*)dout, (const bf16*)qkv,
                                                (const bf16*)out, lse, B, T, C, H, ST(stream)));

@@ -22,9 +22,9 @@ _sigs = {
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
     "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P]),
-    "gpt2_op_attention_forward": (_i, [_i, _P, _P, _P, _i, _i, _i, _i, _P]),
+    "gpt2_op_attention_forward": (_i, [_i, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P]),
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
-    "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _P, _sz, _P]),
+    "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P, _sz, _P]),
     "gpt2_op_softmax_crossentropy": (_i, [_i, _P, _P, _P, _i, _i, _i, _f, _i, _P, _P]),
     "gpt2_op_adamw": (_i, [_P, _P, _P, _P, _P, _ll, _f, _f, _f, _f, _f, _i, _P]),
     "gpt2_op_gelu_forward": (_i, [_i, _P, _P, _ll, _P]),
@@ -106,16 +106,18 @@ def gpt2_op_matmul(A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias=Non
                            _p(aux), ldaux, epilogue, path, _p(flags_dev), _s(stream)), "matmul")
 
 
-def gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, stream=None):
-    _ck(lib.gpt2_op_attention_forward(_dt(qkv), _p(out), _p(lse), _p(qkv), B, T, C, H, _s(stream)),
-        "attention_forward")
+def gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, path=PATH_AUTO, flags_dev=None, stream=None):
+    _ck(lib.gpt2_op_attention_forward(_dt(qkv), _p(out), _p(lse), _p(qkv), B, T, C, H, path, _p(flags_dev),
+                                      _s(stream)), "attention_forward")
 
 
-def gpt2_op_attention_backward(dqkv, dout, qkv, out, lse, B, T, C, H, stream=None):
+def gpt2_op_attention_backward(dqkv, dout, qkv, out, lse, B, T, C, H, path=PATH_AUTO, flags_dev=None, scratch=None,
+                               stream=None):
     n = lib.gpt2_op_attention_backward_scratch_bytes(B, T, H)
-    sc = _scratch(n, qkv.device)
-    _ck(lib.gpt2_op_attention_backward(_dt(qkv), _p(dqkv), _p(dout), _p(qkv), _p(out), _p(lse), B, T, C, H,
-                                       _p(sc), sc.numel(), _s(stream)), "attention_backward")
+    sc = _scratch(n, qkv.device) if scratch is None else scratch
+    _ck(lib.gpt2_op_attention_backward(_dt(qkv), _p(dqkv), _p(dout), _p(qkv), _p(out), _p(lse), B, T, C, H, path,
+                                       _p(flags_dev), _p(sc), sc.numel() * sc.element_size(), _s(stream)),
+        "attention_backward")
 
 
 def gpt2_op_softmax_crossentropy(logits, losses, targets, rows, V, Vp, dloss, write_grad, flags_dev, stream=None):

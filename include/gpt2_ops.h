@@ -92,14 +92,23 @@ int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const 
 
 /* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
  * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of
- * the scaled scores q.k/sqrt(hd) over t2 <= t. */
+ * the scaled scores q.k/sqrt(hd) over t2 <= t (the attention layer and its
+ * causal loop in "llm.c: GPT-2 training in plain C, with every gradient written
+ * by hand", §2 How the code works).
+ * path: 0 = best available, 1 = SIMT kernels, 2 = tensor-core (tcgen05) kernels
+ * only.  The tensor-core kernels need dtype bf16, hd = 64, T % 128 == 0, 16-byte
+ * aligned pointers and flags_dev (a bounded wait that runs out ORs 4 into it);
+ * path 2 outside that returns GPT2_ERR_INVALID_ARG. */
 int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H,
-                              void* stream);
-/* dqkv [B*T][3C] from dout [B*T][C] with P recomputed from lse. */
+                              int path, int* flags_dev, void* stream);
+/* dqkv [B*T][3C] from dout [B*T][C] with P recomputed from lse:
+ * D = rowsum(dO*O), dS = P*(dO.V^T - D), dQ = dS K/sqrt(hd), dK = dS^T Q/sqrt(hd),
+ * dV = P^T dO.  scratch receives D as float [B][H][T]; no atomics, so the result
+ * is deterministic.  path and flags_dev as for the forward. */
 size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H);
 int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* out,
-                               const float* lse, int B, int T, int C, int H, void* scratch, size_t scratch_bytes,
-                               void* stream);
+                               const float* lse, int B, int T, int C, int H, int path, int* flags_dev,
+                               void* scratch, size_t scratch_bytes, void* stream);
 
 /* Per row of logits [rows][Vp]: losses[r] = logsumexp(z[0:V]) - z[target];
  * write_grad: z[v] = (softmax(z[0:V])[v] - [v == target]) * dloss in place, pads 0. */

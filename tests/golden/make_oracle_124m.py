@@ -65,7 +65,10 @@ def main():
         losses.append(loss)
         print(f"step {step} loss {loss:.6f} ({time.time() - t0:.1f}s)", flush=True)
         out["losses"] = np.array(losses, dtype=np.float64)
-        np.savez_compressed(a.out, **out)
+        # write-then-rename, so a reader never sees a half-written file
+        with open(a.out + ".tmp", "wb") as f:
+            np.savez_compressed(f, **out)
+        os.replace(a.out + ".tmp", a.out)
 
 
 if __name__ == "__main__":

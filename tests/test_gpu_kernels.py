@@ -263,7 +263,7 @@ def test_attention_forward_backward(ops, dt, B, T, C, H):
     qs, dos = host(tq), host(tdo)
     out = torch.empty(B * T, C, device="cuda", dtype=DT[dt])
     lse = torch.empty(B * H * T, device="cuda")
-    ops.gpt2_op_attention_forward(out, lse, tq, B, T, C, H)
+    ops.gpt2_op_attention_forward(out, lse, tq, B, T, C, H, path=ops.PATH_SIMT)
     ro, att = O.attention_forward(qs, H)
     tol = 1e-5 if dt == "fp32" else 2 ** -7
     assert rel_l2(host(out).reshape(B, T, C), ro) < tol
@@ -277,7 +277,7 @@ def test_attention_forward_backward(ops, dt, B, T, C, H):
     rlse = mx + np.log(np.exp(s - mx[..., None]).sum(-1))
     assert np.max(np.abs(host(lse).reshape(B, H, T) - rlse)) < (1e-5 if dt == "fp32" else 1e-3)
     dq = torch.empty(B * T, 3 * C, device="cuda", dtype=DT[dt])
-    ops.gpt2_op_attention_backward(dq, tdo, tq, out, lse, B, T, C, H)
+    ops.gpt2_op_attention_backward(dq, tdo, tq, out, lse, B, T, C, H, path=ops.PATH_SIMT)
     # the oracle's backward from the kernel's stored output's inputs
     rd = O.attention_backward(dos, qs, att, H)
     tolb = 1e-4 if dt == "fp32" else 2e-2
@@ -285,6 +285,94 @@ def test_attention_forward_backward(ops, dt, B, T, C, H):
         a = host(dq).reshape(B, T, 3 * C)[..., part * C:(part + 1) * C]
         r = rd[..., part * C:(part + 1) * C]
         assert rel_l2(a, r) < tolb, part
+
+
+def _attention_tc(ops, qkv, dout, B, T, C, H):
+    """Run the tensor-core attention forward + backward; returns device tensors."""
+    tq, tdo = dev(qkv, torch.bfloat16), dev(dout, torch.bfloat16)
+    out = torch.empty(B * T, C, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(B * H * T, device="cuda")
+    dq = torch.empty(B * T, 3 * C, device="cuda", dtype=torch.bfloat16)
+    D = torch.empty(B * H * T, device="cuda")
+    fl = ops.flags()
+    ops.gpt2_op_attention_forward(out, lse, tq, B, T, C, H, path=ops.PATH_TC, flags_dev=fl)
+    ops.gpt2_op_attention_backward(dq, tdo, tq, out, lse, B, T, C, H, path=ops.PATH_TC, flags_dev=fl, scratch=D)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    return tq, tdo, out, lse, dq, D
+
+
+def _lse_ref(qs, B, T, C, H):
+    hd = C // H
+    q = qs[..., :C].reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    k = qs[..., C:2 * C].reshape(B, T, H, hd).transpose(0, 2, 1, 3)
+    s = q @ k.transpose(0, 1, 3, 2) / math.sqrt(hd)
+    s[..., np.triu(np.ones((T, T), bool), 1)] = -np.inf
+    mx = s.max(-1)
+    return mx + np.log(np.exp(s - mx[..., None]).sum(-1))
+
+
+@pytest.mark.parametrize("B,T,C,H,sigma", [(1, 128, 64, 1, 1.0), (2, 256, 128, 2, 1.0), (1, 384, 192, 3, 2.0),
+                                           (2, 640, 128, 2, 3.0), (1, 1024, 64, 1, 1.0)])
+def test_attention_tc_against_oracle(ops, B, T, C, H, sigma):
+    """tcgen05 flash attention (head size 64): one and two query tiles per
+    CTA (odd tile counts leave a lone tile), several key tiles per row with
+    online rescaling, score scales up to sigma^2 * 8."""
+    qkv = normal_array((B, T, 3 * C), 70, sigma)
+    dout = normal_array((B, T, C), 71)
+    tq, tdo, out, lse, dq, D = _attention_tc(ops, qkv, dout, B, T, C, H)
+    qs, dos = host(tq), host(tdo)
+    ro, att = O.attention_forward(qs, H)
+    assert rel_l2(host(out).reshape(B, T, C), ro) < 2 ** -7
+    assert np.max(np.abs(host(lse).reshape(B, H, T) - _lse_ref(qs, B, T, C, H))) < 2e-3
+    # D = rowsum(dO * O) of the kernel's own (stored) output
+    o = host(out).reshape(B, T, H, C // H)
+    rD = (dos.reshape(B, T, H, C // H) * o).sum(-1).transpose(0, 2, 1)
+    assert np.max(np.abs(host(D).reshape(B, H, T) - rD)) < 1e-3 * max(1.0, np.abs(rD).max())
+    rd = O.attention_backward(dos, qs, att, H)
+    for part in range(3):
+        a = host(dq).reshape(B, T, 3 * C)[..., part * C:(part + 1) * C]
+        assert rel_l2(a, rd[..., part * C:(part + 1) * C]) < 2e-2, part
+
+
+def test_attention_tc_deterministic(ops):
+    """No atomics anywhere: two backward runs give identical bits."""
+    B, T, C, H = 2, 512, 128, 2
+    qkv, dout = normal_array((B, T, 3 * C), 72), normal_array((B, T, C), 73)
+    r1 = _attention_tc(ops, qkv, dout, B, T, C, H)
+    r2 = _attention_tc(ops, qkv, dout, B, T, C, H)
+    assert torch.equal(r1[2], r2[2]) and torch.equal(r1[3], r2[3]) and torch.equal(r1[4], r2[4])
+
+
+def test_attention_tc_full_size_sampled_heads(ops):
+    """GPT-2 124M attention shape (B=16, T=1024, C=768, H=12), as the model
+    step launches it; the oracle checks sampled (batch, head) pairs."""
+    B, T, C, H = 16, 1024, 768, 12
+    hd = C // H
+    qkv = normal_array((B, T, 3 * C), 74)
+    dout = normal_array((B, T, C), 75)
+    tq, tdo, out, lse, dq, D = _attention_tc(ops, qkv, dout, B, T, C, H)
+    qs, dos = host(tq), host(tdo)
+    o_all, dq_all, lse_all = host(out).reshape(B, T, C), host(dq).reshape(B, T, 3 * C), host(lse).reshape(B, H, T)
+    for b, h in [(0, 0), (5, 7), (11, 3), (15, 11)]:
+        cols = [slice(p * C + h * hd, p * C + (h + 1) * hd) for p in range(3)]
+        sq = np.concatenate([qs[b:b + 1, :, c] for c in cols], -1)
+        ro, att = O.attention_forward(sq, 1)
+        assert rel_l2(o_all[b:b + 1, :, h * hd:(h + 1) * hd], ro) < 2 ** -7, (b, h)
+        assert np.max(np.abs(lse_all[b, h] - _lse_ref(sq, 1, T, hd, 1)[0, 0])) < 2e-3
+        rd = O.attention_backward(dos[b:b + 1, :, h * hd:(h + 1) * hd], sq, att, 1)
+        for p in range(3):
+            assert rel_l2(dq_all[b:b + 1, :, cols[p]], rd[..., p * hd:(p + 1) * hd]) < 2e-2, (b, h, p)
+
+
+def test_attention_tc_path_rejects_unsupported(ops):
+    """path=2 (tensor cores only) refuses shapes the kernels do not handle."""
+    B, T, C, H = 1, 100, 128, 2  # T not a multiple of 128
+    tq = torch.zeros(B * T, 3 * C, device="cuda", dtype=torch.bfloat16)
+    out = torch.empty(B * T, C, device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(B * H * T, device="cuda")
+    with pytest.raises(Exception):
+        ops.gpt2_op_attention_forward(out, lse, tq, B, T, C, H, path=ops.PATH_TC, flags_dev=ops.flags())
 
 
 # ---------------------------------------------------------------------------
