@@ -1,27 +1,39 @@
 // Tensor-core GEMM for sm_103a: TMA -> shared-memory ring -> tcgen05.mma into
-// TMEM -> tcgen05.ld epilogue.  Used for every matmul of the bf16 training
-// step: the six forward matmuls (qkv, attention projection, fc + GELU, fc
-// projection, tied classifier) and their input- and weight-gradient matmuls.
+// TMEM -> tcgen05.ld epilogue -> shared-memory staging -> TMA store.  Used for
+// every matmul of the bf16 training step: the six forward matmuls (qkv,
+// attention projection, fc + GELU, fc projection, tied classifier) and their
+// input- and weight-gradient matmuls.
 //
 // D(m, n) = sum_k A(m, k) B(n, k); A and B are bf16, either K-major
 // (row-major [rows][K]) or MN-major ([K][rows]), which covers y = x W^T
 // (both K-major), dx = dy W (B MN-major) and dW = dy^T x (both MN-major)
 // without any transpose pass.  Accumulation is fp32 in TMEM.
 //
-// Structure (one CTA per SM, persistent over output tiles, 192 threads):
+// Structure (one CTA per SM, persistent over work units, 192 threads):
 //   warp 0      TMA producer: per k-block one 128x64 A box (or two 64x64
 //               boxes when MN-major) and the matching B boxes, 128-byte
 //               swizzle, into a STAGES-deep ring guarded by mbarriers.
 //   warp 1      allocates 2*BN TMEM columns (two accumulators) and one
 //               thread issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide
 //               k step; tcgen05.commit frees ring stages and, at the end
-//               of a tile, signals the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time from the TMEM
-//               lane quarter each warp may access, bias / GELU / GELU' /
-//               fp32 accumulate, 128-bit stores.  The two accumulators let
-//               the epilogue of tile i overlap the MMAs of tile i+1.
-// Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
-// CTA raises FLAG_TIMEOUT, stops issuing work, frees its TMEM and returns.
+//               of a unit, signals the epilogue.
+//   warps 2..5  epilogue, one 32-row slab each (the TMEM lane quarter the
+//               warp may access): tcgen05.ld 32 columns at a time, bias /
+//               GELU / GELU' in registers, the slab's 32 x 64 bf16 (or
+//               32 x 32 fp32) piece written to a 128-byte-swizzled staging
+//               buffer and sent out by one TMA store per piece; the fp32
+//               weight-gradient epilogue uses a TMA reduce-add into D, so D
+//               is never read back by the SM.  The GELU' input tile comes in
+//               by TMA as well.  The two accumulators let the epilogue of
+//               one unit overlap the MMAs of the next.
+// Weight gradients have few output tiles and a long K = B*T, so K is split
+// into ranges handled by different CTAs.  The splits of one tile add into D
+// strictly in split order through a per-tile turnstile counter (split s
+// waits until the counter reads s, and its reduce-add has completed before
+// it advances the counter), so the result is deterministic.  Such launches
+// are cooperative (every CTA resident), which makes the waits safe.
+// Every wait is bounded (about 2 s of %globaltimer); on expiry the CTA
+// raises FLAG_TIMEOUT, stops issuing work, frees its TMEM and returns.
 #include "kernels.cuh"
 #include "tc_common.cuh"
 
@@ -29,6 +41,7 @@ namespace {
 
 using namespace tc;
 constexpr int BM = 128, BK = 64;
+constexpr uint32_t STG = 4096;  // one staging buffer: 32 rows x 128 B
 
 __device__ __forceinline__ float gelu_tanh(float x) {
   float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
@@ -45,80 +58,85 @@ struct TcParams {
   int M, N, K;
   int a_mn, b_mn;
   int epi;
-  void* D;
-  long long ldd;
   const bf16* bias;
-  void* aux;
-  long long ldaux;
   int* flags;
+  int splits;  // K split into this many ranges (EPI_ACC_F32 only)
+  int* turn;   // [tiles] turnstile counters for splits > 1 (zero between launches)
 };
 
-// epilogue for 32 consecutive columns [col0, col0+32) of one row
-__device__ __forceinline__ void epilogue32(const TcParams& p, int row, int col0, float (&v)[32]) {
-  if (p.epi == EPI_ACC_F32) {
-    float* d = (float*)p.D + (size_t)row * p.ldd + col0;
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// TMA store / reduce-add of a staged box, and bulk-group bookkeeping (per thread)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   (uint64_t)map),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 32 bf16 values (64 B) into 16-byte chunks ch0..ch0+3 of row r of a staging buffer
+__device__ __forceinline__ void stage_bf16(uint32_t buf, uint32_t r, uint32_t ch0, const float (&v)[32]) {
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-      if (col0 + 4 * j < p.N) {
-        float o[4];
-        ld16(d + 4 * j, o);
-        float r[4] = {o[0] + v[4 * j], o[1] + v[4 * j + 1], o[2] + v[4 * j + 2], o[3] + v[4 * j + 3]};
-        st16(d + 4 * j, r);
-      }
-    }
-    return;
-  }
-  bf16* d = (bf16*)p.D + (size_t)row * p.ldd + col0;
-  if (p.epi == EPI_GELU_BWD) {
-    const bf16* h = (const bf16*)p.aux + (size_t)row * p.ldaux + col0;
+  for (int u = 0; u < 4; u++)
+    st_shared_v4(buf + swz(r, ch0 + u), pack_bf16(v[8 * u], v[8 * u + 1]), pack_bf16(v[8 * u + 2], v[8 * u + 3]),
+                 pack_bf16(v[8 * u + 4], v[8 * u + 5]), pack_bf16(v[8 * u + 6], v[8 * u + 7]));
+}
+// 32 fp32 values (128 B) into row r of a staging buffer
+__device__ __forceinline__ void stage_f32(uint32_t buf, uint32_t r, const float (&v)[32]) {
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      if (col0 + 8 * j < p.N) {
-        float hv[8], o[8];
-        ld16(h + 8 * j, hv);
+  for (int u = 0; u < 8; u++)
+    st_shared_v4(buf + swz(r, u), __float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]),
+                 __float_as_uint(v[4 * u + 2]), __float_as_uint(v[4 * u + 3]));
+}
+// 32 bf16 values from chunks ch0..ch0+3 of row r of a staging buffer
+__device__ __forceinline__ void unstage_bf16(const uint8_t* buf, uint32_t r, uint32_t ch0, float (&v)[32]) {
 #pragma unroll
-        for (int k = 0; k < 8; k++) o[k] = v[8 * j + k] * gelu_tanh_grad(hv[k]);
-        st16(d + 8 * j, o);
-      }
-    }
-    return;
-  }
+  for (int u = 0; u < 4; u++) {
+    float f[8];
+    ld16(reinterpret_cast<const bf16*>(buf + swz(r, ch0 + u)), f);
 #pragma unroll
-  for (int j = 0; j < 4; j++) {
-    if (col0 + 8 * j < p.N) {
-      float o[8];
-      if (p.bias) {
-        float bv[8];
-        ld16(p.bias + col0 + 8 * j, bv);
-#pragma unroll
-        for (int k = 0; k < 8; k++) o[k] = v[8 * j + k] + bv[k];
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; k++) o[k] = v[8 * j + k];
-      }
-      if (p.epi == EPI_GELU) {
-        st16((bf16*)p.aux + (size_t)row * p.ldaux + col0 + 8 * j, o);
-#pragma unroll
-        for (int k = 0; k < 8; k++) o[k] = gelu_tanh(o[k]);
-      }
-      st16(d + 8 * j, o);
-    }
+    for (int k = 0; k < 8; k++) v[8 * u + k] = f[k];
   }
 }
 
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, TcParams p) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                   const __grid_constant__ CUtensorMap td, const __grid_constant__ CUtensorMap tx, TcParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = BN * BK * 2;
   constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint64_t* bars = (uint64_t*)(smem + STAGES * STAGE);
+  uint8_t* stg_gen = smem + STAGES * STAGE;  // 4 warps x 2 staging buffers
+  uint64_t* bars = (uint64_t*)(stg_gen + 8 * STG);
   uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * STAGES + 4);
+  uint32_t auxbar0 = smem_u32(bars + 2 * STAGES + 4);  // [4] GELU' input loads, one per epilogue warp
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * STAGES + 8);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   const uint32_t ring = smem_u32(smem);
 
@@ -132,15 +150,15 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4);
     }
+    for (int w = 0; w < 4; w++) mbar_init(auxbar0 + 8 * w, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), 2 * BN);
-  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 2 * BN);
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&ta) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tb) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&td) : "memory");
   }
   fence_before();
   __syncthreads();
@@ -150,14 +168,17 @@ __global__ void __launch_bounds__(192, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int tiles = ((p.M + BM - 1) / BM) * num_n;
   const int nk = (p.K + BK - 1) / BK;
+  const int units = tiles * p.splits;  // unit u: split u / tiles of tile u % tiles
+  auto kb_begin = [&](int sp) { return (int)((long long)nk * sp / p.splits); };
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer
       uint32_t it = 0;
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int t = u % tiles, sp = u / tiles;
         const int m0 = (t / num_n) * BM, n0 = (t % num_n) * BN;
         bool ok = true;
-        for (int kb = 0; kb < nk; kb++, it++) {
+        for (int kb = kb_begin(sp), kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) { ok = false; break; }
           const uint32_t fb = full0 + 8 * s;
@@ -182,7 +203,6 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issuer
-      // instruction descriptor: D f32, A/B bf16, A/B major, N>>3, M>>4
       const uint32_t idesc = idesc_bf16(BM, BN, p.a_mn, p.b_mn);
       // K-major: advance 32 bytes per 16-wide k step inside the swizzled row,
       // SBO = 1024 (8 rows of 128 B).  MN-major: 16 k-rows of 128 B per step,
@@ -190,13 +210,14 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t a_step = p.a_mn ? 2048u : 32u, b_step = p.b_mn ? 2048u : 32u;
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
       uint32_t it = 0, j = 0;
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x, j++) {
+      for (int u = blockIdx.x; u < units; u += gridDim.x, j++) {
         const uint32_t a = j & 1, aph = (j >> 1) & 1;
         if (!mbar_wait(tempty0 + 8 * a, aph ^ 1, abort_flag)) break;
         fence_after();
         const uint32_t d = tmem + a * BN;
         bool ok = true;
-        for (int kb = 0; kb < nk; kb++, it++) {
+        const int sp = u / tiles, kb0 = kb_begin(sp);
+        for (int kb = kb0, kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
           fence_after();
@@ -205,7 +226,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int kk = 0; kk < BK / 16; kk++) {
             const uint64_t ad = sdesc(a_base + kk * a_step, a_lbo, 1024);
             const uint64_t bd = sdesc(b_base + kk * b_step, b_lbo, 1024);
-            mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+            mma_bf16(d, ad, bd, idesc, (kb != kb0) || kk != 0);
           }
           mma_commit(empty0 + 8 * s);
         }
@@ -215,26 +236,173 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {  // ---- epilogue warps 2..5
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int e = warp - 2;  // this warp's staging buffers and aux barrier
+    const uint32_t stg = smem_u32(stg_gen) + e * 2 * STG;
+    const uint8_t* stg_g = stg_gen + e * 2 * STG;
+    const uint32_t auxbar = auxbar0 + 8 * e;
+    uint32_t aux_phase = 0;
     uint32_t j = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, j++) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x, j++) {
+      const int t = u % tiles, sp = u / tiles;
       const int m0 = (t / num_n) * BM, n0 = (t % num_n) * BN;
+      const int rbase = m0 + q * 32;  // first row of this warp's slab
+      const bool rows_in = rbase < p.M;
       const uint32_t a = j & 1, aph = (j >> 1) & 1;
       // warp-uniform wait: tcgen05.ld below needs the whole warp converged
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * a, aph, abort_flag));
-      if (!ok) break;
+      if (!mbar_wait_warp(tfull0 + 8 * a, aph, abort_flag)) break;
       fence_after();
-      const int row = m0 + q * 32 + lane;
+      const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + a * BN;
+      if (p.epi == EPI_ACC_F32) {
+        if (p.splits > 1) {
+          // turnstile: wait until splits 0..sp-1 of this tile have added their part
+          if (threadIdx.x == 64) {
+            uint64_t t0 = 0;
+            for (uint32_t n = 1; ld_acquire(p.turn + t) != sp; n++) {
+              if ((n & 255) == 0) {
+                if (*abort_flag) break;
+                const uint64_t now = gtimer();
+                if (t0 == 0) t0 = now;
+                else if (now - t0 > WAIT_NS) { *abort_flag = 1; break; }
+              }
+            }
+          }
+          epi_bar();
+          if (*abort_flag) break;
+        }
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; c++) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + a * BN + c * 32, v);
-        const int col0 = n0 + c * 32;
-        if (row < p.M && col0 < p.N) epilogue32(p, row, col0, v);
+        for (int c = 0; c < BN / 32; c++) {
+          float v[32];
+          tmem_ld32(tacc + c * 32, v);
+          const int col0 = n0 + c * 32;
+          if (rows_in && col0 < p.N) {
+            const uint32_t buf = stg + (c & 1) * STG;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            stage_f32(buf, lane, v);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&td, col0, rbase, buf);
+              bulk_commit();
+            }
+          }
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * a);
+        if (p.splits > 1) {
+          // this split's additions must be complete before the next split starts
+          if (lane == 0) {
+            bulk_wait<0>();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          __threadfence();
+          epi_bar();
+          if (threadIdx.x == 64) st_release(p.turn + t, sp + 1 == p.splits ? 0 : sp + 1);
+        }
+        continue;
+      }
+      bool ok = true;
+#pragma unroll 1
+      for (int cp = 0; cp < BN / 64; cp++) {
+        const int col0 = n0 + cp * 64;
+        const bool live = rows_in && col0 < p.N;
+        float v0[32], v1[32];
+        tmem_ld32(tacc + cp * 64, v0);
+        tmem_ld32(tacc + cp * 64 + 32, v1);
+        if (!live) continue;
+        const uint32_t bo = stg + (cp & 1) * STG;  // output piece
+        if (p.epi == EPI_STORE) {
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          if (p.bias) {
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+              float b0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, b1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+              if (col0 + 8 * g < p.N) ld16(p.bias + col0 + 8 * g, b0);
+              if (col0 + 32 + 8 * g < p.N) ld16(p.bias + col0 + 32 + 8 * g, b1);
+#pragma unroll
+              for (int k = 0; k < 8; k++) {
+                v0[8 * g + k] += b0[k];
+                v1[8 * g + k] += b1[k];
+              }
+            }
+          }
+          stage_bf16(bo, lane, 0, v0);
+          stage_bf16(bo, lane, 4, v1);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&td, col0, rbase, bo);
+            bulk_commit();
+          }
+        } else if (p.epi == EPI_GELU) {
+          // both buffers: pre-activation (aux) and GELU output
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          if (p.bias) {
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+              float b0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, b1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+              if (col0 + 8 * g < p.N) ld16(p.bias + col0 + 8 * g, b0);
+              if (col0 + 32 + 8 * g < p.N) ld16(p.bias + col0 + 32 + 8 * g, b1);
+#pragma unroll
+              for (int k = 0; k < 8; k++) {
+                v0[8 * g + k] += b0[k];
+                v1[8 * g + k] += b1[k];
+              }
+            }
+          }
+          stage_bf16(stg, lane, 0, v0);
+          stage_bf16(stg, lane, 4, v1);
+#pragma unroll
+          for (int k = 0; k < 32; k++) {
+            v0[k] = gelu_tanh(v0[k]);
+            v1[k] = gelu_tanh(v1[k]);
+          }
+          stage_bf16(stg + STG, lane, 0, v0);
+          stage_bf16(stg + STG, lane, 4, v1);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tx, col0, rbase, stg);
+            tma_store_2d(&td, col0, rbase, stg + STG);
+            bulk_commit();
+          }
+        } else {  // EPI_GELU_BWD: D = acc * GELU'(aux), aux tile fetched by TMA
+          if (lane == 0) {
+            bulk_wait_read<0>();
+            mbar_expect_tx(auxbar, STG);
+            tma_load_2d(stg, &tx, col0, rbase, auxbar);
+          }
+          __syncwarp();
+          if (!mbar_wait_warp(auxbar, aux_phase, abort_flag)) { ok = false; break; }
+          aux_phase ^= 1;
+          float hv[32];
+          unstage_bf16(stg_g, lane, 0, hv);
+#pragma unroll
+          for (int k = 0; k < 32; k++) v0[k] *= gelu_tanh_grad(hv[k]);
+          unstage_bf16(stg_g, lane, 4, hv);
+#pragma unroll
+          for (int k = 0; k < 32; k++) v1[k] *= gelu_tanh_grad(hv[k]);
+          stage_bf16(stg + STG, lane, 0, v0);
+          stage_bf16(stg + STG, lane, 4, v1);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&td, col0, rbase, stg + STG);
+            bulk_commit();
+          }
+        }
       }
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * a);
+      if (!ok) break;
     }
+    // the staging buffers must stay valid until every store has read them
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   }
   fence_before();
   __syncthreads();
@@ -249,9 +417,28 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// K splits for an fp32-accumulate launch: the count (1..16, at least 8
+// k-blocks each) whose units fill the SMs best, the smallest among near ties
+int choose_splits(int tiles, int nk, int sms) {
+  int best = 1;
+  double best_eff = 0;
+  for (int s = 1; s <= 16 && nk / s >= 8; s++) {
+    const long long units = (long long)tiles * s;
+    const double eff = (double)units / (double)(((units + sms - 1) / sms) * sms);
+    if (eff > best_eff + 0.02) best = s, best_eff = eff;
+  }
+  return best;
+}
+
+template <int BN, int STAGES>
+constexpr size_t smem_bytes() {
+  return (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 8 * STG + 1024 + 256;
+}
+
 template <int BN, int STAGES>
 cudaError_t launch(const GemmArgs& g, int* flags, cudaStream_t st) {
-  constexpr size_t smem = (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
+  constexpr size_t smem = smem_bytes<BN, STAGES>();
+  static_assert(smem <= 232448, "shared memory per CTA");
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -259,17 +446,39 @@ cudaError_t launch(const GemmArgs& g, int* flags, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, td, tx;
   bool ok = g.a_kmajor ? tc_make_map(&ta, g.A, g.K, g.M, g.lda, 64, BM) : tc_make_map(&ta, g.A, g.M, g.K, g.lda, 64, 64);
   ok = ok && (g.b_kmajor ? tc_make_map(&tb, g.B, g.K, g.N, g.ldb, 64, BN) : tc_make_map(&tb, g.B, g.N, g.K, g.ldb, 64, 64));
+  if (g.epi == EPI_ACC_F32) ok = ok && tc_make_map_f32(&td, g.D, g.N, g.M, g.ldd, 32, 32);
+  else ok = ok && tc_make_map(&td, g.D, g.N, g.M, g.ldd, 64, 32);
+  if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) ok = ok && tc_make_map(&tx, g.aux, g.N, g.M, g.ldaux, 64, 32);
+  else tx = td;
   if (!ok) return cudaErrorInvalidValue;
-  TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, g.D, g.ldd, (const bf16*)g.bias,
-             g.aux, g.ldaux, flags};
   const int sms = tc_num_sms();
-  long long tiles = ((g.M + BM - 1) / BM) * (long long)((g.N + BN - 1) / BN);
-  unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-  gemm_tc_kernel<BN, STAGES><<<grid, 192, smem, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  const long long tiles = ((g.M + BM - 1) / BM) * (long long)((g.N + BN - 1) / BN);
+  const int nk = (g.K + BK - 1) / BK;
+  int splits = 1;
+  if (g.epi == EPI_ACC_F32 && g.turn && tiles <= g.turn_len) splits = choose_splits((int)tiles, nk, sms);
+  TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
+             g.turn};
+  const long long units = tiles * splits;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
+  if (splits == 1) {
+    gemm_tc_kernel<BN, STAGES><<<grid, 192, smem, st>>>(ta, tb, td, tx, p);
+    return cudaGetLastError();
+  }
+  // split K: every CTA must be resident for the turnstile waits
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES>, ta, tb, td, tx, p);
 }
 
 }  // namespace
@@ -292,17 +501,27 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool tc_available() { return encode_fn() != nullptr; }
 
-bool tc_make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
-                 uint32_t box_outer) {
+static bool make_map_dt(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
+  cuuint64_t strides[1] = {ld * esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+bool tc_make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                 uint32_t box_outer) {
+  return make_map_dt(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, inner, outer, ld, box_inner, box_outer);
+}
+
+bool tc_make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_inner, uint32_t box_outer) {
+  return make_map_dt(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer, ld, box_inner, box_outer);
 }
 
 int tc_num_sms() {
@@ -322,7 +541,9 @@ bool gemm_tc_supported(const GemmArgs& g) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return false;
   if (g.N % 8 || g.lda % 8 || g.ldb % 8 || !al16(g.A) || !al16(g.B) || !al16(g.D)) return false;
   if (g.epi == EPI_ACC_F32 ? (g.ldd % 4) : (g.ldd % 8)) return false;
-  if ((g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) && (!g.aux || g.ldaux % 8 || !al16(g.aux))) return false;
+  if (g.ldd < g.N) return false;
+  if ((g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) && (!g.aux || g.ldaux % 8 || g.ldaux < g.N || !al16(g.aux)))
+    return false;
   if (g.bias && !al16(g.bias)) return false;
   if (g.a_kmajor ? g.lda < g.K : g.lda < g.M) return false;
   if (g.b_kmajor ? g.ldb < g.K : g.ldb < g.N) return false;

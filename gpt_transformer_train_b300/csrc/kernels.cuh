@@ -24,7 +24,12 @@ struct GemmArgs {
   const void* bias;          // [N] of type T or nullptr
   void* aux; long long ldaux;
   int epi;
+  // optional [turn_len] zeroed ints: lets the tensor-core path split K of an
+  // EPI_ACC_F32 product across CTAs (fixed-order, deterministic accumulation);
+  // left zero again when the launch completes
+  int* turn; int turn_len;
 };
+#define GPT2_GEMM_TURN_LEN 4096
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
 // tcgen05/TMA tensor-core path (bf16 operands); returns cudaErrorNotSupported
 // when the shape or layout is outside what the kernel handles.
@@ -44,20 +49,19 @@ template <typename T>
 cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* rstd, const T* a,
                                        const T* b, const T* w, const T* bias, int rows, int C,
                                        cudaStream_t st);
-// dres = (accumulate ? dres : 0) + LN backward(dy); dres_c (optional) = T copy
+// dres = (accumulate ? dres : 0) + LN backward(dy); dres_c (optional) = T copy.
+// With dw, db (and optionally dres_sum): dw += sum_rows dy*xhat, db += sum_rows dy,
+// dres_sum += sum_rows of the new dres, through deterministic per-chunk partials
+// (partial: ln_backward_partial_floats(rows, C) floats of scratch).
 template <typename T>
 cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
-                               const float* rstd, const T* w, int rows, int C, int accumulate,
-                               cudaStream_t st);
-// dw += sum_rows dy*xhat, db += sum_rows dy ; partial: [nchunks][2][C] floats
+                               const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
+                               float* db, float* dres_sum, float* partial, cudaStream_t st);
+size_t ln_backward_partial_floats(int rows, int C);
+// out[c] += sum_rows X[r*ldx + c]; partial: colsum_partial_floats(rows, cols) floats
 template <typename T>
-cudaError_t ln_param_grad(float* dw, float* db, const T* dy, const T* x, const float* mean,
-                          const float* rstd, int rows, int C, float* partial, int nchunks,
-                          cudaStream_t st);
-// out[c] += sum_rows X[r*ldx + c] ; partial: [nchunks][cols] floats
-template <typename T>
-cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial,
-                   int nchunks, cudaStream_t st);
+cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st);
+size_t colsum_partial_floats(int rows, int cols);
 int reduce_chunks(int rows);  // number of row chunks the reductions use
 
 template <typename T>

@@ -113,29 +113,40 @@ __global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restri
   for (int i = threadIdx.x; i < n; i += blockDim.x) keys_out[i] = sk[i];
 }
 
-// block i: if sorted key i starts a token run, sum that run's rows in order
-__global__ void wte_grad_runs_kernel(float* __restrict__ dwte, const float* __restrict__ dres,
-                                     const uint32_t* __restrict__ keys, int BT, int C) {
-  int i = blockIdx.x;
-  uint32_t tk = keys[i] >> 16;
+// Block (i, column chunk of 128): if sorted key i starts a token run, sum that
+// run's rows.  Warp w takes the run's rows w, w+8, ... in order (float4 per
+// lane), then the eight warp sums are added in warp order: a fixed summation
+// order independent of timing, so the result is deterministic.
+__global__ void __launch_bounds__(256) wte_grad_runs_kernel(float* __restrict__ dwte, const float* __restrict__ dres,
+                                                            const uint32_t* __restrict__ keys, int BT, int C) {
+  __shared__ float4 sh[8][32];
+  const int i = blockIdx.x;
+  const uint32_t tk = keys[i] >> 16;
   if (i > 0 && (keys[i - 1] >> 16) == tk) return;
-  int end = i + 1;
-  while (end < BT && (keys[end] >> 16) == tk) end++;
-  for (int cv = threadIdx.x; cv < C / 4; cv += blockDim.x) {
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = i; j < end; j++) {
-      int pos = (int)(keys[j] & 0xFFFFu);
-      float x[4];
-      ld16(dres + (size_t)pos * C + cv * 4, x);
-#pragma unroll
-      for (int q = 0; q < 4; q++) s[q] += x[q];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int cv = blockIdx.y * 32 + lane;  // float4 column
+  const bool on = cv < C / 4;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = i + w; j < BT; j += 8) {
+    const uint32_t kj = keys[j];
+    if ((kj >> 16) != tk) break;
+    if (on) {
+      const float4 x = __ldcs(reinterpret_cast<const float4*>(dres + (size_t)(kj & 0xFFFFu) * C) + cv);
+      s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
     }
-    float* dst = dwte + (size_t)tk * C + cv * 4;
-    float o[4];
-    ld16(dst, o);
+  }
+  sh[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && on) {
+    float4 t = sh[0][lane];
 #pragma unroll
-    for (int q = 0; q < 4; q++) o[q] += s[q];
-    st16(dst, o);
+    for (int q = 1; q < 8; q++) {
+      t.x += sh[q][lane].x; t.y += sh[q][lane].y; t.z += sh[q][lane].z; t.w += sh[q][lane].w;
+    }
+    float4* dst = reinterpret_cast<float4*>(dwte + (size_t)tk * C) + cv;
+    float4 o = *dst;
+    o.x += t.x; o.y += t.y; o.z += t.z; o.w += t.w;
+    *dst = o;
   }
 }
 
@@ -153,7 +164,7 @@ cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const 
     attr_set = true;
   }
   bitonic_sort_keys_kernel<<<1, 1024, smem, st>>>(keys, tok, BT, n);
-  wte_grad_runs_kernel<<<BT, 192, 0, st>>>(dwte, dres, keys, BT, C);
+  wte_grad_runs_kernel<<<dim3((unsigned)BT, (unsigned)cdiv(C / 4, 32)), 256, 0, st>>>(dwte, dres, keys, BT, C);
   return launch_status(3);
 }
 
@@ -244,151 +255,255 @@ cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* r
 }
 
 // ============================================================================
-// LayerNorm backward (input gradient), one warp per row:
+// Deterministic column reductions.  Producers write per-chunk partial sums
+// (a chunk = a fixed block of rows, summed in a fixed order); reduce_partials
+// then adds the chunks into the outputs in a fixed order.  No atomics, so
+// every gradient below is bitwise repeatable.
+// ============================================================================
+constexpr int RED_ROWS = 64;  // rows per chunk
+int reduce_chunks(int rows) {
+  int c = (int)cdiv(rows, RED_ROWS);
+  return c < 1 ? 1 : c;
+}
+size_t ln_backward_partial_floats(int rows, int C) { return (size_t)reduce_chunks(rows) * 3 * C; }
+size_t colsum_partial_floats(int rows, int cols) { return (size_t)reduce_chunks(rows) * cols; }
+
+// out_o[c] += sum_k partial[k][o][c] for o < nout (out_o may be null: skipped).
+// Block (column group of 32, output o); warp w sums chunks w, w+8, ... in
+// order, then the eight warp sums are added in warp order.
+__global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict__ out0, float* __restrict__ out1,
+                                                              float* __restrict__ out2,
+                                                              const float* __restrict__ partial, int nchunks,
+                                                              int C, int nout) {
+  __shared__ float sh[8][32];
+  const int o = blockIdx.y;
+  float* out = o == 0 ? out0 : (o == 1 ? out1 : out2);
+  if (!out) return;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (c < C)
+    for (int k = w; k < nchunks; k += 8) s += partial[((size_t)k * nout + o) * C + c];
+  sh[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && c < C) {
+    float t = sh[0][lane];
+#pragma unroll
+    for (int i = 1; i < 8; i++) t += sh[i][lane];
+    out[c] += t;
+  }
+}
+
+static cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
+                                   int nout, cudaStream_t st) {
+  dim3 grid((unsigned)cdiv(C, 32), nout);
+  reduce_partials_kernel<<<grid, 256, 0, st>>>(out0, out1, out2, partial, nchunks, C, nout);
+  return launch_status(1);
+}
+
+// Partial sums of the eight warps' per-lane column accumulators, added in warp
+// order through shared memory; acc[i][k] is column (lane + 32 i) * N + k.
+template <int NV, int N>
+__device__ __forceinline__ void block_column_sum(float (&acc)[NV][N], float* sh, int nvec, float* dst) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int turn = 0; turn < 8; turn++) {
+    if (w == turn) {
+#pragma unroll
+      for (int i = 0; i < NV; i++) {
+        const int vi = lane + i * 32;
+        if (vi < nvec)
+#pragma unroll
+          for (int k = 0; k < N; k++) sh[vi * N + k] = turn == 0 ? acc[i][k] : sh[vi * N + k] + acc[i][k];
+      }
+    }
+    __syncthreads();
+  }
+  for (int c = threadIdx.x; c < nvec * N; c += blockDim.x) dst[c] = sh[c];
+  __syncthreads();
+}
+
+// ============================================================================
+// LayerNorm backward, one warp per row (RPW rows per warp, 8 warps a block):
 //   dnorm = dy * w; dx = rstd * (dnorm - mean(dnorm) - xhat * mean(dnorm * xhat))
 //   dres = (accumulate ? dres : 0) + dx   (fp32; optional copy in T)
+// With partial: each warp accumulates, in its own shared-memory slice, the
+// column sums over its rows of dy * xhat, dy and (if want_rsum) the new dres;
+// the block adds the eight slices in warp order into partial[block][3][C] for
+// dw, db and the bias gradient of the projection whose output gradient dres is.
 // ============================================================================
+constexpr int LNB_RPW = 8;
 template <typename T, int NV>
-__global__ void layernorm_backward_kernel(float* __restrict__ dres, T* __restrict__ dres_c,
-                                          const T* __restrict__ dy, const T* __restrict__ x,
-                                          const float* __restrict__ mean, const float* __restrict__ rstd,
-                                          const T* __restrict__ w, int rows, int C, int accumulate) {
+__global__ void __launch_bounds__(256, NV <= 4 ? 3 : 1) layernorm_backward_kernel(
+    float* __restrict__ dres, T* __restrict__ dres_c, const T* __restrict__ dy, const T* __restrict__ x,
+    const float* __restrict__ mean, const float* __restrict__ rstd, const T* __restrict__ w, int rows, int C,
+    int accumulate, float* __restrict__ partial, int want_rsum) {
   constexpr int N = VecN<T>::n;
-  int lane = threadIdx.x & 31;
-  int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= rows) return;
+  extern __shared__ float lnb_sh[];  // [8 warps][3][C] when partial
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = C / N;
-  float mu = mean[row], rs = rstd[row];
-  float dn[NV][N], xh[NV][N];
-  float s1 = 0.f, s2 = 0.f;
+  float* acc = lnb_sh + (size_t)warp * 3 * C;
+  if (partial)
+    for (int c = lane; c < 3 * C; c += 32) acc[c] = 0.f;
+  const int r0 = (blockIdx.x * 8 + warp) * LNB_RPW;
+  for (int rr = 0; rr < LNB_RPW; rr++) {
+    const int row = r0 + rr;
+    if (row >= rows) break;
+    const float mu = mean[row], rs = rstd[row];
+    float dn[NV][N], xh[NV][N];
+    float s1 = 0.f, s2 = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV; i++) {
-    int vi = lane + i * 32;
-    if (vi < nvec) {
-      float d[N], xv[N], wv[N];
-      ld16(dy + (size_t)row * C + vi * N, d);
-      ld16(x + (size_t)row * C + vi * N, xv);
-      ld16(w + vi * N, wv);
+    for (int i = 0; i < NV; i++) {
+      const int vi = lane + i * 32;
+      if (vi < nvec) {
+        float xv[N], dv[N], wv[N];
+        ld16_cs(dy + (size_t)row * C + vi * N, dv);
+        ld16_cs(x + (size_t)row * C + vi * N, xv);
+        ld16(w + vi * N, wv);
 #pragma unroll
-      for (int k = 0; k < N; k++) {
-        xh[i][k] = (xv[k] - mu) * rs;
-        dn[i][k] = d[k] * wv[k];
-        s1 += dn[i][k];
-        s2 += dn[i][k] * xh[i][k];
+        for (int k = 0; k < N; k++) {
+          xh[i][k] = (xv[k] - mu) * rs;
+          dn[i][k] = dv[k] * wv[k];
+          s1 += dn[i][k];
+          s2 += dn[i][k] * xh[i][k];
+        }
+        if (partial) {
+          float* aw = acc + vi * N;
+          float* ab = acc + C + vi * N;
+#pragma unroll
+          for (int k = 0; k < N; k++) {
+            aw[k] += dv[k] * xh[i][k];
+            ab[k] += dv[k];
+          }
+        }
+      }
+    }
+    s1 = warp_sum(s1) / (float)C;
+    s2 = warp_sum(s2) / (float)C;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+      const int vi = lane + i * 32;
+      if (vi < nvec) {
+        float o[N];
+#pragma unroll
+        for (int k = 0; k < N; k++) o[k] = (dn[i][k] - s1 - xh[i][k] * s2) * rs;
+        float* dst = dres + (size_t)row * C + vi * N;
+#pragma unroll
+        for (int k = 0; k < N; k += 4) {
+          float a4[4] = {0.f, 0.f, 0.f, 0.f};
+          if (accumulate) ld16_cs(dst + k, a4);
+          float r4[4] = {a4[0] + o[k], a4[1] + o[k + 1], a4[2] + o[k + 2], a4[3] + o[k + 3]};
+          st16(dst + k, r4);
+          o[k] = r4[0]; o[k + 1] = r4[1]; o[k + 2] = r4[2]; o[k + 3] = r4[3];
+        }
+        if (dres_c) st16(dres_c + (size_t)row * C + vi * N, o);
+        if (partial && want_rsum) {
+          float* ar = acc + 2 * C + vi * N;
+#pragma unroll
+          for (int k = 0; k < N; k++) ar[k] += o[k];
+        }
       }
     }
   }
-  s1 = warp_sum(s1) / (float)C;
-  s2 = warp_sum(s2) / (float)C;
+  if (!partial) return;  // uniform over the block
+  __syncthreads();
+  float* dst = partial + (size_t)blockIdx.x * 3 * C;
+  const int nc = want_rsum ? 3 * C : 2 * C;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    float t = lnb_sh[c];
 #pragma unroll
-  for (int i = 0; i < NV; i++) {
-    int vi = lane + i * 32;
-    if (vi < nvec) {
-      float o[N];
-#pragma unroll
-      for (int k = 0; k < N; k++) o[k] = (dn[i][k] - s1 - xh[i][k] * s2) * rs;
-      float* dst = dres + (size_t)row * C + vi * N;
-#pragma unroll
-      for (int k = 0; k < N; k += 4) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (accumulate) ld16(dst + k, acc);
-        float r4[4] = {acc[0] + o[k], acc[1] + o[k + 1], acc[2] + o[k + 2], acc[3] + o[k + 3]};
-        st16(dst + k, r4);
-        o[k] = r4[0]; o[k + 1] = r4[1]; o[k + 2] = r4[2]; o[k + 3] = r4[3];
-      }
-      if (dres_c) st16(dres_c + (size_t)row * C + vi * N, o);
-    }
+    for (int q = 1; q < 8; q++) t += lnb_sh[(size_t)q * 3 * C + c];
+    dst[c] = t;
   }
 }
 
 template <typename T>
 cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
-                               const float* rstd, const T* w, int rows, int C, int accumulate,
-                               cudaStream_t st) {
+                               const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
+                               float* db, float* dres_sum, float* partial, cudaStream_t st) {
   constexpr int N = VecN<T>::n;
-  int nvec = C / N;
-  unsigned grid = (unsigned)cdiv(rows, 8);
-  if (nvec <= 32 * 2)
-    layernorm_backward_kernel<T, 2><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
-  else if (nvec <= 32 * 4)
-    layernorm_backward_kernel<T, 4><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
-  else if (nvec <= 32 * 8)
-    layernorm_backward_kernel<T, 8><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
-  else if (nvec <= 32 * 16)
-    layernorm_backward_kernel<T, 16><<<grid, 256, 0, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, C, accumulate);
-  else
-    return cudaErrorInvalidValue;
-  return launch_status(1);
-}
-
-// ============================================================================
-// deterministic column reductions: per-chunk partials, then an ordered sum
-// ============================================================================
-int reduce_chunks(int rows) {
-  int c = (int)cdiv(rows, 128);
-  return c < 1 ? 1 : c;
-}
-
-template <typename T>
-__global__ void ln_param_grad_partial_kernel(float* __restrict__ partial, const T* __restrict__ dy,
-                                             const T* __restrict__ x, const float* __restrict__ mean,
-                                             const float* __restrict__ rstd, int rows, int C, int rows_per) {
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  int chunk = blockIdx.y;
-  if (c >= C) return;
-  int r0 = chunk * rows_per, r1 = min(rows, r0 + rows_per);
-  float sw = 0.f, sb = 0.f;
-  for (int r = r0; r < r1; r++) {
-    float d = to_f(dy[(size_t)r * C + c]);
-    float xh = (to_f(x[(size_t)r * C + c]) - mean[r]) * rstd[r];
-    sw += d * xh;
-    sb += d;
+  const int nvec = C / N;
+  const bool sums = dw || db || dres_sum;
+  if (sums && (!dw || !db || !partial)) return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)cdiv(rows, 8 * LNB_RPW);
+  const size_t smem = sums ? (size_t)8 * 3 * C * sizeof(float) : 0;
+  static bool attr[2] = {false, false};
+  if (sums && !attr[sizeof(T) == 2]) {
+    const int mx = 8 * 3 * 2048 * (int)sizeof(float);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(layernorm_backward_kernel<T, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    attr[sizeof(T) == 2] = true;
   }
-  partial[((size_t)chunk * 2 + 0) * C + c] = sw;
-  partial[((size_t)chunk * 2 + 1) * C + c] = sb;
+  float* part = sums ? partial : nullptr;
+  const int rsum = dres_sum != nullptr;
+#define LNB(NVv) layernorm_backward_kernel<T, NVv><<<grid, 256, smem, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, \
+                                                                            C, accumulate, part, rsum)
+  if (nvec <= 32) LNB(1);
+  else if (nvec <= 64) LNB(2);
+  else if (nvec <= 96) LNB(3);
+  else if (nvec <= 128) LNB(4);
+  else if (nvec <= 192) LNB(6);
+  else if (nvec <= 256) LNB(8);
+  else if (nvec <= 384) LNB(12);
+  else if (nvec <= 512) LNB(16);
+  else return cudaErrorInvalidValue;
+#undef LNB
+  cudaError_t e = launch_status(1);
+  if (e != cudaSuccess || !sums) return e;
+  // rows of 64 per chunk = 8 warps x LNB_RPW rows per block
+  return reduce_partials(dw, db, dres_sum, partial, (int)grid, C, 3, st);
 }
 
-__global__ void sum_chunks_kernel(float* __restrict__ out, const float* __restrict__ partial, int nchunks,
-                                  int cols, long long chunk_stride) {
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
-  float s = 0.f;
-  for (int k = 0; k < nchunks; k++) s += partial[(size_t)k * chunk_stride + c];
-  out[c] += s;
+// ============================================================================
+// column sums: out[c] += sum_r X[r*ldx + c], chunks of RED_ROWS rows
+// ============================================================================
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ X,
+                                                             int rows, int cols, long long ldx) {
+  constexpr int N = VecN<T>::n;
+  extern __shared__ float cs_sh[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v0 = blockIdx.x * 32;  // first vector column of this block
+  const int nvec = cols / N;
+  const int vi = v0 + lane;
+  float acc[1][N];
+#pragma unroll
+  for (int k = 0; k < N; k++) acc[0][k] = 0.f;
+  const int r0 = blockIdx.y * RED_ROWS;
+  if (vi < nvec)
+    for (int r = r0 + warp; r < min(rows, r0 + RED_ROWS); r += 8) {
+      float v[N];
+      ld16(X + (size_t)r * ldx + (size_t)vi * N, v);
+#pragma unroll
+      for (int k = 0; k < N; k++) acc[0][k] += v[k];
+    }
+  // warp-ordered combine of this block's 32 vector columns
+  for (int turn = 0; turn < 8; turn++) {
+    if (warp == turn && vi < nvec)
+#pragma unroll
+      for (int k = 0; k < N; k++) cs_sh[lane * N + k] = turn == 0 ? acc[0][k] : cs_sh[lane * N + k] + acc[0][k];
+    __syncthreads();
+  }
+  float* dst = partial + (size_t)blockIdx.y * cols + (size_t)v0 * N;
+  for (int c = threadIdx.x; c < 32 * N; c += blockDim.x)
+    if (v0 * N + c < cols) dst[c] = cs_sh[c];
 }
 
 template <typename T>
-cudaError_t ln_param_grad(float* dw, float* db, const T* dy, const T* x, const float* mean,
-                          const float* rstd, int rows, int C, float* partial, int nchunks,
-                          cudaStream_t st) {
-  int rows_per = (int)cdiv(rows, nchunks);
-  dim3 grid((unsigned)cdiv(C, 128), nchunks);
-  ln_param_grad_partial_kernel<T><<<grid, 128, 0, st>>>(partial, dy, x, mean, rstd, rows, C, rows_per);
-  sum_chunks_kernel<<<(unsigned)cdiv(C, 256), 256, 0, st>>>(dw, partial, nchunks, C, 2LL * C);
-  sum_chunks_kernel<<<(unsigned)cdiv(C, 256), 256, 0, st>>>(db, partial + C, nchunks, C, 2LL * C);
-  return launch_status(3);
-}
-
-template <typename T>
-__global__ void colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ X, int rows,
-                                      int cols, long long ldx, int rows_per) {
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
-  int chunk = blockIdx.y;
-  if (c >= cols) return;
-  int r0 = chunk * rows_per, r1 = min(rows, r0 + rows_per);
-  float s = 0.f;
-  for (int r = r0; r < r1; r++) s += to_f(X[(size_t)r * ldx + c]);
-  partial[(size_t)chunk * cols + c] = s;
-}
-
-template <typename T>
-cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial,
-                   int nchunks, cudaStream_t st) {
-  int rows_per = (int)cdiv(rows, nchunks);
-  dim3 grid((unsigned)cdiv(cols, 128), nchunks);
-  colsum_partial_kernel<T><<<grid, 128, 0, st>>>(partial, X, rows, cols, ldx, rows_per);
-  sum_chunks_kernel<<<(unsigned)cdiv(cols, 256), 256, 0, st>>>(out, partial, nchunks, cols, cols);
-  return launch_status(2);
+cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  if (cols % N || ldx % N) return cudaErrorInvalidValue;
+  const int nch = reduce_chunks(rows);
+  dim3 grid((unsigned)cdiv(cols / N, 32), nch);
+  colsum_partial_kernel<T><<<grid, 256, 32 * N * sizeof(float), st>>>(partial, X, rows, cols, ldx);
+  cudaError_t e = launch_status(1);
+  if (e != cudaSuccess) return e;
+  return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st);
 }
 
 // ============================================================================
@@ -787,11 +902,134 @@ __global__ void __launch_bounds__(1024) softmax_ce_kernel(T* __restrict__ logits
   }
 }
 
+// Register-resident variant: the row is read from HBM once into registers
+// (VPT 16-byte words per thread), max and sum are block reductions over the
+// registers, and dlogits is written from them: one read and one write of the
+// row.  exp2 of pre-scaled arguments (ex2.approx).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+template <typename T, int VPT>
+__global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ logits, float* __restrict__ losses,
+                                                              const int* __restrict__ targets, int V, int Vp,
+                                                              float dloss, int write_grad, int* flags) {
+  constexpr int N = VecN<T>::n;
+  constexpr float L2E = 1.4426950408889634f;
+  __shared__ float red[32];
+  __shared__ float s_bcast[2];
+  T* z = logits + (size_t)blockIdx.x * Vp;
+  const int nvec = Vp / N;
+  uint4 raw[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * 1024;
+    if (vi < nvec) raw[k] = __ldcs(reinterpret_cast<const uint4*>(z) + vi);
+  }
+  auto unpack = [&](int k, float (&f)[N]) {
+    if constexpr (N == 8) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[k]);
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x; f[2 * i + 1] = t.y;
+      }
+    } else {
+      const float* q = reinterpret_cast<const float*>(&raw[k]);
+#pragma unroll
+      for (int i = 0; i < N; i++) f[i] = q[i];
+    }
+  };
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // row max over the first V columns
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * 1024;
+    if (vi < nvec) {
+      float f[N];
+      unpack(k, f);
+#pragma unroll
+      for (int i = 0; i < N; i++)
+        if (vi * N + i < V) m = fmaxf(m, f[i]);
+    }
+  }
+  m = warp_max(m);
+  if (lane == 0) red[w] = m;
+  __syncthreads();
+  if (w == 0) {
+    float t = red[lane];
+    t = warp_max(t);
+    if (lane == 0) s_bcast[0] = t;
+  }
+  __syncthreads();
+  m = s_bcast[0];
+  const float ml = m * L2E;
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * 1024;
+    if (vi < nvec) {
+      float f[N];
+      unpack(k, f);
+#pragma unroll
+      for (int i = 0; i < N; i++)
+        if (vi * N + i < V) s += fast_exp2(fmaf(f[i], L2E, -ml));
+    }
+  }
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) {
+    int tg = targets[blockIdx.x];
+    if (tg < 0 || tg >= V) {
+      atomicOr(flags, FLAG_TARGET_RANGE);
+      tg = 0;
+    }
+    const float lse = m + logf(s);
+    losses[blockIdx.x] = lse - to_f(z[tg]);
+    s_bcast[1] = (float)tg;
+  }
+  if (!write_grad) return;
+  __syncthreads();
+  const int tg = (int)s_bcast[1];
+  // p = exp(z - m) / s, computed as exp2(z*log2e - (m*log2e + log2 s))
+  const float off = ml + __log2f(s);
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * 1024;
+    if (vi < nvec) {
+      float f[N];
+      unpack(k, f);
+#pragma unroll
+      for (int i = 0; i < N; i++) {
+        const int idx = vi * N + i;
+        f[i] = idx < V ? (fast_exp2(fmaf(f[i], L2E, -off)) - (idx == tg ? 1.f : 0.f)) * dloss : 0.f;
+      }
+      st16_cs(z + (size_t)vi * N, f);
+    }
+  }
+}
+
 template <typename T>
 cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,
                        float dloss, int write_grad, int* flags, cudaStream_t st) {
-  if (Vp % VecN<T>::n) return cudaErrorInvalidValue;
-  softmax_ce_kernel<T><<<rows, 1024, 0, st>>>(logits, losses, targets, V, Vp, dloss, write_grad, flags);
+  constexpr int N = VecN<T>::n;
+  if (Vp % N) return cudaErrorInvalidValue;
+  const int vpt = (int)cdiv(Vp / N, 1024);
+#define SCE(K) softmax_ce_reg_kernel<T, K><<<rows, 1024, 0, st>>>(logits, losses, targets, V, Vp, dloss, write_grad, flags)
+  switch (vpt) {
+    case 1: SCE(1); break;
+    case 2: SCE(2); break;
+    case 3: SCE(3); break;
+    case 4: SCE(4); break;
+    case 5: SCE(5); break;
+    case 6: SCE(6); break;
+    case 7: SCE(7); break;
+    case 8: SCE(8); break;
+    default:
+      softmax_ce_kernel<T><<<rows, 1024, 0, st>>>(logits, losses, targets, V, Vp, dloss, write_grad, flags);
+  }
+#undef SCE
   return launch_status(1);
 }
 
@@ -919,10 +1157,9 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   template cudaError_t residual_layernorm_forward<T>(T*, T*, float*, float*, const T*, const T*, const T*, \
                                                      const T*, int, int, cudaStream_t);                  \
   template cudaError_t layernorm_backward<T>(float*, T*, const T*, const T*, const float*, const float*,  \
-                                             const T*, int, int, int, cudaStream_t);                     \
-  template cudaError_t ln_param_grad<T>(float*, float*, const T*, const T*, const float*, const float*,   \
-                                        int, int, float*, int, cudaStream_t);                            \
-  template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, int, cudaStream_t);       \
+                                             const T*, int, int, int, float*, float*, float*, float*,     \
+                                             cudaStream_t);                                               \
+  template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t);            \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \
   template cudaError_t attention_forward_simt<T>(T*, float*, const T*, int, int, int, int, cudaStream_t); \
   template cudaError_t attention_backward_simt<T>(T*, float*, const T*, const T*, const T*, const float*, \

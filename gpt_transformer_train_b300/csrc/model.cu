@@ -121,9 +121,10 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.dbig = take(BT * 4 * C * es);
   b.dsmall = take(BT * C * es);
   b.attD = take(BT * c.H * 4);
-  size_t nch = (size_t)reduce_chunks((int)BT);
-  b.partial = take(nch * 4 * C * 4);
+  b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), colsum_partial_floats((int)BT, 4 * (int)C)) *
+                   sizeof(float));
   b.keys = take(encoder_backward_scratch_bytes((int)BT));
+  b.turn = take(GPT2_GEMM_TURN_LEN * sizeof(int));
   b.flags = take(256);
   b.tok = take(BT * 4);
   b.tgt = take(BT * 4);
@@ -194,7 +195,8 @@ struct Step {
   }
   // dW[N][K] += dY[M][N]^T . X[M][K]
   cudaError_t linear_wgrad(float* dW, const T* dY, const T* X, int M, int N, int K) {
-    GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32};
+    GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32,
+               m->at<int>(m->bl.turn), GPT2_GEMM_TURN_LEN};
     return gemm(a);
   }
 
@@ -250,44 +252,40 @@ struct Step {
     cudaStream_t st = m->st;
     int Ci = c.C, Li = c.L, BTi = m->BT;
     size_t CC = C * C;
-    int nch = reduce_chunks(BTi);
     float* part = m->at<float>(m->bl.partial);
     size_t f = 2 * L;
     // classifier (tied wte): dlnf = dlogits . wte ; dwte += dlogits^T . lnf
     CK(m, linear_dgrad(dsmall(), logits(), W(GPT2_WTE), BTi, c.Vp, Ci));
     CK(m, linear_wgrad(G(GPT2_WTE), logits(), ln(f), BTi, c.Vp, Ci));
+    // final LayerNorm; the column sums of the resulting dres are the bias
+    // gradient of the last fc projection (its output gradient is dres)
     CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
-                                Ci, 0, st));
-    CK(m, ln_param_grad<T>(G(GPT2_LNFW), G(GPT2_LNFB), dsmall(), resid(f), mean(f), rstd(f), BTi, Ci, part, nch, st));
+                                Ci, 0, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part, st));
     for (int l = Li - 1; l >= 0; l--) {
       // fc projection (+ GELU backward fused into its input-gradient GEMM)
       CK(m, linear_dgrad(dbig(), dres_c(), W(GPT2_FCPROJW, l, 4 * CC), BTi, Ci, 4 * Ci, fch(l)));
       CK(m, linear_wgrad(G(GPT2_FCPROJW, l, 4 * CC), dres_c(), fchg(l), BTi, Ci, 4 * Ci));
-      CK(m, colsum<float>(G(GPT2_FCPROJB, l, C), dres(), BTi, Ci, Ci, part, nch, st));
       // fc
       CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_FCW, l, 4 * CC), BTi, 4 * Ci, Ci));
       CK(m, linear_wgrad(G(GPT2_FCW, l, 4 * CC), dbig(), ln(2 * l + 1), BTi, 4 * Ci, Ci));
-      CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dbig(), BTi, 4 * Ci, 4 * Ci, part, nch, st));
-      // LN2 (+ residual gradient)
+      CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dbig(), BTi, 4 * Ci, 4 * Ci, part, st));
+      // LN2 (+ residual gradient; its column sums give the attention-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
-                                  rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, st));
-      CK(m, ln_param_grad<T>(G(GPT2_LN2W, l, C), G(GPT2_LN2B, l, C), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
-                             rstd(2 * l + 1), BTi, Ci, part, nch, st));
+                                  rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, G(GPT2_LN2W, l, C),
+                                  G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C), part, st));
       // attention projection
       CK(m, linear_dgrad(dsmall(), dres_c(), W(GPT2_ATTPROJW, l, CC), BTi, Ci, Ci));
       CK(m, linear_wgrad(G(GPT2_ATTPROJW, l, CC), dres_c(), atty(l), BTi, Ci, Ci));
-      CK(m, colsum<float>(G(GPT2_ATTPROJB, l, C), dres(), BTi, Ci, Ci, part, nch, st));
       // attention
       CK(m, attention_bwd(dbig(), dsmall(), qkv(l), atty(l), lse(l)));
       // qkv
       CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
       CK(m, linear_wgrad(G(GPT2_QKVW, l, 3 * CC), dbig(), ln(2 * l), BTi, 3 * Ci, Ci));
-      CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dbig(), BTi, 3 * Ci, 3 * Ci, part, nch, st));
-      // LN1 (+ residual gradient)
+      CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dbig(), BTi, 3 * Ci, 3 * Ci, part, st));
+      // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(2 * l), mean(2 * l), rstd(2 * l),
-                                  W(GPT2_LN1W, l, C), BTi, Ci, 1, st));
-      CK(m, ln_param_grad<T>(G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C), dsmall(), resid(2 * l), mean(2 * l),
-                             rstd(2 * l), BTi, Ci, part, nch, st));
+                                  W(GPT2_LN1W, l, C), BTi, Ci, 1, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
+                                  l > 0 ? G(GPT2_FCPROJB, l - 1, C) : nullptr, part, st));
     }
     CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
     return GPT2_OK;

@@ -49,39 +49,32 @@ int gpt2_op_residual_layernorm_forward(int dtype, void* resid_out, void* y, floa
 
 size_t gpt2_op_layernorm_backward_scratch_bytes(int rows, int C) {
   if (rows <= 0 || C <= 0) return 0;
-  return (size_t)reduce_chunks(rows) * 2 * C * sizeof(float);
+  return ln_backward_partial_floats(rows, C) * sizeof(float);
 }
 
 int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void* dy, const void* x, const float* mean,
-                               const float* rstd, const void* w, float* dw, float* db, int rows, int C, int accumulate,
-                               void* scratch, size_t scratch_bytes, void* stream) {
+                               const float* rstd, const void* w, float* dw, float* db, float* dres_sum, int rows,
+                               int C, int accumulate, void* scratch, size_t scratch_bytes, void* stream) {
   if (bad_dtype(dtype) || !dres || !dy || !x || !mean || !rstd || !w || rows <= 0 || C <= 0) return GPT2_ERR_INVALID_ARG;
   if (C % (dtype ? 8 : 4) || C > 2048) return GPT2_ERR_INVALID_ARG;
-  bool grads = dw && db;
-  if (grads && (!scratch || scratch_bytes < gpt2_op_layernorm_backward_scratch_bytes(rows, C))) return GPT2_ERR_INVALID_ARG;
-  int nch = reduce_chunks(rows);
-  cudaError_t e;
-  if (dtype == GPT2_PRECISION_BF16) {
-    e = layernorm_backward<bf16>(dres, (bf16*)dres_c, (const bf16*)dy, (const bf16*)x, mean, rstd, (const bf16*)w, rows, C,
-                                 accumulate, ST(stream));
-    if (e == cudaSuccess && grads)
-      e = ln_param_grad<bf16>(dw, db, (const bf16*)dy, (const bf16*)x, mean, rstd, rows, C, (float*)scratch, nch, ST(stream));
-  } else {
-    e = layernorm_backward<float>(dres, (float*)dres_c, (const float*)dy, (const float*)x, mean, rstd, (const float*)w,
-                                  rows, C, accumulate, ST(stream));
-    if (e == cudaSuccess && grads)
-      e = ln_param_grad<float>(dw, db, (const float*)dy, (const float*)x, mean, rstd, rows, C, (float*)scratch, nch,
-                               ST(stream));
-  }
-  return rc_of(e);
+  const bool sums = dw || db || dres_sum;
+  if (sums && (!dw || !db || !scratch || scratch_bytes < gpt2_op_layernorm_backward_scratch_bytes(rows, C)))
+    return GPT2_ERR_INVALID_ARG;
+  float* part = sums ? (float*)scratch : nullptr;
+  if (dtype == GPT2_PRECISION_BF16)
+    return rc_of(layernorm_backward<bf16>(dres, (bf16*)dres_c, (const bf16*)dy, (const bf16*)x, mean, rstd,
+                                          (const bf16*)w, rows, C, accumulate, dw, db, dres_sum, part, ST(stream)));
+  return rc_of(layernorm_backward<float>(dres, (float*)dres_c, (const float*)dy, (const float*)x, mean, rstd,
+                                         (const float*)w, rows, C, accumulate, dw, db, dres_sum, part, ST(stream)));
 }
 
 int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const void* B, long long ldb, int b_kmajor,
                    int M, int N, int K, void* D, long long ldd, const void* bias, void* aux, long long ldaux,
-                   int epilogue, int path, int* flags_dev, void* stream) {
+                   int epilogue, int path, int* flags_dev, int* counters_dev, void* stream) {
   if (bad_dtype(dtype) || !A || !B || !D || M <= 0 || N <= 0 || K <= 0 || epilogue < 0 || epilogue > 3) return GPT2_ERR_INVALID_ARG;
   if ((epilogue == EPI_GELU || epilogue == EPI_GELU_BWD) && !aux) return GPT2_ERR_INVALID_ARG;
-  GemmArgs a{A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias, aux, ldaux, epilogue};
+  GemmArgs a{A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias, aux, ldaux, epilogue,
+             counters_dev, counters_dev ? GPT2_GEMM_COUNTERS : 0};
   if (path == 2 || (path == 0 && dtype == GPT2_PRECISION_BF16 && gemm_tc_supported(a))) {
     if (dtype != GPT2_PRECISION_BF16 || !flags_dev || !gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
     return rc_of(gemm_tc(a, flags_dev, ST(stream)));
@@ -165,17 +158,17 @@ int gpt2_op_gelu_backward(int dtype, void* dinp, const void* inp, const void* do
 
 size_t gpt2_op_colsum_scratch_bytes(int rows, int cols) {
   if (rows <= 0 || cols <= 0) return 0;
-  return (size_t)reduce_chunks(rows) * cols * sizeof(float);
+  return colsum_partial_floats(rows, cols) * sizeof(float);
 }
 
 int gpt2_op_colsum(int dtype, float* out, const void* X, int rows, int cols, long long ldx, void* scratch,
                    size_t scratch_bytes, void* stream) {
   if (bad_dtype(dtype) || !out || !X || !scratch || rows <= 0 || cols <= 0 || ldx < cols) return GPT2_ERR_INVALID_ARG;
   if (scratch_bytes < gpt2_op_colsum_scratch_bytes(rows, cols)) return GPT2_ERR_INVALID_ARG;
-  int nch = reduce_chunks(rows);
+  if (cols % (dtype ? 8 : 4) || ldx % (dtype ? 8 : 4) || !aligned16(X)) return GPT2_ERR_INVALID_ARG;
   if (dtype == GPT2_PRECISION_BF16)
-    return rc_of(colsum<bf16>(out, (const bf16*)X, rows, cols, ldx, (float*)scratch, nch, ST(stream)));
-  return rc_of(colsum<float>(out, (const float*)X, rows, cols, ldx, (float*)scratch, nch, ST(stream)));
+    return rc_of(colsum<bf16>(out, (const bf16*)X, rows, cols, ldx, (float*)scratch, ST(stream)));
+  return rc_of(colsum<float>(out, (const float*)X, rows, cols, ldx, (float*)scratch, ST(stream)));
 }
 
 }  // extern "C"

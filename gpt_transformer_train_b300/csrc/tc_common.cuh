@@ -161,5 +161,8 @@ __device__ __forceinline__ float ex2(float x) {
 // swizzle.  False when the driver entry point is missing or rejects the map.
 bool tc_make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
                  uint32_t box_outer);
+// the same over fp32 elements
+bool tc_make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                     uint32_t box_inner, uint32_t box_outer);
 bool tc_available();
 int tc_num_sms();

@@ -20,8 +20,8 @@ _sigs = {
     "gpt2_op_encoder_backward_noalloc": (_i, [_P, _P, _P, _P, _i, _i, _i, _P]),
     "gpt2_op_residual_layernorm_forward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _P]),
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
-    "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
-    "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P]),
+    "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
+    "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P, _P]),
     "gpt2_op_attention_forward": (_i, [_i, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P]),
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P, _sz, _P]),
@@ -92,18 +92,27 @@ def gpt2_op_residual_layernorm_forward(resid_out, y, mean, rstd, a, b, w, bias, 
                                                _p(w), _p(bias), rows, C, _s(stream)), "residual_layernorm_forward")
 
 
-def gpt2_op_layernorm_backward(dres, dres_c, dy, x, mean, rstd, w, dw, db, rows, C, accumulate, stream=None):
+def gpt2_op_layernorm_backward(dres, dres_c, dy, x, mean, rstd, w, dw, db, rows, C, accumulate, stream=None,
+                               dres_sum=None):
     n = lib.gpt2_op_layernorm_backward_scratch_bytes(rows, C)
     sc = _scratch(n, dy.device)
     _ck(lib.gpt2_op_layernorm_backward(_dt(dy), _p(dres), _p(dres_c), _p(dy), _p(x), _p(mean), _p(rstd), _p(w),
-                                       _p(dw), _p(db), rows, C, accumulate, _p(sc), sc.numel(), _s(stream)),
-        "layernorm_backward")
+                                       _p(dw), _p(db), _p(dres_sum), rows, C, accumulate, _p(sc), sc.numel(),
+                                       _s(stream)), "layernorm_backward")
+
+
+GEMM_COUNTERS = 4096
+
+
+def gemm_counters(device="cuda"):
+    """Zeroed turnstile counters that let the fp32-accumulate GEMM split K."""
+    return torch.zeros(GEMM_COUNTERS, dtype=torch.int32, device=device)
 
 
 def gpt2_op_matmul(A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias=None, aux=None, ldaux=0,
-                   epilogue=EPI_STORE, path=PATH_AUTO, flags_dev=None, stream=None):
+                   epilogue=EPI_STORE, path=PATH_AUTO, flags_dev=None, counters_dev=None, stream=None):
     _ck(lib.gpt2_op_matmul(_dt(A), _p(A), lda, a_kmajor, _p(B), ldb, b_kmajor, M, N, K, _p(D), ldd, _p(bias),
-                           _p(aux), ldaux, epilogue, path, _p(flags_dev), _s(stream)), "matmul")
+                           _p(aux), ldaux, epilogue, path, _p(flags_dev), _p(counters_dev), _s(stream)), "matmul")
 
 
 def gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, path=PATH_AUTO, flags_dev=None, stream=None):

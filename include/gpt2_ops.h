@@ -74,21 +74,32 @@ int gpt2_op_residual_layernorm_forward(int dtype, void* resid_out, void* y, floa
                                        int C, void* stream);
 
 /* dres = (accumulate ? dres : 0) + dx with dx = rstd*(dnorm - mean(dnorm) - xhat*mean(dnorm*xhat)),
- * dnorm = dy*w; dres_c (optional) receives dres in dtype; dw += sum dy*xhat, db += sum dy (if non-NULL). */
+ * dnorm = dy*w; dres_c (optional) receives dres in dtype.  If dw and db are given:
+ * dw += sum dy*xhat, db += sum dy, and (if dres_sum is given) dres_sum += the column
+ * sums of the new dres, which is the bias gradient of the projection whose output
+ * gradient dres is.  The sums go through per-chunk partials in scratch and are added
+ * in a fixed order (deterministic). */
 size_t gpt2_op_layernorm_backward_scratch_bytes(int rows, int C);
 int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void* dy, const void* x,
                                const float* mean, const float* rstd, const void* w, float* dw, float* db,
-                               int rows, int C, int accumulate, void* scratch, size_t scratch_bytes, void* stream);
+                               float* dres_sum, int rows, int C, int accumulate, void* scratch,
+                               size_t scratch_bytes, void* stream);
 
 /* D(m,n) = sum_k A(m,k) B(n,k) then an epilogue:
  *   A(m,k) = a_kmajor ? A[m*lda+k] : A[k*lda+m];  B(n,k) = b_kmajor ? B[n*ldb+k] : B[k*ldb+n]
  *   epilogue 0: D = acc (+bias[n])          1: aux = acc + bias[n], D = GELU_tanh(aux)
  *            2: D = acc * GELU_tanh'(aux)   3: D (float) += acc
  * path: 0 = best available, 1 = SIMT kernel, 2 = tensor-core (tcgen05) kernel only
- * (GPT2_ERR_INVALID_ARG if the shape/layout is outside what it handles). */
+ * (GPT2_ERR_INVALID_ARG if the shape/layout is outside what it handles).
+ * counters_dev (optional, tensor-core path, epilogue 3): GPT2_GEMM_COUNTERS ints that
+ * are zero before the call and are zero again when it completes.  With them the
+ * kernel may split K across CTAs; the splits of an output tile then add into D one
+ * after another in a fixed order, so the result is still deterministic.  Calls that
+ * share one counter array must not overlap on the GPU. */
+#define GPT2_GEMM_COUNTERS 4096
 int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const void* B, long long ldb,
                    int b_kmajor, int M, int N, int K, void* D, long long ldd, const void* bias, void* aux,
-                   long long ldaux, int epilogue, int path, int* flags_dev, void* stream);
+                   long long ldaux, int epilogue, int path, int* flags_dev, int* counters_dev, void* stream);
 
 /* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
  * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of
@@ -124,7 +135,8 @@ int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* p_bf16, lo
 int gpt2_op_gelu_forward(int dtype, void* out, const void* in, long long n, void* stream);
 int gpt2_op_gelu_backward(int dtype, void* dinp, const void* inp, const void* dout, long long n, void* stream);
 
-/* out[c] += sum_r X[r*ldx + c] (deterministic order). */
+/* out[c] += sum_r X[r*ldx + c] (deterministic order); cols and ldx multiples of
+ * 4 floats / 8 bf16, X 16-byte aligned. */
 size_t gpt2_op_colsum_scratch_bytes(int rows, int cols);
 int gpt2_op_colsum(int dtype, float* out, const void* X, int rows, int cols, long long ldx, void* scratch,
                    size_t scratch_bytes, void* stream);

@@ -83,18 +83,30 @@ def test_encoder_forward_flags_bad_tokens(ops):
     assert fl[0].item() & 1
 
 
-@pytest.mark.parametrize("B,T,C", [(2, 7, 64), (4, 64, 192), (1, 300, 768)])
+@pytest.mark.parametrize("B,T,C", [(2, 7, 64), (4, 64, 192), (1, 300, 768), (16, 1024, 768)])
 def test_encoder_backward_deterministic_scatter(ops, B, T, C):
-    V = 97
+    """Scatter-add without atomics: repeated calls give identical bits; values
+    match the float64 sums within fp32 rounding; dwpe (a plain sum over the
+    batch in increasing b) matches the oracle's float32 sum exactly."""
+    V = 97 if B * T < 4096 else 50257
     tok, _ = zipf_tokens(B, T, V, B * T)
     dres = normal_array((B, T, C), 8)
-    dwte = torch.zeros(V, C, device="cuda")
-    dwpe = torch.zeros(T + 3, C, device="cuda")
-    ops.gpt2_op_encoder_backward(dwte, dwpe, dev(dres), dev(tok, torch.int32), B, T, C)
-    rw, rp = O.encoder_backward(dres, tok, V, T + 3)
-    # same summation order as the definition (positions in increasing order)
-    assert np.array_equal(dwte.cpu().numpy(), rw)
-    assert np.array_equal(dwpe.cpu().numpy(), rp)
+    td, tt = dev(dres), dev(tok, torch.int32)
+    outs = []
+    for _ in range(2):
+        dwte = torch.zeros(V, C, device="cuda")
+        dwpe = torch.zeros(T + 3, C, device="cuda")
+        ops.gpt2_op_encoder_backward(dwte, dwpe, td, tt, B, T, C)
+        outs.append((dwte, dwpe))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    rw, rp = O.encoder_backward(dres.astype(np.float64), tok, V, T + 3)
+    dwte, dwpe = host(outs[0][0]), host(outs[0][1])
+    # the row sum of n fp32 values is within n * 2^-24 * sum|x| of the exact sum
+    bound = np.zeros((V, C))
+    np.add.at(bound, tok.reshape(-1), np.abs(dres.reshape(-1, C).astype(np.float64)))
+    cnt = np.bincount(tok.reshape(-1), minlength=V)[:, None]
+    assert np.all(np.abs(dwte - rw) <= cnt * 2.0 ** -24 * bound + 1e-30)
+    assert np.array_equal(host(outs[0][1]).astype(np.float32), O.encoder_backward(dres, tok, V, T + 3)[1])
 
 
 # ---------------------------------------------------------------------------
@@ -127,7 +139,7 @@ def test_residual_layernorm_forward(ops, dt, rows, C, fused):
 
 
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
-@pytest.mark.parametrize("rows,C", [(3, 64), (129, 768), (64, 1600)])
+@pytest.mark.parametrize("rows,C", [(3, 64), (129, 768), (64, 1600), (1000, 1024)])
 def test_layernorm_backward(ops, dt, rows, C):
     x = normal_array((rows, C), 20, 1.5)
     w = normal_array((C,), 21, 0.2) + 1
@@ -140,13 +152,21 @@ def test_layernorm_backward(ops, dt, rows, C):
     dres_c = torch.empty(rows, C, device="cuda", dtype=DT[dt])
     dw = torch.zeros(C, device="cuda")
     db = torch.full((C,), 0.5, device="cuda")
-    ops.gpt2_op_layernorm_backward(dres, dres_c, tdy, tx, dev(mean.astype(np.float32)), dev(rstd.astype(np.float32)),
-                                   tw, dw, db, rows, C, 1)
+    rsum = torch.full((C,), -0.25, device="cuda")
+    tmean, trstd = dev(mean.astype(np.float32)), dev(rstd.astype(np.float32))
+    ops.gpt2_op_layernorm_backward(dres, dres_c, tdy, tx, tmean, trstd, tw, dw, db, rows, C, 1, dres_sum=rsum)
     rdx, rdw, rdb = O.layernorm_backward(dys, xs, mean, rstd, ws)
     assert rel_l2(host(dres), dres0 + rdx) < 1e-5
     assert rel_l2(host(dw), rdw) < 1e-5
     assert rel_l2(host(db), rdb + 0.5) < 1e-5
+    # column sums of the new residual gradient (the next projection's bias gradient)
+    assert rel_l2(host(rsum), (dres0 + rdx).sum(0) - 0.25) < 1e-5
     assert np.max(np.abs(host(dres_c) - as_stored(host(dres), DT[dt]))) == 0
+    # the same call again from the same state gives identical bits (fixed-order sums)
+    dres2, dw2, db2, rsum2 = dev(dres0), torch.zeros(C, device="cuda"), torch.full((C,), 0.5, device="cuda"), \
+        torch.full((C,), -0.25, device="cuda")
+    ops.gpt2_op_layernorm_backward(dres2, None, tdy, tx, tmean, trstd, tw, dw2, db2, rows, C, 1, dres_sum=rsum2)
+    assert torch.equal(dres, dres2) and torch.equal(dw, dw2) and torch.equal(db, db2) and torch.equal(rsum, rsum2)
 
 
 # ---------------------------------------------------------------------------
@@ -251,6 +271,29 @@ def test_matmul_tc_weight_gradient_pattern(ops):
     ref = W0 + host(tdy).T @ host(tx)
     assert rel_l2(host(dW), ref) < 2e-5
     assert fl.sum().item() == 0
+
+
+@pytest.mark.parametrize("BT,N,K", [(16384, 768, 768), (8192, 2304, 768), (4096 + 192, 136, 264)])
+def test_matmul_tc_split_k_weight_gradient(ops, BT, N, K):
+    """Weight-gradient GEMM with turnstile counters: K = BT is split across
+    CTAs, the splits add in a fixed order (bitwise repeatable), and the
+    counters are zero again afterwards."""
+    dY, X = normal_array((BT, N), 153), normal_array((BT, K), 154)
+    tdy, tx = dev(dY, torch.bfloat16), dev(X, torch.bfloat16)
+    W0 = normal_array((N, K), 155)
+    fl, cnt = ops.flags(), ops.gemm_counters()
+    outs = []
+    for _ in range(2):
+        dW = dev(W0)
+        ops.gpt2_op_matmul(tdy, N, 0, tx, K, 0, N, K, BT, dW, K, epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC,
+                           flags_dev=fl, counters_dev=cnt)
+        outs.append(dW)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    assert int(cnt.abs().sum().item()) == 0
+    assert torch.equal(outs[0], outs[1])
+    ref = W0.astype(np.float64) + host(tdy).T @ host(tx)
+    assert rel_l2(host(outs[0]), ref) < 2e-5
 
 
 # ---------------------------------------------------------------------------
@@ -446,8 +489,8 @@ def test_gelu_standalone(ops, dt):
 
 
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
-def test_colsum(ops, dt):
-    rows, cols, ldx = 300, 200, 208
+@pytest.mark.parametrize("rows,cols,ldx", [(300, 200, 208), (16384, 2304, 2304)])
+def test_colsum(ops, dt, rows, cols, ldx):
     X = normal_array((rows, ldx), 90)
     tX = dev(X, DT[dt])
     out = dev(np.ones(cols, np.float32))
