@@ -22,8 +22,10 @@
 // per instruction), warps 2-5 run the online softmax of query tile 0 and
 // warps 6-9 that of tile 1, one query row per thread.  The two tiles share
 // every K/V tile, and their softmax phases interleave on the tensor core.
-// Each P V product lands in a fresh TMEM accumulator and is folded into
-// registers with the running rescale, so no TMEM read-modify-write is needed.
+// Each softmax warp reads its 128 scores with four TMEM loads and one wait,
+// then releases the S accumulator at once, so the next Q K^T runs while it
+// computes the exponentials; P is double-buffered, and O accumulates in TMEM
+// (rescaled in place only when a row's maximum jumps by more than 2^8).
 //
 // Backward: two kernels, so that no gradient is accumulated with atomics
 // (the result is deterministic).  The dQ kernel walks the key tiles of one
@@ -99,23 +101,48 @@ struct AttnParams {
 // ============================================================================
 // forward
 // ============================================================================
-constexpr int FWD_STAGES = 3;
+// 32 lanes x 32 consecutive fp32 columns into TMEM (the inverse of tmem_ld32)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+// 32 lanes x 128 consecutive fp32 columns, four loads in flight, one wait
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+#pragma unroll
+  for (int c = 0; c < 4; c++) tmem_ld32_async(taddr + 32 * c, *reinterpret_cast<float(*)[32]>(v + 32 * c));
+  tmem_wait_ld();
+}
+
+// Online softmax with a lazily rescaled accumulator: the probabilities of a
+// row are taken against a reference max m_ref; O (in TMEM) and the row sum l
+// are only rescaled when a new block's max exceeds m_ref by more than
+// RESCALE_LOG2 (then P stays <= 2^RESCALE_LOG2, harmless in fp32 and bf16).
+// The result is the same softmax: every term and l share one reference.
+constexpr float RESCALE_LOG2 = 8.f;
+constexpr int FWD_STAGES = 2;
 constexpr uint32_t FWD_KV = 2 * TILE;  // K tile then V tile
-constexpr size_t FWD_SMEM = 1024 + 2 * TILE + FWD_STAGES * FWD_KV + 2 * PTILE + 256;
+constexpr size_t FWD_SMEM = 1024 + 2 * TILE + FWD_STAGES * FWD_KV + 4 * PTILE + 256;
 
 __global__ void __launch_bounds__(320, 1) attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tqkv, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sQ = smem_u32(smem);                  // 2 query tiles
   const uint32_t sKV = sQ + 2 * TILE;                  // ring of K/V tiles
-  const uint32_t sP = sKV + FWD_STAGES * FWD_KV;       // 2 P tiles (128 x 128)
-  uint64_t* bars = (uint64_t*)(smem + 2 * TILE + FWD_STAGES * FWD_KV + 2 * PTILE);
+  const uint32_t sP = sKV + FWD_STAGES * FWD_KV;       // P tiles [query tile][buffer] (128 x 128)
+  uint64_t* bars = (uint64_t*)(smem + 2 * TILE + FWD_STAGES * FWD_KV + 4 * PTILE);
   const uint32_t b_q = smem_u32(bars);
   const uint32_t b_kvfull = b_q + 8, b_kvempty = b_kvfull + 8 * FWD_STAGES;
-  const uint32_t b_sfull = b_kvempty + 8 * FWD_STAGES;  // [2]
-  const uint32_t b_pfull = b_sfull + 16;                // [2]
-  const uint32_t b_ofull = b_pfull + 16;                // [2]
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 + 2 * FWD_STAGES + 6);
+  const uint32_t b_sfull = b_kvempty + 8 * FWD_STAGES;  // [2] S of tile t computed
+  const uint32_t b_sfree = b_sfull + 16;                // [2] S of tile t read by its softmax warps
+  const uint32_t b_pfull = b_sfree + 16;                // [2 tiles][2 buffers] P written
+  const uint32_t b_pempty = b_pfull + 32;               // [2 tiles][2 buffers] P V done with it
+  uint32_t* tmem_holder = (uint32_t*)(bars + 1 + 2 * FWD_STAGES + 12);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,8 +164,11 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_tc_kernel(const __grid_consta
     }
     for (int t = 0; t < 2; t++) {
       mbar_init(b_sfull + 8 * t, 1);
-      mbar_init(b_pfull + 8 * t, 4);
-      mbar_init(b_ofull + 8 * t, 1);
+      mbar_init(b_sfree + 8 * t, 4);
+      for (int u = 0; u < 2; u++) {
+        mbar_init(b_pfull + 16 * t + 8 * u, 4);
+        mbar_init(b_pempty + 16 * t + 8 * u, 1);
+      }
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -168,14 +198,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_tc_kernel(const __grid_consta
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issuer
       constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);  // S = Q K^T
-      constexpr uint32_t ID_O = idesc_bf16(128, HD, 0, 1);   // O = P V (V is MN-major)
+      constexpr uint32_t ID_O = idesc_bf16(128, HD, 0, 1);   // O += P V (V is MN-major)
       auto active = [&](int t, int j) { return t == 0 ? j <= qt0 : (two && j <= qt0 + 1); };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t k = sKV + (j % FWD_STAGES) * FWD_KV, q = sQ + t * TILE;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; kk++) mma_bf16(tmem + 128 * t, desc_k(q, kk), desc_k(k, kk), ID_S, kk > 0);
-        mma_commit(b_sfull + 8 * t);
-      };
       int kv_ready = -1;
       auto wait_kv = [&](int j) {
         if (kv_ready >= j) return true;
@@ -184,6 +208,12 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_tc_kernel(const __grid_consta
         fence_after();
         return true;
       };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t k = sKV + (j % FWD_STAGES) * FWD_KV, q = sQ + t * TILE;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; kk++) mma_bf16(tmem + 128 * t, desc_k(q, kk), desc_k(k, kk), ID_S, kk > 0);
+        mma_commit(b_sfull + 8 * t);
+      };
       bool ok = mbar_wait(b_q, 0, abort_flag) && wait_kv(0);
       if (ok) {
         fence_after();
@@ -191,20 +221,24 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_tc_kernel(const __grid_consta
         if (active(1, 0)) issue_s(1, 0);
       }
       for (int j = 0; ok && j < nkv; j++) {
+        // next scores first: S of tile t is free as soon as its softmax warps have read it
+        for (int t = 0; t < 2 && ok; t++) {
+          if (j + 1 >= nkv || !active(t, j + 1)) continue;
+          if (!mbar_wait(b_sfree + 8 * t, j & 1, abort_flag) || !wait_kv(j + 1)) { ok = false; break; }
+          fence_after();
+          issue_s(t, j + 1);
+        }
         const uint32_t v = sKV + (j % FWD_STAGES) * FWD_KV + TILE;
         for (int t = 0; t < 2 && ok; t++) {
           if (!active(t, j)) continue;
-          if (!mbar_wait(b_pfull + 8 * t, j & 1, abort_flag)) { ok = false; break; }
+          const uint32_t pb = b_pfull + 16 * t + 8 * (j & 1);
+          if (!mbar_wait(pb, (j >> 1) & 1, abort_flag)) { ok = false; break; }
           fence_after();
-          const uint32_t pt = sP + t * PTILE;
+          const uint32_t pt = sP + (2 * t + (j & 1)) * PTILE;
 #pragma unroll
           for (int kk = 0; kk < 128 / 16; kk++)
-            mma_bf16(tmem + 256 + HD * t, desc_k128(pt, kk), desc_mn(v, kk), ID_O, kk > 0);
-          mma_commit(b_ofull + 8 * t);
-          if (j + 1 < nkv && active(t, j + 1)) {
-            if (!wait_kv(j + 1)) { ok = false; break; }
-            issue_s(t, j + 1);
-          }
+            mma_bf16(tmem + 256 + HD * t, desc_k128(pt, kk), desc_mn(v, kk), ID_O, (j | kk) > 0);
+          mma_commit(b_pempty + 16 * t + 8 * (j & 1));
         }
         if (ok) mma_commit(b_kvempty + 8 * (j % FWD_STAGES));
       }
@@ -216,75 +250,88 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_tc_kernel(const __grid_consta
       const uint32_t r = q * 32 + lane;             // row inside the tile
       const uint32_t lrow = (uint32_t)(q * 32) << 16;
       const uint32_t tS = tmem + lrow + 128 * t, tO = tmem + lrow + 256 + HD * t;
-      const uint32_t pt = sP + t * PTILE;
-      float o[HD];
-#pragma unroll
-      for (int d = 0; d < HD; d++) o[d] = 0.f;
-      float m_prev = -INFINITY, m_o = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j <= qt; j++) {
         if (!mbar_wait_warp(b_sfull + 8 * t, j & 1, abort_flag)) { ok = false; break; }
         fence_after();
+        float sv[128];
+        tmem_ld128(tS, sv);
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_sfree + 8 * t);  // the MMA may overwrite S now
         const bool diag = j == qt;
-        float v[32];
-        // pass 1: row maximum of the raw scores
         float mx = -INFINITY;
+        if (diag) {
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
-          tmem_ld32(tS + 32 * c, v);
+          for (int i = 0; i < 128; i++)
+            if (i <= (int)r) mx = fmaxf(mx, sv[i]);
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; i++)
-            if (!diag || 32 * c + i <= (int)r) mx = fmaxf(mx, v[i]);
+          for (int i = 0; i < 128; i++) mx = fmaxf(mx, sv[i]);
         }
-        const float m_new = fmaxf(m_prev, mx * p.sl2);
-        // fold in the previous block's P V (computed against m_prev)
-        if (j > 0) {
-          if (!mbar_wait_warp(b_ofull + 8 * t, (j - 1) & 1, abort_flag)) { ok = false; break; }
-          fence_after();
-          const float alpha = ex2(m_o - m_prev);
-#pragma unroll
-          for (int c = 0; c < 2; c++) {
-            tmem_ld32(tO + 32 * c, v);
-#pragma unroll
-            for (int i = 0; i < 32; i++) o[32 * c + i] = fmaf(o[32 * c + i], alpha, v[i]);
-          }
-          m_o = m_prev;
+        mx *= p.sl2;
+        // move the reference when this block's max runs too far above it; O and
+        // l are rescaled below, once the probabilities no longer need registers
+        const bool need = j > 0 && mx > m_ref + RESCALE_LOG2;
+        const float m_old = j == 0 ? mx : m_ref;
+        if (j == 0 || need) m_ref = mx;
+        // P buffer (j & 1) is free once the P V of block j-2 is done
+        const uint32_t pt = sP + (2 * t + (j & 1)) * PTILE;
+        if (j >= 2 && !mbar_wait_warp(b_pempty + 16 * t + 8 * (j & 1), ((j - 2) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        // pass 2: probabilities (bf16) into the P tile, row sum in fp32
         float rs = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; c++) {
-          tmem_ld32(tS + 32 * c, v);
+          float(&pv)[32] = *reinterpret_cast<float(*)[32]>(sv + 32 * c);  // probabilities overwrite the scores
 #pragma unroll
           for (int i = 0; i < 32; i++) {
-            float pv = ex2(fmaf(v[i], p.sl2, -m_new));
-            if (diag && 32 * c + i > (int)r) pv = 0.f;
-            v[i] = pv;
-            rs += pv;
+            float e = ex2(fmaf(pv[i], p.sl2, -m_ref));
+            if (diag && 32 * c + i > (int)r) e = 0.f;
+            pv[i] = e;
+            rs += e;
           }
-          store_row32(pt, r, 32 * c, v);
+          store_row32(pt, r, 32 * c, pv);
         }
-        l = l * ex2(m_prev - m_new) + rs;
-        m_prev = m_new;
+        if (__any_sync(0xffffffffu, need)) {
+          // the previous block's P V must have landed in O before O is rescaled
+          if (!mbar_wait_warp(b_pempty + 16 * t + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const float alpha = need ? ex2(m_old - m_ref) : 1.f;
+#pragma unroll
+          for (int c = 0; c < 2; c++) {
+            float ov[32];
+            tmem_ld32(tO + 32 * c, ov);
+#pragma unroll
+            for (int i = 0; i < 32; i++) ov[i] *= alpha;
+            tmem_st32(tO + 32 * c, ov);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          l *= alpha;
+        }
+        l += rs;
         fence_before();
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_pfull + 8 * t);
+        if (lane == 0) mbar_arrive(b_pfull + 16 * t + 8 * (j & 1));
       }
-      if (ok && mbar_wait_warp(b_ofull + 8 * t, qt & 1, abort_flag)) {
+      // the last block's P V completes the accumulator
+      if (ok && mbar_wait_warp(b_pempty + 16 * t + 8 * (qt & 1), (qt >> 1) & 1, abort_flag)) {
         fence_after();
-        const float alpha = ex2(m_o - m_prev);
-        float v[32];
         const float inv = 1.f / l;
         bf16* dst = p.out + (size_t)(row0 + qt * 128 + r) * p.C + h * HD;
 #pragma unroll
         for (int c = 0; c < 2; c++) {
+          float v[32];
           tmem_ld32(tO + 32 * c, v);
-#pragma unroll
-          for (int i = 0; i < 32; i++) v[i] = fmaf(o[32 * c + i], alpha, v[i]);
           store_global32(dst + 32 * c, v, inv);
         }
-        p.lse[((size_t)b * p.H + h) * p.T + qt * 128 + r] = (m_prev + __log2f(l)) * LN2;
+        p.lse[((size_t)b * p.H + h) * p.T + qt * 128 + r] = (m_ref + log2f(l)) * LN2;
       }
     }
   }
@@ -430,9 +477,10 @@ __global__ void __launch_bounds__(320, 1)
       float s[2][32], dp[2][32];
 #pragma unroll
       for (int c = 0; c < 2; c++) {
-        tmem_ld32(tmem + lrow + hf * 64 + 32 * c, s[c]);
-        tmem_ld32(tmem + lrow + 128 + hf * 64 + 32 * c, dp[c]);
+        tmem_ld32_async(tmem + lrow + hf * 64 + 32 * c, s[c]);
+        tmem_ld32_async(tmem + lrow + 128 + hf * 64 + 32 * c, dp[c]);
       }
+      tmem_wait_ld();
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_sfree);
@@ -593,9 +641,10 @@ __global__ void __launch_bounds__(320, 1)
       float s[2][32], dp[2][32];
 #pragma unroll
       for (int c = 0; c < 2; c++) {
-        tmem_ld32(tmem + lrow + hf * 64 + 32 * c, s[c]);
-        tmem_ld32(tmem + lrow + 128 + hf * 64 + 32 * c, dp[c]);
+        tmem_ld32_async(tmem + lrow + hf * 64 + 32 * c, s[c]);
+        tmem_ld32_async(tmem + lrow + 128 + hf * 64 + 32 * c, dp[c]);
       }
+      tmem_wait_ld();
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_sfree);

@@ -26,6 +26,17 @@
 //               is never read back by the SM.  The GELU' input tile comes in
 //               by TMA as well.  The two accumulators let the epilogue of
 //               one unit overlap the MMAs of the next.
+// CTA pairs (CL = 2, tcgen05 cta_group::2): the two CTAs of a cluster
+// compute one 256 x BN tile together.  Each CTA loads its own 128 rows of A
+// and one half (BN/2 rows) of the B tile; one thread of the even CTA issues
+// M=256 MMAs that read A and B from both CTAs' shared memory and write each
+// CTA's 128 rows into its own TMEM.  Every SM then receives 32 KB of operands
+// per 64-deep k-block instead of 48 KB for the same work, which is what
+// bounds this kernel (operand delivery into the SM, not the tensor pipe),
+// and the ring gets 6 stages.  The odd CTA's TMA loads signal the even
+// CTA's "full" barrier; the MMA commit arrives on both CTAs' "empty" and
+// "accumulator full" barriers; both CTAs' epilogues arrive on the even CTA's
+// "accumulator empty" barrier.
 // Weight gradients have few output tiles and a long K = B*T, so K is split
 // into ranges handled by different CTAs.  The splits of one tile add into D
 // strictly in split order through a per-tile turnstile counter (split s
@@ -74,6 +85,57 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 }
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// shared::cluster address of the same shared variable in the even CTA of the pair
+__device__ __forceinline__ uint32_t leader_addr(uint32_t a) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
+  return r;
+}
+// TMA load into this CTA's shared memory, completion signalled on a barrier of
+// either CTA of the pair (cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// arrive once on the barrier at this offset in both CTAs of the pair when the
+// pair's MMAs issued so far have completed
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t holder_smem, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder_smem), "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 // TMA store / reduce-add of a staged box, and bulk-group bookkeeping (per thread)
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
@@ -121,12 +183,12 @@ __device__ __forceinline__ void unstage_bf16(const uint8_t* buf, uint32_t r, uin
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CL>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                    const __grid_constant__ CUtensorMap td, const __grid_constant__ CUtensorMap tx, TcParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
-  constexpr uint32_t B_BYTES = BN * BK * 2;
+  constexpr uint32_t B_BYTES = (BN / CL) * BK * 2;  // this CTA's share of the B tile
   constexpr uint32_t STAGE = A_BYTES + B_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint32_t raw = smem_u32(smem_raw);
@@ -148,13 +210,18 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; a++) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, 4 * CL);  // the epilogue warps of both CTAs of a pair
     }
     for (int w = 0; w < 4; w++) mbar_init(auxbar0 + 8 * w, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 2 * BN);
+  // the peer's loads, commits and arrivals target this CTA's barriers: they must exist first
+  if (CL > 1) cluster_sync();
+  if (warp == 1) {
+    if (CL == 1) tmem_alloc(smem_u32(tmem_holder), 2 * BN);
+    else tmem_alloc_pair(smem_u32(tmem_holder), 2 * BN);
+  }
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&ta) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tb) : "memory");
@@ -166,51 +233,74 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_holder;
 
   const int num_n = (p.N + BN - 1) / BN;
-  const int tiles = ((p.M + BM - 1) / BM) * num_n;
+  // a "tile" here is CL vertically adjacent 128-row tiles (one per CTA of the pair)
+  const int tiles = ((p.M + CL * BM - 1) / (CL * BM)) * num_n;
   const int nk = (p.K + BK - 1) / BK;
   const int units = tiles * p.splits;  // unit u: split u / tiles of tile u % tiles
   auto kb_begin = [&](int sp) { return (int)((long long)nk * sp / p.splits); };
+  const uint32_t crank = CL > 1 ? cluster_rank() : 0;
+  const int ustart = (int)(blockIdx.x / CL), ustep = (int)(gridDim.x / CL);
+  auto tile_m0 = [&](int t) { return ((t / num_n) * CL + (int)crank) * BM; };
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer
       uint32_t it = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      for (int u = ustart; u < units; u += ustep) {
         const int t = u % tiles, sp = u / tiles;
-        const int m0 = (t / num_n) * BM, n0 = (t % num_n) * BN;
+        const int m0 = tile_m0(t), n0 = (t % num_n) * BN;
         bool ok = true;
         for (int kb = kb_begin(sp), kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag)) { ok = false; break; }
-          const uint32_t fb = full0 + 8 * s;
-          mbar_expect_tx(fb, STAGE);
           const uint32_t a_dst = ring + s * STAGE, b_dst = a_dst + A_BYTES;
           const int k0 = kb * BK;
-          if (!p.a_mn) {
-            tma_load_2d(a_dst, &ta, k0, m0, fb);
-          } else {
-            tma_load_2d(a_dst, &ta, m0, k0, fb);
-            tma_load_2d(a_dst + 8192, &ta, m0 + 64, k0, fb);
-          }
-          if (!p.b_mn) {
-            tma_load_2d(b_dst, &tb, k0, n0, fb);
-          } else {
+          if (CL == 1) {
+            const uint32_t fb = full0 + 8 * s;
+            mbar_expect_tx(fb, STAGE);
+            if (!p.a_mn) {
+              tma_load_2d(a_dst, &ta, k0, m0, fb);
+            } else {
+              tma_load_2d(a_dst, &ta, m0, k0, fb);
+              tma_load_2d(a_dst + 8192, &ta, m0 + 64, k0, fb);
+            }
+            if (!p.b_mn) {
+              tma_load_2d(b_dst, &tb, k0, n0, fb);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; j++) tma_load_2d(b_dst + 8192 * j, &tb, n0 + 64 * j, k0, fb);
+              for (int j = 0; j < BN / 64; j++) tma_load_2d(b_dst + 8192 * j, &tb, n0 + 64 * j, k0, fb);
+            }
+          } else {
+            // both CTAs' loads complete on the even CTA's barrier, which expects all of them
+            const uint32_t fb = leader_addr(full0 + 8 * s);
+            if (crank == 0) mbar_expect_tx(full0 + 8 * s, 2 * STAGE);
+            if (!p.a_mn) {
+              tma_load_2d_pair(a_dst, &ta, k0, m0, fb);
+            } else {
+              tma_load_2d_pair(a_dst, &ta, m0, k0, fb);
+              tma_load_2d_pair(a_dst + 8192, &ta, m0 + 64, k0, fb);
+            }
+            const int nb = n0 + (int)crank * (BN / 2);  // this CTA's half of the B tile
+            if (!p.b_mn) {
+              tma_load_2d_pair(b_dst, &tb, k0, nb, fb);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 128; j++) tma_load_2d_pair(b_dst + 8192 * j, &tb, nb + 64 * j, k0, fb);
+            }
           }
         }
         if (!ok) break;
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // ---- MMA issuer
-      const uint32_t idesc = idesc_bf16(BM, BN, p.a_mn, p.b_mn);
+    if (lane == 0 && crank == 0) {  // ---- MMA issuer (the even CTA of a pair)
+      const uint32_t idesc = idesc_bf16(CL * BM, BN, p.a_mn, p.b_mn);
       // K-major: advance 32 bytes per 16-wide k step inside the swizzled row,
       // SBO = 1024 (8 rows of 128 B).  MN-major: 16 k-rows of 128 B per step,
       // LBO = 8192 between 64-element MN blocks, SBO = 1024 between 8-row k groups.
       const uint32_t a_step = p.a_mn ? 2048u : 32u, b_step = p.b_mn ? 2048u : 32u;
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
       uint32_t it = 0, j = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x, j++) {
+      for (int u = ustart; u < units; u += ustep, j++) {
         const uint32_t a = j & 1, aph = (j >> 1) & 1;
         if (!mbar_wait(tempty0 + 8 * a, aph ^ 1, abort_flag)) break;
         fence_after();
@@ -226,12 +316,15 @@ __global__ void __launch_bounds__(192, 1)
           for (int kk = 0; kk < BK / 16; kk++) {
             const uint64_t ad = sdesc(a_base + kk * a_step, a_lbo, 1024);
             const uint64_t bd = sdesc(b_base + kk * b_step, b_lbo, 1024);
-            mma_bf16(d, ad, bd, idesc, (kb != kb0) || kk != 0);
+            if (CL == 1) mma_bf16(d, ad, bd, idesc, (kb != kb0) || kk != 0);
+            else mma_bf16_pair(d, ad, bd, idesc, (kb != kb0) || kk != 0);
           }
-          mma_commit(empty0 + 8 * s);
+          if (CL == 1) mma_commit(empty0 + 8 * s);
+          else mma_commit_pair(empty0 + 8 * s);
         }
         if (!ok) break;
-        mma_commit(tfull0 + 8 * a);
+        if (CL == 1) mma_commit(tfull0 + 8 * a);
+        else mma_commit_pair(tfull0 + 8 * a);
       }
     }
   } else {  // ---- epilogue warps 2..5
@@ -241,10 +334,15 @@ __global__ void __launch_bounds__(192, 1)
     const uint8_t* stg_g = stg_gen + e * 2 * STG;
     const uint32_t auxbar = auxbar0 + 8 * e;
     uint32_t aux_phase = 0;
+    // the accumulator is free again: tell the CTA whose thread issues the MMAs
+    auto release_acc = [&](uint32_t bar) {
+      if (CL == 1) mbar_arrive(bar);
+      else mbar_arrive_cluster(leader_addr(bar));
+    };
     uint32_t j = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, j++) {
+    for (int u = ustart; u < units; u += ustep, j++) {
       const int t = u % tiles, sp = u / tiles;
-      const int m0 = (t / num_n) * BM, n0 = (t % num_n) * BN;
+      const int m0 = tile_m0(t), n0 = (t % num_n) * BN;
       const int rbase = m0 + q * 32;  // first row of this warp's slab
       const bool rows_in = rbase < p.M;
       const uint32_t a = j & 1, aph = (j >> 1) & 1;
@@ -289,7 +387,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty0 + 8 * a);
+        if (lane == 0) release_acc(tempty0 + 8 * a);
         if (p.splits > 1) {
           // this split's additions must be complete before the next split starts
           if (lane == 0) {
@@ -397,7 +495,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * a);
+      if (lane == 0) release_acc(tempty0 + 8 * a);
       if (!ok) break;
     }
     // the staging buffers must stay valid until every store has read them
@@ -406,10 +504,13 @@ __global__ void __launch_bounds__(192, 1)
   }
   fence_before();
   __syncthreads();
+  // neither CTA of a pair may leave while the other can still write into it
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     fence_after();
-    tmem_dealloc(tmem, 2 * BN);
+    if (CL == 1) tmem_dealloc(tmem, 2 * BN);
+    else tmem_dealloc_pair(tmem, 2 * BN);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.flags, FLAG_TIMEOUT);
 }
@@ -430,55 +531,73 @@ int choose_splits(int tiles, int nk, int sms) {
   return best;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CL>
 constexpr size_t smem_bytes() {
-  return (size_t)STAGES * (BM * BK * 2 + BN * BK * 2) + 8 * STG + 1024 + 256;
+  return (size_t)STAGES * (BM * BK * 2 + (BN / CL) * BK * 2) + 8 * STG + 1024 + 256;
 }
 
-template <int BN, int STAGES>
-cudaError_t launch(const GemmArgs& g, int* flags, cudaStream_t st) {
-  constexpr size_t smem = smem_bytes<BN, STAGES>();
+template <int BN, int STAGES, int CL>
+cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
+  constexpr size_t smem = smem_bytes<BN, STAGES, CL>();
   static_assert(smem <= 232448, "shared memory per CTA");
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, CL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   CUtensorMap ta, tb, td, tx;
   bool ok = g.a_kmajor ? tc_make_map(&ta, g.A, g.K, g.M, g.lda, 64, BM) : tc_make_map(&ta, g.A, g.M, g.K, g.lda, 64, 64);
-  ok = ok && (g.b_kmajor ? tc_make_map(&tb, g.B, g.K, g.N, g.ldb, 64, BN) : tc_make_map(&tb, g.B, g.N, g.K, g.ldb, 64, 64));
+  ok = ok && (g.b_kmajor ? tc_make_map(&tb, g.B, g.K, g.N, g.ldb, 64, BN / CL)
+                         : tc_make_map(&tb, g.B, g.N, g.K, g.ldb, 64, 64));
   if (g.epi == EPI_ACC_F32) ok = ok && tc_make_map_f32(&td, g.D, g.N, g.M, g.ldd, 32, 32);
   else ok = ok && tc_make_map(&td, g.D, g.N, g.M, g.ldd, 64, 32);
   if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) ok = ok && tc_make_map(&tx, g.aux, g.N, g.M, g.ldaux, 64, 32);
   else tx = td;
   if (!ok) return cudaErrorInvalidValue;
   const int sms = tc_num_sms();
-  const long long tiles = ((g.M + BM - 1) / BM) * (long long)((g.N + BN - 1) / BN);
-  const int nk = (g.K + BK - 1) / BK;
-  int splits = 1;
-  if (g.epi == EPI_ACC_F32 && g.turn && tiles <= g.turn_len) splits = choose_splits((int)tiles, nk, sms);
+  const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
   TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
              g.turn};
   const long long units = tiles * splits;
-  const unsigned grid = (unsigned)(units < sms ? units : sms);
-  if (splits == 1) {
-    gemm_tc_kernel<BN, STAGES><<<grid, 192, smem, st>>>(ta, tb, td, tx, p);
-    return cudaGetLastError();
-  }
-  // split K: every CTA must be resident for the turnstile waits
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeCooperative;
-  at[0].val.cooperative = 1;
+  long long slots = sms / CL;  // clusters that can run at once
+  if (CL > 1) {
+    static int max_clusters = 0;
+    if (!max_clusters) {
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = CL;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      cfg.gridDim = dim3((unsigned)(slots * CL));
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_tc_kernel<BN, STAGES, CL>, &cfg) != cudaSuccess ||
+          max_clusters <= 0)
+        max_clusters = (int)slots;
+    }
+    if (max_clusters < slots) slots = max_clusters;
+  }
+  const unsigned grid = (unsigned)((units < slots ? units : slots) * CL);
+  cfg.gridDim = dim3(grid);
+  if (CL > 1) {
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+  } else {
+    // split K: every CTA must be resident for the turnstile waits
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = splits > 1 ? 1 : 0;
+  }
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES>, ta, tb, td, tx, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL>, ta, tb, td, tx, p);
 }
 
 }  // namespace
@@ -553,6 +672,15 @@ bool gemm_tc_supported(const GemmArgs& g) {
 cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
   gpt2_count_launches(1);
-  if (g.N % 256 == 0) return launch<256, 4>(g, flags, st);
-  return launch<128, 6>(g, flags, st);
+  const bool wide = g.N >= 512;  // 256-wide tiles (a ragged last column tile is clipped by TMA)
+  const int BN = wide ? 256 : 128;
+  const int sms = tc_num_sms();
+  const long long mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN;
+  const int nk = (g.K + BK - 1) / BK;
+  int splits = 1;
+  if (g.epi == EPI_ACC_F32 && g.turn && mt * nt <= g.turn_len) splits = choose_splits((int)(mt * nt), nk, sms);
+  // CTA pairs (cta_group::2) when there are enough row tiles to pair up
+  const bool pair = splits == 1 && mt >= 2 && mt * nt >= sms;
+  if (wide) return pair ? launch<256, 6, 2>(g, 1, flags, st) : launch<256, 4, 1>(g, splits, flags, st);
+  return pair ? launch<128, 8, 2>(g, 1, flags, st) : launch<128, 6, 1>(g, splits, flags, st);
 }

@@ -215,7 +215,10 @@ def test_matmul_simt_epilogues(ops, dt):
 # ---- tensor-core (tcgen05/TMA) GEMM --------------------------------------
 # Row strides must be multiples of 8 bf16 (16 bytes) for TMA; M, N, K need
 # not be tile multiples (K=104, M=136, N=136/264 exercise the ragged edges).
-TC_SHAPES = [(128, 256, 64), (256, 512, 192), (200, 136, 104), (384, 128, 320), (1024, 768, 768), (136, 264, 72)]
+# The last two have enough output tiles for the cluster-pair path (two CTAs
+# sharing B tiles by multicast), with an odd number of 128-row tiles.
+TC_SHAPES = [(128, 256, 64), (256, 512, 192), (200, 136, 104), (384, 128, 320), (1024, 768, 768), (136, 264, 72),
+             (4200, 1280, 320), (8200, 264, 200)]
 
 
 @pytest.mark.parametrize("akm,bkm", [(1, 1), (1, 0), (0, 0), (0, 1)])
@@ -233,9 +236,8 @@ def test_matmul_tc_layouts(ops, akm, bkm, M, N, K):
     assert rel_l2(host(D), ref) < 2 ** -7
 
 
-@pytest.mark.parametrize("N", [256, 384])
-def test_matmul_tc_epilogues(ops, N):
-    M, K = 256, 320
+@pytest.mark.parametrize("M,N,K", [(256, 256, 320), (256, 384, 320), (8200, 640, 136)])
+def test_matmul_tc_epilogues(ops, M, N, K):
     A, B, bias = normal_array((M, K), 140), normal_array((N, K), 141), normal_array((N,), 142)
     tA, tB, tbias = dev(A, torch.bfloat16), dev(B, torch.bfloat16), dev(bias, torch.bfloat16)
     acc = host(tA) @ host(tB).T
