@@ -38,13 +38,15 @@
 // "accumulator full" barriers; both CTAs' epilogues arrive on the even CTA's
 // "accumulator empty" barrier.
 // Weight gradients have few output tiles and a long K = B*T, so K is split
-// into ranges handled by different CTAs.  The splits of one tile add into D
-// strictly in split order through a per-tile turnstile counter (split s
-// waits until the counter reads s, and its reduce-add has completed before
-// it advances the counter), so the result is deterministic.  Such launches
-// are cooperative (every CTA resident), which makes the waits safe.
+// into ranges handled by different CTAs.  Split 0 adds its fp32 partial tile
+// into D (TMA reduce-add; no other CTA touches that tile in this kernel);
+// split s > 0 stores its tile into slot s-1 of a workspace (TMA store, no
+// waiting on other CTAs); splitk_reduce then adds the slots into D in split
+// order, so the result, (D + P0) + (P1 + P2 + ...), is deterministic.
 // Every wait is bounded (about 2 s of %globaltimer); on expiry the CTA
 // raises FLAG_TIMEOUT, stops issuing work, frees its TMEM and returns.
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "tc_common.cuh"
 
@@ -72,17 +74,8 @@ struct TcParams {
   const bf16* bias;
   int* flags;
   int splits;  // K split into this many ranges (EPI_ACC_F32 only)
-  int* turn;   // [tiles] turnstile counters for splits > 1 (zero between launches)
 };
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // shared::cluster address of the same shared variable in the even CTA of the pair
@@ -140,6 +133,11 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
                "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"((uint64_t)map),
+               "r"(x), "r"(y), "r"(z), "r"(src)
                : "memory");
 }
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
@@ -351,22 +349,7 @@ __global__ void __launch_bounds__(192, 1)
       fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + a * BN;
       if (p.epi == EPI_ACC_F32) {
-        if (p.splits > 1) {
-          // turnstile: wait until splits 0..sp-1 of this tile have added their part
-          if (threadIdx.x == 64) {
-            uint64_t t0 = 0;
-            for (uint32_t n = 1; ld_acquire(p.turn + t) != sp; n++) {
-              if ((n & 255) == 0) {
-                if (*abort_flag) break;
-                const uint64_t now = gtimer();
-                if (t0 == 0) t0 = now;
-                else if (now - t0 > WAIT_NS) { *abort_flag = 1; break; }
-              }
-            }
-          }
-          epi_bar();
-          if (*abort_flag) break;
-        }
+        // split 0: D += tile (TMA reduce-add); split s > 0: workspace slot s - 1
 #pragma unroll 1
         for (int c = 0; c < BN / 32; c++) {
           float v[32];
@@ -380,7 +363,8 @@ __global__ void __launch_bounds__(192, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_2d(&td, col0, rbase, buf);
+              if (sp == 0) tma_reduce_add_2d(&td, col0, rbase, buf);
+              else tma_store_3d(&tx, col0, rbase, sp - 1, buf);  // workspace slot sp - 1
               bulk_commit();
             }
           }
@@ -388,16 +372,6 @@ __global__ void __launch_bounds__(192, 1)
         fence_before();
         __syncwarp();
         if (lane == 0) release_acc(tempty0 + 8 * a);
-        if (p.splits > 1) {
-          // this split's additions must be complete before the next split starts
-          if (lane == 0) {
-            bulk_wait<0>();
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-          }
-          __threadfence();
-          epi_bar();
-          if (threadIdx.x == 64) st_release(p.turn + t, sp + 1 == p.splits ? 0 : sp + 1);
-        }
         continue;
       }
       bool ok = true;
@@ -519,13 +493,14 @@ __global__ void __launch_bounds__(192, 1)
 // host side
 // ---------------------------------------------------------------------------
 // K splits for an fp32-accumulate launch: the count (1..16, at least 8
-// k-blocks each) whose units fill the SMs best, the smallest among near ties
-int choose_splits(int tiles, int nk, int sms) {
+// k-blocks each) whose units fill the `slots` concurrent CTAs (or CTA pairs)
+// best, the smallest among near ties
+int choose_splits(int tiles, int nk, int slots) {
   int best = 1;
   double best_eff = 0;
   for (int s = 1; s <= 16 && nk / s >= 8; s++) {
     const long long units = (long long)tiles * s;
-    const double eff = (double)units / (double)(((units + sms - 1) / sms) * sms);
+    const double eff = (double)units / (double)(((units + slots - 1) / slots) * slots);
     if (eff > best_eff + 0.02) best = s, best_eff = eff;
   }
   return best;
@@ -554,12 +529,12 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   if (g.epi == EPI_ACC_F32) ok = ok && tc_make_map_f32(&td, g.D, g.N, g.M, g.ldd, 32, 32);
   else ok = ok && tc_make_map(&td, g.D, g.N, g.M, g.ldd, 64, 32);
   if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) ok = ok && tc_make_map(&tx, g.aux, g.N, g.M, g.ldaux, 64, 32);
+  else if (g.epi == EPI_ACC_F32 && splits > 1) ok = ok && tc_make_map_f32_3d(&tx, g.ws, g.N, g.M, splits - 1, 32, 32);
   else tx = td;
   if (!ok) return cudaErrorInvalidValue;
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
-  TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
-             g.turn};
+  TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits};
   const long long units = tiles * splits;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(192);
@@ -585,18 +560,15 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   }
   const unsigned grid = (unsigned)((units < slots ? units : slots) * CL);
   cfg.gridDim = dim3(grid);
+  cfg.numAttrs = 0;
   if (CL > 1) {
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = CL;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
-  } else {
-    // split K: every CTA must be resident for the turnstile waits
-    at[0].id = cudaLaunchAttributeCooperative;
-    at[0].val.cooperative = splits > 1 ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
   }
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL>, ta, tb, td, tx, p);
 }
 
@@ -643,14 +615,28 @@ bool tc_make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return make_map_dt(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer, ld, box_inner, box_outer);
 }
 
+// dense fp32 [depth][outer][inner] (contiguous), box = box_inner x box_outer x 1
+bool tc_make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t depth,
+                        uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, outer, depth};
+  cuuint64_t strides[2] = {inner * 4, inner * outer * 4};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_num_sms() {
   static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      sms = n;
   }
-  return sms;
+  return sms > 0 ? sms : 148;
 }
 
 extern void gpt2_count_launches(int n);
@@ -669,18 +655,69 @@ bool gemm_tc_supported(const GemmArgs& g) {
   return tc_available();
 }
 
+// K splits a weight-gradient (fp32 accumulate) product would use, and the
+// workspace floats they need (splits * M * N, 0 when no split pays off)
+// Split count of a weight-gradient (fp32 accumulate) product on CTA pairs and
+// the workspace floats it needs: (splits - 1) * M * N, 0 when there is no split
+static int splits_for(int M, int N, int K, size_t ws_floats, int sms) {
+  const int BN = N >= 512 ? 256 : 128;
+  const long long tiles = ((M + 2 * BM - 1) / (2 * BM)) * (long long)((N + BN - 1) / BN);
+  int s = choose_splits((int)tiles, (K + BK - 1) / BK, sms / 2);
+  while (s > 1 && (size_t)(s - 1) * M * N > ws_floats) s--;
+  return s;
+}
+int gemm_tc_splits(int M, int N, int K, size_t ws_floats) { return splits_for(M, N, K, ws_floats, tc_num_sms()); }
+// sized for a given SM count (the planner uses the B300's 148 so that the
+// buffer size does not depend on the machine that asks); a run on a GPU with
+// more SMs caps its splits to what fits
+size_t gemm_tc_workspace_floats(int M, int N, int K, int sms) {
+  const int s = splits_for(M, N, K, (size_t)-1, sms);
+  return s > 1 ? (size_t)(s - 1) * M * N : 0;
+}
+
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(float* __restrict__ D, long long ldd,
+                                                            const float* __restrict__ ws, int M, int N, int splits) {
+  // D[m][n] += ws[0][m][n] + ws[1][m][n] + ... (the partials of splits 1, 2,
+  // ... in order); four columns per thread, every load issued before the additions
+  const long long nv = (long long)M * (N / 4);
+  const size_t plane = (size_t)M * N;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(i / (N / 4)), n = (int)(i % (N / 4)) * 4;
+    const float* src = ws + (size_t)m * N + n;
+    float4 u[16];
+#pragma unroll
+    for (int sp = 0; sp < 16; sp++)
+      if (sp < splits) u[sp] = __ldcs(reinterpret_cast<const float4*>(src + sp * plane));
+    float4 t = u[0];
+#pragma unroll
+    for (int sp = 1; sp < 16; sp++)
+      if (sp < splits) {
+        t.x += u[sp].x; t.y += u[sp].y; t.z += u[sp].z; t.w += u[sp].w;
+      }
+    float4* d = reinterpret_cast<float4*>(D + (size_t)m * ldd + n);
+    float4 o = *d;
+    o.x += t.x; o.y += t.y; o.z += t.z; o.w += t.w;
+    *d = o;
+  }
+}
+
 cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
   gpt2_count_launches(1);
   const bool wide = g.N >= 512;  // 256-wide tiles (a ragged last column tile is clipped by TMA)
-  const int BN = wide ? 256 : 128;
   const int sms = tc_num_sms();
-  const long long mt = (g.M + BM - 1) / BM, nt = (g.N + BN - 1) / BN;
-  const int nk = (g.K + BK - 1) / BK;
+  const long long mt = (g.M + BM - 1) / BM, nt = (g.N + (wide ? 256 : 128) - 1) / (wide ? 256 : 128);
   int splits = 1;
-  if (g.epi == EPI_ACC_F32 && g.turn && mt * nt <= g.turn_len) splits = choose_splits((int)(mt * nt), nk, sms);
-  // CTA pairs (cta_group::2) when there are enough row tiles to pair up
-  const bool pair = splits == 1 && mt >= 2 && mt * nt >= sms;
-  if (wide) return pair ? launch<256, 6, 2>(g, 1, flags, st) : launch<256, 4, 1>(g, splits, flags, st);
-  return pair ? launch<128, 8, 2>(g, 1, flags, st) : launch<128, 6, 1>(g, splits, flags, st);
+  if (g.epi == EPI_ACC_F32 && g.ws && g.N % 4 == 0 && mt >= 2) splits = gemm_tc_splits(g.M, g.N, g.K, g.ws_floats);
+  // CTA pairs (cta_group::2) when there are enough row tiles to pair up, or for a split K
+  const bool pair = mt >= 2 && (splits > 1 || mt * nt >= sms);
+  cudaError_t e;
+  if (wide) e = pair ? launch<256, 6, 2>(g, splits, flags, st) : launch<256, 4, 1>(g, 1, flags, st);
+  else e = pair ? launch<128, 8, 2>(g, splits, flags, st) : launch<128, 6, 1>(g, 1, flags, st);
+  if (e != cudaSuccess || splits == 1) return e;
+  gpt2_count_launches(1);
+  const long long nv = (long long)g.M * (g.N / 4);
+  const unsigned grid = (unsigned)std::min<long long>((nv + 255) / 256, (long long)sms * 8);
+  splitk_reduce_kernel<<<grid, 256, 0, st>>>((float*)g.D, g.ldd, g.ws, g.M, g.N, splits - 1);
+  return cudaGetLastError();
 }

@@ -24,16 +24,18 @@ struct GemmArgs {
   const void* bias;          // [N] of type T or nullptr
   void* aux; long long ldaux;
   int epi;
-  // optional [turn_len] zeroed ints: lets the tensor-core path split K of an
-  // EPI_ACC_F32 product across CTAs (fixed-order, deterministic accumulation);
-  // left zero again when the launch completes
-  int* turn; int turn_len;
+  // optional fp32 workspace: lets the tensor-core path split K of an
+  // EPI_ACC_F32 product across CTAs (partials added in split order afterwards)
+  float* ws; size_t ws_floats;
 };
-#define GPT2_GEMM_TURN_LEN 4096
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
 // tcgen05/TMA tensor-core path (bf16 operands); returns cudaErrorNotSupported
 // when the shape or layout is outside what the kernel handles.
 cudaError_t gemm_tc(const GemmArgs& a, int* flags, cudaStream_t st);
+// workspace floats a split-K weight-gradient product of this shape uses on a
+// GPU with `sms` SMs (0: no split)
+size_t gemm_tc_workspace_floats(int M, int N, int K, int sms);
+#define GPT2_NOMINAL_SMS 148
 bool gemm_tc_supported(const GemmArgs& a);
 
 // ---- bandwidth kernels ---------------------------------------------------

@@ -299,9 +299,21 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict_
   if (!out) return;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + lane;
+  // chunks w, w+8, w+16, ... in increasing order; eight loads in flight, added in that order
   float s = 0.f;
-  if (c < C)
-    for (int k = w; k < nchunks; k += 8) s += partial[((size_t)k * nout + o) * C + c];
+  if (c < C) {
+    const float* src = partial + (size_t)o * C + c;
+    const size_t stride = (size_t)nout * C;
+    int k = w;
+    for (; k + 56 < nchunks; k += 64) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) v[u] = src[(size_t)(k + 8 * u) * stride];
+#pragma unroll
+      for (int u = 0; u < 8; u++) s += v[u];
+    }
+    for (; k < nchunks; k += 8) s += src[(size_t)k * stride];
+  }
   sh[w][lane] = s;
   __syncthreads();
   if (w == 0 && c < C) {
@@ -431,13 +443,12 @@ __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kerne
   // sum the eight warps' slices in warp order; column c = vi * N + k
   float* dst = partial + (size_t)blockIdx.x * 3 * C;
   const int nc = want_rsum ? 3 * C : 2 * C;
-  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
-    const int a = c / C, cc = c - a * C, vi = cc / N, k = cc - vi * N;
-    const int idx = (a * N + k) * nvec + vi;
+  for (int idx = threadIdx.x; idx < nc; idx += blockDim.x) {  // shared-memory order: no bank conflicts
+    const int a = idx / C, rem = idx - a * C, k = rem / nvec, vi = rem - k * nvec;
     float t = lnb_sh[idx];
 #pragma unroll
     for (int q = 1; q < 8; q++) t += lnb_sh[(size_t)q * 3 * C + idx];
-    dst[c] = t;
+    dst[a * C + vi * N + k] = t;
   }
 }
 
@@ -967,7 +978,7 @@ __global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ lo
     }
   };
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  // row max over the first V columns
+  // row max over the first V columns (only a vector reaching past V needs the mask)
   float m = -INFINITY;
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
@@ -975,9 +986,14 @@ __global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ lo
     if (vi < nvec) {
       float f[N];
       unpack(k, f);
+      if (vi * N + N <= V) {
 #pragma unroll
-      for (int i = 0; i < N; i++)
-        if (vi * N + i < V) m = fmaxf(m, f[i]);
+        for (int i = 0; i < N; i++) m = fmaxf(m, f[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < N; i++)
+          if (vi * N + i < V) m = fmaxf(m, f[i]);
+      }
     }
   }
   m = warp_max(m);
@@ -1001,11 +1017,15 @@ __global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ lo
     if (vi < nvec) {
       float f[N];
       unpack(k, f);
+      if (vi * N + N <= V) {
 #pragma unroll
-      for (int i = 0; i < N; i++) {
-        f[i] = vi * N + i < V ? fast_exp2(fmaf(f[i], L2E, -ml)) : 0.f;
-        s += f[i];
+        for (int i = 0; i < N; i++) f[i] = fast_exp2(fmaf(f[i], L2E, -ml));
+      } else {
+#pragma unroll
+        for (int i = 0; i < N; i++) f[i] = vi * N + i < V ? fast_exp2(fmaf(f[i], L2E, -ml)) : 0.f;
       }
+#pragma unroll
+      for (int i = 0; i < N; i++) s += f[i];
       if constexpr (N == 8) {
         __half2* hp = reinterpret_cast<__half2*>(&raw[k]);
 #pragma unroll
@@ -1055,10 +1075,8 @@ __global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ lo
         for (int i = 0; i < N; i++) f[i] = q[i];
       }
 #pragma unroll
-      for (int i = 0; i < N; i++) {
-        const int idx = vi * N + i;
-        f[i] = idx == tg ? g_tg : f[i] * scale;  // pads hold exp = 0
-      }
+      for (int i = 0; i < N; i++) f[i] *= scale;  // pads hold exp = 0
+      if (tg >= vi * N && tg < vi * N + N) f[tg - vi * N] = g_tg;
       st16_cs(z + (size_t)vi * N, f);
     }
   }

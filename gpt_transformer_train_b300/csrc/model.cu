@@ -124,7 +124,15 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), colsum_partial_floats((int)BT, 4 * (int)C)) *
                    sizeof(float));
   b.keys = take(encoder_backward_scratch_bytes((int)BT));
-  b.turn = take(GPT2_GEMM_TURN_LEN * sizeof(int));
+  // split-K workspace of the weight-gradient GEMMs (bf16 mode): the largest any layer needs
+  b.ws_floats = 0;
+  if (c.precision == GPT2_PRECISION_BF16) {
+    const int iBT = (int)BT, iC = (int)C;
+    const int shapes[5][2] = {{c.Vp, iC}, {iC, 4 * iC}, {4 * iC, iC}, {iC, iC}, {3 * iC, iC}};
+    for (auto& sh : shapes)
+      b.ws_floats = std::max(b.ws_floats, gemm_tc_workspace_floats(sh[0], sh[1], iBT, GPT2_NOMINAL_SMS));
+  }
+  b.ws = take(std::max<size_t>(b.ws_floats, 1) * sizeof(float));
   b.flags = take(256);
   b.tok = take(BT * 4);
   b.tgt = take(BT * 4);
@@ -196,7 +204,7 @@ struct Step {
   // dW[N][K] += dY[M][N]^T . X[M][K]
   cudaError_t linear_wgrad(float* dW, const T* dY, const T* X, int M, int N, int K) {
     GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32,
-               m->at<int>(m->bl.turn), GPT2_GEMM_TURN_LEN};
+               m->at<float>(m->bl.ws), m->bl.ws_floats};
     return gemm(a);
   }
 

@@ -68,13 +68,20 @@ int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void*
                                          (const float*)w, rows, C, accumulate, dw, db, dres_sum, part, ST(stream)));
 }
 
+size_t gpt2_op_matmul_workspace_bytes(int M, int N, int K, int epilogue) {
+  if (M <= 0 || N <= 0 || K <= 0 || epilogue != EPI_ACC_F32) return 0;
+  return gemm_tc_workspace_floats(M, N, K, GPT2_NOMINAL_SMS) * sizeof(float);
+}
+
 int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const void* B, long long ldb, int b_kmajor,
                    int M, int N, int K, void* D, long long ldd, const void* bias, void* aux, long long ldaux,
-                   int epilogue, int path, int* flags_dev, int* counters_dev, void* stream) {
+                   int epilogue, int path, int* flags_dev, void* workspace, size_t workspace_bytes,
+                   void* stream) {
   if (bad_dtype(dtype) || !A || !B || !D || M <= 0 || N <= 0 || K <= 0 || epilogue < 0 || epilogue > 3) return GPT2_ERR_INVALID_ARG;
   if ((epilogue == EPI_GELU || epilogue == EPI_GELU_BWD) && !aux) return GPT2_ERR_INVALID_ARG;
+  if (workspace && ((uintptr_t)workspace & 15)) return GPT2_ERR_INVALID_ARG;
   GemmArgs a{A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias, aux, ldaux, epilogue,
-             counters_dev, counters_dev ? GPT2_GEMM_COUNTERS : 0};
+             (float*)workspace, workspace ? workspace_bytes / sizeof(float) : 0};
   if (path == 2 || (path == 0 && dtype == GPT2_PRECISION_BF16 && gemm_tc_supported(a))) {
     if (dtype != GPT2_PRECISION_BF16 || !flags_dev || !gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
     return rc_of(gemm_tc(a, flags_dev, ST(stream)));

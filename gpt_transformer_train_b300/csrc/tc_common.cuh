@@ -167,5 +167,8 @@ bool tc_make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 // the same over fp32 elements
 bool tc_make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                      uint32_t box_inner, uint32_t box_outer);
+// dense fp32 [depth][outer][inner], box = box_inner x box_outer x 1
+bool tc_make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t depth,
+                        uint32_t box_inner, uint32_t box_outer);
 bool tc_available();
 int tc_num_sms();

@@ -21,7 +21,8 @@ _sigs = {
     "gpt2_op_residual_layernorm_forward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _P]),
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
-    "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P, _P]),
+    "gpt2_op_matmul_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P, _sz, _P]),
     "gpt2_op_attention_forward": (_i, [_i, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P]),
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P, _sz, _P]),
@@ -101,18 +102,17 @@ def gpt2_op_layernorm_backward(dres, dres_c, dy, x, mean, rstd, w, dw, db, rows,
                                        _s(stream)), "layernorm_backward")
 
 
-GEMM_COUNTERS = 4096
-
-
-def gemm_counters(device="cuda"):
-    """Zeroed turnstile counters that let the fp32-accumulate GEMM split K."""
-    return torch.zeros(GEMM_COUNTERS, dtype=torch.int32, device=device)
+def gemm_workspace(M, N, K, epilogue=EPI_ACC_F32, device="cuda"):
+    """Workspace that lets the fp32-accumulate GEMM split K (None when it would not)."""
+    n = lib.gpt2_op_matmul_workspace_bytes(M, N, K, epilogue)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
 
 
 def gpt2_op_matmul(A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias=None, aux=None, ldaux=0,
-                   epilogue=EPI_STORE, path=PATH_AUTO, flags_dev=None, counters_dev=None, stream=None):
+                   epilogue=EPI_STORE, path=PATH_AUTO, flags_dev=None, workspace=None, stream=None):
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _ck(lib.gpt2_op_matmul(_dt(A), _p(A), lda, a_kmajor, _p(B), ldb, b_kmajor, M, N, K, _p(D), ldd, _p(bias),
-                           _p(aux), ldaux, epilogue, path, _p(flags_dev), _p(counters_dev), _s(stream)), "matmul")
+                           _p(aux), ldaux, epilogue, path, _p(flags_dev), _p(workspace), wsb, _s(stream)), "matmul")
 
 
 def gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, path=PATH_AUTO, flags_dev=None, stream=None):

@@ -133,9 +133,9 @@ def make_case(name, ops):
                     2.0 * BT * N * K, "FLOP")
         dy, x = randn((BT, N), 25), randn((BT, K), 26)  # dW[N][K] += dy^T x
         dW = torch.zeros(N, K, device="cuda")
-        cnt = ops.gemm_counters()
+        ws = ops.gemm_workspace(N, K, BT)
         return (lambda: ops.gpt2_op_matmul(dy, N, 0, x, K, 0, N, K, BT, dW, K, epilogue=ops.EPI_ACC_F32,
-                                           path=ops.PATH_TC, flags_dev=fl, counters_dev=cnt),
+                                           path=ops.PATH_TC, flags_dev=fl, workspace=ws),
                 2.0 * BT * N * K, "FLOP")
     raise SystemExit(f"unknown kernel {name}")
 

@@ -91,15 +91,17 @@ int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void*
  *            2: D = acc * GELU_tanh'(aux)   3: D (float) += acc
  * path: 0 = best available, 1 = SIMT kernel, 2 = tensor-core (tcgen05) kernel only
  * (GPT2_ERR_INVALID_ARG if the shape/layout is outside what it handles).
- * counters_dev (optional, tensor-core path, epilogue 3): GPT2_GEMM_COUNTERS ints that
- * are zero before the call and are zero again when it completes.  With them the
- * kernel may split K across CTAs; the splits of an output tile then add into D one
- * after another in a fixed order, so the result is still deterministic.  Calls that
- * share one counter array must not overlap on the GPU. */
-#define GPT2_GEMM_COUNTERS 4096
+ * workspace (optional, tensor-core path, epilogue 3): device memory of at least
+ * gpt2_op_matmul_workspace_bytes(M, N, K, 3) bytes, 16-byte aligned, overwritten.
+ * With it the kernel may split K across CTAs: each split stores its partial
+ * product in the workspace and a second kernel adds the partials into D in
+ * split order, so the result is deterministic.  Calls that share one workspace
+ * must not overlap on the GPU.  Without it (NULL) there is no split. */
+size_t gpt2_op_matmul_workspace_bytes(int M, int N, int K, int epilogue);
 int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const void* B, long long ldb,
                    int b_kmajor, int M, int N, int K, void* D, long long ldd, const void* bias, void* aux,
-                   long long ldaux, int epilogue, int path, int* flags_dev, int* counters_dev, void* stream);
+                   long long ldaux, int epilogue, int path, int* flags_dev, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
  * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of
