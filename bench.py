@@ -37,6 +37,13 @@ WORKLOADS = {
     "1.6b": dict(L=48, C=1600, H=25, V=50257, Vp=50304, maxT=1024, B=8, T=1024),
 }
 METRIC = "GPT-2 124M train tokens/sec and MFU on 1 B300 (B=16,T=1024,bf16)"
+
+
+def metric_name(key, w):
+    """The headline metric for the default workload, the same wording for the others."""
+    if key == "124m":
+        return METRIC
+    return f"GPT-2 {key.upper()} train tokens/sec and MFU on 1 B300 (B={w['B']},T={w['T']},bf16)"
 LR, B1, B2, EPS, WD = 6e-4, 0.9, 0.95, 1e-8, 0.1
 SEED = 1234
 CPU_SAMPLE_T = 512  # the CPU legs time one sequence of this many tokens
@@ -190,7 +197,7 @@ def run_reference(args, w):
     times = [step() for _ in range(args.steps)]
     tot = sum(times)
     value = CPU_SAMPLE_T * args.steps / tot
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_name(args.workload, w), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (Zipf(1.1) tokens, N(0,0.02) weights)",
@@ -299,7 +306,7 @@ def run_ours(args, w):
             "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside the step)"}
     out = None
     if rank == 0:
-        out = {"metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        out = {"metric": metric_name(args.workload, w), "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                "data": "synthetic (Zipf(1.1) tokens, seeded N(0,0.02) init)",
