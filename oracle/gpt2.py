@@ -509,6 +509,39 @@ class GPT2:
             adamw_update(self.params[n], self.grads[n], self.m[n], self.v[n],
                          lr, b1, b2, eps, wd if n in DECAYED else 0.0, t)
 
+    def grad_norm(self):
+        """Global L2 norm of all parameter gradients, sqrt(sum over every
+        tensor of sum g^2), accumulated in float64 (the pages' global_norm
+        component, "llm.c" tour, detail graph: a cross-tensor gradient norm)."""
+        return float(np.sqrt(sum(float(np.sum(np.asarray(g, np.float64) ** 2)) for g in self.grads.values())))
+
+    def clip_grad_norm(self, max_norm):
+        """Scale every gradient by min(1, max_norm / (norm + 1e-6)) and return
+        the norm before clipping.  The pages name gradient-norm clipping
+        without a formula; this is the plainest reading (the 1e-6 guards a
+        zero norm)."""
+        norm = self.grad_norm()
+        coef = max_norm / (norm + 1e-6)
+        if coef < 1.0:
+            for g in self.grads.values():
+                g *= g.dtype.type(coef)
+        return norm
+
+
+def lr_schedule(max_lr, final_frac, warmup, total, step):
+    """Learning rate at 0-based `step`: linear warmup to max_lr over `warmup`
+    steps (step s gets max_lr (s + 1) / warmup), then cosine decay from max_lr
+    to min_lr = final_frac * max_lr at step `total`, min_lr after that.  The
+    pages list LR warmup and decay schedulers without formulas (the "llm.c"
+    tour, detail graph); this is the plainest reading of "warmup then decay"."""
+    if step < warmup:
+        return max_lr * (step + 1) / warmup
+    min_lr = final_frac * max_lr
+    if step >= total:
+        return min_lr
+    ratio = (step - warmup) / (total - warmup)
+    return min_lr + 0.5 * (1.0 + math.cos(math.pi * ratio)) * (max_lr - min_lr)
+
 
 def adamw_update(p, g, m, v, lr, b1, b2, eps, wd, t):
     """One AdamW update of p, m, v in place (see GPT2.adamw_step)."""

@@ -273,6 +273,55 @@ def test_adamw_matches_torch_optim_over_steps():
 
 
 # ---------------------------------------------------------------------------
+# gradient-norm clipping and the learning-rate schedule
+# ---------------------------------------------------------------------------
+def test_grad_norm_and_clip_match_torch_clip_grad_norm():
+    """The oracle's global norm and clipping against torch.nn.utils.clip_grad_norm_
+    (an independent implementation of the same definition) on the tiny model's
+    real gradients, once clipping and once not."""
+    for max_norm in (0.05, 1e6):
+        m, tok, tgt = _tiny_model()
+        m.forward(tok, tgt)
+        m.backward()
+        ts = [torch.tensor(m.grads[n].copy()) for n in O.PARAM_NAMES]
+        ps = [torch.nn.Parameter(torch.zeros_like(t)) for t in ts]
+        for p, t in zip(ps, ts):
+            p.grad = t
+        tnorm = float(torch.nn.utils.clip_grad_norm_(ps, max_norm))
+        norm = m.clip_grad_norm(max_norm)
+        assert abs(norm - tnorm) <= 1e-12 * tnorm
+        for n, p in zip(O.PARAM_NAMES, ps):
+            assert np.allclose(m.grads[n], p.grad.numpy(), rtol=1e-12, atol=0), n
+        if max_norm < norm:
+            assert abs(m.grad_norm() - max_norm) < 1e-6 * max_norm  # clipped to the threshold
+
+
+def test_grad_norm_brute_force():
+    """Every gradient element squared and summed by a plain Python loop."""
+    m, tok, tgt = _tiny_model()
+    m.forward(tok, tgt)
+    m.backward()
+    total = 0.0
+    for g in m.grads.values():
+        for x in np.asarray(g, np.float64).reshape(-1).tolist():
+            total += x * x
+    assert abs(m.grad_norm() - math.sqrt(total)) < 1e-12 * math.sqrt(total)
+
+
+def test_lr_schedule_closed_forms():
+    lr, frac, W, N = 6e-4, 0.1, 10, 110
+    assert abs(O.lr_schedule(lr, frac, W, N, 0) - lr / W) < 1e-18
+    assert abs(O.lr_schedule(lr, frac, W, N, W - 1) - lr) < 1e-18          # warmup ends at max_lr
+    assert abs(O.lr_schedule(lr, frac, W, N, W) - lr) < 1e-18              # cosine starts at max_lr
+    mid = W + (N - W) // 2
+    assert abs(O.lr_schedule(lr, frac, W, N, mid) - (lr + frac * lr) / 2) < 1e-15  # halfway
+    assert abs(O.lr_schedule(lr, frac, W, N, N) - frac * lr) < 1e-18       # floor
+    assert abs(O.lr_schedule(lr, frac, W, N, N + 50) - frac * lr) < 1e-18
+    seq = [O.lr_schedule(lr, frac, W, N, s) for s in range(W, N + 1)]
+    assert all(a >= b for a, b in zip(seq, seq[1:]))                       # monotone decay
+
+
+# ---------------------------------------------------------------------------
 # whole model
 # ---------------------------------------------------------------------------
 def _tiny_model(dtype=np.float64, seed=1234):
