@@ -52,6 +52,9 @@ _sigs = {
     "gpt2_backward": (ctypes.c_int, [_P]),
     "gpt2_zero_grad": (ctypes.c_int, [_P]),
     "gpt2_adamw_step": (ctypes.c_int, [_P, _f, _f, _f, _f, _f, ctypes.c_int]),
+    "gpt2_clip_grad_norm": (ctypes.c_int, [_P, _f]),
+    "gpt2_get_grad_norm": (ctypes.c_int, [_P, _P]),
+    "gpt2_lr_schedule": (_f, [_f, _f, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "gpt2_step_host": (ctypes.c_int, [_P, _P, _P, _f, _f, _f, _f, _f, ctypes.c_int, _P]),
     "gpt2_get_params": (ctypes.c_int, [_P, ctypes.c_int, _P]),
     "gpt2_set_params": (ctypes.c_int, [_P, ctypes.c_int, _P]),
@@ -95,6 +98,10 @@ def make_config(L, C, H, V, Vp, max_T, B, T, precision=PRECISION_BF16):
 
 def num_parameters(cfg):
     return gpt2_num_parameters(ctypes.byref(cfg))
+
+
+def lr_schedule(max_lr, final_frac, warmup, total, step):
+    return float(gpt2_lr_schedule(max_lr, final_frac, warmup, total, step))
 
 
 def required_bytes(cfg):
@@ -149,6 +156,14 @@ class GPT2:
 
     def gpt2_adamw_step(self, lr, b1, b2, eps, wd, t):
         self._check(gpt2_adamw_step(self.h, lr, b1, b2, eps, wd, t))
+
+    def gpt2_clip_grad_norm(self, max_norm):
+        self._check(gpt2_clip_grad_norm(self.h, max_norm))
+
+    def gpt2_get_grad_norm(self):
+        out = np.zeros(1, np.float32)
+        self._check(gpt2_get_grad_norm(self.h, out.ctypes.data))
+        return float(out[0])
 
     def gpt2_step_host(self, tokens_host, targets_host, lr, b1, b2, eps, wd, t):
         loss = np.zeros(1, np.float32)

@@ -91,9 +91,14 @@ struct AdamSegments {
   long long off[GPT2_MAX_SEGS + 1];
   float wd[GPT2_MAX_SEGS];
 };
+// gscale (optional, device): every gradient is multiplied by *gscale first
 cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* pc, long long n, float lr,
                   float b1, float b2, float eps, float bc1, float bc2, const AdamSegments& seg,
-                  cudaStream_t st);
+                  const float* gscale, cudaStream_t st);
+// out2[0] = ||g||_2, out2[1] = min(1, max_norm / (norm + 1e-6)); partial:
+// grad_norm_scratch_floats() floats of scratch; deterministic
+cudaError_t grad_norm(const float* g, long long n, float max_norm, float* out2, float* partial, cudaStream_t st);
+size_t grad_norm_scratch_floats();
 cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream_t st);
 
 template <typename T>

@@ -1124,7 +1124,10 @@ cudaError_t mean_loss(float* loss, const float* losses, int n, cudaStream_t st) 
 // ============================================================================
 __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                              float* __restrict__ v, bf16* __restrict__ pc, long long nvec, float lr, float b1,
-                             float b2, float eps, float bc1, float bc2, AdamSegments seg) {
+                             float b2, float eps, float bc1, float bc2, AdamSegments seg,
+                             const float* __restrict__ gscale) {
+  // gscale (optional): the clip factor the gradient-norm kernels left on the device
+  const float gs = gscale ? *gscale : 1.f;
   long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
     long long e = i * 4;
@@ -1138,6 +1141,7 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
     ld16_cs(v + e, vv);
 #pragma unroll
     for (int k = 0; k < 4; k++) {
+      gv[k] *= gs;
       mv[k] = b1 * mv[k] + (1.f - b1) * gv[k];
       vv[k] = b2 * vv[k] + (1.f - b2) * gv[k] * gv[k];
       float mh = mv[k] / bc1, vh = vv[k] / bc2;
@@ -1158,7 +1162,7 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
 
 cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* pc, long long n, float lr,
                   float b1, float b2, float eps, float bc1, float bc2, const AdamSegments& seg,
-                  cudaStream_t st) {
+                  const float* gscale, cudaStream_t st) {
   if (n % 4) return cudaErrorInvalidValue;
   long long nvec = n / 4;
   int dev = 0, sms = 148;
@@ -1166,8 +1170,65 @@ cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* pc, long l
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   long long blocks = cdiv(nvec, 256);
   if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-  adamw_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, g, m, v, pc, nvec, lr, b1, b2, eps, bc1, bc2, seg);
+  adamw_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, g, m, v, pc, nvec, lr, b1, b2, eps, bc1, bc2, seg, gscale);
   return launch_status(1);
+}
+
+// ============================================================================
+// global gradient norm (the pages' global_norm component) and the clip factor
+// min(1, max_norm / (norm + 1e-6)): GN_CHUNKS fixed chunks of the vector (the
+// partition does not depend on the GPU), each summed by one block in a fixed
+// order, then one block adds the chunk sums in order, in double.
+// ============================================================================
+constexpr int GN_CHUNKS = 1024;
+size_t grad_norm_scratch_floats() { return GN_CHUNKS; }
+
+__global__ void __launch_bounds__(256) grad_sq_partial_kernel(const float* __restrict__ g, long long n,
+                                                              long long chunk, float* __restrict__ partial) {
+  __shared__ float red[32];
+  const long long b0 = (long long)blockIdx.x * chunk, b1 = min(n, b0 + chunk);
+  float s = 0.f;
+  for (long long i = b0 + 4LL * threadIdx.x; i < b1; i += 4LL * blockDim.x) {
+    if (i + 4 <= b1) {
+      float x[4];
+      ld16_cs(g + i, x);
+      s = fmaf(x[0], x[0], s);
+      s = fmaf(x[1], x[1], s);
+      s = fmaf(x[2], x[2], s);
+      s = fmaf(x[3], x[3], s);
+    } else {
+      for (long long j = i; j < b1; j++) s = fmaf(g[j], g[j], s);
+    }
+  }
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = s;
+}
+
+__global__ void __launch_bounds__(256) grad_norm_finalize_kernel(const float* __restrict__ partial, float max_norm,
+                                                                 float* __restrict__ out) {
+  __shared__ double red[256];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < GN_CHUNKS; i += 256) s += (double)partial[i];  // 4 per thread, in order
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {  // fixed tree
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double norm = sqrt(red[0]);
+    out[0] = (float)norm;
+    const double coef = (double)max_norm / (norm + 1e-6);
+    out[1] = coef < 1.0 ? (float)coef : 1.f;
+  }
+}
+
+cudaError_t grad_norm(const float* g, long long n, float max_norm, float* out2, float* partial, cudaStream_t st) {
+  if (n < 0 || (n > 0 && ((uintptr_t)g & 15))) return cudaErrorInvalidValue;
+  const long long chunk = ((cdiv(n, GN_CHUNKS) + 3) / 4) * 4;  // chunks start 16-byte aligned
+  grad_sq_partial_kernel<<<GN_CHUNKS, 256, 0, st>>>(g, n, chunk > 0 ? chunk : 4, partial);
+  grad_norm_finalize_kernel<<<1, 256, 0, st>>>(partial, max_norm, out2);
+  return launch_status(2);
 }
 
 __global__ void convert_f32_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ in, long long n) {

@@ -33,6 +33,7 @@ struct gpt2 {
   bool logits_valid = false;   // last forward kept the logits
   bool loss_valid = false;
   const int32_t* fwd_tokens = nullptr;
+  bool clip_pending = false;   // gpt2_clip_grad_norm ran since the last AdamW step
   std::string err;
   // GEMM event trace (roofline measurement)
   bool prof_on = false;
@@ -133,6 +134,7 @@ BufferLayout buffer_layout(const gpt2_config& c) {
       b.ws_floats = std::max(b.ws_floats, gemm_tc_workspace_floats(sh[0], sh[1], iBT, GPT2_NOMINAL_SMS));
   }
   b.ws = take(std::max<size_t>(b.ws_floats, 1) * sizeof(float));
+  b.gnorm = take((2 + grad_norm_scratch_floats()) * sizeof(float));  // norm, clip factor, chunk sums
   b.flags = take(256);
   b.tok = take(BT * 4);
   b.tgt = take(BT * 4);
@@ -425,9 +427,35 @@ int gpt2_adamw_step(gpt2* m, float lr, float b1, float b2, float eps, float wd, 
   float bc1 = (float)(1.0 - std::pow((double)b1, (double)t));
   float bc2 = (float)(1.0 - std::pow((double)b2, (double)t));
   bf16* pc = m->cfg.precision == GPT2_PRECISION_BF16 ? m->at<bf16>(m->bl.pbf) : nullptr;
+  const float* gscale = m->clip_pending ? m->at<float>(m->bl.gnorm) + 1 : nullptr;
+  m->clip_pending = false;
   CK(m, adamw(m->at<float>(m->bl.params), m->at<float>(m->bl.grads), m->at<float>(m->bl.m), m->at<float>(m->bl.v),
-              pc, (long long)m->pl.total, lr, b1, b2, eps, bc1, bc2, seg, m->st));
+              pc, (long long)m->pl.total, lr, b1, b2, eps, bc1, bc2, seg, gscale, m->st));
   return GPT2_OK;
+}
+
+int gpt2_clip_grad_norm(gpt2* m, float max_norm) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!(max_norm > 0.f)) FAIL(m, GPT2_ERR_INVALID_ARG, "max_norm must be > 0");
+  float* gn = m->at<float>(m->bl.gnorm);
+  CK(m, grad_norm(m->at<float>(m->bl.grads), (long long)m->pl.total, max_norm, gn, gn + 2, m->st));
+  m->clip_pending = true;
+  return GPT2_OK;
+}
+
+int gpt2_get_grad_norm(gpt2* m, float* norm_host) {
+  if (!m || !norm_host) return GPT2_ERR_INVALID_ARG;
+  CK(m, cudaMemcpyAsync(norm_host, m->at<float>(m->bl.gnorm), sizeof(float), cudaMemcpyDeviceToHost, m->st));
+  CK(m, cudaStreamSynchronize(m->st));
+  return GPT2_OK;
+}
+
+float gpt2_lr_schedule(float max_lr, float final_frac, int warmup, int total, int step) {
+  if (step < warmup) return max_lr * (float)(step + 1) / (float)warmup;
+  const double min_lr = (double)final_frac * max_lr;
+  if (step >= total) return (float)min_lr;
+  const double ratio = (double)(step - warmup) / (double)(total - warmup);
+  return (float)(min_lr + 0.5 * (1.0 + std::cos(3.141592653589793 * ratio)) * ((double)max_lr - min_lr));
 }
 
 int gpt2_step_host(gpt2* m, const int32_t* tokens_host, const int32_t* targets_host, float lr, float b1, float b2,

@@ -138,7 +138,7 @@ int gpt2_op_softmax_crossentropy(int dtype, void* logits, float* losses, const i
 }
 
 int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* p_bf16, long long n, float lr, float b1,
-                  float b2, float eps, float wd, int t, void* stream) {
+                  float b2, float eps, float wd, int t, const float* gscale_dev, void* stream) {
   if (!p || !g || !m || !v || n <= 0 || n % 4 || t < 1) return GPT2_ERR_INVALID_ARG;
   AdamSegments seg{};
   seg.n = 1;
@@ -147,7 +147,16 @@ int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* p_bf16, lo
   seg.wd[0] = wd;
   float bc1 = (float)(1.0 - std::pow((double)b1, (double)t));
   float bc2 = (float)(1.0 - std::pow((double)b2, (double)t));
-  return rc_of(adamw(p, g, m, v, (bf16*)p_bf16, n, lr, b1, b2, eps, bc1, bc2, seg, ST(stream)));
+  return rc_of(adamw(p, g, m, v, (bf16*)p_bf16, n, lr, b1, b2, eps, bc1, bc2, seg, gscale_dev, ST(stream)));
+}
+
+size_t gpt2_op_grad_norm_scratch_bytes(void) { return grad_norm_scratch_floats() * sizeof(float); }
+
+int gpt2_op_grad_norm(const float* g, long long n, float max_norm, float* out2_dev, void* scratch,
+                      size_t scratch_bytes, void* stream) {
+  if (!g || !out2_dev || !scratch || n <= 0 || !(max_norm > 0.f) || !aligned16(g)) return GPT2_ERR_INVALID_ARG;
+  if (scratch_bytes < gpt2_op_grad_norm_scratch_bytes()) return GPT2_ERR_INVALID_ARG;
+  return rc_of(grad_norm(g, n, max_norm, out2_dev, (float*)scratch, ST(stream)));
 }
 
 int gpt2_op_gelu_forward(int dtype, void* out, const void* in, long long n, void* stream) {

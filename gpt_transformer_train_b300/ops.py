@@ -27,7 +27,9 @@ _sigs = {
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P, _sz, _P]),
     "gpt2_op_softmax_crossentropy": (_i, [_i, _P, _P, _P, _i, _i, _i, _f, _i, _P, _P]),
-    "gpt2_op_adamw": (_i, [_P, _P, _P, _P, _P, _ll, _f, _f, _f, _f, _f, _i, _P]),
+    "gpt2_op_adamw": (_i, [_P, _P, _P, _P, _P, _ll, _f, _f, _f, _f, _f, _i, _P, _P]),
+    "gpt2_op_grad_norm_scratch_bytes": (_sz, []),
+    "gpt2_op_grad_norm": (_i, [_P, _ll, _f, _P, _P, _sz, _P]),
     "gpt2_op_gelu_forward": (_i, [_i, _P, _P, _ll, _P]),
     "gpt2_op_gelu_backward": (_i, [_i, _P, _P, _P, _ll, _P]),
     "gpt2_op_colsum_scratch_bytes": (_sz, [_i, _i]),
@@ -134,9 +136,15 @@ def gpt2_op_softmax_crossentropy(logits, losses, targets, rows, V, Vp, dloss, wr
                                          write_grad, _p(flags_dev), _s(stream)), "softmax_crossentropy")
 
 
-def gpt2_op_adamw(p, g, m, v, p_bf16, lr, b1, b2, eps, wd, t, stream=None):
-    _ck(lib.gpt2_op_adamw(_p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel(), lr, b1, b2, eps, wd, t, _s(stream)),
-        "adamw")
+def gpt2_op_adamw(p, g, m, v, p_bf16, lr, b1, b2, eps, wd, t, gscale=None, stream=None):
+    _ck(lib.gpt2_op_adamw(_p(p), _p(g), _p(m), _p(v), _p(p_bf16), p.numel(), lr, b1, b2, eps, wd, t, _p(gscale),
+                          _s(stream)), "adamw")
+
+
+def gpt2_op_grad_norm(g, max_norm, out2, stream=None):
+    """out2[0] = ||g||, out2[1] = clip factor min(1, max_norm / (norm + 1e-6))."""
+    sc = _scratch(lib.gpt2_op_grad_norm_scratch_bytes(), g.device)
+    _ck(lib.gpt2_op_grad_norm(_p(g), g.numel(), max_norm, _p(out2), _p(sc), sc.numel(), _s(stream)), "grad_norm")
 
 
 def gpt2_op_gelu_forward(out, inp, stream=None):

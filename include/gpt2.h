@@ -112,6 +112,22 @@ int gpt2_zero_grad(gpt2* m);
  * (wte, wpe, qkvw, attprojw, fcw, fcprojw) only.  Refreshes the bf16 copy. */
 int gpt2_adamw_step(gpt2* m, float lr, float b1, float b2, float eps, float wd, int t);
 
+/* Gradient-norm clipping, the step before AdamW (the llm.c tour names a
+ * global_norm component and LR warmup/decay schedulers; no formulas are given,
+ * the plainest readings are taken).  gpt2_clip_grad_norm enqueues the global L2
+ * norm of the whole gradient buffer and the factor min(1, max_norm /
+ * (norm + 1e-6)); the next gpt2_adamw_step multiplies every gradient by that
+ * factor (on the device, no synchronisation), later steps do not unless this
+ * is called again.  max_norm > 0.  gpt2_get_grad_norm synchronises and returns
+ * the norm (before clipping) of the last gpt2_clip_grad_norm. */
+int gpt2_clip_grad_norm(gpt2* m, float max_norm);
+int gpt2_get_grad_norm(gpt2* m, float* norm_host);
+
+/* Learning rate at 0-based step: linear warmup to max_lr over `warmup` steps
+ * (step s gets max_lr (s+1)/warmup), then a cosine from max_lr down to
+ * final_frac * max_lr at step `total`, and that floor afterwards.  Host only. */
+float gpt2_lr_schedule(float max_lr, float final_frac, int warmup, int total, int step);
+
 /* One whole step from HOST token arrays (pinned or pageable int32 [B][T]):
  * upload, forward with loss, backward (grads are zeroed first), AdamW at step
  * t, and read the mean loss back into *loss_host (synchronises). */

@@ -129,9 +129,20 @@ int gpt2_op_softmax_crossentropy(int dtype, void* logits, float* losses, const i
                                  int Vp, float dloss, int write_grad, int* flags_dev, void* stream);
 
 /* AdamW on n floats (n % 4 == 0), bias-corrected at step t >= 1, decay wd;
- * p_bf16 (optional) receives the updated parameters rounded to bf16. */
+ * p_bf16 (optional) receives the updated parameters rounded to bf16;
+ * gscale_dev (optional, one device float): every gradient is multiplied by it
+ * first (the clip factor gpt2_op_grad_norm leaves in out2_dev[1]). */
 int gpt2_op_adamw(float* p, const float* g, float* m, float* v, void* p_bf16, long long n, float lr, float b1,
-                  float b2, float eps, float wd, int t, void* stream);
+                  float b2, float eps, float wd, int t, const float* gscale_dev, void* stream);
+
+/* Global gradient norm and clip factor (the llm.c tour's global_norm component;
+ * the pages give no formula, the plainest reading is taken):
+ * out2_dev[0] = sqrt(sum_i g_i^2), out2_dev[1] = min(1, max_norm / (norm + 1e-6)).
+ * g 16-byte aligned, n > 0, max_norm > 0; scratch of gpt2_op_grad_norm_scratch_bytes()
+ * bytes.  The sum runs over fixed chunks in a fixed order: deterministic. */
+size_t gpt2_op_grad_norm_scratch_bytes(void);
+int gpt2_op_grad_norm(const float* g, long long n, float max_norm, float* out2_dev, void* scratch,
+                      size_t scratch_bytes, void* stream);
 
 /* tanh-form GELU forward / backward (dinp = dout * GELU'(inp)) over n elements. */
 int gpt2_op_gelu_forward(int dtype, void* out, const void* in, long long n, void* stream);

@@ -113,3 +113,11 @@ def test_host_init_is_bit_equal_to_oracle_init(g, cfgargs, seed):
     ref = O.flatten(O.init_params(O.Config(L, C, H, V, Vp, maxT), seed), O.Config(L, C, H, V, Vp, maxT))
     assert lib_init.dtype == np.float32 and ref.dtype == np.float32
     assert np.array_equal(lib_init.view(np.uint32), ref.view(np.uint32))
+
+
+def test_lr_schedule_matches_oracle(g):
+    """gpt2_lr_schedule (host function of the library) against the oracle's schedule."""
+    for step in list(range(0, 30)) + [55, 60, 99, 100, 101, 500]:
+        mine = g.lr_schedule(6e-4, 0.1, 10, 100, step)
+        ref = O.lr_schedule(6e-4, 0.1, 10, 100, step)
+        assert abs(mine - ref) <= 1e-6 * ref, (step, mine, ref)

@@ -471,6 +471,38 @@ def test_adamw(ops, t):
     assert torch.equal(pb, tp.to(torch.bfloat16))
 
 
+@pytest.mark.parametrize("n", [5, 4 * 1001 + 3, 124475904])
+def test_grad_norm_and_clip_factor(ops, n):
+    """Global norm against a float64 sum; clip factor min(1, max/(norm+1e-6));
+    bitwise repeatable (fixed chunks, fixed order).  n = 124475904 is the 124M
+    parameter count."""
+    g = normal_array((n,), 80, 1e-3) if n < 10**7 else None
+    tg = dev(g) if g is not None else torch.randn(n, device="cuda", generator=torch.Generator("cuda").manual_seed(5)) * 1e-3
+    ref = float(np.sqrt(np.sum(host(tg) ** 2)))
+    for max_norm in (ref / 4, ref * 4):
+        out = torch.zeros(2, device="cuda")
+        ops.gpt2_op_grad_norm(tg, max_norm, out)
+        out2 = torch.zeros(2, device="cuda")
+        ops.gpt2_op_grad_norm(tg, max_norm, out2)
+        assert torch.equal(out, out2)
+        norm, scale = out.tolist()
+        assert abs(norm - ref) <= 1e-5 * ref
+        assert abs(scale - min(1.0, max_norm / (ref + 1e-6))) <= 2e-6
+
+
+def test_adamw_with_clip_factor(ops):
+    n = 4 * 1001
+    p, g = normal_array((n,), 81), normal_array((n,), 82, 1e-2)
+    m, v = normal_array((n,), 83, 1e-3), np.abs(normal_array((n,), 84, 1e-4))
+    tp, tg, tm, tv = dev(p), dev(g), dev(m), dev(v)
+    scale = torch.tensor([0.37], device="cuda")
+    ops.gpt2_op_adamw(tp, tg, tm, tv, None, 6e-4, 0.9, 0.95, 1e-8, 0.1, 3, gscale=scale)
+    rp, rm, rv = p.astype(np.float64), m.astype(np.float64), v.astype(np.float64)
+    O.adamw_update(rp, g.astype(np.float64) * np.float64(np.float32(0.37)), rm, rv, 6e-4, 0.9, 0.95, 1e-8, 0.1, 3)
+    assert rel_l2(host(tm), rm) < 1e-6 and rel_l2(host(tv), rv) < 1e-6
+    assert np.max(np.abs(host(tp) - rp)) < 1e-6
+
+
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 def test_gelu_standalone(ops, dt):

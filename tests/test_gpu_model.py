@@ -78,6 +78,41 @@ def test_fp32_tiny_forward_backward_adamw(g):
         assert rel_l2(mine, theirs) <= 1e-5, step
 
 
+def test_fp32_tiny_with_clipping_and_schedule(g):
+    """Gradient-norm clipping (active: max_norm below the norm) and the
+    warmup+cosine learning rate over 6 steps against the oracle."""
+    cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
+    for step in range(6):
+        lr = g.lr_schedule(1e-3, 0.1, 2, 6, step)
+        assert abs(lr - O.lr_schedule(1e-3, 0.1, 2, 6, step)) <= 1e-6 * lr
+        m.gpt2_zero_grad()
+        ref.zero_grad()
+        m.gpt2_forward(ttok, ttgt)
+        ref.forward(tok, tgt)
+        m.gpt2_backward()
+        ref.backward()
+        rnorm = ref.grad_norm()
+        max_norm = 0.5 * rnorm if step % 2 == 0 else 2.0 * rnorm  # clip on even steps only
+        m.gpt2_clip_grad_norm(max_norm)
+        ref.clip_grad_norm(max_norm)
+        assert abs(m.gpt2_get_grad_norm() - rnorm) <= 1e-5 * rnorm, step
+        m.gpt2_adamw_step(lr, 0.9, 0.999, 1e-8, 0.01, step + 1)
+        ref.adamw_step(lr, 0.9, 0.999, 1e-8, 0.01, step + 1)
+        mine = np.concatenate([m.gpt2_get_params(n) for n in g.TENSORS])
+        assert rel_l2(mine, O.flatten(ref.params, ref.cfg)) <= 1e-5, step
+    # without a new clip call the next update does not scale (factor is one-shot)
+    m.gpt2_zero_grad()
+    ref.zero_grad()
+    m.gpt2_forward(ttok, ttgt)
+    ref.forward(tok, tgt)
+    m.gpt2_backward()
+    ref.backward()
+    m.gpt2_adamw_step(1e-4, 0.9, 0.999, 1e-8, 0.01, 7)
+    ref.adamw_step(1e-4, 0.9, 0.999, 1e-8, 0.01, 7)
+    mine = np.concatenate([m.gpt2_get_params(n) for n in g.TENSORS])
+    assert rel_l2(mine, O.flatten(ref.params, ref.cfg)) <= 1e-5
+
+
 def test_fp32_deterministic(g):
     outs = []
     for _ in range(2):
