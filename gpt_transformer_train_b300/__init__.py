@@ -53,6 +53,7 @@ _sigs = {
     "gpt2_zero_grad": (ctypes.c_int, [_P]),
     "gpt2_adamw_step": (ctypes.c_int, [_P, _f, _f, _f, _f, _f, ctypes.c_int]),
     "gpt2_clip_grad_norm": (ctypes.c_int, [_P, _f]),
+    "gpt2_graph_step": (ctypes.c_int, [_P, _P, _P]),
     "gpt2_get_grad_norm": (ctypes.c_int, [_P, _P]),
     "gpt2_lr_schedule": (_f, [_f, _f, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "gpt2_step_host": (ctypes.c_int, [_P, _P, _P, _f, _f, _f, _f, _f, ctypes.c_int, _P]),
@@ -156,6 +157,9 @@ class GPT2:
 
     def gpt2_adamw_step(self, lr, b1, b2, eps, wd, t):
         self._check(gpt2_adamw_step(self.h, lr, b1, b2, eps, wd, t))
+
+    def gpt2_graph_step(self, tokens, targets):
+        self._check(gpt2_graph_step(self.h, _ptr(tokens), _ptr(targets)))
 
     def gpt2_clip_grad_norm(self, max_norm):
         self._check(gpt2_clip_grad_norm(self.h, max_norm))

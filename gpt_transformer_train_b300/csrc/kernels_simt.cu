@@ -17,7 +17,7 @@
 
 #include <atomic>
 static std::atomic<unsigned long long> g_launches{0};
-void gpt2_count_launches(int n) { g_launches += (unsigned long long)n; }
+void gpt2_count_launches(int n) { g_launches += (unsigned long long)(long long)n; }
 unsigned long long gpt2_total_launches() { return g_launches.load(); }
 // status of the kernels just enqueued; n = how many were launched
 static inline cudaError_t launch_status(int n) {

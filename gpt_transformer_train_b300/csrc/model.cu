@@ -34,6 +34,11 @@ struct gpt2 {
   bool loss_valid = false;
   const int32_t* fwd_tokens = nullptr;
   bool clip_pending = false;   // gpt2_clip_grad_norm ran since the last AdamW step
+  // captured zero_grad + forward + backward (gpt2_graph_step), for these token pointers
+  cudaGraphExec_t gexec = nullptr;
+  const int32_t* g_tok = nullptr;
+  const int32_t* g_tgt = nullptr;
+  unsigned long long g_launches = 0;  // kernels in the captured graph
   std::string err;
   // GEMM event trace (roofline measurement)
   bool prof_on = false;
@@ -467,12 +472,62 @@ int gpt2_step_host(gpt2* m, const int32_t* tokens_host, const int32_t* targets_h
   int32_t* tgt = m->at<int32_t>(m->bl.tgt);
   CK(m, cudaMemcpyAsync(tok, tokens_host, nb, cudaMemcpyHostToDevice, m->st));
   CK(m, cudaMemcpyAsync(tgt, targets_host, nb, cudaMemcpyHostToDevice, m->st));
-  int rc = gpt2_zero_grad(m);
-  if (!rc) rc = gpt2_forward(m, tok, tgt, nullptr);
-  if (!rc) rc = gpt2_backward(m);
+  int rc;
+  if (m->st) {  // the model's own token buffers never move: replay one captured graph
+    rc = gpt2_graph_step(m, tok, tgt);
+  } else {
+    rc = gpt2_zero_grad(m);
+    if (!rc) rc = gpt2_forward(m, tok, tgt, nullptr);
+    if (!rc) rc = gpt2_backward(m);
+  }
   if (!rc) rc = gpt2_adamw_step(m, lr, b1, b2, eps, wd, t);
   if (!rc) rc = gpt2_get_loss(m, loss_host);
   return rc;
+}
+
+int gpt2_graph_step(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_dev) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!tokens_dev || !targets_dev) FAIL(m, GPT2_ERR_INVALID_ARG, "tokens_dev and targets_dev are required");
+  if (!m->st) FAIL(m, GPT2_ERR_INVALID_ARG, "graph capture needs a created stream, not the legacy default one");
+  if (!m->gexec || m->g_tok != tokens_dev || m->g_tgt != targets_dev) {
+    if (m->gexec) {
+      cudaGraphExecDestroy(m->gexec);
+      m->gexec = nullptr;
+    }
+    const unsigned long long l0 = gpt2_total_launches();
+    const bool prof = m->prof_on;
+    m->prof_on = false;  // no event records inside the graph
+    CK(m, cudaStreamBeginCapture(m->st, cudaStreamCaptureModeThreadLocal));
+    int rc = gpt2_zero_grad(m);
+    if (!rc) rc = gpt2_forward(m, tokens_dev, targets_dev, nullptr);
+    if (!rc) rc = gpt2_backward(m);
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamEndCapture(m->st, &graph);
+    m->prof_on = prof;
+    if (rc) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (e != cudaSuccess) FAIL(m, GPT2_ERR_CUDA, "stream capture failed: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&m->gexec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+      m->gexec = nullptr;
+      FAIL(m, GPT2_ERR_CUDA, "graph instantiation failed: %s", cudaGetErrorString(e));
+    }
+    // the capture counted its launches once; replays count them again below
+    m->g_launches = gpt2_total_launches() - l0;
+    gpt2_count_launches(-(int)m->g_launches);
+    m->g_tok = tokens_dev;
+    m->g_tgt = targets_dev;
+  }
+  CK(m, cudaGraphLaunch(m->gexec, m->st));
+  gpt2_count_launches((int)m->g_launches);
+  m->have_targets = false;  // the backward in the graph consumed dlogits
+  m->logits_valid = false;
+  m->loss_valid = true;
+  m->fwd_tokens = tokens_dev;
+  return GPT2_OK;
 }
 
 int gpt2_get_loss(gpt2* m, float* loss_host) {
@@ -586,6 +641,7 @@ int gpt2_profile_read(gpt2* m, double* ms_total, uint64_t* launches, double* flo
 
 void gpt2_destroy(gpt2* m) {
   if (!m) return;
+  if (m->gexec) cudaGraphExecDestroy(m->gexec);
   for (auto& e : m->prof_ev) cudaEventDestroy(e);
   delete m;
 }

@@ -112,6 +112,16 @@ int gpt2_zero_grad(gpt2* m);
  * (wte, wpe, qkvw, attprojw, fcw, fcprojw) only.  Refreshes the bf16 copy. */
 int gpt2_adamw_step(gpt2* m, float lr, float b1, float b2, float eps, float wd, int t);
 
+/* zero_grad + forward (with targets) + backward as ONE captured CUDA graph.
+ * The first call captures the launches on the model's stream for these
+ * token/target device pointers and instantiates the graph; later calls with
+ * the same pointers replay it (one launch; the step's ~300 kernels run
+ * without host gaps).  New pointers recapture.  The contents of the token
+ * arrays are read at replay time.  Needs a created (non-default) stream;
+ * run AdamW (and clipping) after it as usual.  Equivalent to
+ * gpt2_zero_grad; gpt2_forward(tokens, targets, NULL); gpt2_backward. */
+int gpt2_graph_step(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_dev);
+
 /* Gradient-norm clipping, the step before AdamW (the llm.c tour names a
  * global_norm component and LR warmup/decay schedulers; no formulas are given,
  * the plainest readings are taken).  gpt2_clip_grad_norm enqueues the global L2
@@ -130,7 +140,9 @@ float gpt2_lr_schedule(float max_lr, float final_frac, int warmup, int total, in
 
 /* One whole step from HOST token arrays (pinned or pageable int32 [B][T]):
  * upload, forward with loss, backward (grads are zeroed first), AdamW at step
- * t, and read the mean loss back into *loss_host (synchronises). */
+ * t, and read the mean loss back into *loss_host (synchronises).  On a
+ * created stream the forward/backward part runs as gpt2_graph_step over the
+ * model's own token buffers. */
 int gpt2_step_host(gpt2* m, const int32_t* tokens_host, const int32_t* targets_host,
                    float lr, float b1, float b2, float eps, float wd, int t, float* loss_host);
 

@@ -167,6 +167,42 @@ def test_bf16_step_host_matches_device_calls(g):
     assert np.array_equal(m.gpt2_get_params("fcw"), m2.gpt2_get_params("fcw"))
 
 
+def test_graph_step_matches_direct_calls(g):
+    """gpt2_graph_step (captured zero_grad+forward+backward, replayed) gives the
+    same bits as the direct calls, and a replay reads the token arrays' current
+    contents."""
+    import torch
+    L, C, H, V, Vp, maxT, B, T = SMALL_BF16.values()
+    stream = torch.cuda.Stream()
+    outs = []
+    for use_graph in (False, True):
+        cfg = g.make_config(L, C, H, V, Vp, maxT, B, T, 1)
+        m = g.GPT2(cfg, 1234, stream=stream)
+        tok, tgt = zipf_tokens(B, T, V, 1234)
+        tok2, tgt2 = zipf_tokens(B, T, V, 99)
+        ttok, ttgt = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+        res = []
+        for step, (a, b) in enumerate([(tok, tgt), (tok2, tgt2), (tok, tgt)], start=1):
+            with torch.cuda.stream(stream):
+                ttok.copy_(torch.from_numpy(a))
+                ttgt.copy_(torch.from_numpy(b))
+            if use_graph:
+                m.gpt2_graph_step(ttok, ttgt)
+            else:
+                m.gpt2_zero_grad()
+                m.gpt2_forward(ttok, ttgt, want_loss=False)
+                m.gpt2_backward()
+            loss = m.gpt2_get_loss()
+            res.append((loss, np.concatenate([m.gpt2_get_grads(n) for n in g.TENSORS])))
+            m.gpt2_adamw_step(1e-3, 0.9, 0.95, 1e-8, 0.1, step)
+        outs.append(res)
+        m.close()
+    for (la, ga), (lb, gb) in zip(*outs):
+        assert la == lb
+        assert np.array_equal(ga.view(np.uint32), gb.view(np.uint32))
+    assert outs[1][0][0] != outs[1][1][0]  # the second batch really was different
+
+
 def test_error_paths_on_device(g):
     cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
     with pytest.raises(g.GPT2Error) as e:
