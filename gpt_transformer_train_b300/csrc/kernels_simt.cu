@@ -510,14 +510,26 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__
   float acc[1][N];
 #pragma unroll
   for (int k = 0; k < N; k++) acc[0][k] = 0.f;
-  const int r0 = blockIdx.y * RED_ROWS;
-  if (vi < nvec)
-    for (int r = r0 + warp; r < min(rows, r0 + RED_ROWS); r += 8) {
+  const int r0 = blockIdx.y * RED_ROWS, r1 = min(rows, r0 + RED_ROWS);
+  if (vi < nvec) {
+    // rows warp, warp+8, ... in order; four loads in flight, added in that order
+    int r = r0 + warp;
+    for (; r + 24 < r1; r += 32) {
+      float v[4][N];
+#pragma unroll
+      for (int u = 0; u < 4; u++) ld16_cs(X + (size_t)(r + 8 * u) * ldx + (size_t)vi * N, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+#pragma unroll
+        for (int k = 0; k < N; k++) acc[0][k] += v[u][k];
+    }
+    for (; r < r1; r += 8) {
       float v[N];
-      ld16(X + (size_t)r * ldx + (size_t)vi * N, v);
+      ld16_cs(X + (size_t)r * ldx + (size_t)vi * N, v);
 #pragma unroll
       for (int k = 0; k < N; k++) acc[0][k] += v[k];
     }
+  }
   // warp-ordered combine of this block's 32 vector columns
   for (int turn = 0; turn < 8; turn++) {
     if (warp == turn && vi < nvec)
