@@ -118,6 +118,7 @@ struct AttnParams {
   float sl2;          // softmax scale * log2(e)
   float scale;        // softmax scale
   int* flags;
+  uint8_t* ds;        // backward: dS blocks (see ds_block)
 };
 
 // ============================================================================
@@ -430,218 +431,165 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
 }
 
 // ============================================================================
-// backward, dQ (+ D = rowsum(dO * O)).  Persistent: items are (b, h, query
-// tile), heaviest first; per item the key tiles 0..qt stream through a ring.
+// backward.  D = rowsum(dO * O) first (attn_rowdot_kernel); then the dK/dV
+// kernel, which also writes every dS block it forms to global memory; then
+// the dQ kernel, a plain blocked product dQ = dS K over those blocks.
 // ============================================================================
-constexpr int DQ_STAGES = 5;             // K/V ring of the dQ kernel
 constexpr int DKV_STAGES = 3;            // Q/dO/lse/D ring of the dK/dV kernel
-constexpr int EW_WARPS = 8;              // elementwise warps of the backward kernels
+constexpr int EW_WARPS = 8;              // elementwise warps of the dK/dV kernel
 constexpr int EW_COLS = 128 / (EW_WARPS / 4);  // columns of S each elementwise warp handles
 constexpr int BWD_THREADS = 64 + 32 * EW_WARPS;
-constexpr uint32_t BWD_KV = 2 * TILE;
-constexpr size_t DQ_SMEM = 1024 + 2 * TILE + DQ_STAGES * BWD_KV + PTILE + 256;
+static_assert(EW_COLS == 64, "an elementwise warp's share of a dS block is one 32-row slice of one 64-wide half");
 
-__global__ void __launch_bounds__(BWD_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
-                          AttnParams p) {
+// D[b][h][t] = sum over the head's 64 channels of dO * O: one thread per 8
+// channels, the 8 threads of a head added by a fixed shuffle tree.
+__global__ void __launch_bounds__(256) attn_rowdot_kernel(float* D, const bf16* dout, const bf16* o, long long n8,
+                                                          int T, int C, int H) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  float acc = 0.f;
+  if (i < n8) {
+    float a[8], c[8];
+    ld16(dout + i * 8, a);
+    ld16(o + i * 8, c);
+#pragma unroll
+    for (int e = 0; e < 8; e++) acc = fmaf(a[e], c[e], acc);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  if (i < n8 && (i & 7) == 0) {
+    const long long row = i / (C / 8);
+    const int h = (int)(i % (C / 8)) / 8;
+    const long long b = row / T, t = row % T;
+    D[(b * H + h) * T + t] = acc;
+  }
+}
+
+// dS blocks in global memory: for each (b, h), the causal blocks (key tile
+// kt, query tile qt >= kt) in order of kt then qt, each the 32 KB shared-memory
+// image of the dS^T tile (two 64-query halves of 128 key rows, 128-byte
+// swizzled), so that a 1024-aligned bulk copy brings it back operand-ready.
+__host__ __device__ __forceinline__ long long ds_block(int bh, int nq, int kt, int qt) {
+  const long long per_bh = (long long)nq * (nq + 1) / 2;
+  return bh * per_bh + (long long)kt * nq - (long long)kt * (kt - 1) / 2 + (qt - kt);
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"((uint64_t)dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---- dQ = dS K: persistent, items (b, h, query tile) heaviest first; per
+// item the blocks kt = 0..qt stream through a ring (dS^T block + K tile) and
+// accumulate into one of two TMEM accumulators, so that one item's read-out
+// overlaps the next item's products.  Bandwidth-bound: 48 KB in per block
+// for 2*128*128*64 flops.
+constexpr int DQ_STAGES = 4;
+constexpr uint32_t DQ_STAGE = PTILE + TILE;  // dS^T block, K tile
+constexpr int DQ_THREADS = 64 + 32 * 4;      // producer, MMA, 4 read-out warps
+constexpr size_t DQ_SMEM = 1024 + DQ_STAGES * DQ_STAGE + 256;
+
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const uint8_t* __restrict__ ds, AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const uint32_t sQ = smem_u32(smem), sDO = sQ + TILE;
-  const uint32_t sKV = sQ + 2 * TILE;
-  const uint32_t sDS = sKV + DQ_STAGES * BWD_KV;
-  uint64_t* bars = (uint64_t*)(smem + 2 * TILE + DQ_STAGES * BWD_KV + PTILE);
-  const uint32_t b_qfull = smem_u32(bars), b_qempty = b_qfull + 8;  // Q and dO tiles of an item
-  const uint32_t b_kvfull = b_qempty + 8, b_kvempty = b_kvfull + 8 * DQ_STAGES;
-  const uint32_t b_sfull = b_kvempty + 8 * DQ_STAGES;  // S and dP in TMEM
-  const uint32_t b_sfree = b_sfull + 8;                 // ... read by all 8 warps
-  const uint32_t b_dsfull = b_sfree + 8;                // dS tile written
-  const uint32_t b_dsfree = b_dsfull + 8;               // dQ MMA done reading dS
-  const uint32_t b_dqfull = b_dsfree + 8;               // an item's dQ complete in TMEM
-  const uint32_t b_dqfree = b_dqfull + 8;               // ... and read out
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 + 2 * DQ_STAGES + 6);
+  const uint32_t ring = smem_u32(smem);
+  uint64_t* bars = (uint64_t*)(smem + DQ_STAGES * DQ_STAGE);
+  const uint32_t b_full = smem_u32(bars), b_empty = b_full + 8 * DQ_STAGES;
+  const uint32_t b_accfull = b_empty + 8 * DQ_STAGES;  // [2] an item's dQ complete in TMEM
+  const uint32_t b_accfree = b_accfull + 16;           // [2] ... and read out
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * DQ_STAGES + 4);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = p.T / 128, BH = p.B * p.H;
   const int n_items = BH * nq;
-  struct Item { int qt, b, h, row0; };
-  auto item = [&](int i) {
-    Item it;
-    it.qt = nq - 1 - i / BH;  // heaviest tiles first
-    const int bh = i % BH;
-    it.b = bh / p.H;
-    it.h = bh % p.H;
-    it.row0 = it.b * p.T;
-    return it;
-  };
+  auto item_qt = [&](int i) { return nq - 1 - i / BH; };  // heaviest tiles first
 
   if (threadIdx.x == 0) {
-    mbar_init(b_qfull, 1);
-    mbar_init(b_qempty, 1);
     for (int s = 0; s < DQ_STAGES; s++) {
-      mbar_init(b_kvfull + 8 * s, 1);
-      mbar_init(b_kvempty + 8 * s, 1);
+      mbar_init(b_full + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 1);
     }
-    mbar_init(b_sfull, 1);
-    mbar_init(b_sfree, EW_WARPS);
-    mbar_init(b_dsfull, EW_WARPS);
-    mbar_init(b_dsfree, 1);
-    mbar_init(b_dqfull, 1);
-    mbar_init(b_dqfree, EW_WARPS);
+    for (int a = 0; a < 2; a++) {
+      mbar_init(b_accfull + 8 * a, 1);
+      mbar_init(b_accfree + 8 * a, 4);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
-  if (warp == 0 && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tqkv) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tdo) : "memory");
-  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 128);
+  if (warp == 0 && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tqkv) : "memory");
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
-  // TMEM columns: S at 0, dP at 128, dQ at 256
+  // TMEM columns: dQ accumulator a at 64 a
 
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t g = 0, n = 0;
+      uint32_t g = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
-        const Item it = item(i);
-        if (!mbar_wait(b_qempty, (n & 1) ^ 1, abort_flag)) break;
-        mbar_expect_tx(b_qfull, 2 * TILE);
-        tma_load_2d(sQ, &tqkv, it.h * HD, it.row0 + it.qt * 128, b_qfull);
-        tma_load_2d(sDO, &tdo, it.h * HD, it.row0 + it.qt * 128, b_qfull);
-        for (int j = 0; j <= it.qt; j++, g++) {
+      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+        const int qt = item_qt(i), bh = i % BH, h = bh % p.H, row0 = (bh / p.H) * p.T;
+        for (int kt = 0; kt <= qt; kt++, g++) {
           const uint32_t s = g % DQ_STAGES, ph = (g / DQ_STAGES) & 1;
-          if (!mbar_wait(b_kvempty + 8 * s, ph ^ 1, abort_flag)) { ok = false; break; }
-          const uint32_t dst = sKV + s * BWD_KV, fb = b_kvfull + 8 * s;
-          mbar_expect_tx(fb, BWD_KV);
-          tma_load_2d(dst, &tqkv, p.C + it.h * HD, it.row0 + j * 128, fb);
-          tma_load_2d(dst + TILE, &tqkv, 2 * p.C + it.h * HD, it.row0 + j * 128, fb);
+          if (!mbar_wait(b_empty + 8 * s, ph ^ 1, abort_flag)) { ok = false; break; }
+          const uint32_t dst = ring + s * DQ_STAGE, fb = b_full + 8 * s;
+          mbar_expect_tx(fb, DQ_STAGE);
+          bulk_load(dst, ds + ds_block(bh, nq, kt, qt) * PTILE, PTILE, fb);
+          tma_load_2d(dst + PTILE, &tqkv, p.C + h * HD, row0 + kt * 128, fb);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);   // S = Q K^T, dP = dO V^T
-      constexpr uint32_t ID_DQ = idesc_bf16(128, HD, 0, 1);   // dQ += dS K (K is MN-major here)
-      uint32_t g0 = 0, n = 0, nS = 0, nD = 0;
+      // A = dS (M = 128 queries, MN-major: the dS^T tile's 64-query halves
+      // 16 KB apart, 16 key rows per step); B = K tile (N = 64, MN-major)
+      constexpr uint32_t ID_DQ = idesc_bf16(128, HD, 1, 1);
+      uint32_t g = 0, n = 0;
       bool ok = true;
-      // dQ += dS_j K_j for the item's block j (global K/V block g0 + j)
-      auto issue_dq = [&](int j) {
-        if (!mbar_wait(b_dsfull, nD & 1, abort_flag)) return false;
-        // the first dQ MMA of an item overwrites dQ: the previous item's must be read out
-        if (j == 0 && n > 0 && !mbar_wait(b_dqfree, (n - 1) & 1, abort_flag)) return false;
-        fence_after();
-        const uint32_t k = sKV + ((g0 + j) % DQ_STAGES) * BWD_KV;
-#pragma unroll
-        for (int kk = 0; kk < 128 / 16; kk++)
-          mma_bf16(tmem + 256, desc_k128(sDS, kk), desc_mn(k, kk), ID_DQ, (j | kk) > 0);
-        mma_commit(b_dsfree);
-        mma_commit(b_kvempty + 8 * ((g0 + j) % DQ_STAGES));
-        nD++;
-        return true;
-      };
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
-        const Item it = item(i);
-        const int nkv = it.qt + 1;
-        if (!mbar_wait(b_qfull, n & 1, abort_flag)) break;
-        for (int j = 0; ok && j < nkv; j++) {
-          const uint32_t gj = g0 + j, s = gj % DQ_STAGES;
-          if (!mbar_wait(b_kvfull + 8 * s, (gj / DQ_STAGES) & 1, abort_flag)) { ok = false; break; }
-          if (nS > 0 && !mbar_wait(b_sfree, (nS - 1) & 1, abort_flag)) { ok = false; break; }
+        const int qt = item_qt(i);
+        const uint32_t a = n & 1, acc = tmem + 64 * a;
+        if (!mbar_wait(b_accfree + 8 * a, ((n >> 1) & 1) ^ 1, abort_flag)) break;
+        fence_after();
+        for (int kt = 0; kt <= qt; kt++, g++) {
+          const uint32_t s = g % DQ_STAGES;
+          if (!mbar_wait(b_full + 8 * s, (g / DQ_STAGES) & 1, abort_flag)) { ok = false; break; }
           fence_after();
-          const uint32_t k = sKV + s * BWD_KV, v = k + TILE;
+          const uint32_t st = ring + s * DQ_STAGE;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; kk++) mma_bf16(tmem, desc_k(sQ, kk), desc_k(k, kk), ID_S, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; kk++) mma_bf16(tmem + 128, desc_k(sDO, kk), desc_k(v, kk), ID_S, kk > 0);
-          mma_commit(b_sfull);
-          nS++;
-          if (j == nkv - 1) mma_commit(b_qempty);  // the item's last use of Q and dO is issued
-          if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
+          for (int kk = 0; kk < 128 / 16; kk++)
+            mma_bf16(acc, sdesc(st + kk * 2048, TILE, 1024), desc_mn(st + PTILE, kk), ID_DQ, (kt | kk) > 0);
+          mma_commit(b_empty + 8 * s);
         }
-        if (ok && issue_dq(nkv - 1)) mma_commit(b_dqfull);
-        else ok = false;
-        g0 += nkv;
+        if (ok) mma_commit(b_accfull + 8 * a);
       }
     }
-  } else {  // ---- elementwise warps: lane quarter q, column group cq (EW_COLS columns)
-    const int q = warp & 3, cq = (warp - 2) >> 2;
-    const int c0 = cq * EW_COLS;
-    const uint32_t r = q * 32 + lane;
+  } else {  // ---- read-out warps: lane quarter q, rows q*32 .. q*32+31 of the item's query tile
+    const int q = warp & 3;
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
-    uint32_t n = 0, nS = 0, nD = 0;
-    bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
-      const Item it = item(i);
-      const int tq = it.qt * 128 + r;                  // query position in the sequence
-      const size_t grow = (size_t)(it.row0 + tq);
-      const size_t sidx = ((size_t)it.b * p.H + it.h) * p.T + tq;
-      // D = rowsum(dO * O) for this row (every column group computes it, group 0 stores it)
-      float Dr = 0.f;
-      {
-        const bf16* dor = p.dout + grow * p.C + it.h * HD;
-        const bf16* orow = p.o + grow * p.C + it.h * HD;
-#pragma unroll
-        for (int u = 0; u < HD / 8; u++) {
-          float a[8], c[8];
-          ld16(dor + 8 * u, a);
-          ld16(orow + 8 * u, c);
-#pragma unroll
-          for (int e = 0; e < 8; e++) Dr = fmaf(a[e], c[e], Dr);
-        }
-        if (cq == 0) p.D[sidx] = Dr;
-      }
-      const float lse2 = p.lse[sidx] * LOG2E;
-      for (int j = 0; j <= it.qt; j++) {
-        if (!mbar_wait_warp(b_sfull, nS & 1, abort_flag)) { ok = false; break; }
-        fence_after();
-        float sv[EW_COLS], dp[EW_COLS];
-#pragma unroll
-        for (int c = 0; c < EW_COLS / 32; c++) {
-          tmem_ld32_async(tmem + lrow + c0 + 32 * c, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
-          tmem_ld32_async(tmem + lrow + 128 + c0 + 32 * c, *reinterpret_cast<float(*)[32]>(dp + 32 * c));
-        }
-        tmem_wait_ld();
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_sfree);
-        nS++;
-        const bool diag = j == it.qt;
-#pragma unroll
-        for (int e = 0; e < EW_COLS; e++) {
-          const float x = fmaf(sv[e], p.sl2, -lse2);
-          sv[e] = (e & 3) == 3 ? exp2_poly(x) : ex2(x);
-        }
-        if (diag) {
-#pragma unroll
-          for (int e = 0; e < EW_COLS; e++)
-            if (c0 + e > (int)r) sv[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < EW_COLS; e++) sv[e] *= dp[e] - Dr;
-        // the dS tile is free once the previous dQ MMA has read it
-        if (nD > 0 && !mbar_wait_warp(b_dsfree, (nD - 1) & 1, abort_flag)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < EW_COLS / 32; c++)
-          store_row32(sDS, r, c0 + 32 * c, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_dsfull);
-        nD++;
-      }
-      if (!ok || !mbar_wait_warp(b_dqfull, n & 1, abort_flag)) break;
+    uint32_t n = 0;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x, n++) {
+      const int qt = item_qt(i), bh = i % BH, h = bh % p.H, row0 = (bh / p.H) * p.T;
+      const uint32_t a = n & 1;
+      if (!mbar_wait_warp(b_accfull + 8 * a, (n >> 1) & 1, abort_flag)) break;
       fence_after();
-      // dQ has 64 columns: the first two column groups take 32 each
-      constexpr int DQ_GROUPS = EW_WARPS / 4 < 2 ? EW_WARPS / 4 : 2;
-      float v[32];
-      if (cq < DQ_GROUPS) tmem_ld32(tmem + lrow + 256 + 32 * cq, v);
+      float v0[32], v1[32];
+      tmem_ld32_async(tmem + lrow + 64 * a, v0);
+      tmem_ld32_async(tmem + lrow + 64 * a + 32, v1);
+      tmem_wait_ld();
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_dqfree);
-      if (cq < DQ_GROUPS) store_global32(p.out + grow * 3 * p.C + it.h * HD + 32 * cq, v, p.scale);
+      if (lane == 0) mbar_arrive(b_accfree + 8 * a);
+      bf16* dst = p.out + (size_t)(row0 + qt * 128 + q * 32 + lane) * 3 * p.C + h * HD;
+      store_global32(dst, v0, p.scale);
+      store_global32(dst + 32, v1, p.scale);
     }
   }
   fence_before();
@@ -649,7 +597,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 128);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.flags, FLAG_TIMEOUT);
 }
@@ -657,7 +605,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // ============================================================================
 // backward, dK and dV.  Persistent: items are (b, h, key tile), heaviest
 // first; per item the query tiles kt..nq-1 stream through a ring (Q, dO and
-// their lse and D).  Needs D from the dQ kernel.
+// their lse and D).  Needs D from attn_rowdot_kernel; writes each dS^T tile
+// it forms to the dS block buffer for the dQ kernel (each elementwise warp
+// bulk-copies its own 4 KB slice: 32 key rows of one 64-query half).
 // ============================================================================
 constexpr uint32_t BWD_QD = 2 * TILE + 1024;  // Q tile, dO tile, lse[128], D[128]
 constexpr size_t DKV_SMEM = 1024 + 2 * TILE + DKV_STAGES * BWD_QD + 2 * PTILE + 256;
@@ -687,11 +637,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = p.T / 128, BH = p.B * p.H;
   const int n_items = BH * nq;
-  struct Item { int kt, nit, b, h, row0; size_t sbase; };
+  struct Item { int kt, nit, bh, b, h, row0; size_t sbase; };
   auto item = [&](int i) {
     Item it;
     it.kt = i / BH;  // key tile; small kt = more query tiles = heavier, first
     const int bh = i % BH;
+    it.bh = bh;
     it.b = bh / p.H;
     it.h = bh % p.H;
     it.row0 = it.b * p.T;
@@ -837,6 +788,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < EW_COLS; e++) dp[e] = sv[e] * (dp[e] - dq[e]);
         if (nG > 0 && !mbar_wait_warp(b_pfree, (nG - 1) & 1, abort_flag)) { ok = false; break; }
+        // ... and this warp's copy of its previous dS^T slice has read it
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < EW_COLS / 32; c++) {
           store_row32(sPT, r, c0 + 32 * c, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
@@ -844,7 +798,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(b_pfull);
+        if (lane == 0) {
+          mbar_arrive(b_pfull);
+          const uint32_t slice = (uint32_t)cq * TILE + (uint32_t)q * 32 * 128;
+          bulk_store(p.ds + ds_block(it.bh, nq, it.kt, it.kt + k) * PTILE + slice, sDST + slice, 32 * 128);
+        }
         nG++;
       }
       if (!ok || !mbar_wait_warp(b_accfull, n & 1, abort_flag)) break;
@@ -871,6 +829,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       g0 += it.nit;
     }
+    if (lane == 0) bulk_wait_all();
   }
   fence_before();
   __syncthreads();
@@ -916,11 +875,18 @@ cudaError_t attention_forward_tc(bf16* out, float* lse, const bf16* qkv, int B, 
   return cudaGetLastError();
 }
 
-cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, const bf16* dout, const bf16* qkv, const bf16* out,
-                                  const float* lse, int B, int T, int C, int H, int* flags, cudaStream_t st) {
+size_t attention_tc_ds_bytes(int B, int T, int H) {
+  if (B <= 0 || T <= 0 || H <= 0 || T % 128) return 0;
+  const long long nq = T / 128;
+  return (size_t)((long long)B * H * nq * (nq + 1) / 2) * PTILE;
+}
+
+cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16* dout, const bf16* qkv,
+                                  const bf16* out, const float* lse, int B, int T, int C, int H, int* flags,
+                                  cudaStream_t st) {
   if (!attention_tc_supported(B, T, C, H) || !flags) return cudaErrorNotSupported;
   if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15) ||
-      ((uintptr_t)lse & 15) || ((uintptr_t)Dbuf & 15))
+      ((uintptr_t)lse & 15) || ((uintptr_t)Dbuf & 15) || !dS || ((uintptr_t)dS & 15))
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
@@ -934,14 +900,18 @@ cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, const bf16* dout, con
       !tc_make_map(&td, dout, (uint64_t)C, (uint64_t)B * T, (uint64_t)C, HD, 128))
     return cudaErrorInvalidValue;
   AttnParams p{dqkv, const_cast<float*>(lse), Dbuf, out, dout, B, T, C, H, LOG2E / sqrtf((float)HD),
-               1.f / sqrtf((float)HD), flags};
+               1.f / sqrtf((float)HD), flags, (uint8_t*)dS};
   const long long items = (long long)B * H * (T / 128);
   const int sms = tc_num_sms();
   const unsigned grid = (unsigned)(items < sms ? items : sms);
-  gpt2_count_launches(2);
-  attn_bwd_dq_tc_kernel<<<grid, BWD_THREADS, DQ_SMEM, st>>>(tq, td, p);
+  const long long n8 = (long long)B * T * C / 8;
+  gpt2_count_launches(3);
+  attn_rowdot_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(Dbuf, dout, out, n8, T, C, H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_bwd_dkv_tc_kernel<<<grid, BWD_THREADS, DKV_SMEM, st>>>(tq, td, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_bwd_dq_tc_kernel<<<grid, DQ_THREADS, DQ_SMEM, st>>>(tq, (const uint8_t*)dS, p);
   return cudaGetLastError();
 }

@@ -73,13 +73,17 @@ template <typename T>
 cudaError_t attention_backward_simt(T* dqkv, float* Dbuf, const T* dout, const T* qkv, const T* out,
                                     const float* lse, int B, int T_, int C, int H, cudaStream_t st);
 
-// tcgen05 flash attention (bf16, head size 64, T % 128 == 0); backward
-// writes D = rowsum(dO * O) into Dbuf [B][H][T] on the way
+// tcgen05 flash attention (bf16, head size 64, T % 128 == 0).  The backward
+// writes D = rowsum(dO * O) into Dbuf [B][H][T] and passes the bf16 dS blocks
+// of the causal triangle from its dK/dV kernel to its dQ kernel through dS
+// (attention_tc_ds_bytes(B, T, H) bytes, 16-byte aligned; 0 when T % 128).
 bool attention_tc_supported(int B, int T, int C, int H);
+size_t attention_tc_ds_bytes(int B, int T, int H);
 cudaError_t attention_forward_tc(bf16* out, float* lse, const bf16* qkv, int B, int T, int C, int H, int* flags,
                                  cudaStream_t st);
-cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, const bf16* dout, const bf16* qkv, const bf16* out,
-                                  const float* lse, int B, int T, int C, int H, int* flags, cudaStream_t st);
+cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16* dout, const bf16* qkv,
+                                  const bf16* out, const float* lse, int B, int T, int C, int H, int* flags,
+                                  cudaStream_t st);
 
 template <typename T>
 cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,

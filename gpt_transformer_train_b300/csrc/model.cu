@@ -127,6 +127,9 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.dbig = take(BT * 4 * C * es);
   b.dsmall = take(BT * C * es);
   b.attD = take(BT * c.H * 4);
+  // dS blocks of the tensor-core attention backward (by shape alone, so the
+  // size does not depend on the machine the layout is computed on)
+  b.attS = c.precision == GPT2_PRECISION_BF16 && c.C == 64 * c.H ? take(attention_tc_ds_bytes(c.B, c.T, c.H)) : 0;
   b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), colsum_partial_floats((int)BT, 4 * (int)C)) *
                    sizeof(float));
   b.keys = take(encoder_backward_scratch_bytes((int)BT));
@@ -227,8 +230,8 @@ struct Step {
   cudaError_t attention_bwd(T* dqkv, const T* dout, const T* qkv_, const T* out, const float* lse_) {
     float* Dbuf = m->at<float>(m->bl.attD);
     if (attention_on_tc())
-      return attention_backward_tc((bf16*)dqkv, Dbuf, (const bf16*)dout, (const bf16*)qkv_, (const bf16*)out, lse_,
-                                   c.B, c.T, c.C, c.H, flags(), m->st);
+      return attention_backward_tc((bf16*)dqkv, Dbuf, m->at<uint8_t>(m->bl.attS), (const bf16*)dout,
+                                   (const bf16*)qkv_, (const bf16*)out, lse_, c.B, c.T, c.C, c.H, flags(), m->st);
     return attention_backward_simt<T>(dqkv, Dbuf, dout, qkv_, out, lse_, c.B, c.T, c.C, c.H, m->st);
   }
 

@@ -46,7 +46,7 @@ struct BufferLayout {
   size_t qkv, atty, lse, fch, fchg;         // per layer
   size_t proj, logits, losses, loss;        // temporaries / classifier
   size_t dres, dres_c, dbig, dsmall;        // activation gradients
-  size_t attD, partial, keys, ws, ws_floats, gnorm, flags, tok, tgt;
+  size_t attD, attS, partial, keys, ws, ws_floats, gnorm, flags, tok, tgt;
   size_t total;
 };
 

@@ -103,9 +103,12 @@ int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv,
   return rc_of(attention_forward_simt<float>((float*)out, lse, (const float*)qkv, B, T, C, H, ST(stream)));
 }
 
+// D [B][H][T] fp32, padded to 1 KB, then (T % 128 == 0) the dS block buffer
+// of the tensor-core backward
+static size_t attn_d_bytes(int B, int T, int H) { return ((size_t)B * T * H * sizeof(float) + 1023) & ~(size_t)1023; }
 size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H) {
   if (B <= 0 || T <= 0 || H <= 0) return 0;
-  return (size_t)B * T * H * sizeof(float);
+  return attn_d_bytes(B, T, H) + attention_tc_ds_bytes(B, T, H);
 }
 
 int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* out,
@@ -119,8 +122,9 @@ int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const vo
   const bool tc = dtype == GPT2_PRECISION_BF16 && flags_dev && attention_tc_supported(B, T, C, H);
   if (path == 2 && !tc) return GPT2_ERR_INVALID_ARG;
   if (tc && path != 1)
-    return rc_of(attention_backward_tc((bf16*)dqkv, (float*)scratch, (const bf16*)dout, (const bf16*)qkv,
-                                       (const bf16*)out, lse, B, T, C, H, flags_dev, ST(stream)));
+    return rc_of(attention_backward_tc((bf16*)dqkv, (float*)scratch, (uint8_t*)scratch + attn_d_bytes(B, T, H),
+                                       (const bf16*)dout, (const bf16*)qkv, (const bf16*)out, lse, B, T, C, H,
+                                       flags_dev, ST(stream)));
   if (dtype == GPT2_PRECISION_BF16)
     return rc_of(attention_backward_simt<bf16>((bf16*)dqkv, (float*)scratch, (const bf16*)dout, (const bf16*)qkv,
                                                (const bf16*)out, lse, B, T, C, H, ST(stream)));

@@ -112,7 +112,7 @@ def make_case(name, ops):
         ops.gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, path=ops.PATH_TC, flags_dev=fl)
         dout = randn((BT, C), 21)
         dqkv = torch.empty(BT, 3 * C, device="cuda", dtype=BF)
-        D = torch.empty(B * H * T, device="cuda")
+        D = torch.empty(ops.lib.gpt2_op_attention_backward_scratch_bytes(B, T, H), device="cuda", dtype=torch.uint8)
         # backward: dV, dP, dQ, dK plus the S recompute = 2.5x the forward's matmuls
         return (lambda: ops.gpt2_op_attention_backward(dqkv, dout, qkv, out, lse, B, T, C, H, path=ops.PATH_TC,
                                                        flags_dev=fl, scratch=D),

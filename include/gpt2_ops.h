@@ -116,8 +116,11 @@ int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv,
                               int path, int* flags_dev, void* stream);
 /* dqkv [B*T][3C] from dout [B*T][C] with P recomputed from lse:
  * D = rowsum(dO*O), dS = P*(dO.V^T - D), dQ = dS K/sqrt(hd), dK = dS^T Q/sqrt(hd),
- * dV = P^T dO.  scratch receives D as float [B][H][T]; no atomics, so the result
- * is deterministic.  path and flags_dev as for the forward. */
+ * dV = P^T dO.  scratch (16-byte aligned) receives D as float [B][H][T] at its
+ * start and, when T % 128 == 0, the bf16 dS blocks of the causal triangle that
+ * the tensor-core dK/dV kernel hands to its dQ kernel (B*H*n(n+1)/2 blocks of
+ * 32 KB, n = T/128) after it; no atomics, so the result is deterministic.
+ * path and flags_dev as for the forward. */
 size_t gpt2_op_attention_backward_scratch_bytes(int B, int T, int H);
 int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const void* qkv, const void* out,
                                const float* lse, int B, int T, int C, int H, int path, int* flags_dev,

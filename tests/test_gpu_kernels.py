@@ -340,10 +340,11 @@ def _attention_tc(ops, qkv, dout, B, T, C, H):
     out = torch.empty(B * T, C, device="cuda", dtype=torch.bfloat16)
     lse = torch.empty(B * H * T, device="cuda")
     dq = torch.empty(B * T, 3 * C, device="cuda", dtype=torch.bfloat16)
-    D = torch.empty(B * H * T, device="cuda")
+    sc = torch.empty(ops.lib.gpt2_op_attention_backward_scratch_bytes(B, T, H), device="cuda", dtype=torch.uint8)
+    D = sc[:B * H * T * 4].view(torch.float32)  # D leads the scratch
     fl = ops.flags()
     ops.gpt2_op_attention_forward(out, lse, tq, B, T, C, H, path=ops.PATH_TC, flags_dev=fl)
-    ops.gpt2_op_attention_backward(dq, tdo, tq, out, lse, B, T, C, H, path=ops.PATH_TC, flags_dev=fl, scratch=D)
+    ops.gpt2_op_attention_backward(dq, tdo, tq, out, lse, B, T, C, H, path=ops.PATH_TC, flags_dev=fl, scratch=sc)
     torch.cuda.synchronize()
     assert fl.sum().item() == 0
     return tq, tdo, out, lse, dq, D
