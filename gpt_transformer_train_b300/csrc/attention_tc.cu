@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_enter();  // global memory only from here on
   // TMEM columns: S of tile t at 128 t, O of tile t at 256 + 64 t
 
   if (warp == 0) {
@@ -445,6 +446,7 @@ static_assert(EW_COLS == 64, "an elementwise warp's share of a dS block is one 3
 // channels, the 8 threads of a head added by a fixed shuffle tree.
 __global__ void __launch_bounds__(256) attn_rowdot_kernel(float* D, const bf16* dout, const bf16* o, long long n8,
                                                           int T, int C, int H) {
+  pdl_enter();
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   float acc = 0.f;
   if (i < n8) {
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_enter();  // global memory only from here on
   // TMEM columns: dQ accumulator a at 64 a
 
   if (warp == 0) {
@@ -676,6 +679,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_enter();  // global memory only from here on
   // TMEM columns: S^T at 0, dP^T at 128, dV at 256, dK at 320
 
   if (warp == 0) {
@@ -871,7 +875,7 @@ cudaError_t attention_forward_tc(bf16* out, float* lse, const bf16* qkv, int B, 
   const long long items = (long long)B * H * npair;
   const int sms = tc_num_sms();
   gpt2_count_launches(1);
-  attn_fwd_tc_kernel<<<(unsigned)(items < sms ? items : sms), FWD_THREADS, FWD_SMEM, st>>>(tq, p);
+  launch_k(attn_fwd_tc_kernel, dim3((unsigned)(items < sms ? items : sms)), dim3(FWD_THREADS), FWD_SMEM, st, tq, p);
   return cudaGetLastError();
 }
 
@@ -906,12 +910,12 @@ cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16*
   const unsigned grid = (unsigned)(items < sms ? items : sms);
   const long long n8 = (long long)B * T * C / 8;
   gpt2_count_launches(3);
-  attn_rowdot_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(Dbuf, dout, out, n8, T, C, H);
+  launch_k(attn_rowdot_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, st, Dbuf, dout, out, n8, T, C, H);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dkv_tc_kernel<<<grid, BWD_THREADS, DKV_SMEM, st>>>(tq, td, p);
+  launch_k(attn_bwd_dkv_tc_kernel, dim3(grid), dim3(BWD_THREADS), DKV_SMEM, st, tq, td, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_tc_kernel<<<grid, DQ_THREADS, DQ_SMEM, st>>>(tq, (const uint8_t*)dS, p);
+  launch_k(attn_bwd_dq_tc_kernel, dim3(grid), dim3(DQ_THREADS), DQ_SMEM, st, tq, (const uint8_t*)dS, p);
   return cudaGetLastError();
 }

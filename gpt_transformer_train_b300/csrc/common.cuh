@@ -9,6 +9,40 @@
 
 typedef __nv_bfloat16 bf16;
 
+// ---- programmatic dependent launch ---------------------------------------
+// Every kernel of the library is launched with launch_k(), which lets it
+// start while the kernel before it on the stream is still finishing (its
+// CTAs set up shared memory, barriers and TMEM meanwhile).  Each kernel calls
+// pdl_wait() before its first access to global memory, in every CTA: that
+// returns once the previous kernel has completed and its writes are visible,
+// so the stream order of the results is unchanged (and, as every kernel
+// waits, a kernel's completion still implies that of all kernels before it).
+// pdl_trigger() right after it lets the next kernel be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
+
+// cudaLaunchKernelEx with the programmatic-serialisation attribute (plus an
+// optional cluster size)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // elements per 16-byte word
 template <typename T> struct VecN;
 template <> struct VecN<float> { static constexpr int n = 4; };

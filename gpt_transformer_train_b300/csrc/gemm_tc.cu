@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_enter();  // global memory only from here on
 
   const int num_n = (p.N + BN - 1) / BN;
   // a "tile" here is CL vertically adjacent 128-row tiles (one per CTA of the pair)
@@ -540,7 +541,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   long long slots = sms / CL;  // clusters that can run at once
   if (CL > 1) {
     static int max_clusters = 0;
@@ -560,14 +561,18 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   }
   const unsigned grid = (unsigned)((units < slots ? units : slots) * CL);
   cfg.gridDim = dim3(grid);
-  cfg.numAttrs = 0;
+  // programmatic dependent launch (the kernel waits for its predecessor
+  // after its prologue), and the CTA-pair cluster
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
   if (CL > 1) {
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = CL;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = CL;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL>, ta, tb, td, tx, p);
 }
@@ -677,6 +682,7 @@ size_t gemm_tc_workspace_floats(int M, int N, int K, int sms) {
 
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(float* __restrict__ D, long long ldd,
                                                             const float* __restrict__ ws, int M, int N, int splits) {
+  pdl_enter();
   // D[m][n] += ws[0][m][n] + ws[1][m][n] + ... (the partials of splits 1, 2,
   // ... in order); four columns per thread, every load issued before the additions
   const long long nv = (long long)M * (N / 4);
@@ -718,6 +724,6 @@ cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   gpt2_count_launches(1);
   const long long nv = (long long)g.M * (g.N / 4);
   const unsigned grid = (unsigned)std::min<long long>((nv + 255) / 256, (long long)sms * 8);
-  splitk_reduce_kernel<<<grid, 256, 0, st>>>((float*)g.D, g.ldd, g.ws, g.M, g.N, splits - 1);
+  launch_k(splitk_reduce_kernel, dim3(grid), dim3(256), 0, st, (float*)g.D, g.ldd, g.ws, g.M, g.N, splits - 1);
   return cudaGetLastError();
 }

@@ -32,6 +32,7 @@ template <typename T>
 __global__ void encoder_forward_kernel(T* __restrict__ out, const int* __restrict__ tok,
                                        const T* __restrict__ wte, const T* __restrict__ wpe, int BT,
                                        int T_, int C, int V, int* flags) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   const int nvec = C / N;
   long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -55,7 +56,7 @@ template <typename T>
 cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, int B, int T_, int C,
                             int V, int* flags, cudaStream_t st) {
   long long n = (long long)B * T_ * (C / VecN<T>::n);
-  encoder_forward_kernel<T><<<(unsigned)cdiv(n, 256), 256, 0, st>>>(out, tok, wte, wpe, B * T_, T_, C, V, flags);
+  launch_k(encoder_forward_kernel<T>, dim3((unsigned)cdiv(n, 256)), dim3(256), 0, st, out, tok, wte, wpe, B * T_, T_, C, V, flags);
   return launch_status(1);
 }
 
@@ -66,6 +67,7 @@ cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, 
 // Positions are bucketed by a single-CTA bitonic sort of (token << 16 | pos).
 // ----------------------------------------------------------------------------
 __global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dres, int B, int T_, int C) {
+  pdl_enter();
   int nvec = C / 4;
   long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)T_ * nvec) return;
@@ -94,6 +96,7 @@ size_t encoder_backward_scratch_bytes(int BT) { return (size_t)pow2_at_least(BT)
 
 // one CTA sorts n (power of two, <= 32768) keys in shared memory
 __global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restrict__ tok, int BT, int n) {
+  pdl_enter();
   extern __shared__ uint32_t sk[];
   for (int i = threadIdx.x; i < n; i += blockDim.x)
     sk[i] = i < BT ? (((uint32_t)tok[i] & 0xFFFFu) << 16) | (uint32_t)i : 0xFFFFFFFFu;
@@ -120,6 +123,7 @@ __global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restri
 // order independent of timing, so the result is deterministic.
 __global__ void __launch_bounds__(256) wte_grad_runs_kernel(float* __restrict__ dwte, const float* __restrict__ dres,
                                                             const uint32_t* __restrict__ keys, int BT, int C) {
+  pdl_enter();
   __shared__ float4 sh[8][32];
   const int i = blockIdx.x;
   const uint32_t tk = keys[i] >> 16;
@@ -157,15 +161,15 @@ cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const 
   int n = pow2_at_least(BT);
   if (n > 32768) return cudaErrorInvalidValue;
   long long nv = (long long)T_ * (C / 4);
-  wpe_grad_kernel<<<(unsigned)cdiv(nv, 256), 256, 0, st>>>(dwpe, dres, B, T_, C);
+  launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C);
   size_t smem = (size_t)n * sizeof(uint32_t);
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(bitonic_sort_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768 * 4);
     attr_set = true;
   }
-  bitonic_sort_keys_kernel<<<1, 1024, smem, st>>>(keys, tok, BT, n);
-  wte_grad_runs_kernel<<<dim3((unsigned)BT, (unsigned)cdiv(C / 4, 32)), 256, 0, st>>>(dwte, dres, keys, BT, C);
+  launch_k(bitonic_sort_keys_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT, n);
+  launch_k(wte_grad_runs_kernel, dim3((unsigned)BT, (unsigned)cdiv(C / 4, 32)), dim3(256), 0, st, dwte, dres, keys, BT, C);
   return launch_status(3);
 }
 
@@ -179,6 +183,7 @@ __global__ void __launch_bounds__(256) residual_layernorm_forward_kernel(
     T* __restrict__ resid_out, T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd,
     const T* __restrict__ a, const T* __restrict__ b, const T* __restrict__ w, const T* __restrict__ bias, int rows,
     int C) {
+  pdl_enter();
   // R rows per warp, all of their loads issued before any reduction (R = 1
   // measured fastest at GPT-2 widths)
   constexpr int N = VecN<T>::n;
@@ -258,7 +263,7 @@ cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* r
   constexpr int N = VecN<T>::n;
   const int nvec = C / N;
 #define LNF(NVv, Rv)                                                                                      \
-  residual_layernorm_forward_kernel<T, NVv, Rv><<<(unsigned)cdiv(rows, 8 * Rv), 256, 0, st>>>(resid_out, y, mean, \
+  launch_k(residual_layernorm_forward_kernel<T, NVv, Rv>, dim3((unsigned)cdiv(rows, 8 * Rv)), dim3(256), 0, st, resid_out, y, mean, \
                                                                                              rstd, a, b, w, bias, \
                                                                                              rows, C)
   if (nvec <= 32) LNF(1, 1);
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict_
                                                               float* __restrict__ out2,
                                                               const float* __restrict__ partial, int nchunks,
                                                               int C, int nout) {
+  pdl_enter();
   __shared__ float sh[8][32];
   const int o = blockIdx.y;
   float* out = o == 0 ? out0 : (o == 1 ? out1 : out2);
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict_
 static cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
                                    int nout, cudaStream_t st) {
   dim3 grid((unsigned)cdiv(C, 32), nout);
-  reduce_partials_kernel<<<grid, 256, 0, st>>>(out0, out1, out2, partial, nchunks, C, nout);
+  launch_k(reduce_partials_kernel, dim3(grid), dim3(256), 0, st, out0, out1, out2, partial, nchunks, C, nout);
   return launch_status(1);
 }
 
@@ -367,6 +373,7 @@ __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kerne
     float* __restrict__ dres, T* __restrict__ dres_c, const T* __restrict__ dy, const T* __restrict__ x,
     const float* __restrict__ mean, const float* __restrict__ rstd, const T* __restrict__ w, int rows, int C,
     int accumulate, float* __restrict__ partial, int want_rsum) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   extern __shared__ float lnb_sh[];  // [8 warps][3][N][nvec] when partial
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -477,7 +484,7 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
   }
   float* part = sums ? partial : nullptr;
   const int rsum = dres_sum != nullptr;
-#define LNB(NVv) layernorm_backward_kernel<T, NVv><<<grid, 256, smem, st>>>(dres, dres_c, dy, x, mean, rstd, w, rows, \
+#define LNB(NVv) launch_k(layernorm_backward_kernel<T, NVv>, dim3(grid), dim3(256), smem, st, dres, dres_c, dy, x, mean, rstd, w, rows, \
                                                                             C, accumulate, part, rsum)
   if (nvec <= 32) LNB(1);
   else if (nvec <= 64) LNB(2);
@@ -501,6 +508,7 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ X,
                                                              int rows, int cols, long long ldx) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   extern __shared__ float cs_sh[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -548,7 +556,7 @@ cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, fl
   if (cols % N || ldx % N) return cudaErrorInvalidValue;
   const int nch = reduce_chunks(rows);
   dim3 grid((unsigned)cdiv(cols / N, 32), nch);
-  colsum_partial_kernel<T><<<grid, 256, 32 * N * sizeof(float), st>>>(partial, X, rows, cols, ldx);
+  launch_k(colsum_partial_kernel<T>, dim3(grid), dim3(256), 32 * N * sizeof(float), st, partial, X, rows, cols, ldx);
   cudaError_t e = launch_status(1);
   if (e != cudaSuccess) return e;
   return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st);
@@ -571,6 +579,7 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
+  pdl_enter();
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const T* A = (const T*)g.A;
@@ -649,7 +658,7 @@ template <typename T>
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaErrorInvalidValue;
   dim3 grid((unsigned)cdiv(a.N, 64), (unsigned)cdiv(a.M, 64));
-  gemm_simt_kernel<T><<<grid, 256, 0, st>>>(a);
+  launch_k(gemm_simt_kernel<T>, dim3(grid), dim3(256), 0, st, a);
   return launch_status(1);
 }
 
@@ -664,6 +673,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) attention_forward_simt_kernel(T* __restrict__ out, float* __restrict__ lse,
                                                                      const T* __restrict__ qkv, int B, int T_, int C,
                                                                      int H, float scale) {
+  pdl_enter();
   __shared__ float qs[ATT_WARPS][128];
   int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   long long gq = (long long)blockIdx.x * ATT_WARPS + warp;
@@ -718,8 +728,7 @@ cudaError_t attention_forward_simt(T* out, float* lse, const T* qkv, int B, int 
   int hd = C / H;
   if (hd > 128 || C % H) return cudaErrorInvalidValue;
   long long rows = (long long)B * H * T_;
-  attention_forward_simt_kernel<T><<<(unsigned)cdiv(rows, ATT_WARPS), 32 * ATT_WARPS, 0, st>>>(
-      out, lse, qkv, B, T_, C, H, 1.0f / sqrtf((float)hd));
+  launch_k(attention_forward_simt_kernel<T>, dim3((unsigned)cdiv(rows, ATT_WARPS)), dim3(32 * ATT_WARPS), 0, st, out, lse, qkv, B, T_, C, H, 1.0f / sqrtf((float)hd));
   return launch_status(1);
 }
 
@@ -727,6 +736,7 @@ cudaError_t attention_forward_simt(T* out, float* lse, const T* qkv, int B, int 
 template <typename T>
 __global__ void attention_bwd_dot_kernel(float* __restrict__ Dbuf, const T* __restrict__ dout,
                                          const T* __restrict__ out, int B, int T_, int C, int H) {
+  pdl_enter();
   int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   long long gq = (long long)blockIdx.x * ATT_WARPS + warp;
   if (gq >= (long long)B * H * T_) return;
@@ -745,6 +755,7 @@ __global__ void __launch_bounds__(256) attention_bwd_dq_kernel(T* __restrict__ d
                                                                const T* __restrict__ qkv, const float* __restrict__ lse,
                                                                const float* __restrict__ Dbuf, int B, int T_, int C,
                                                                int H, float scale) {
+  pdl_enter();
   __shared__ float qs[ATT_WARPS][128];
   __shared__ float dos[ATT_WARPS][128];
   int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -800,6 +811,7 @@ __global__ void __launch_bounds__(256) attention_bwd_dkv_kernel(T* __restrict__ 
                                                                 const T* __restrict__ qkv, const float* __restrict__ lse,
                                                                 const float* __restrict__ Dbuf, int B, int T_, int C,
                                                                 int H, float scale) {
+  pdl_enter();
   __shared__ float ks[ATT_WARPS][128];
   __shared__ float vs[ATT_WARPS][128];
   int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -865,9 +877,9 @@ cudaError_t attention_backward_simt(T* dqkv, float* Dbuf, const T* dout, const T
   long long rows = (long long)B * H * T_;
   unsigned grid = (unsigned)cdiv(rows, ATT_WARPS);
   float scale = 1.0f / sqrtf((float)hd);
-  attention_bwd_dot_kernel<T><<<grid, 32 * ATT_WARPS, 0, st>>>(Dbuf, dout, out, B, T_, C, H);
-  attention_bwd_dq_kernel<T><<<grid, 32 * ATT_WARPS, 0, st>>>(dqkv, dout, qkv, lse, Dbuf, B, T_, C, H, scale);
-  attention_bwd_dkv_kernel<T><<<grid, 32 * ATT_WARPS, 0, st>>>(dqkv, dout, qkv, lse, Dbuf, B, T_, C, H, scale);
+  launch_k(attention_bwd_dot_kernel<T>, dim3(grid), dim3(32 * ATT_WARPS), 0, st, Dbuf, dout, out, B, T_, C, H);
+  launch_k(attention_bwd_dq_kernel<T>, dim3(grid), dim3(32 * ATT_WARPS), 0, st, dqkv, dout, qkv, lse, Dbuf, B, T_, C, H, scale);
+  launch_k(attention_bwd_dkv_kernel<T>, dim3(grid), dim3(32 * ATT_WARPS), 0, st, dqkv, dout, qkv, lse, Dbuf, B, T_, C, H, scale);
   return launch_status(3);
 }
 
@@ -881,6 +893,7 @@ template <typename T>
 __global__ void __launch_bounds__(1024) softmax_ce_kernel(T* __restrict__ logits, float* __restrict__ losses,
                                                           const int* __restrict__ targets, int V, int Vp,
                                                           float dloss, int write_grad, int* flags) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   __shared__ float sm[32], ss[32];
   __shared__ float s_lse;
@@ -963,6 +976,7 @@ template <typename T, int VPT>
 __global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ logits, float* __restrict__ losses,
                                                               const int* __restrict__ targets, int V, int Vp,
                                                               float dloss, int write_grad, int* flags) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   constexpr float L2E = 1.4426950408889634f;
   __shared__ float red[32];
@@ -1100,7 +1114,7 @@ cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, i
   constexpr int N = VecN<T>::n;
   if (Vp % N) return cudaErrorInvalidValue;
   const int vpt = (int)cdiv(Vp / N, 1024);
-#define SCE(K) softmax_ce_reg_kernel<T, K><<<rows, 1024, 0, st>>>(logits, losses, targets, V, Vp, dloss, write_grad, flags)
+#define SCE(K) launch_k(softmax_ce_reg_kernel<T, K>, dim3(rows), dim3(1024), 0, st, logits, losses, targets, V, Vp, dloss, write_grad, flags)
   switch (vpt) {
     case 1: SCE(1); break;
     case 2: SCE(2); break;
@@ -1111,7 +1125,7 @@ cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, i
     case 7: SCE(7); break;
     case 8: SCE(8); break;
     default:
-      softmax_ce_kernel<T><<<rows, 1024, 0, st>>>(logits, losses, targets, V, Vp, dloss, write_grad, flags);
+      launch_k(softmax_ce_kernel<T>, dim3(rows), dim3(1024), 0, st, logits, losses, targets, V, Vp, dloss, write_grad, flags);
   }
 #undef SCE
   return launch_status(1);
@@ -1119,6 +1133,7 @@ cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, i
 
 // mean of n per-position losses, one CTA, fixed summation order
 __global__ void mean_loss_kernel(float* loss, const float* __restrict__ losses, int n) {
+  pdl_enter();
   __shared__ float sh[32];
   float s = 0.f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) s += losses[i];
@@ -1126,7 +1141,7 @@ __global__ void mean_loss_kernel(float* loss, const float* __restrict__ losses, 
   if (threadIdx.x == 0) *loss = s / (float)n;
 }
 cudaError_t mean_loss(float* loss, const float* losses, int n, cudaStream_t st) {
-  mean_loss_kernel<<<1, 1024, 0, st>>>(loss, losses, n);
+  launch_k(mean_loss_kernel, dim3(1), dim3(1024), 0, st, loss, losses, n);
   return launch_status(1);
 }
 
@@ -1138,6 +1153,7 @@ __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g,
                              float* __restrict__ v, bf16* __restrict__ pc, long long nvec, float lr, float b1,
                              float b2, float eps, float bc1, float bc2, AdamSegments seg,
                              const float* __restrict__ gscale) {
+  pdl_enter();
   // gscale (optional): the clip factor the gradient-norm kernels left on the device
   const float gs = gscale ? *gscale : 1.f;
   long long stride = (long long)gridDim.x * blockDim.x;
@@ -1182,7 +1198,7 @@ cudaError_t adamw(float* p, const float* g, float* m, float* v, bf16* pc, long l
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   long long blocks = cdiv(nvec, 256);
   if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-  adamw_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, g, m, v, pc, nvec, lr, b1, b2, eps, bc1, bc2, seg, gscale);
+  launch_k(adamw_kernel, dim3((unsigned)blocks), dim3(256), 0, st, p, g, m, v, pc, nvec, lr, b1, b2, eps, bc1, bc2, seg, gscale);
   return launch_status(1);
 }
 
@@ -1197,6 +1213,7 @@ size_t grad_norm_scratch_floats() { return GN_CHUNKS; }
 
 __global__ void __launch_bounds__(256) grad_sq_partial_kernel(const float* __restrict__ g, long long n,
                                                               long long chunk, float* __restrict__ partial) {
+  pdl_enter();
   __shared__ float red[32];
   const long long b0 = (long long)blockIdx.x * chunk, b1 = min(n, b0 + chunk);
   float s = 0.f;
@@ -1218,6 +1235,7 @@ __global__ void __launch_bounds__(256) grad_sq_partial_kernel(const float* __res
 
 __global__ void __launch_bounds__(256) grad_norm_finalize_kernel(const float* __restrict__ partial, float max_norm,
                                                                  float* __restrict__ out) {
+  pdl_enter();
   __shared__ double red[256];
   double s = 0.0;
   for (int i = threadIdx.x; i < GN_CHUNKS; i += 256) s += (double)partial[i];  // 4 per thread, in order
@@ -1238,18 +1256,19 @@ __global__ void __launch_bounds__(256) grad_norm_finalize_kernel(const float* __
 cudaError_t grad_norm(const float* g, long long n, float max_norm, float* out2, float* partial, cudaStream_t st) {
   if (n < 0 || (n > 0 && ((uintptr_t)g & 15))) return cudaErrorInvalidValue;
   const long long chunk = ((cdiv(n, GN_CHUNKS) + 3) / 4) * 4;  // chunks start 16-byte aligned
-  grad_sq_partial_kernel<<<GN_CHUNKS, 256, 0, st>>>(g, n, chunk > 0 ? chunk : 4, partial);
-  grad_norm_finalize_kernel<<<1, 256, 0, st>>>(partial, max_norm, out2);
+  launch_k(grad_sq_partial_kernel, dim3(GN_CHUNKS), dim3(256), 0, st, g, n, chunk > 0 ? chunk : 4, partial);
+  launch_k(grad_norm_finalize_kernel, dim3(1), dim3(256), 0, st, partial, max_norm, out2);
   return launch_status(2);
 }
 
 __global__ void convert_f32_bf16_kernel(bf16* __restrict__ out, const float* __restrict__ in, long long n) {
+  pdl_enter();
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) out[i] = __float2bfloat16_rn(in[i]);
 }
 cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  convert_f32_bf16_kernel<<<(unsigned)cdiv(n, 256), 256, 0, st>>>(out, in, n);
+  launch_k(convert_f32_bf16_kernel, dim3((unsigned)cdiv(n, 256)), dim3(256), 0, st, out, in, n);
   return launch_status(1);
 }
 
@@ -1258,6 +1277,7 @@ cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream
 // ============================================================================
 template <typename T>
 __global__ void gelu_forward_kernel(T* __restrict__ out, const T* __restrict__ in, long long nvec) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nvec) return;
@@ -1270,6 +1290,7 @@ __global__ void gelu_forward_kernel(T* __restrict__ out, const T* __restrict__ i
 template <typename T>
 __global__ void gelu_backward_kernel(T* __restrict__ dinp, const T* __restrict__ inp, const T* __restrict__ dout,
                                      long long nvec) {
+  pdl_enter();
   constexpr int N = VecN<T>::n;
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nvec) return;
@@ -1284,14 +1305,14 @@ template <typename T>
 cudaError_t gelu_forward(T* out, const T* in, long long n, cudaStream_t st) {
   constexpr int N = VecN<T>::n;
   if (n % N) return cudaErrorInvalidValue;
-  gelu_forward_kernel<T><<<(unsigned)cdiv(n / N, 256), 256, 0, st>>>(out, in, n / N);
+  launch_k(gelu_forward_kernel<T>, dim3((unsigned)cdiv(n / N, 256)), dim3(256), 0, st, out, in, n / N);
   return launch_status(1);
 }
 template <typename T>
 cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cudaStream_t st) {
   constexpr int N = VecN<T>::n;
   if (n % N) return cudaErrorInvalidValue;
-  gelu_backward_kernel<T><<<(unsigned)cdiv(n / N, 256), 256, 0, st>>>(dinp, inp, dout, n / N);
+  launch_k(gelu_backward_kernel<T>, dim3((unsigned)cdiv(n / N, 256)), dim3(256), 0, st, dinp, inp, dout, n / N);
   return launch_status(1);
 }
 
