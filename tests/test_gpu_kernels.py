@@ -448,6 +448,42 @@ def test_softmax_crossentropy(ops, dt, rows, V, Vp):
     assert fl.sum().item() == 0
 
 
+@pytest.mark.parametrize("write_grad", [1, 0])
+def test_softmax_crossentropy_many_rows(ops, write_grad):
+    """GPT-2 vocabulary with more rows than two per SM: the persistent bf16
+    kernel's double-buffered row pipeline, a ragged last CTA, one target at
+    the last real column; write_grad=0 leaves the logits untouched."""
+    rows, V, Vp = 400, 50257, 50304
+    z = normal_array((rows, Vp), 63, 3.0)
+    z[:, V:] = 100.0
+    tgt = np.random.default_rng(64).integers(0, V, size=rows).astype(np.int32)
+    tgt[7] = V - 1
+    tz = dev(z, torch.bfloat16)
+    zs = host(tz)
+    losses = torch.empty(rows, device="cuda")
+    fl = ops.flags()
+    dloss = 1.0 / rows
+    ops.gpt2_op_softmax_crossentropy(tz, losses, dev(tgt, torch.int32), rows, V, Vp, dloss, write_grad, fl)
+    assert fl.sum().item() == 0
+    rl = O.crossentropy_forward(zs[None], tgt[None], V)[0]
+    assert np.max(np.abs(host(losses) - rl)) < 1e-4
+    got = host(tz)
+    if not write_grad:
+        assert np.array_equal(got, zs)
+        return
+    rd = O.crossentropy_softmax_backward(O.softmax_forward(zs[None], V), tgt[None], np.full((1, rows), dloss))[0]
+    assert np.all(got[:, V:] == 0)
+    assert np.max(np.abs(got - rd)) < 2 ** -8 * dloss
+
+
+def test_softmax_crossentropy_flags_bad_target_large_vocab(ops):
+    z = dev(normal_array((3, 50304), 65), torch.bfloat16)
+    fl = ops.flags()
+    ops.gpt2_op_softmax_crossentropy(z, torch.empty(3, device="cuda"), dev(np.array([1, 50257, 5], np.int32), torch.int32),
+                                     3, 50257, 50304, 0.5, 1, fl)
+    assert fl[0].item() & 2
+
+
 def test_softmax_crossentropy_flags_bad_target(ops):
     z = dev(normal_array((2, 64), 62))
     fl = ops.flags()
