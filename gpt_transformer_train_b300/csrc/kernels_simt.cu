@@ -8,8 +8,11 @@
 // Compilers", [13:50] Avengers Assemble (fused residual+LayerNorm, fused
 // classifier, full determinism: no floating-point atomics anywhere here).
 #include "kernels.cuh"
+#include "tc_common.cuh"
 #include <cuda_fp16.h>
 #include <math.h>
+
+#include <algorithm>
 
 #define LN_EPS 1e-5f
 #define GELU_SCALE 0.7978845608028654f   // sqrt(2/pi)
@@ -459,6 +462,137 @@ __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kerne
   }
 }
 
+// bf16 rows of at most 1024 columns: one CTA of LNBP_WARPS warps per SM, each
+// warp owning a contiguous range of rpw rows and keeping the next row's dy
+// and x in flight (registers) while it computes the current one; the
+// incoming dres of a row is fetched before that row's reductions.  Same
+// arithmetic, per-warp shared-memory accumulators and partial layout
+// (partial[block][3][C]) as layernorm_backward_kernel.
+constexpr int LNBP_WARPS = 16;
+template <int NV>
+__device__ __forceinline__ void lnbp_fetch(uint4 (&vdy)[NV], uint4 (&vx)[NV], const bf16* dy, const bf16* x, size_t off,
+                                           int lane, int nvec) {
+#pragma unroll
+  for (int i = 0; i < NV; i++) {
+    const int vi = lane + i * 32;
+    if (vi < nvec) {
+      vdy[i] = __ldcs(reinterpret_cast<const uint4*>(dy + off) + vi);
+      vx[i] = __ldcs(reinterpret_cast<const uint4*>(x + off) + vi);
+    }
+  }
+}
+__device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+template <int NV>
+__global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_kernel(
+    float* __restrict__ dres, bf16* __restrict__ dres_c, const bf16* __restrict__ dy, const bf16* __restrict__ x,
+    const float* __restrict__ mean, const float* __restrict__ rstd, const bf16* __restrict__ w, int rows, int C,
+    int accumulate, float* __restrict__ partial, int want_rsum, int rpw) {
+  pdl_enter();
+  constexpr int N = 8;
+  extern __shared__ float lnb_sh[];  // [LNBP_WARPS][3][N][nvec] when partial
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nvec = C / N;
+  float* acc = lnb_sh + (size_t)warp * 3 * C;
+  if (partial)
+    for (int c = lane; c < 3 * C; c += 32) acc[c] = 0.f;
+  uint4 wv[NV];
+#pragma unroll
+  for (int i = 0; i < NV; i++)
+    if (lane + i * 32 < nvec) wv[i] = reinterpret_cast<const uint4*>(w)[lane + i * 32];
+  const int r0 = (blockIdx.x * LNBP_WARPS + warp) * rpw;
+  const int r1 = min(rows, r0 + rpw);
+  uint4 ndy[NV], nx[NV];
+  if (r0 < r1) lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)r0 * C, lane, nvec);
+  for (int row = r0; row < r1; row++) {
+    uint4 cdy[NV], cx[NV];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+      cdy[i] = ndy[i];
+      cx[i] = nx[i];
+    }
+    if (row + 1 < r1) lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)(row + 1) * C, lane, nvec);
+    const float mu = mean[row], rs = rstd[row];
+    float4 din[NV][2];
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+      const int vi = lane + i * 32;
+      din[i][0] = din[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (accumulate && vi < nvec) {
+        const float4* src = reinterpret_cast<const float4*>(dres + (size_t)row * C) + 2 * vi;
+        din[i][0] = __ldcs(src);
+        din[i][1] = __ldcs(src + 1);
+      }
+    }
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+      const int vi = lane + i * 32;
+      if (vi < nvec) {
+        float dv[N], xv[N], ww[N];
+        unpack_bf16x8(cdy[i], dv);
+        unpack_bf16x8(cx[i], xv);
+        unpack_bf16x8(wv[i], ww);
+#pragma unroll
+        for (int k = 0; k < N; k++) {
+          const float xh = (xv[k] - mu) * rs, dn = dv[k] * ww[k];
+          s1 += dn;
+          s2 += dn * xh;
+          if (partial) {
+            acc[k * nvec + vi] += dv[k] * xh;
+            acc[(N + k) * nvec + vi] += dv[k];
+          }
+        }
+      }
+    }
+    s1 = warp_sum(s1) / (float)C;
+    s2 = warp_sum(s2) / (float)C;
+#pragma unroll
+    for (int i = 0; i < NV; i++) {
+      const int vi = lane + i * 32;
+      if (vi < nvec) {
+        float dv[N], xv[N], ww[N], o[N];
+        unpack_bf16x8(cdy[i], dv);
+        unpack_bf16x8(cx[i], xv);
+        unpack_bf16x8(wv[i], ww);
+        const float a[N] = {din[i][0].x, din[i][0].y, din[i][0].z, din[i][0].w,
+                            din[i][1].x, din[i][1].y, din[i][1].z, din[i][1].w};
+#pragma unroll
+        for (int k = 0; k < N; k++) {
+          const float xh = (xv[k] - mu) * rs, dn = dv[k] * ww[k];
+          o[k] = a[k] + (dn - s1 - xh * s2) * rs;
+        }
+        float4* dst = reinterpret_cast<float4*>(dres + (size_t)row * C) + 2 * vi;
+        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+        if (dres_c) st16(dres_c + (size_t)row * C + vi * N, o);
+        if (partial && want_rsum) {
+#pragma unroll
+          for (int k = 0; k < N; k++) acc[(2 * N + k) * nvec + vi] += o[k];
+        }
+      }
+    }
+  }
+  if (!partial) return;  // uniform over the block
+  __syncthreads();
+  float* dst = partial + (size_t)blockIdx.x * 3 * C;
+  const int nc = want_rsum ? 3 * C : 2 * C;
+  for (int idx = threadIdx.x; idx < nc; idx += blockDim.x) {
+    const int a = idx / C, rem = idx - a * C, k = rem / nvec, vi = rem - k * nvec;
+    float t = lnb_sh[idx];
+#pragma unroll
+    for (int q = 1; q < LNBP_WARPS; q++) t += lnb_sh[(size_t)q * 3 * C + idx];
+    dst[a * C + vi * N + k] = t;
+  }
+}
+
 template <typename T>
 cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
                                const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
@@ -484,6 +618,36 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
   }
   float* part = sums ? partial : nullptr;
   const int rsum = dres_sum != nullptr;
+  if constexpr (sizeof(T) == 2) {
+    if (nvec <= 128 && ((uintptr_t)dres & 15) == 0 && ((uintptr_t)w & 15) == 0) {
+      // one CTA per SM, never more CTAs than the partial buffer has chunks
+      const int pgrid = std::min(tc_num_sms(), reduce_chunks(rows));
+      const int rpw = (int)cdiv(rows, (long long)pgrid * LNBP_WARPS);
+      const size_t psmem = sums ? (size_t)LNBP_WARPS * 3 * C * sizeof(float) : 0;
+      static bool pattr = false;
+      if (!pattr) {
+        const int mx = LNBP_WARPS * 3 * 1024 * (int)sizeof(float);
+        for (auto k : {layernorm_backward_pipe_kernel<1>, layernorm_backward_pipe_kernel<2>,
+                       layernorm_backward_pipe_kernel<3>, layernorm_backward_pipe_kernel<4>}) {
+          cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+          if (e != cudaSuccess) return e;
+        }
+        pattr = true;
+      }
+#define LNBP(NVv)                                                                                            \
+  launch_k(layernorm_backward_pipe_kernel<NVv>, dim3(pgrid), dim3(32 * LNBP_WARPS), psmem, st, dres,          \
+           (bf16*)dres_c, (const bf16*)dy, (const bf16*)x, mean, rstd, (const bf16*)w, rows, C, accumulate, \
+           part, rsum, rpw)
+      if (nvec <= 32) LNBP(1);
+      else if (nvec <= 64) LNBP(2);
+      else if (nvec <= 96) LNBP(3);
+      else LNBP(4);
+#undef LNBP
+      cudaError_t e = launch_status(1);
+      if (e != cudaSuccess || !sums) return e;
+      return reduce_partials(dw, db, dres_sum, partial, pgrid, C, 3, st);
+    }
+  }
 #define LNB(NVv) launch_k(layernorm_backward_kernel<T, NVv>, dim3(grid), dim3(256), smem, st, dres, dres_c, dy, x, mean, rstd, w, rows, \
                                                                             C, accumulate, part, rsum)
   if (nvec <= 32) LNB(1);

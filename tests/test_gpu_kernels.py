@@ -139,7 +139,7 @@ def test_residual_layernorm_forward(ops, dt, rows, C, fused):
 
 
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
-@pytest.mark.parametrize("rows,C", [(3, 64), (129, 768), (64, 1600), (1000, 1024)])
+@pytest.mark.parametrize("rows,C", [(3, 64), (129, 768), (64, 1600), (1000, 1024), (2000, 512), (16384, 768)])
 def test_layernorm_backward(ops, dt, rows, C):
     x = normal_array((rows, C), 20, 1.5)
     w = normal_array((C,), 21, 0.2) + 1
@@ -167,6 +167,21 @@ def test_layernorm_backward(ops, dt, rows, C):
         torch.full((C,), -0.25, device="cuda")
     ops.gpt2_op_layernorm_backward(dres2, None, tdy, tx, tmean, trstd, tw, dw2, db2, rows, C, 1, dres_sum=rsum2)
     assert torch.equal(dres, dres2) and torch.equal(dw, dw2) and torch.equal(db, db2) and torch.equal(rsum, rsum2)
+
+
+@pytest.mark.parametrize("rows,C", [(77, 768), (16384, 768)])
+def test_layernorm_backward_overwrite(ops, rows, C):
+    """accumulate=0: the residual gradient is overwritten with dx (the first
+    LayerNorm backward of the step), without parameter sums."""
+    x, w, dy = normal_array((rows, C), 24, 1.5), normal_array((C,), 25, 0.2) + 1, normal_array((rows, C), 26)
+    tx, tw, tdy = dev(x, torch.bfloat16), dev(w, torch.bfloat16), dev(dy, torch.bfloat16)
+    xs, ws, dys = host(tx), host(tw), host(tdy)
+    _, mean, rstd = O.layernorm_forward(xs, ws, np.zeros(C))
+    dres = dev(normal_array((rows, C), 27))  # garbage that must not leak in
+    ops.gpt2_op_layernorm_backward(dres, None, tdy, tx, dev(mean.astype(np.float32)), dev(rstd.astype(np.float32)),
+                                   tw, None, None, rows, C, 0)
+    rdx, _, _ = O.layernorm_backward(dys, xs, mean, rstd, ws)
+    assert rel_l2(host(dres), rdx) < 1e-5
 
 
 # ---------------------------------------------------------------------------
