@@ -74,6 +74,7 @@ struct TcParams {
   const bf16* bias;
   int* flags;
   int splits;  // K split into this many ranges (EPI_ACC_F32 only)
+  int batch;   // independent products, item z at depth z of every tensor map
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -84,13 +85,22 @@ __device__ __forceinline__ uint32_t leader_addr(uint32_t a) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
   return r;
 }
-// TMA load into this CTA's shared memory, completion signalled on a barrier of
-// either CTA of the pair (cluster address)
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// TMA load of box (x, y) of batch item z into this CTA's shared memory
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+// the same with completion signalled on a barrier of either CTA of the pair
+// (cluster address)
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
@@ -130,21 +140,17 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 
 // TMA store / reduce-add of a staged box, and bulk-group bookkeeping (per thread)
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"((uint64_t)map),
                "r"(x), "r"(y), "r"(z), "r"(src)
                : "memory");
 }
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   (uint64_t)map),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          (uint64_t)map),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
@@ -235,7 +241,8 @@ __global__ void __launch_bounds__(192, 1)
   // a "tile" here is CL vertically adjacent 128-row tiles (one per CTA of the pair)
   const int tiles = ((p.M + CL * BM - 1) / (CL * BM)) * num_n;
   const int nk = (p.K + BK - 1) / BK;
-  const int units = tiles * p.splits;  // unit u: split u / tiles of tile u % tiles
+  // unit u: batch item u / (splits * tiles), split (u / tiles) % splits, tile u % tiles
+  const int units = tiles * p.splits * p.batch;
   auto kb_begin = [&](int sp) { return (int)((long long)nk * sp / p.splits); };
   const uint32_t crank = CL > 1 ? cluster_rank() : 0;
   const int ustart = (int)(blockIdx.x / CL), ustep = (int)(gridDim.x / CL);
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {  // ---- TMA producer
       uint32_t it = 0;
       for (int u = ustart; u < units; u += ustep) {
-        const int t = u % tiles, sp = u / tiles;
+        const int t = u % tiles, sp = (u / tiles) % p.splits, z = u / (tiles * p.splits);
         const int m0 = tile_m0(t), n0 = (t % num_n) * BN;
         bool ok = true;
         for (int kb = kb_begin(sp), kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
@@ -257,33 +264,33 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t fb = full0 + 8 * s;
             mbar_expect_tx(fb, STAGE);
             if (!p.a_mn) {
-              tma_load_2d(a_dst, &ta, k0, m0, fb);
+              tma_load_3d(a_dst, &ta, k0, m0, z, fb);
             } else {
-              tma_load_2d(a_dst, &ta, m0, k0, fb);
-              tma_load_2d(a_dst + 8192, &ta, m0 + 64, k0, fb);
+              tma_load_3d(a_dst, &ta, m0, k0, z, fb);
+              tma_load_3d(a_dst + 8192, &ta, m0 + 64, k0, z, fb);
             }
             if (!p.b_mn) {
-              tma_load_2d(b_dst, &tb, k0, n0, fb);
+              tma_load_3d(b_dst, &tb, k0, n0, z, fb);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; j++) tma_load_2d(b_dst + 8192 * j, &tb, n0 + 64 * j, k0, fb);
+              for (int j = 0; j < BN / 64; j++) tma_load_3d(b_dst + 8192 * j, &tb, n0 + 64 * j, k0, z, fb);
             }
           } else {
             // both CTAs' loads complete on the even CTA's barrier, which expects all of them
             const uint32_t fb = leader_addr(full0 + 8 * s);
             if (crank == 0) mbar_expect_tx(full0 + 8 * s, 2 * STAGE);
             if (!p.a_mn) {
-              tma_load_2d_pair(a_dst, &ta, k0, m0, fb);
+              tma_load_3d_pair(a_dst, &ta, k0, m0, z, fb);
             } else {
-              tma_load_2d_pair(a_dst, &ta, m0, k0, fb);
-              tma_load_2d_pair(a_dst + 8192, &ta, m0 + 64, k0, fb);
+              tma_load_3d_pair(a_dst, &ta, m0, k0, z, fb);
+              tma_load_3d_pair(a_dst + 8192, &ta, m0 + 64, k0, z, fb);
             }
             const int nb = n0 + (int)crank * (BN / 2);  // this CTA's half of the B tile
             if (!p.b_mn) {
-              tma_load_2d_pair(b_dst, &tb, k0, nb, fb);
+              tma_load_3d_pair(b_dst, &tb, k0, nb, z, fb);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 128; j++) tma_load_2d_pair(b_dst + 8192 * j, &tb, nb + 64 * j, k0, fb);
+              for (int j = 0; j < BN / 128; j++) tma_load_3d_pair(b_dst + 8192 * j, &tb, nb + 64 * j, k0, z, fb);
             }
           }
         }
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(192, 1)
         fence_after();
         const uint32_t d = tmem + a * BN;
         bool ok = true;
-        const int sp = u / tiles, kb0 = kb_begin(sp);
+        const int sp = (u / tiles) % p.splits, kb0 = kb_begin(sp);
         for (int kb = kb0, kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(192, 1)
     };
     uint32_t j = 0;
     for (int u = ustart; u < units; u += ustep, j++) {
-      const int t = u % tiles, sp = u / tiles;
+      const int t = u % tiles, sp = (u / tiles) % p.splits, z = u / (tiles * p.splits);
       const int m0 = tile_m0(t), n0 = (t % num_n) * BN;
       const int rbase = m0 + q * 32;  // first row of this warp's slab
       const bool rows_in = rbase < p.M;
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(192, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (sp == 0) tma_reduce_add_2d(&td, col0, rbase, buf);
+              if (sp == 0) tma_reduce_add_3d(&td, col0, rbase, z, buf);
               else tma_store_3d(&tx, col0, rbase, sp - 1, buf);  // workspace slot sp - 1
               bulk_commit();
             }
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(192, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&td, col0, rbase, bo);
+            tma_store_3d(&td, col0, rbase, z, bo);
             bulk_commit();
           }
         } else if (p.epi == EPI_GELU) {
@@ -438,15 +445,15 @@ __global__ void __launch_bounds__(192, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tx, col0, rbase, stg);
-            tma_store_2d(&td, col0, rbase, stg + STG);
+            tma_store_3d(&tx, col0, rbase, z, stg);
+            tma_store_3d(&td, col0, rbase, z, stg + STG);
             bulk_commit();
           }
         } else {  // EPI_GELU_BWD: D = acc * GELU'(aux), aux tile fetched by TMA
           if (lane == 0) {
             bulk_wait_read<0>();
             mbar_expect_tx(auxbar, STG);
-            tma_load_2d(stg, &tx, col0, rbase, auxbar);
+            tma_load_3d(stg, &tx, col0, rbase, z, auxbar);
           }
           __syncwarp();
           if (!mbar_wait_warp(auxbar, aux_phase, abort_flag)) { ok = false; break; }
@@ -463,7 +470,7 @@ __global__ void __launch_bounds__(192, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&td, col0, rbase, stg + STG);
+            tma_store_3d(&td, col0, rbase, z, stg + STG);
             bulk_commit();
           }
         }
@@ -507,6 +514,12 @@ int choose_splits(int tiles, int nk, int slots) {
   return best;
 }
 
+// 3-D tiled map with 128-byte swizzle: [depth][outer][inner] with row stride
+// ld and item stride bstride (elements); box = box_inner x box_outer x 1
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t ld, uint64_t depth, uint64_t bstride, uint32_t box_inner,
+                 uint32_t box_outer);
+
 template <int BN, int STAGES, int CL>
 constexpr size_t smem_bytes() {
   return (size_t)STAGES * (BM * BK * 2 + (BN / CL) * BK * 2) + 8 * STG + 1024 + 256;
@@ -523,20 +536,26 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  // every operand map is 3-D: depth = batch items, g.sX elements apart
   CUtensorMap ta, tb, td, tx;
-  bool ok = g.a_kmajor ? tc_make_map(&ta, g.A, g.K, g.M, g.lda, 64, BM) : tc_make_map(&ta, g.A, g.M, g.K, g.lda, 64, 64);
-  ok = ok && (g.b_kmajor ? tc_make_map(&tb, g.B, g.K, g.N, g.ldb, 64, BN / CL)
-                         : tc_make_map(&tb, g.B, g.N, g.K, g.ldb, 64, 64));
-  if (g.epi == EPI_ACC_F32) ok = ok && tc_make_map_f32(&td, g.D, g.N, g.M, g.ldd, 32, 32);
-  else ok = ok && tc_make_map(&td, g.D, g.N, g.M, g.ldd, 64, 32);
-  if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) ok = ok && tc_make_map(&tx, g.aux, g.N, g.M, g.ldaux, 64, 32);
+  const uint64_t nb = (uint64_t)(g.batch > 1 ? g.batch : 1);
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = g.a_kmajor ? make_map_3d(&ta, bf, 2, g.A, g.K, g.M, g.lda, nb, g.sA, 64, BM)
+                       : make_map_3d(&ta, bf, 2, g.A, g.M, g.K, g.lda, nb, g.sA, 64, 64);
+  ok = ok && (g.b_kmajor ? make_map_3d(&tb, bf, 2, g.B, g.K, g.N, g.ldb, nb, g.sB, 64, BN / CL)
+                         : make_map_3d(&tb, bf, 2, g.B, g.N, g.K, g.ldb, nb, g.sB, 64, 64));
+  if (g.epi == EPI_ACC_F32)
+    ok = ok && make_map_3d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.D, g.N, g.M, g.ldd, nb, g.sD, 32, 32);
+  else ok = ok && make_map_3d(&td, bf, 2, g.D, g.N, g.M, g.ldd, nb, g.sD, 64, 32);
+  if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) ok = ok && make_map_3d(&tx, bf, 2, g.aux, g.N, g.M, g.ldaux, nb, g.sAux, 64, 32);
   else if (g.epi == EPI_ACC_F32 && splits > 1) ok = ok && tc_make_map_f32_3d(&tx, g.ws, g.N, g.M, splits - 1, 32, 32);
   else tx = td;
   if (!ok) return cudaErrorInvalidValue;
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
-  TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits};
-  const long long units = tiles * splits;
+  TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
+             (int)nb};
+  const long long units = tiles * splits * (long long)nb;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = smem;
@@ -620,6 +639,23 @@ bool tc_make_map_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return make_map_dt(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer, ld, box_inner, box_outer);
 }
 
+namespace {
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t inner,
+                 uint64_t outer, uint64_t ld, uint64_t depth, uint64_t bstride, uint32_t box_inner,
+                 uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  if (depth <= 1) bstride = ld * outer;  // unused, any valid stride
+  cuuint64_t dims[3] = {inner, outer, depth};
+  cuuint64_t strides[2] = {ld * esize, bstride * esize};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+}  // namespace
+
 // dense fp32 [depth][outer][inner] (contiguous), box = box_inner x box_outer x 1
 bool tc_make_map_f32_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t depth,
                         uint32_t box_inner, uint32_t box_outer) {
@@ -657,6 +693,11 @@ bool gemm_tc_supported(const GemmArgs& g) {
   if (g.bias && !al16(g.bias)) return false;
   if (g.a_kmajor ? g.lda < g.K : g.lda < g.M) return false;
   if (g.b_kmajor ? g.ldb < g.K : g.ldb < g.N) return false;
+  if (g.batch > 1) {
+    const bool f32 = g.epi == EPI_ACC_F32;
+    if (g.bias || g.sA <= 0 || g.sB <= 0 || g.sD <= 0 || g.sA % 8 || g.sB % 8 || g.sD % (f32 ? 4 : 8)) return false;
+    if (g.aux && (g.sAux <= 0 || g.sAux % 8)) return false;
+  }
   return tc_available();
 }
 
@@ -713,10 +754,12 @@ cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   const bool wide = g.N >= 512;  // 256-wide tiles (a ragged last column tile is clipped by TMA)
   const int sms = tc_num_sms();
   const long long mt = (g.M + BM - 1) / BM, nt = (g.N + (wide ? 256 : 128) - 1) / (wide ? 256 : 128);
+  const long long nb = g.batch > 1 ? g.batch : 1;
   int splits = 1;
-  if (g.epi == EPI_ACC_F32 && g.ws && g.N % 4 == 0 && mt >= 2) splits = gemm_tc_splits(g.M, g.N, g.K, g.ws_floats);
+  if (g.epi == EPI_ACC_F32 && g.ws && g.N % 4 == 0 && mt >= 2 && nb == 1)
+    splits = gemm_tc_splits(g.M, g.N, g.K, g.ws_floats);
   // CTA pairs (cta_group::2) when there are enough row tiles to pair up, or for a split K
-  const bool pair = mt >= 2 && (splits > 1 || mt * nt >= sms);
+  const bool pair = mt >= 2 && (splits > 1 || mt * nt * nb >= sms);
   cudaError_t e;
   if (wide) e = pair ? launch<256, 6, 2>(g, splits, flags, st) : launch<256, 4, 1>(g, 1, flags, st);
   else e = pair ? launch<128, 8, 2>(g, splits, flags, st) : launch<128, 6, 1>(g, 1, flags, st);

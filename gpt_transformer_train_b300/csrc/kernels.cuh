@@ -27,6 +27,10 @@ struct GemmArgs {
   // optional fp32 workspace: lets the tensor-core path split K of an
   // EPI_ACC_F32 product across CTAs (partials added in split order afterwards)
   float* ws; size_t ws_floats;
+  // batch > 1: that many independent products, item z reading A + z*sA,
+  // B + z*sB (and aux + z*sAux) and writing D + z*sD (element strides); no
+  // bias, no K split
+  int batch; long long sA, sB, sD, sAux;
 };
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
 // tcgen05/TMA tensor-core path (bf16 operands); returns cudaErrorNotSupported

@@ -822,8 +822,19 @@ template <typename T>
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaErrorInvalidValue;
   dim3 grid((unsigned)cdiv(a.N, 64), (unsigned)cdiv(a.M, 64));
-  launch_k(gemm_simt_kernel<T>, dim3(grid), dim3(256), 0, st, a);
-  return launch_status(1);
+  const int nb = a.batch > 1 ? a.batch : 1;
+  if (nb > 1 && a.bias) return cudaErrorInvalidValue;
+  const size_t dsz = a.epi == EPI_ACC_F32 ? sizeof(float) : sizeof(T);
+  for (int z = 0; z < nb; z++) {  // a batch is launched item by item
+    GemmArgs b = a;
+    b.batch = 1;
+    b.A = (const T*)a.A + z * a.sA;
+    b.B = (const T*)a.B + z * a.sB;
+    b.D = (char*)a.D + z * a.sD * dsz;
+    if (a.aux) b.aux = (T*)a.aux + z * a.sAux;
+    launch_k(gemm_simt_kernel<T>, dim3(grid), dim3(256), 0, st, b);
+  }
+  return launch_status(nb);
 }
 
 // ============================================================================

@@ -123,8 +123,13 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.losses = take(BT * 4);
   b.loss = take(256);
   b.dres = take(BT * C * 4);
-  b.dres_c = c.precision == GPT2_PRECISION_BF16 ? take(BT * C * es) : b.dres;
-  b.dbig = take(BT * 4 * C * es);
+  // output gradients every layer keeps until the weight gradients of all
+  // layers are taken together after the backward pass: the residual gradient
+  // entering the fc projection and the attention projection ([L][2][BT][C]),
+  // the fc output gradient ([L][BT][4C]) and the qkv gradient ([L][BT][3C])
+  b.dresc = take(L * 2 * BT * C * es);
+  b.dfch = take(L * BT * 4 * C * es);
+  b.dqkv = take(L * BT * 3 * C * es);
   b.dsmall = take(BT * C * es);
   b.attD = take(BT * c.H * 4);
   // dS blocks of the tensor-core attention backward (by shape alone, so the
@@ -133,13 +138,12 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), colsum_partial_floats((int)BT, 4 * (int)C)) *
                    sizeof(float));
   b.keys = take(encoder_backward_scratch_bytes((int)BT));
-  // split-K workspace of the weight-gradient GEMMs (bf16 mode): the largest any layer needs
+  // split-K workspace of the classifier weight gradient (bf16 mode)
   b.ws_floats = 0;
   if (c.precision == GPT2_PRECISION_BF16) {
     const int iBT = (int)BT, iC = (int)C;
-    const int shapes[5][2] = {{c.Vp, iC}, {iC, 4 * iC}, {4 * iC, iC}, {iC, iC}, {3 * iC, iC}};
-    for (auto& sh : shapes)
-      b.ws_floats = std::max(b.ws_floats, gemm_tc_workspace_floats(sh[0], sh[1], iBT, GPT2_NOMINAL_SMS));
+    // (the per-layer weight gradients run batched over the layers, unsplit)
+    b.ws_floats = gemm_tc_workspace_floats(c.Vp, iC, iBT, GPT2_NOMINAL_SMS);
   }
   b.ws = take(std::max<size_t>(b.ws_floats, 1) * sizeof(float));
   b.gnorm = take((2 + grad_norm_scratch_floats()) * sizeof(float));  // norm, clip factor, chunk sums
@@ -183,9 +187,11 @@ struct Step {
   float* losses() const { return m->at<float>(m->bl.losses); }
   float* dres() const { return m->at<float>(m->bl.dres); }
   // operand copy of dres for the GEMMs (== dres in fp32 mode)
-  T* dres_c() const { return m->at<T>(m->bl.dres_c); }
-  T* dres_c_or_null() const { return c.precision == GPT2_PRECISION_BF16 ? dres_c() : nullptr; }
-  T* dbig() const { return m->at<T>(m->bl.dbig); }
+  // copy of the residual gradient that enters layer l's fc projection (k = 0)
+  // or attention projection (k = 1)
+  T* dresc(size_t l, int k) const { return m->at<T>(m->bl.dresc) + (2 * l + k) * BT * C; }
+  T* dfch(size_t l) const { return m->at<T>(m->bl.dfch) + l * BT * 4 * C; }
+  T* dqkv(size_t l) const { return m->at<T>(m->bl.dqkv) + l * BT * 3 * C; }
   T* dsmall() const { return m->at<T>(m->bl.dsmall); }
   int* flags() const { return m->at<int>(m->bl.flags); }
 
@@ -197,7 +203,7 @@ struct Step {
     else e = gemm_simt<T>(a, m->st);
     if (rec) {
       cudaEventRecord(m->prof_ev[2 * m->prof_n + 1], m->st);
-      m->prof_flops[m->prof_n++] = 2.0 * a.M * a.N * (double)a.K;
+      m->prof_flops[m->prof_n++] = 2.0 * a.M * a.N * (double)a.K * (a.batch > 1 ? a.batch : 1);
     }
     return e;
   }
@@ -215,6 +221,14 @@ struct Step {
   cudaError_t linear_wgrad(float* dW, const T* dY, const T* X, int M, int N, int K) {
     GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32,
                m->at<float>(m->bl.ws), m->bl.ws_floats};
+    return gemm(a);
+  }
+  // the same for every layer at once: item l reads dY + l*sY and X + l*sX and
+  // adds into dW + l*N*K (the [L]-stacked gradient of one weight type)
+  cudaError_t linear_wgrad_layers(float* dW, const T* dY, long long sY, const T* X, long long sX, int M, int N,
+                                  int K) {
+    GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32, nullptr, 0,
+               (int)c.L, sY, sX, (long long)N * K, 0};
     return gemm(a);
   }
 
@@ -277,33 +291,40 @@ struct Step {
     CK(m, linear_wgrad(G(GPT2_WTE), logits(), ln(f), BTi, c.Vp, Ci));
     // final LayerNorm; the column sums of the resulting dres are the bias
     // gradient of the last fc projection (its output gradient is dres)
-    CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
+    CK(m, layernorm_backward<T>(dres(), dresc(L - 1, 0), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
                                 Ci, 0, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part, st));
+    // the input-gradient chain, layer by layer; every weight gradient waits
+    // for the end (below), so its operands are kept per layer
     for (int l = Li - 1; l >= 0; l--) {
       // fc projection (+ GELU backward fused into its input-gradient GEMM)
-      CK(m, linear_dgrad(dbig(), dres_c(), W(GPT2_FCPROJW, l, 4 * CC), BTi, Ci, 4 * Ci, fch(l)));
-      CK(m, linear_wgrad(G(GPT2_FCPROJW, l, 4 * CC), dres_c(), fchg(l), BTi, Ci, 4 * Ci));
+      CK(m, linear_dgrad(dfch(l), dresc(l, 0), W(GPT2_FCPROJW, l, 4 * CC), BTi, Ci, 4 * Ci, fch(l)));
       // fc
-      CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_FCW, l, 4 * CC), BTi, 4 * Ci, Ci));
-      CK(m, linear_wgrad(G(GPT2_FCW, l, 4 * CC), dbig(), ln(2 * l + 1), BTi, 4 * Ci, Ci));
-      CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dbig(), BTi, 4 * Ci, 4 * Ci, part, st));
+      CK(m, linear_dgrad(dsmall(), dfch(l), W(GPT2_FCW, l, 4 * CC), BTi, 4 * Ci, Ci));
       // LN2 (+ residual gradient; its column sums give the attention-projection bias gradient)
-      CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
+      CK(m, layernorm_backward<T>(dres(), dresc(l, 1), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
                                   rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, G(GPT2_LN2W, l, C),
                                   G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C), part, st));
       // attention projection
-      CK(m, linear_dgrad(dsmall(), dres_c(), W(GPT2_ATTPROJW, l, CC), BTi, Ci, Ci));
-      CK(m, linear_wgrad(G(GPT2_ATTPROJW, l, CC), dres_c(), atty(l), BTi, Ci, Ci));
+      CK(m, linear_dgrad(dsmall(), dresc(l, 1), W(GPT2_ATTPROJW, l, CC), BTi, Ci, Ci));
       // attention
-      CK(m, attention_bwd(dbig(), dsmall(), qkv(l), atty(l), lse(l)));
+      CK(m, attention_bwd(dqkv(l), dsmall(), qkv(l), atty(l), lse(l)));
       // qkv
-      CK(m, linear_dgrad(dsmall(), dbig(), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
-      CK(m, linear_wgrad(G(GPT2_QKVW, l, 3 * CC), dbig(), ln(2 * l), BTi, 3 * Ci, Ci));
-      CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dbig(), BTi, 3 * Ci, 3 * Ci, part, st));
+      CK(m, linear_dgrad(dsmall(), dqkv(l), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
       // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)
-      CK(m, layernorm_backward<T>(dres(), dres_c_or_null(), dsmall(), resid(2 * l), mean(2 * l), rstd(2 * l),
-                                  W(GPT2_LN1W, l, C), BTi, Ci, 1, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
+      CK(m, layernorm_backward<T>(dres(), l > 0 ? dresc(l - 1, 0) : nullptr, dsmall(), resid(2 * l), mean(2 * l),
+                                  rstd(2 * l), W(GPT2_LN1W, l, C), BTi, Ci, 1, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
                                   l > 0 ? G(GPT2_FCPROJB, l - 1, C) : nullptr, part, st));
+    }
+    // weight gradients of every layer, one batched product per weight type
+    const long long sBT = (long long)BTi * Ci;
+    CK(m, linear_wgrad_layers(G(GPT2_FCPROJW), dresc(0, 0), 2 * sBT, fchg(0), 4 * sBT, BTi, Ci, 4 * Ci));
+    CK(m, linear_wgrad_layers(G(GPT2_FCW), dfch(0), 4 * sBT, ln(1), 2 * sBT, BTi, 4 * Ci, Ci));
+    CK(m, linear_wgrad_layers(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, BTi, Ci, Ci));
+    CK(m, linear_wgrad_layers(G(GPT2_QKVW), dqkv(0), 3 * sBT, ln(0), 2 * sBT, BTi, 3 * Ci, Ci));
+    // bias gradients of the fc and qkv layers: column sums of their output gradients
+    for (int l = 0; l < Li; l++) {
+      CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dfch(l), BTi, 4 * Ci, 4 * Ci, part, st));
+      CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dqkv(l), BTi, 3 * Ci, 3 * Ci, part, st));
     }
     CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
     return GPT2_OK;

@@ -90,6 +90,24 @@ int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const 
   return rc_of(gemm_simt<float>(a, ST(stream)));
 }
 
+int gpt2_op_matmul_batched(int dtype, int batch, const void* A, long long lda, long long sA, int a_kmajor,
+                           const void* B, long long ldb, long long sB, int b_kmajor, int M, int N, int K, void* D,
+                           long long ldd, long long sD, void* aux, long long ldaux, long long sAux, int epilogue,
+                           int path, int* flags_dev, void* stream) {
+  if (bad_dtype(dtype) || batch <= 0 || !A || !B || !D || M <= 0 || N <= 0 || K <= 0 || epilogue < 0 || epilogue > 3)
+    return GPT2_ERR_INVALID_ARG;
+  if ((epilogue == EPI_GELU || epilogue == EPI_GELU_BWD) && !aux) return GPT2_ERR_INVALID_ARG;
+  if (sA < 0 || sB < 0 || sD < 0 || sAux < 0 || path < 0 || path > 2) return GPT2_ERR_INVALID_ARG;
+  GemmArgs a{A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, nullptr, aux, ldaux, epilogue,
+             nullptr, 0, batch, sA, sB, sD, sAux};
+  if (path == 2 || (path == 0 && dtype == GPT2_PRECISION_BF16 && gemm_tc_supported(a))) {
+    if (dtype != GPT2_PRECISION_BF16 || !flags_dev || !gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
+    return rc_of(gemm_tc(a, flags_dev, ST(stream)));
+  }
+  if (dtype == GPT2_PRECISION_BF16) return rc_of(gemm_simt<bf16>(a, ST(stream)));
+  return rc_of(gemm_simt<float>(a, ST(stream)));
+}
+
 int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H, int path,
                               int* flags_dev, void* stream) {
   if (bad_dtype(dtype) || !out || !lse || !qkv || B <= 0 || T <= 0 || C <= 0 || H <= 0 || C % H) return GPT2_ERR_INVALID_ARG;

@@ -23,6 +23,8 @@ _sigs = {
     "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
     "gpt2_op_matmul_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P, _sz, _P]),
+    "gpt2_op_matmul_batched": (_i, [_i, _i, _P, _ll, _ll, _i, _P, _ll, _ll, _i, _i, _i, _i, _P, _ll, _ll, _P, _ll, _ll,
+                                    _i, _i, _P, _P]),
     "gpt2_op_attention_forward": (_i, [_i, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P]),
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P, _sz, _P]),
@@ -115,6 +117,13 @@ def gpt2_op_matmul(A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias=Non
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _ck(lib.gpt2_op_matmul(_dt(A), _p(A), lda, a_kmajor, _p(B), ldb, b_kmajor, M, N, K, _p(D), ldd, _p(bias),
                            _p(aux), ldaux, epilogue, path, _p(flags_dev), _p(workspace), wsb, _s(stream)), "matmul")
+
+
+def gpt2_op_matmul_batched(batch, A, lda, sA, a_kmajor, B, ldb, sB, b_kmajor, M, N, K, D, ldd, sD, aux=None, ldaux=0,
+                           sAux=0, epilogue=EPI_STORE, path=PATH_AUTO, flags_dev=None, stream=None):
+    _ck(lib.gpt2_op_matmul_batched(_dt(A), batch, _p(A), lda, sA, a_kmajor, _p(B), ldb, sB, b_kmajor, M, N, K, _p(D),
+                                   ldd, sD, _p(aux), ldaux, sAux, epilogue, path, _p(flags_dev), _s(stream)),
+        "matmul_batched")
 
 
 def gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, path=PATH_AUTO, flags_dev=None, stream=None):

@@ -102,6 +102,17 @@ int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const 
                    int b_kmajor, int M, int N, int K, void* D, long long ldd, const void* bias, void* aux,
                    long long ldaux, int epilogue, int path, int* flags_dev, void* workspace,
                    size_t workspace_bytes, void* stream);
+/* `batch` independent products of the same shape in one launch: item z uses
+ * A + z*sA, B + z*sB, D + z*sD and aux + z*sAux (strides in elements of each
+ * array's type; multiples of 16 bytes on the tensor-core path), with the
+ * layouts and epilogues of gpt2_op_matmul but no bias and no K split.  Each
+ * item's output tile is written by exactly one CTA, so epilogue 3 (D +=) stays
+ * deterministic.  The weight-gradient products of all layers of a model, taken
+ * together after the backward pass, are the intended use. */
+int gpt2_op_matmul_batched(int dtype, int batch, const void* A, long long lda, long long sA, int a_kmajor,
+                           const void* B, long long ldb, long long sB, int b_kmajor, int M, int N, int K, void* D,
+                           long long ldd, long long sD, void* aux, long long ldaux, long long sAux, int epilogue,
+                           int path, int* flags_dev, void* stream);
 
 /* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
  * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of

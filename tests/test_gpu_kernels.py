@@ -315,6 +315,66 @@ def test_matmul_tc_split_k_weight_gradient(ops, BT, N, K):
     assert rel_l2(host(outs[0]), ref) < 2e-5
 
 
+@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("batch,BT,N,K,gap", [(3, 1024 + 64, 264, 136, 0), (12, 2048, 256, 512, 16),
+                                              (2, 16384, 768, 768, 8)])
+def test_matmul_batched_weight_gradient(ops, path, batch, BT, N, K, gap):
+    """Batched weight gradients dW_z[N][K] += dY_z^T X_z (both operands
+    MN-major) with items `gap` rows apart in their arrays (strided, as a
+    model's per-layer tensors are): each item against the float64 product,
+    bitwise repeatable."""
+    if path == "simt" and BT * N * K * batch > 2e9:
+        pytest.skip("SIMT reference path: small cases only")
+    sY, sX, sW = (BT + gap) * N, (BT + gap) * K, (N + gap) * K
+    dY = normal_array((batch * sY,), 156)
+    X = normal_array((batch * sX,), 157)
+    W0 = normal_array((batch * sW,), 158)
+    tdy, tx = dev(dY, torch.bfloat16), dev(X, torch.bfloat16)
+    fl = ops.flags()
+    p = ops.PATH_TC if path == "tc" else ops.PATH_SIMT
+    outs = []
+    for _ in range(2):
+        dW = dev(W0)
+        ops.gpt2_op_matmul_batched(batch, tdy, N, sY, 0, tx, K, sX, 0, N, K, BT, dW, K, sW,
+                                   epilogue=ops.EPI_ACC_F32, path=p, flags_dev=fl)
+        outs.append(dW)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    assert torch.equal(outs[0], outs[1])
+    hy, hx, got = host(tdy), host(tx), host(outs[0])
+    for z in range(batch):
+        Y = hy[z * sY:z * sY + BT * N].reshape(BT, N).astype(np.float64)
+        Xz = hx[z * sX:z * sX + BT * K].reshape(BT, K).astype(np.float64)
+        ref = W0[z * sW:z * sW + N * K].reshape(N, K) + Y.T @ Xz
+        assert rel_l2(got[z * sW:z * sW + N * K].reshape(N, K), ref) < 2e-5, z
+        # the gap rows between items are untouched
+        assert np.array_equal(got[z * sW + N * K:(z + 1) * sW], W0[z * sW + N * K:(z + 1) * sW])
+
+
+@pytest.mark.parametrize("epi", ["store", "gelu_bwd"])
+def test_matmul_batched_bf16_epilogues(ops, epi):
+    """Batched K-major products with bf16 output (and the GELU' epilogue with a
+    strided aux), the shape of per-layer input gradients."""
+    batch, M, N, K = 3, 1000, 384, 200
+    A, B = normal_array((batch, M, K), 159), normal_array((batch, N, K), 160)
+    tA, tB = dev(A, torch.bfloat16), dev(B, torch.bfloat16)
+    D = torch.full((batch, M, N), float("nan"), device="cuda", dtype=torch.bfloat16)
+    fl = ops.flags()
+    if epi == "store":
+        ops.gpt2_op_matmul_batched(batch, tA, K, M * K, 1, tB, K, N * K, 1, M, N, K, D, N, M * N, path=ops.PATH_TC,
+                                   flags_dev=fl)
+    else:
+        pre = dev(normal_array((batch, M, N), 161), torch.bfloat16)
+        ops.gpt2_op_matmul_batched(batch, tA, K, M * K, 1, tB, K, N * K, 1, M, N, K, D, N, M * N, aux=pre, ldaux=N,
+                                   sAux=M * N, epilogue=ops.EPI_GELU_BWD, path=ops.PATH_TC, flags_dev=fl)
+    assert fl.sum().item() == 0
+    hA, hB, got = host(tA), host(tB), host(D)
+    for z in range(batch):
+        acc = hA[z] @ hB[z].T
+        ref = acc if epi == "store" else O.gelu_backward(host(pre)[z], acc)
+        assert rel_l2(got[z], ref) < 2 ** -7, z
+
+
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 @pytest.mark.parametrize("B,T,C,H", [(2, 13, 64, 4), (1, 70, 128, 2), (2, 129, 192, 3)])
