@@ -64,9 +64,12 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
                                const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
                                float* db, float* dres_sum, float* partial, cudaStream_t st);
 size_t ln_backward_partial_floats(int rows, int C);
-// out[c] += sum_rows X[r*ldx + c]; partial: colsum_partial_floats(rows, cols) floats
+// out[c] += sum_rows X[r*ldx + c]; partial: colsum_partial_floats(rows, cols) floats.
+// nbatch > 1: the same for items z = 0..nbatch-1 at out + z*sOut, X + z*sX
+// (partial: nbatch times as many floats), in one pair of launches.
 template <typename T>
-cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st);
+cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st,
+                   int nbatch = 1, long long sOut = 0, long long sX = 0);
 size_t colsum_partial_floats(int rows, int cols);
 int reduce_chunks(int rows);  // number of row chunks the reductions use
 

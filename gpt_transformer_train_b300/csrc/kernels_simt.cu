@@ -295,17 +295,20 @@ size_t ln_backward_partial_floats(int rows, int C) { return (size_t)reduce_chunk
 size_t colsum_partial_floats(int rows, int cols) { return (size_t)reduce_chunks(rows) * cols; }
 
 // out_o[c] += sum_k partial[k][o][c] for o < nout (out_o may be null: skipped).
-// Block (column group of 32, output o); warp w sums chunks w, w+8, ... in
-// order, then the eight warp sums are added in warp order.
+// Block (column group of 32, output o, batch item z: partial and out_o
+// advance by nchunks*nout*C and sOut per item); warp w sums chunks w, w+8,
+// ... in order, then the eight warp sums are added in warp order.
 __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict__ out0, float* __restrict__ out1,
                                                               float* __restrict__ out2,
                                                               const float* __restrict__ partial, int nchunks,
-                                                              int C, int nout) {
+                                                              int C, int nout, long long sOut) {
   pdl_enter();
   __shared__ float sh[8][32];
   const int o = blockIdx.y;
   float* out = o == 0 ? out0 : (o == 1 ? out1 : out2);
   if (!out) return;
+  out += blockIdx.z * sOut;
+  partial += (size_t)blockIdx.z * nchunks * nout * C;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + lane;
   // chunks w, w+8, w+16, ... in increasing order; eight loads in flight, added in that order
@@ -334,9 +337,9 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict_
 }
 
 static cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
-                                   int nout, cudaStream_t st) {
-  dim3 grid((unsigned)cdiv(C, 32), nout);
-  launch_k(reduce_partials_kernel, dim3(grid), dim3(256), 0, st, out0, out1, out2, partial, nchunks, C, nout);
+                                   int nout, cudaStream_t st, int nbatch = 1, long long sOut = 0) {
+  dim3 grid((unsigned)cdiv(C, 32), nout, nbatch);
+  launch_k(reduce_partials_kernel, dim3(grid), dim3(256), 0, st, out0, out1, out2, partial, nchunks, C, nout, sOut);
   return launch_status(1);
 }
 
@@ -671,8 +674,10 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
 // ============================================================================
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ X,
-                                                             int rows, int cols, long long ldx) {
+                                                             int rows, int cols, long long ldx, long long sX) {
   pdl_enter();
+  X += blockIdx.z * sX;  // batch item z: its own matrix and partial rows
+  partial += (size_t)blockIdx.z * gridDim.y * cols;
   constexpr int N = VecN<T>::n;
   extern __shared__ float cs_sh[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -715,15 +720,17 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__
 }
 
 template <typename T>
-cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st) {
+cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st,
+                   int nbatch, long long sOut, long long sX) {
   constexpr int N = VecN<T>::n;
-  if (cols % N || ldx % N) return cudaErrorInvalidValue;
+  if (cols % N || ldx % N || nbatch < 1 || nbatch > 65535) return cudaErrorInvalidValue;
   const int nch = reduce_chunks(rows);
-  dim3 grid((unsigned)cdiv(cols / N, 32), nch);
-  launch_k(colsum_partial_kernel<T>, dim3(grid), dim3(256), 32 * N * sizeof(float), st, partial, X, rows, cols, ldx);
+  dim3 grid((unsigned)cdiv(cols / N, 32), nch, nbatch);
+  launch_k(colsum_partial_kernel<T>, dim3(grid), dim3(256), 32 * N * sizeof(float), st, partial, X, rows, cols, ldx,
+           sX);
   cudaError_t e = launch_status(1);
   if (e != cudaSuccess) return e;
-  return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st);
+  return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st, nbatch, sOut);
 }
 
 // ============================================================================
@@ -1500,7 +1507,8 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   template cudaError_t layernorm_backward<T>(float*, T*, const T*, const T*, const float*, const float*,  \
                                              const T*, int, int, int, float*, float*, float*, float*,     \
                                              cudaStream_t);                                               \
-  template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t);            \
+  template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t, int, long long,  \
+                                 long long);                                                              \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \
   template cudaError_t attention_forward_simt<T>(T*, float*, const T*, int, int, int, int, cudaStream_t); \
   template cudaError_t attention_backward_simt<T>(T*, float*, const T*, const T*, const T*, const float*, \

@@ -135,7 +135,8 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   // dS blocks of the tensor-core attention backward (by shape alone, so the
   // size does not depend on the machine the layout is computed on)
   b.attS = c.precision == GPT2_PRECISION_BF16 && c.C == 64 * c.H ? take(attention_tc_ds_bytes(c.B, c.T, c.H)) : 0;
-  b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), colsum_partial_floats((int)BT, 4 * (int)C)) *
+  // LayerNorm-backward partials, or the column-sum partials of all layers' fc output gradients
+  b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), L * colsum_partial_floats((int)BT, 4 * (int)C)) *
                    sizeof(float));
   b.keys = take(encoder_backward_scratch_bytes((int)BT));
   // split-K workspace of the classifier weight gradient (bf16 mode)
@@ -321,11 +322,9 @@ struct Step {
     CK(m, linear_wgrad_layers(G(GPT2_FCW), dfch(0), 4 * sBT, ln(1), 2 * sBT, BTi, 4 * Ci, Ci));
     CK(m, linear_wgrad_layers(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, BTi, Ci, Ci));
     CK(m, linear_wgrad_layers(G(GPT2_QKVW), dqkv(0), 3 * sBT, ln(0), 2 * sBT, BTi, 3 * Ci, Ci));
-    // bias gradients of the fc and qkv layers: column sums of their output gradients
-    for (int l = 0; l < Li; l++) {
-      CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dfch(l), BTi, 4 * Ci, 4 * Ci, part, st));
-      CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dqkv(l), BTi, 3 * Ci, 3 * Ci, part, st));
-    }
+    // bias gradients of the fc and qkv layers of every layer: column sums of their output gradients
+    CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT));
+    CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT));
     CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
     return GPT2_OK;
   }

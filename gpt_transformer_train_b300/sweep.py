@@ -10,8 +10,9 @@ against the measured peaks (HBM copy GB/s, bf16 burst TFLOP/s).
   python -m gpt_transformer_train_b300.sweep [--kernel NAME ...] [--reps N] [--warmup N]
 
 Kernel names: ln_fwd ln_bwd gelu_fwd gelu_bwd softmax_ce adamw encoder_fwd
-encoder_bwd attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096} and
-gemm_<layer>_{fwd,dgrad,wgrad} for layer in qkv attproj fc fcproj classifier.
+encoder_bwd attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096},
+gemm_<layer>_{fwd,dgrad,wgrad} for layer in qkv attproj fc fcproj classifier,
+and wgradL_<layer> (that weight gradient for 12 layers in one batched launch).
 """
 from __future__ import annotations
 
@@ -117,6 +118,15 @@ def make_case(name, ops):
         return (lambda: ops.gpt2_op_attention_backward(dqkv, dout, qkv, out, lse, B, T, C, H, path=ops.PATH_TC,
                                                        flags_dev=fl, scratch=D),
                 2.5 * flops_fwd, "FLOP")
+    if name.startswith("wgradL_"):  # the weight gradient of one layer type for all 12 layers, one batched launch
+        layer = name.split("_")[1]
+        N, K = GEMM_LAYERS[layer]
+        L = 12
+        dy, x = randn((L, BT, N), 27), randn((L, BT, K), 28)
+        dW = torch.zeros(L, N, K, device="cuda")
+        return (lambda: ops.gpt2_op_matmul_batched(L, dy, N, BT * N, 0, x, K, BT * K, 0, N, K, BT, dW, K, N * K,
+                                                   epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC, flags_dev=fl),
+                2.0 * L * BT * N * K, "FLOP")
     if name.startswith("gemm_"):
         _, layer, kind = name.split("_")
         N, K = GEMM_LAYERS[layer]
@@ -142,7 +152,8 @@ def make_case(name, ops):
 
 ALL = (["ln_fwd", "ln_bwd", "gelu_fwd", "gelu_bwd", "softmax_ce", "adamw", "encoder_fwd", "encoder_bwd"] +
        [f"attn_{d}_T{t}" for d in ("fwd", "bwd") for t in (256, 1024, 4096)] +
-       [f"gemm_{l}_{k}" for l in GEMM_LAYERS for k in ("fwd", "dgrad", "wgrad")])
+       [f"gemm_{l}_{k}" for l in GEMM_LAYERS for k in ("fwd", "dgrad", "wgrad")] +
+       [f"wgradL_{l}" for l in ("qkv", "attproj", "fc", "fcproj")])
 
 
 def main():
