@@ -50,6 +50,12 @@ cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, 
 cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
                              int C, uint32_t* keys, cudaStream_t st);
 size_t encoder_backward_scratch_bytes(int BT);
+// the same with a larger scratch (BT <= 16384): radix-sorted keys and
+// fixed-size chunks of the per-token sums, so no CTA waits on a long run
+bool encoder_backward_fast_supported(int BT, int C);
+size_t encoder_backward_fast_scratch_bytes(int BT, int C);
+cudaError_t encoder_backward_fast(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_, int C,
+                                  void* scratch, cudaStream_t st);
 
 template <typename T>
 cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* rstd, const T* a,

@@ -121,45 +121,78 @@ __global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restri
 }
 
 // Block (i, column chunk of 128): if sorted key i starts a token run, sum that
-// run's rows.  Warp w takes the run's rows w, w+8, ... in order (float4 per
-// lane), then the eight warp sums are added in warp order: a fixed summation
-// order independent of timing, so the result is deterministic.
-__global__ void __launch_bounds__(256) wte_grad_runs_kernel(float* __restrict__ dwte, const float* __restrict__ dres,
-                                                            const uint32_t* __restrict__ keys, int BT, int C) {
+// run's rows.  The run is cut at the multiples of WTE_CH in sorted order (the
+// chunks of the large-scratch form below); warp w sums segments w, w+8, ...,
+// each in entry order, and warp 0 adds the segment sums in order: the same
+// additions in the same order as the large-scratch form, so both forms give
+// identical bits.
+constexpr int WTE_CH = 32;  // sorted entries per chunk
+constexpr int RUNS_WARPS = 8;
+__global__ void __launch_bounds__(32 * RUNS_WARPS) wte_grad_runs_kernel(float* __restrict__ dwte,
+                                                                        const float* __restrict__ dres,
+                                                                        const uint32_t* __restrict__ keys, int BT,
+                                                                        int C) {
   pdl_enter();
-  __shared__ float4 sh[8][32];
+  __shared__ float4 part[RUNS_WARPS][32];
   const int i = blockIdx.x;
   const uint32_t tk = keys[i] >> 16;
   if (i > 0 && (keys[i - 1] >> 16) == tk) return;
+  int lo = i + 1, hi = BT;  // first entry past the run
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((keys[mid] >> 16) <= tk) lo = mid + 1;
+    else hi = mid;
+  }
+  const int j = lo, c0 = i / WTE_CH, nseg = (j - 1) / WTE_CH - c0 + 1;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int cv = blockIdx.y * 32 + lane;  // float4 column
   const bool on = cv < C / 4;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = i + w; j < BT; j += 8) {
-    const uint32_t kj = keys[j];
-    if ((kj >> 16) != tk) break;
-    if (on) {
-      const float4 x = __ldcs(reinterpret_cast<const float4*>(dres + (size_t)(kj & 0xFFFFu) * C) + cv);
-      s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-    }
-  }
-  sh[w][lane] = s;
-  __syncthreads();
-  if (w == 0 && on) {
-    float4 t = sh[0][lane];
+  float4 total = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < nseg; base += RUNS_WARPS) {
+    const int k = base + w;
+    float4 sg = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k < nseg) {
+      const int a = max(i, (c0 + k) * WTE_CH), b = min(j, (c0 + k + 1) * WTE_CH);
+      const uint32_t mykey = a + lane < b ? keys[a + lane] : 0u;  // the segment's keys, one per lane
+      for (int e = 0; e < b - a; e += 8) {
+        float4 x[8];
 #pragma unroll
-    for (int q = 1; q < 8; q++) {
-      t.x += sh[q][lane].x; t.y += sh[q][lane].y; t.z += sh[q][lane].z; t.w += sh[q][lane].w;
+        for (int u = 0; u < 8; u++) {
+          const uint32_t ku = __shfl_sync(0xffffffffu, mykey, (e + u) & 31);
+          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (on && e + u < b - a) x[u] = __ldcs(reinterpret_cast<const float4*>(dres + (size_t)(ku & 0xFFFFu) * C) + cv);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+          if (e + u < b - a) {
+            sg.x += x[u].x; sg.y += x[u].y; sg.z += x[u].z; sg.w += x[u].w;
+          }
+      }
     }
+    part[w][lane] = sg;
+    __syncthreads();
+    if (w == 0) {
+      const int nq = min(RUNS_WARPS, nseg - base);
+      for (int q = 0; q < nq; q++) {
+        const float4 y = part[q][lane];
+        if (base == 0 && q == 0) total = y;
+        else {
+          total.x += y.x; total.y += y.y; total.z += y.z; total.w += y.w;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (w == 0 && on) {
     float4* dst = reinterpret_cast<float4*>(dwte + (size_t)tk * C) + cv;
     float4 o = *dst;
-    o.x += t.x; o.y += t.y; o.z += t.z; o.w += t.w;
+    o.x += total.x; o.y += total.y; o.z += total.z; o.w += total.w;
     *dst = o;
   }
 }
 
 cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
-                             int C, uint32_t* keys, cudaStream_t st) {
+                             int C, uint32_t* keys, cudaStream_t st) {  // the small-scratch form
   int BT = B * T_;
   int n = pow2_at_least(BT);
   if (n > 32768) return cudaErrorInvalidValue;
@@ -174,6 +207,202 @@ cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const 
   launch_k(bitonic_sort_keys_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT, n);
   launch_k(wte_grad_runs_kernel, dim3((unsigned)BT, (unsigned)cdiv(C / 4, 32)), dim3(256), 0, st, dwte, dres, keys, BT, C);
   return launch_status(3);
+}
+
+// ----------------------------------------------------------------------------
+// The same encoder backward with a larger scratch (encoder_backward_fast_*):
+// the keys are sorted by one CTA with a two-pass least-significant-digit
+// radix sort on the token (8 bits a pass; positions start in order and every
+// pass is stable, so equal tokens stay in position order), and the dwte sums
+// go over fixed chunks of WTE_CH sorted entries, so that no CTA waits on a
+// long run of one frequent token:
+//   - a run of one token that starts and ends inside a chunk is summed there
+//     and added into dwte;
+//   - a run crossing chunk boundaries leaves one partial sum per chunk it
+//     touches (slot 0: the chunk's first segment, slot 1: its last), and the
+//     chunk where the run starts adds those partials into dwte in chunk order.
+// Every dwte row is written by exactly one CTA and every sum has a fixed
+// order: the result is deterministic.
+// ----------------------------------------------------------------------------
+constexpr int RADIX_MAX = 16384;  // keys the one-CTA radix sort holds in shared memory (twice)
+static size_t fast_keys_bytes(int BT) { return ((size_t)BT * 4 + 255) & ~(size_t)255; }
+size_t encoder_backward_fast_scratch_bytes(int BT, int C) {
+  return fast_keys_bytes(BT) + (size_t)cdiv(BT, WTE_CH) * 2 * C * sizeof(float);
+}
+bool encoder_backward_fast_supported(int BT, int C) { return BT > 0 && BT <= RADIX_MAX && C % 4 == 0; }
+
+__global__ void __launch_bounds__(1024) radix_sort_tokens_kernel(uint32_t* __restrict__ keys_out,
+                                                                 const int* __restrict__ tok, int BT) {
+  pdl_enter();
+  extern __shared__ uint32_t rs_sh[];
+  uint32_t* bufA = rs_sh;
+  uint32_t* bufB = rs_sh + BT;
+  uint32_t* cur = rs_sh + 2 * BT;  // [32 warps][256 digits]: counts, then scatter cursors
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int seg = ((BT + 31) / 32 + 31) & ~31;  // keys per warp, a multiple of 32
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < BT; i += blockDim.x) bufA[i] = (((uint32_t)tok[i] & 0xFFFFu) << 16) | (uint32_t)i;
+  for (int pass = 0; pass < 2; pass++) {
+    const int shift = 16 + 8 * pass;
+    const uint32_t* src = pass == 0 ? bufA : bufB;
+    uint32_t* dst = pass == 0 ? bufB : bufA;
+    for (int i = threadIdx.x; i < 32 * 256; i += blockDim.x) cur[i] = 0;
+    __syncthreads();
+    for (int i = w * seg + lane; i < min(BT, (w + 1) * seg); i += 32) atomicAdd(&cur[w * 256 + ((src[i] >> shift) & 255)], 1u);
+    __syncthreads();
+    // exclusive scan in (digit, warp) order: thread t owns entries 8t .. 8t+7
+    // of that order (digit = e / 32, warp = e % 32)
+    uint32_t v[8], tsum = 0;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const int e = 8 * threadIdx.x + q;
+      v[q] = cur[(e & 31) * 256 + (e >> 5)];
+      tsum += v[q];
+    }
+    uint32_t incl = tsum;  // inclusive scan of the thread sums: within the warp, then over the warps
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __shared__ uint32_t wsum[32];
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    uint32_t wpre = 0;
+    for (int q = 0; q < w; q++) wpre += wsum[q];
+    uint32_t run = wpre + incl - tsum;  // exclusive prefix of this thread's first entry
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+      const int e = 8 * threadIdx.x + q;
+      cur[(e & 31) * 256 + (e >> 5)] = run;
+      run += v[q];
+    }
+    __syncthreads();
+    // stable scatter: each warp walks its keys in order, 32 at a time
+    for (int base = w * seg; base < (w + 1) * seg; base += 32) {
+      const int i = base + lane;
+      const bool valid = i < BT;
+      const uint32_t key = valid ? src[i] : 0u;
+      const uint32_t d = valid ? (key >> shift) & 255 : 256u + lane;  // invalid lanes match nobody
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      uint32_t pos = 0;
+      if (valid) pos = cur[w * 256 + d] + __popc(peers & lt);
+      __syncwarp();
+      if (valid) {
+        dst[pos] = key;
+        if (lane == 31 - __clz(peers)) cur[w * 256 + d] += __popc(peers);
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < BT; i += blockDim.x) keys_out[i] = bufA[i];
+}
+
+// Block (chunk c, 128 float4 columns): the segments of equal tokens among
+// sorted entries [c*WTE_CH, (c+1)*WTE_CH), each summed in entry order
+__global__ void __launch_bounds__(128) wte_chunk_kernel(float* __restrict__ dwte, const float* __restrict__ dres,
+                                                        const uint32_t* __restrict__ keys,
+                                                        float* __restrict__ slots, int BT, int C) {
+  pdl_enter();
+  __shared__ uint32_t sk[WTE_CH + 2];  // tokens of entries e0-1 .. e1 (0xFFFFFFFF outside 0..BT-1)
+  const int c = blockIdx.x, e0 = c * WTE_CH, e1 = min(BT, e0 + WTE_CH), ne = e1 - e0;
+  if (threadIdx.x < ne + 2) {
+    const int e = e0 - 1 + (int)threadIdx.x;
+    sk[threadIdx.x] = (e >= 0 && e < BT) ? keys[e] : 0xFFFFFFFFu;
+  }
+  __syncthreads();
+  auto tok_at = [&](int e) { return sk[e - e0 + 1] >> 16; };  // e in e0-1 .. e1
+  const int cv = blockIdx.y * 128 + threadIdx.x;
+  const bool on = cv < C / 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int seg_first = e0;
+  for (int b = e0; b < e1; b += 8) {
+    float4 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (on && b + u < e1)
+        x[u] = __ldcs(reinterpret_cast<const float4*>(dres + (size_t)(sk[b + u - e0 + 1] & 0xFFFFu) * C) + cv);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int e = b + u;
+      if (e >= e1) break;
+      acc.x += x[u].x; acc.y += x[u].y; acc.z += x[u].z; acc.w += x[u].w;
+      const uint32_t t = tok_at(e);
+      if (e == e1 - 1 || tok_at(e + 1) != t) {  // end of a segment
+        const bool run_start = seg_first > e0 || tok_at(e0 - 1) != t;
+        const bool run_end = tok_at(e + 1) != t;
+        if (on) {
+          if (run_start && run_end) {
+            float4* dst = reinterpret_cast<float4*>(dwte + (size_t)t * C) + cv;
+            float4 o = *dst;
+            o.x += acc.x; o.y += acc.y; o.z += acc.z; o.w += acc.w;
+            *dst = o;
+          } else {
+            reinterpret_cast<float4*>(slots + ((size_t)c * 2 + (seg_first == e0 ? 0 : 1)) * C)[cv] = acc;
+          }
+        }
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        seg_first = e + 1;
+      }
+    }
+  }
+}
+
+// Block (chunk c, 128 float4 columns): if a run that crosses into the next
+// chunk starts in chunk c, add its partial sums into dwte in chunk order
+__global__ void __launch_bounds__(128) wte_span_kernel(float* __restrict__ dwte, const uint32_t* __restrict__ keys,
+                                                       const float* __restrict__ slots, int BT, int C) {
+  pdl_enter();
+  const int c = blockIdx.x, e0 = c * WTE_CH, e1 = min(BT, e0 + WTE_CH);
+  const uint32_t tk = keys[e1 - 1] >> 16;
+  if (e1 >= BT || (keys[e1] >> 16) != tk) return;  // the chunk's last run ends here
+  int s = e1 - 1;
+  while (s > e0 && (keys[s - 1] >> 16) == tk) s--;
+  if (s == e0 && e0 > 0 && (keys[e0 - 1] >> 16) == tk) return;  // the run started in an earlier chunk
+  int lo = e1, hi = BT;  // first entry past the run
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((keys[mid] >> 16) <= tk) lo = mid + 1;
+    else hi = mid;
+  }
+  const int c1 = (lo - 1) / WTE_CH;
+  const int cv = blockIdx.y * 128 + threadIdx.x;
+  if (cv >= C / 4) return;
+  float4 sum = reinterpret_cast<const float4*>(slots + ((size_t)c * 2 + (s == e0 ? 0 : 1)) * C)[cv];
+  for (int cc = c + 1; cc <= c1; cc++) {
+    const float4 x = reinterpret_cast<const float4*>(slots + (size_t)cc * 2 * C)[cv];
+    sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+  }
+  float4* dst = reinterpret_cast<float4*>(dwte + (size_t)tk * C) + cv;
+  float4 o = *dst;
+  o.x += sum.x; o.y += sum.y; o.z += sum.z; o.w += sum.w;
+  *dst = o;
+}
+
+cudaError_t encoder_backward_fast(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_, int C,
+                                  void* scratch, cudaStream_t st) {
+  const int BT = B * T_;
+  if (!encoder_backward_fast_supported(BT, C)) return cudaErrorInvalidValue;
+  uint32_t* keys = (uint32_t*)scratch;
+  float* slots = (float*)((char*)scratch + fast_keys_bytes(BT));
+  const long long nv = (long long)T_ * (C / 4);
+  launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C);
+  const size_t smem = ((size_t)2 * BT + 32 * 256) * sizeof(uint32_t);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(radix_sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(((size_t)2 * RADIX_MAX + 32 * 256) * sizeof(uint32_t)));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  launch_k(radix_sort_tokens_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT);
+  const dim3 grid((unsigned)cdiv(BT, WTE_CH), (unsigned)cdiv(C / 4, 128));
+  launch_k(wte_chunk_kernel, grid, dim3(128), 0, st, dwte, dres, keys, slots, BT, C);
+  launch_k(wte_span_kernel, grid, dim3(128), 0, st, dwte, keys, slots, BT, C);
+  return launch_status(4);
 }
 
 // ============================================================================

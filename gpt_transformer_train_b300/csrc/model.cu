@@ -138,7 +138,7 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   // LayerNorm-backward partials, or the column-sum partials of all layers' fc output gradients
   b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), L * colsum_partial_floats((int)BT, 4 * (int)C)) *
                    sizeof(float));
-  b.keys = take(encoder_backward_scratch_bytes((int)BT));
+  b.keys = take(std::max(encoder_backward_scratch_bytes((int)BT), encoder_backward_fast_scratch_bytes((int)BT, (int)C)));
   // split-K workspace of the classifier weight gradient (bf16 mode)
   b.ws_floats = 0;
   if (c.precision == GPT2_PRECISION_BF16) {
@@ -325,7 +325,10 @@ struct Step {
     // bias gradients of the fc and qkv layers of every layer: column sums of their output gradients
     CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT));
     CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT));
-    CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
+    if (encoder_backward_fast_supported(BTi, Ci))
+      CK(m, encoder_backward_fast(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
+    else
+      CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
     return GPT2_OK;
   }
 };

@@ -24,15 +24,18 @@ int gpt2_op_encoder_forward(int dtype, void* out, const int32_t* tokens, const v
   return rc_of(encoder_forward<float>((float*)out, tokens, (const float*)wte, (const float*)wpe, B, T, C, V, flags_dev, ST(stream)));
 }
 
-size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T) {
+size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T, int C) {
   if (B <= 0 || T <= 0 || (long long)B * T > 32768) return 0;
+  if (C > 0 && encoder_backward_fast_supported(B * T, C)) return encoder_backward_fast_scratch_bytes(B * T, C);
   return encoder_backward_scratch_bytes(B * T);
 }
 
 int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B, int T, int C,
                              void* scratch, size_t scratch_bytes, void* stream) {
   if (!dwte || !dwpe || !dres || !tokens || !scratch || B <= 0 || T <= 0 || C <= 0 || C % 4) return GPT2_ERR_INVALID_ARG;
-  if ((long long)B * T > 32768 || scratch_bytes < encoder_backward_scratch_bytes(B * T)) return GPT2_ERR_INVALID_ARG;
+  if ((long long)B * T > 32768 || scratch_bytes < gpt2_op_encoder_backward_scratch_bytes(B, T, C)) return GPT2_ERR_INVALID_ARG;
+  if (encoder_backward_fast_supported(B * T, C))
+    return rc_of(encoder_backward_fast(dwte, dwpe, dres, tokens, B, T, C, scratch, ST(stream)));
   return rc_of(encoder_backward(dwte, dwpe, dres, tokens, B, T, C, (uint32_t*)scratch, ST(stream)));
 }
 

@@ -15,7 +15,7 @@ from . import GPT2Error, PRECISION_BF16, PRECISION_FP32, lib
 _P, _i, _ll, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
 _sigs = {
     "gpt2_op_encoder_forward": (_i, [_i, _P, _P, _P, _P, _i, _i, _i, _i, _P, _P]),
-    "gpt2_op_encoder_backward_scratch_bytes": (_sz, [_i, _i]),
+    "gpt2_op_encoder_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_encoder_backward": (_i, [_P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
     "gpt2_op_encoder_backward_noalloc": (_i, [_P, _P, _P, _P, _i, _i, _i, _P]),
     "gpt2_op_residual_layernorm_forward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _P]),
@@ -80,7 +80,7 @@ def gpt2_op_encoder_forward(out, tokens, wte, wpe, B, T, C, V, flags_dev, stream
 
 
 def gpt2_op_encoder_backward(dwte, dwpe, dres, tokens, B, T, C, stream=None):
-    n = lib.gpt2_op_encoder_backward_scratch_bytes(B, T)
+    n = lib.gpt2_op_encoder_backward_scratch_bytes(B, T, C)
     sc = _scratch(n, dres.device)
     _ck(lib.gpt2_op_encoder_backward(_p(dwte), _p(dwpe), _p(dres), _p(tokens), B, T, C, _p(sc), sc.numel(),
                                      _s(stream)), "encoder_backward")

@@ -42,9 +42,13 @@ extern "C" {
 int gpt2_op_encoder_forward(int dtype, void* out, const int32_t* tokens, const void* wte, const void* wpe,
                             int B, int T, int C, int V, int* flags_dev, void* stream);
 
-/* dwpe[t] += sum_b dres[b,t];  dwte[v] += sum of dres rows with token v, summed in
- * increasing position order (deterministic).  dres: float [B*T][C]. */
-size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T);
+/* dwpe[t] += sum_b dres[b,t];  dwte[v] += sum of dres rows with token v, in a
+ * fixed order (deterministic).  dres: float [B*T][C].  With B*T <= 16384 the
+ * positions are grouped by a radix sort on the token and each token's sum is
+ * taken over fixed chunks of the sorted positions (chunk partials added in
+ * chunk order); otherwise a bitonic sort and one sum per token in position
+ * order.  scratch: gpt2_op_encoder_backward_scratch_bytes(B, T, C) bytes. */
+size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T, int C);
 int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B, int T,
                              int C, void* scratch, size_t scratch_bytes, void* stream);
 

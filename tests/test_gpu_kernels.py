@@ -83,7 +83,8 @@ def test_encoder_forward_flags_bad_tokens(ops):
     assert fl[0].item() & 1
 
 
-@pytest.mark.parametrize("B,T,C", [(2, 7, 64), (4, 64, 192), (1, 300, 768), (16, 1024, 768)])
+@pytest.mark.parametrize("B,T,C", [(2, 7, 64), (4, 64, 192), (1, 300, 768), (3, 700, 64), (16, 1024, 768),
+                                   (32, 1000, 64)])
 def test_encoder_backward_deterministic_scatter(ops, B, T, C):
     """Scatter-add without atomics: repeated calls give identical bits; values
     match the float64 sums within fp32 rounding; dwpe (a plain sum over the
@@ -107,6 +108,37 @@ def test_encoder_backward_deterministic_scatter(ops, B, T, C):
     cnt = np.bincount(tok.reshape(-1), minlength=V)[:, None]
     assert np.all(np.abs(dwte - rw) <= cnt * 2.0 ** -24 * bound + 1e-30)
     assert np.array_equal(host(outs[0][1]).astype(np.float32), O.encoder_backward(dres, tok, V, T + 3)[1])
+
+
+@pytest.mark.parametrize("pattern", ["one_token", "blocks_of_32", "blocks_of_33", "ascending"])
+def test_encoder_backward_run_patterns(ops, pattern):
+    """Token runs that fill whole sorted chunks, end exactly on a chunk
+    boundary, straddle one, or are all length 1: the chunked dwte sums against
+    float64, bitwise repeatable."""
+    B, T, C, V = 4, 256, 128, 600
+    n = B * T
+    if pattern == "one_token":
+        tok = np.full(n, 7, np.int32)
+    elif pattern == "blocks_of_32":
+        tok = (np.arange(n) // 32).astype(np.int32)[::-1].copy()
+    elif pattern == "blocks_of_33":
+        tok = ((np.arange(n) * 7919) % n // 33).astype(np.int32)
+    else:
+        tok = (np.arange(n) % V).astype(np.int32)
+    tok = tok.reshape(B, T)
+    dres = normal_array((B, T, C), 9)
+    td, tt = dev(dres), dev(tok, torch.int32)
+    outs = []
+    for _ in range(2):
+        dwte, dwpe = torch.zeros(V, C, device="cuda"), torch.zeros(T, C, device="cuda")
+        ops.gpt2_op_encoder_backward(dwte, dwpe, td, tt, B, T, C)
+        outs.append(dwte)
+    assert torch.equal(outs[0], outs[1])
+    rw, _ = O.encoder_backward(dres.astype(np.float64), tok, V, T)
+    bound = np.zeros((V, C))
+    np.add.at(bound, tok.reshape(-1), np.abs(dres.reshape(-1, C).astype(np.float64)))
+    cnt = np.bincount(tok.reshape(-1), minlength=V)[:, None]
+    assert np.all(np.abs(host(outs[0]) - rw) <= cnt * 2.0 ** -24 * bound + 1e-30)
 
 
 # ---------------------------------------------------------------------------
