@@ -68,7 +68,15 @@ cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* r
 template <typename T>
 cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
                                const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
-                               float* db, float* dres_sum, float* partial, cudaStream_t st);
+                               float* db, float* dres_sum, float* partial, cudaStream_t st,
+                               int* deferred_chunks = nullptr);
+// With deferred_chunks, layernorm_backward only writes its per-chunk partial
+// sums (partial[chunk][3][C]) and stores the chunk count there; the sums are
+// added later by reduce_partials, possibly for several calls at once:
+// out_o[z*sOut + c] += sum_k partial[z*sPart + (k*nout + o)*C + c] (sPart = 0:
+// nchunks*nout*C), chunks in a fixed order.
+cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
+                            int nout, cudaStream_t st, int nbatch = 1, long long sOut = 0, long long sPart = 0);
 size_t ln_backward_partial_floats(int rows, int C);
 // out[c] += sum_rows X[r*ldx + c]; partial: colsum_partial_floats(rows, cols) floats.
 // nbatch > 1: the same for items z = 0..nbatch-1 at out + z*sOut, X + z*sX

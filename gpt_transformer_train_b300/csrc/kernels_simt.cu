@@ -525,19 +525,19 @@ size_t colsum_partial_floats(int rows, int cols) { return (size_t)reduce_chunks(
 
 // out_o[c] += sum_k partial[k][o][c] for o < nout (out_o may be null: skipped).
 // Block (column group of 32, output o, batch item z: partial and out_o
-// advance by nchunks*nout*C and sOut per item); warp w sums chunks w, w+8,
-// ... in order, then the eight warp sums are added in warp order.
+// advance by sPart and sOut per item); warp w sums chunks w, w+8, ... in
+// order, then the eight warp sums are added in warp order.
 __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict__ out0, float* __restrict__ out1,
                                                               float* __restrict__ out2,
                                                               const float* __restrict__ partial, int nchunks,
-                                                              int C, int nout, long long sOut) {
+                                                              int C, int nout, long long sOut, long long sPart) {
   pdl_enter();
   __shared__ float sh[8][32];
   const int o = blockIdx.y;
   float* out = o == 0 ? out0 : (o == 1 ? out1 : out2);
   if (!out) return;
   out += blockIdx.z * sOut;
-  partial += (size_t)blockIdx.z * nchunks * nout * C;
+  partial += blockIdx.z * sPart;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int c = blockIdx.x * 32 + lane;
   // chunks w, w+8, w+16, ... in increasing order; eight loads in flight, added in that order
@@ -565,10 +565,13 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict_
   }
 }
 
-static cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
-                                   int nout, cudaStream_t st, int nbatch = 1, long long sOut = 0) {
+cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
+                            int nout, cudaStream_t st, int nbatch, long long sOut, long long sPart) {
+  if (nbatch < 1 || nbatch > 65535) return cudaErrorInvalidValue;
+  if (sPart == 0) sPart = (long long)nchunks * nout * C;
   dim3 grid((unsigned)cdiv(C, 32), nout, nbatch);
-  launch_k(reduce_partials_kernel, dim3(grid), dim3(256), 0, st, out0, out1, out2, partial, nchunks, C, nout, sOut);
+  launch_k(reduce_partials_kernel, dim3(grid), dim3(256), 0, st, out0, out1, out2, partial, nchunks, C, nout, sOut,
+           sPart);
   return launch_status(1);
 }
 
@@ -828,7 +831,7 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
 template <typename T>
 cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
                                const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
-                               float* db, float* dres_sum, float* partial, cudaStream_t st) {
+                               float* db, float* dres_sum, float* partial, cudaStream_t st, int* deferred_chunks) {
   constexpr int N = VecN<T>::n;
   const int nvec = C / N;
   const bool sums = dw || db || dres_sum;
@@ -877,6 +880,10 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
 #undef LNBP
       cudaError_t e = launch_status(1);
       if (e != cudaSuccess || !sums) return e;
+      if (deferred_chunks) {
+        *deferred_chunks = pgrid;
+        return cudaSuccess;
+      }
       return reduce_partials(dw, db, dres_sum, partial, pgrid, C, 3, st);
     }
   }
@@ -895,6 +902,10 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
   cudaError_t e = launch_status(1);
   if (e != cudaSuccess || !sums) return e;
   // rows of 64 per chunk = 8 warps x LNB_RPW rows per block
+  if (deferred_chunks) {
+    *deferred_chunks = (int)grid;
+    return cudaSuccess;
+  }
   return reduce_partials(dw, db, dres_sum, partial, (int)grid, C, 3, st);
 }
 
@@ -1735,7 +1746,7 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
                                                      const T*, int, int, cudaStream_t);                  \
   template cudaError_t layernorm_backward<T>(float*, T*, const T*, const T*, const float*, const float*,  \
                                              const T*, int, int, int, float*, float*, float*, float*,     \
-                                             cudaStream_t);                                               \
+                                             cudaStream_t, int*);                                         \
   template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t, int, long long,  \
                                  long long);                                                              \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \

@@ -135,8 +135,11 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   // dS blocks of the tensor-core attention backward (by shape alone, so the
   // size does not depend on the machine the layout is computed on)
   b.attS = c.precision == GPT2_PRECISION_BF16 && c.C == 64 * c.H ? take(attention_tc_ds_bytes(c.B, c.T, c.H)) : 0;
-  // LayerNorm-backward partials, or the column-sum partials of all layers' fc output gradients
-  b.partial = take(std::max(ln_backward_partial_floats((int)BT, (int)C), L * colsum_partial_floats((int)BT, 4 * (int)C)) *
+  // the parameter-sum partials of all 2L+1 LayerNorm backwards (reduced
+  // together after the layer loop), later the column-sum partials of all
+  // layers' fc output gradients
+  b.partial = take(std::max((2 * L + 1) * ln_backward_partial_floats((int)BT, (int)C),
+                            L * colsum_partial_floats((int)BT, 4 * (int)C)) *
                    sizeof(float));
   b.keys = take(std::max(encoder_backward_scratch_bytes((int)BT), encoder_backward_fast_scratch_bytes((int)BT, (int)C)));
   // split-K workspace of the classifier weight gradient (bf16 mode)
@@ -292,8 +295,13 @@ struct Step {
     CK(m, linear_wgrad(G(GPT2_WTE), logits(), ln(f), BTi, c.Vp, Ci));
     // final LayerNorm; the column sums of the resulting dres are the bias
     // gradient of the last fc projection (its output gradient is dres)
+    // every LayerNorm backward leaves its parameter-sum partials in its own
+    // slot (LN1 of layer l: 2l, LN2: 2l+1, final: 2L); they are reduced after the loop
+    const size_t lnslot = ln_backward_partial_floats(BTi, Ci);
+    int nch = 0;
     CK(m, layernorm_backward<T>(dres(), dresc(L - 1, 0), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
-                                Ci, 0, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part, st));
+                                Ci, 0, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part + 2 * L * lnslot, st,
+                                &nch));
     // the input-gradient chain, layer by layer; every weight gradient waits
     // for the end (below), so its operands are kept per layer
     for (int l = Li - 1; l >= 0; l--) {
@@ -304,7 +312,7 @@ struct Step {
       // LN2 (+ residual gradient; its column sums give the attention-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), dresc(l, 1), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
                                   rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, G(GPT2_LN2W, l, C),
-                                  G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C), part, st));
+                                  G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C), part + (2 * l + 1) * lnslot, st, &nch));
       // attention projection
       CK(m, linear_dgrad(dsmall(), dresc(l, 1), W(GPT2_ATTPROJW, l, CC), BTi, Ci, Ci));
       // attention
@@ -314,8 +322,18 @@ struct Step {
       // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), l > 0 ? dresc(l - 1, 0) : nullptr, dsmall(), resid(2 * l), mean(2 * l),
                                   rstd(2 * l), W(GPT2_LN1W, l, C), BTi, Ci, 1, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
-                                  l > 0 ? G(GPT2_FCPROJB, l - 1, C) : nullptr, part, st));
+                                  l > 0 ? G(GPT2_FCPROJB, l - 1, C) : nullptr, part + 2 * l * lnslot, st, &nch));
     }
+    // LayerNorm weight / bias sums and the projection biases they give, for
+    // all layers: final LN, every LN2 (one batched launch), LN1 of layers
+    // 1..L-1 (one batched launch), LN1 of layer 0
+    const long long sl = (long long)lnslot;
+    CK(m, reduce_partials(G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part + 2 * L * lnslot, nch, Ci, 3, st));
+    CK(m, reduce_partials(G(GPT2_LN2W), G(GPT2_LN2B), G(GPT2_ATTPROJB), part + lnslot, nch, Ci, 3, st, Li, Ci, 2 * sl));
+    if (Li > 1)
+      CK(m, reduce_partials(G(GPT2_LN1W, 1, C), G(GPT2_LN1B, 1, C), G(GPT2_FCPROJB), part + 2 * lnslot, nch, Ci, 3, st,
+                            Li - 1, Ci, 2 * sl));
+    CK(m, reduce_partials(G(GPT2_LN1W), G(GPT2_LN1B), nullptr, part, nch, Ci, 3, st));
     // weight gradients of every layer, one batched product per weight type
     const long long sBT = (long long)BTi * Ci;
     CK(m, linear_wgrad_layers(G(GPT2_FCPROJW), dresc(0, 0), 2 * sBT, fchg(0), 4 * sBT, BTi, Ci, 4 * Ci));
