@@ -887,7 +887,7 @@ size_t attention_tc_ds_bytes(int B, int T, int H) {
 
 cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16* dout, const bf16* qkv,
                                   const bf16* out, const float* lse, int B, int T, int C, int H, int* flags,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, bool d_ready) {
   if (!attention_tc_supported(B, T, C, H) || !flags) return cudaErrorNotSupported;
   if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15) ||
       ((uintptr_t)lse & 15) || ((uintptr_t)Dbuf & 15) || !dS || ((uintptr_t)dS & 15))
@@ -909,10 +909,13 @@ cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16*
   const int sms = tc_num_sms();
   const unsigned grid = (unsigned)(items < sms ? items : sms);
   const long long n8 = (long long)B * T * C / 8;
-  gpt2_count_launches(3);
-  launch_k(attn_rowdot_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, st, Dbuf, dout, out, n8, T, C, H);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  gpt2_count_launches(d_ready ? 2 : 3);
+  cudaError_t e;
+  if (!d_ready) {
+    launch_k(attn_rowdot_kernel, dim3((unsigned)((n8 + 255) / 256)), dim3(256), 0, st, Dbuf, dout, out, n8, T, C, H);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   launch_k(attn_bwd_dkv_tc_kernel, dim3(grid), dim3(BWD_THREADS), DKV_SMEM, st, tq, td, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

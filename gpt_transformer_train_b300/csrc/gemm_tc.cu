@@ -75,6 +75,8 @@ struct TcParams {
   int* flags;
   int splits;  // K split into this many ranges (EPI_ACC_F32 only)
   int batch;   // independent products, item z at depth z of every tensor map
+  float* dvec;  // EPI_ROWDOT: the per-row, per-head dot products
+  int dT, dH;
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(192, 1)
             tma_store_3d(&td, col0, rbase, z, stg + STG);
             bulk_commit();
           }
-        } else {  // EPI_GELU_BWD: D = acc * GELU'(aux), aux tile fetched by TMA
+        } else {  // EPI_GELU_BWD: D = acc * GELU'(aux); EPI_ROWDOT: D = acc and its dot with aux; aux tile by TMA
           if (lane == 0) {
             bulk_wait_read<0>();
             mbar_expect_tx(auxbar, STG);
@@ -459,12 +461,28 @@ __global__ void __launch_bounds__(192, 1)
           if (!mbar_wait_warp(auxbar, aux_phase, abort_flag)) { ok = false; break; }
           aux_phase ^= 1;
           float hv[32];
-          unstage_bf16(stg_g, lane, 0, hv);
+          if (p.epi == EPI_GELU_BWD) {
+            unstage_bf16(stg_g, lane, 0, hv);
 #pragma unroll
-          for (int k = 0; k < 32; k++) v0[k] *= gelu_tanh_grad(hv[k]);
-          unstage_bf16(stg_g, lane, 4, hv);
+            for (int k = 0; k < 32; k++) v0[k] *= gelu_tanh_grad(hv[k]);
+            unstage_bf16(stg_g, lane, 4, hv);
 #pragma unroll
-          for (int k = 0; k < 32; k++) v1[k] *= gelu_tanh_grad(hv[k]);
+            for (int k = 0; k < 32; k++) v1[k] *= gelu_tanh_grad(hv[k]);
+          } else {
+            // the head's 64 columns: products of the stored (bf16) values with aux, in column order
+            float d = 0.f;
+            unstage_bf16(stg_g, lane, 0, hv);
+#pragma unroll
+            for (int k = 0; k < 32; k++) d = fmaf(__bfloat162float(__float2bfloat16_rn(v0[k])), hv[k], d);
+            unstage_bf16(stg_g, lane, 4, hv);
+#pragma unroll
+            for (int k = 0; k < 32; k++) d = fmaf(__bfloat162float(__float2bfloat16_rn(v1[k])), hv[k], d);
+            const int row = rbase + lane;
+            if (row < p.M) {
+              const int b = row / p.dT, t = row - b * p.dT;
+              p.dvec[((size_t)b * p.dH + col0 / 64) * p.dT + t] = d;
+            }
+          }
           stage_bf16(stg + STG, lane, 0, v0);
           stage_bf16(stg + STG, lane, 4, v1);
           fence_async_smem();
@@ -547,14 +565,15 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   if (g.epi == EPI_ACC_F32)
     ok = ok && make_map_3d(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.D, g.N, g.M, g.ldd, nb, g.sD, 32, 32);
   else ok = ok && make_map_3d(&td, bf, 2, g.D, g.N, g.M, g.ldd, nb, g.sD, 64, 32);
-  if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) ok = ok && make_map_3d(&tx, bf, 2, g.aux, g.N, g.M, g.ldaux, nb, g.sAux, 64, 32);
+  if (g.epi == EPI_GELU || g.epi == EPI_GELU_BWD || g.epi == EPI_ROWDOT)
+    ok = ok && make_map_3d(&tx, bf, 2, g.aux, g.N, g.M, g.ldaux, nb, g.sAux, 64, 32);
   else if (g.epi == EPI_ACC_F32 && splits > 1) ok = ok && tc_make_map_f32_3d(&tx, g.ws, g.N, g.M, splits - 1, 32, 32);
   else tx = td;
   if (!ok) return cudaErrorInvalidValue;
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
   TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
-             (int)nb};
+             (int)nb, g.dvec, g.dT, g.dH};
   const long long units = tiles * splits * (long long)nb;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(192);
@@ -688,7 +707,12 @@ bool gemm_tc_supported(const GemmArgs& g) {
   if (g.N % 8 || g.lda % 8 || g.ldb % 8 || !al16(g.A) || !al16(g.B) || !al16(g.D)) return false;
   if (g.epi == EPI_ACC_F32 ? (g.ldd % 4) : (g.ldd % 8)) return false;
   if (g.ldd < g.N) return false;
-  if ((g.epi == EPI_GELU || g.epi == EPI_GELU_BWD) && (!g.aux || g.ldaux % 8 || g.ldaux < g.N || !al16(g.aux)))
+  if ((g.epi == EPI_GELU || g.epi == EPI_GELU_BWD || g.epi == EPI_ROWDOT) &&
+      (!g.aux || g.ldaux % 8 || g.ldaux < g.N || !al16(g.aux)))
+    return false;
+  // rows are (b, t) with t < dT; 64-column heads; one product only
+  if (g.epi == EPI_ROWDOT &&
+      (!g.dvec || g.dT <= 0 || g.dH <= 0 || g.N != 64 * g.dH || g.M % g.dT || g.batch > 1 || g.bias))
     return false;
   if (g.bias && !al16(g.bias)) return false;
   if (g.a_kmajor ? g.lda < g.K : g.lda < g.M) return false;

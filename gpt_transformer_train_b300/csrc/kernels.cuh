@@ -15,6 +15,10 @@ enum GemmEpi : int {
   EPI_GELU = 1,      // aux[m,n] = acc + bias[n]; D[m,n] = GELU(aux)   (type T)
   EPI_GELU_BWD = 2,  // D[m,n] = acc * GELU'(aux[m,n])                 (type T)
   EPI_ACC_F32 = 3,   // D[m,n] += acc                                  (float)
+  // D[m,n] = acc (type T), and for every row m = b*dT + t and 64-column
+  // head h: dvec[(b*dH + h)*dT + t] = sum over the head's columns of
+  // D[m,n] * aux[m,n] (D as stored), the attention backward's rowsum(dO * O)
+  EPI_ROWDOT = 4,
 };
 struct GemmArgs {
   const void* A; long long lda; int a_kmajor;
@@ -31,6 +35,7 @@ struct GemmArgs {
   // B + z*sB (and aux + z*sAux) and writing D + z*sD (element strides); no
   // bias, no K split
   int batch; long long sA, sB, sD, sAux;
+  float* dvec; int dT, dH;  // EPI_ROWDOT only
 };
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
 // tcgen05/TMA tensor-core path (bf16 operands); returns cudaErrorNotSupported
@@ -102,9 +107,11 @@ bool attention_tc_supported(int B, int T, int C, int H);
 size_t attention_tc_ds_bytes(int B, int T, int H);
 cudaError_t attention_forward_tc(bf16* out, float* lse, const bf16* qkv, int B, int T, int C, int H, int* flags,
                                  cudaStream_t st);
+// (d_ready: Dbuf already holds D, e.g. from the EPI_ROWDOT epilogue of the
+// GEMM that produced dout)
 cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16* dout, const bf16* qkv,
                                   const bf16* out, const float* lse, int B, int T, int C, int H, int* flags,
-                                  cudaStream_t st);
+                                  cudaStream_t st, bool d_ready = false);
 
 template <typename T>
 cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,

@@ -245,11 +245,28 @@ struct Step {
       return attention_forward_tc((bf16*)out, lse_, (const bf16*)qkv_, c.B, c.T, c.C, c.H, flags(), m->st);
     return attention_forward_simt<T>(out, lse_, qkv_, c.B, c.T, c.C, c.H, m->st);
   }
-  cudaError_t attention_bwd(T* dqkv, const T* dout, const T* qkv_, const T* out, const float* lse_) {
+  // attention-projection input gradient; on the tensor-core path its epilogue
+  // also takes the attention backward's D = rowsum(dO * O) (returns whether it did)
+  cudaError_t attproj_dgrad(T* dX, const T* dY, const T* Wt, const T* O, bool* d_ready) {
+    const int M = m->BT, N = c.C, K = c.C;
+    *d_ready = false;
+    if (attention_on_tc()) {
+      GemmArgs a{dY, N, 1, Wt, K, 0, M, K, N, dX, K, nullptr, (void*)O, K, EPI_ROWDOT, nullptr, 0,
+                 1, 0, 0, 0, 0, m->at<float>(m->bl.attD), c.T, c.H};
+      if (gemm_tc_supported(a)) {
+        *d_ready = true;
+        return gemm(a);
+      }
+    }
+    return linear_dgrad(dX, dY, Wt, M, N, K);
+  }
+  cudaError_t attention_bwd(T* dqkv, const T* dout, const T* qkv_, const T* out, const float* lse_,
+                            bool d_ready = false) {
     float* Dbuf = m->at<float>(m->bl.attD);
     if (attention_on_tc())
       return attention_backward_tc((bf16*)dqkv, Dbuf, m->at<uint8_t>(m->bl.attS), (const bf16*)dout,
-                                   (const bf16*)qkv_, (const bf16*)out, lse_, c.B, c.T, c.C, c.H, flags(), m->st);
+                                   (const bf16*)qkv_, (const bf16*)out, lse_, c.B, c.T, c.C, c.H, flags(), m->st,
+                                   d_ready);
     return attention_backward_simt<T>(dqkv, Dbuf, dout, qkv_, out, lse_, c.B, c.T, c.C, c.H, m->st);
   }
 
@@ -313,10 +330,11 @@ struct Step {
       CK(m, layernorm_backward<T>(dres(), dresc(l, 1), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
                                   rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, G(GPT2_LN2W, l, C),
                                   G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C), part + (2 * l + 1) * lnslot, st, &nch));
-      // attention projection
-      CK(m, linear_dgrad(dsmall(), dresc(l, 1), W(GPT2_ATTPROJW, l, CC), BTi, Ci, Ci));
+      // attention projection (its epilogue also forms the attention backward's D)
+      bool d_ready = false;
+      CK(m, attproj_dgrad(dsmall(), dresc(l, 1), W(GPT2_ATTPROJW, l, CC), atty(l), &d_ready));
       // attention
-      CK(m, attention_bwd(dqkv(l), dsmall(), qkv(l), atty(l), lse(l)));
+      CK(m, attention_bwd(dqkv(l), dsmall(), qkv(l), atty(l), lse(l), d_ready));
       // qkv
       CK(m, linear_dgrad(dsmall(), dqkv(l), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
       // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)

@@ -111,6 +111,17 @@ int gpt2_op_matmul_batched(int dtype, int batch, const void* A, long long lda, l
   return rc_of(gemm_simt<float>(a, ST(stream)));
 }
 
+int gpt2_op_matmul_rowdot(const void* dY, long long ldy, const void* W, long long ldw, int M, int N, int K, void* dX,
+                          long long ldx, const void* O, long long ldo, float* D, int T, int H, int* flags_dev,
+                          void* stream) {
+  if (!dY || !W || !dX || !O || !D || !flags_dev || M <= 0 || N <= 0 || K <= 0 || T <= 0 || H <= 0)
+    return GPT2_ERR_INVALID_ARG;
+  GemmArgs a{dY, ldy, 1, W, ldw, 0, M, K, N, dX, ldx, nullptr, const_cast<void*>(O), ldo, EPI_ROWDOT,
+             nullptr, 0, 1, 0, 0, 0, 0, D, T, H};
+  if (!gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
+  return rc_of(gemm_tc(a, flags_dev, ST(stream)));
+}
+
 int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H, int path,
                               int* flags_dev, void* stream) {
   if (bad_dtype(dtype) || !out || !lse || !qkv || B <= 0 || T <= 0 || C <= 0 || H <= 0 || C % H) return GPT2_ERR_INVALID_ARG;

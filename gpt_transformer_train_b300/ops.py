@@ -23,6 +23,7 @@ _sigs = {
     "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
     "gpt2_op_matmul_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P, _sz, _P]),
+    "gpt2_op_matmul_rowdot": (_i, [_P, _ll, _P, _ll, _i, _i, _i, _P, _ll, _P, _ll, _P, _i, _i, _P, _P]),
     "gpt2_op_matmul_batched": (_i, [_i, _i, _P, _ll, _ll, _i, _P, _ll, _ll, _i, _i, _i, _i, _P, _ll, _ll, _P, _ll, _ll,
                                     _i, _i, _P, _P]),
     "gpt2_op_attention_forward": (_i, [_i, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P]),
@@ -124,6 +125,11 @@ def gpt2_op_matmul_batched(batch, A, lda, sA, a_kmajor, B, ldb, sB, b_kmajor, M,
     _ck(lib.gpt2_op_matmul_batched(_dt(A), batch, _p(A), lda, sA, a_kmajor, _p(B), ldb, sB, b_kmajor, M, N, K, _p(D),
                                    ldd, sD, _p(aux), ldaux, sAux, epilogue, path, _p(flags_dev), _s(stream)),
         "matmul_batched")
+
+
+def gpt2_op_matmul_rowdot(dY, ldy, W, ldw, M, N, K, dX, ldx, O, ldo, D, T, H, flags_dev, stream=None):
+    _ck(lib.gpt2_op_matmul_rowdot(_p(dY), ldy, _p(W), ldw, M, N, K, _p(dX), ldx, _p(O), ldo, _p(D), T, H,
+                                  _p(flags_dev), _s(stream)), "matmul_rowdot")
 
 
 def gpt2_op_attention_forward(out, lse, qkv, B, T, C, H, path=PATH_AUTO, flags_dev=None, stream=None):

@@ -118,6 +118,19 @@ int gpt2_op_matmul_batched(int dtype, int batch, const void* A, long long lda, l
                            long long ldd, long long sD, void* aux, long long ldaux, long long sAux, int epilogue,
                            int path, int* flags_dev, void* stream);
 
+/* The attention-projection input gradient with the attention backward's
+ * D = rowsum(dO * O) taken in its epilogue (bf16, tensor-core path only):
+ * dX[M][K] = dY[M][N] . W[N][K] (dY row-major [M][ldy], W row-major [N][ldw],
+ * dX row-major [M][ldx]), and for every row m = b*T + t and head h (64
+ * columns of dX): D[(b*H + h)*T + t] = sum of dX[m][c] * O[m][c] over the
+ * head's columns, with dX as stored in bf16 and O [M][ldo] the attention
+ * output.  K must be 64*H and M a multiple of T.  The result feeds
+ * gpt2_op_attention_backward's D.  flags_dev: a bounded wait that runs out
+ * ORs 4 into it. */
+int gpt2_op_matmul_rowdot(const void* dY, long long ldy, const void* W, long long ldw, int M, int N, int K, void* dX,
+                          long long ldx, const void* O, long long ldo, float* D, int T, int H, int* flags_dev,
+                          void* stream);
+
 /* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
  * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of
  * the scaled scores q.k/sqrt(hd) over t2 <= t (the attention layer and its

@@ -383,6 +383,26 @@ def test_matmul_batched_weight_gradient(ops, path, batch, BT, N, K, gap):
         assert np.array_equal(got[z * sW + N * K:(z + 1) * sW], W0[z * sW + N * K:(z + 1) * sW])
 
 
+@pytest.mark.parametrize("B,T,H,N", [(2, 512, 12, 640), (3, 128, 4, 256)])
+def test_matmul_rowdot_epilogue(ops, B, T, H, N):
+    """Attention-projection input gradient whose epilogue also forms the
+    attention backward's D[b][h][t] = sum over the head of dX * O (dX as
+    stored in bf16), against numpy."""
+    M, K = B * T, 64 * H
+    dY, W, Oa = normal_array((M, N), 162), normal_array((N, K), 163, 0.05), normal_array((M, K), 164)
+    tdy, tw, to = dev(dY, torch.bfloat16), dev(W, torch.bfloat16), dev(Oa, torch.bfloat16)
+    dX = torch.full((M, K), float("nan"), device="cuda", dtype=torch.bfloat16)
+    D = torch.full((B * H * T,), float("nan"), device="cuda")
+    fl = ops.flags()
+    ops.gpt2_op_matmul_rowdot(tdy, N, tw, K, M, N, K, dX, K, to, K, D, T, H, fl)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    assert rel_l2(host(dX), host(tdy) @ host(tw)) < 2 ** -7
+    x = host(dX).astype(np.float64).reshape(B, T, H, 64)
+    rD = (x * host(to).astype(np.float64).reshape(B, T, H, 64)).sum(-1).transpose(0, 2, 1)
+    assert np.max(np.abs(host(D).reshape(B, H, T) - rD)) < 1e-4 * max(1.0, np.abs(rD).max())
+
+
 @pytest.mark.parametrize("epi", ["store", "gelu_bwd"])
 def test_matmul_batched_bf16_epilogues(ops, epi):
     """Batched K-major products with bf16 output (and the GELU' epilogue with a
