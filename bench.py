@@ -129,14 +129,14 @@ class Clocks:
                 "power_w_max": max(pw) if pw else None}
 
 
-def kernel_traffic(kernel_key):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's
-    source is unchanged since the capture (else None)."""
+def kernel_traffic(kernel_key, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    this workload and the kernel's source is unchanged since (else None)."""
     p = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel_key)
-    if not d:
+    if not d or d.get("workload") != workload:
         return None
     src = os.path.join(ROOT, d["source"])
     if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
@@ -317,7 +317,7 @@ def run_ours(args, w):
     roof = {"kernel": "GEMM (all matmul launches of the step)", "bound": "tensor", "achieved": achieved,
             "peak": peaks["bf16_sus"], "unit": "TFLOP/s",
             "frac": (achieved / peaks["bf16_sus"]) if achieved else None,
-            "traffic": kernel_traffic("gemm"), "launches_timed": g_n,
+            "traffic": kernel_traffic("gemm", args.workload), "launches_timed": g_n,
             "time_share_of_step": g_ms / prof_ms if prof_ms > 0 else None,
             "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside the step)"}
     out = None
