@@ -230,7 +230,8 @@ def run_ours(args, w):
 
     B, T = w["B"], w["T"]
     BT = B * T
-    cfg = g.make_config(w["L"], w["C"], w["H"], w["V"], w["Vp"], w["maxT"], B, T, g.PRECISION_BF16)
+    cfg = g.make_config(w["L"], w["C"], w["H"], w["V"], w["Vp"], w["maxT"], B, T, g.PRECISION_BF16,
+                        recompute=args.recompute)
     stream = torch.cuda.Stream(dev)
     m = g.GPT2(cfg, SEED, stream=stream)
     tok, tgt = zipf_tokens(B, T, w["V"], SEED + rank)
@@ -326,7 +327,9 @@ def run_ours(args, w):
                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                "data": "synthetic (Zipf(1.1) tokens, seeded N(0,0.02) init)",
-               "config": {"workload": workload_name(args.workload, w), "global_batch": B * ws, "seq_len": T,
+               "config": {"workload": workload_name(args.workload, w) +
+                          (f", activation recompute {args.recompute}" if args.recompute else ""),
+                          "global_batch": B * ws, "seq_len": T,
                           "parallelism": "replicas" if ws > 1 else "single GPU",
                           "l2": "inputs larger than L2 (multi-GB working set per step)"},
                "mfu": mfu, "mfu_peak_tflops": peaks["bf16"], "flops_per_step": step_flops,
@@ -361,6 +364,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="124m", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--recompute", type=int, default=0, choices=[0, 1, 2],
+                    help="activation recompute level (0: keep all activations)")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -36,7 +36,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 
 class gpt2_config(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("L", "C", "H", "max_T", "V", "Vp", "B", "T", "precision")]
+    _fields_ = [(n, ctypes.c_int) for n in ("L", "C", "H", "max_T", "V", "Vp", "B", "T", "precision", "recompute")]
 
 
 _P = ctypes.c_void_p
@@ -93,8 +93,8 @@ def _ptr(a):
     return a.data_ptr()  # torch tensor
 
 
-def make_config(L, C, H, V, Vp, max_T, B, T, precision=PRECISION_BF16):
-    return gpt2_config(L, C, H, max_T, V, Vp, B, T, precision)
+def make_config(L, C, H, V, Vp, max_T, B, T, precision=PRECISION_BF16, recompute=0):
+    return gpt2_config(L, C, H, max_T, V, Vp, B, T, precision, recompute)
 
 
 def num_parameters(cfg):

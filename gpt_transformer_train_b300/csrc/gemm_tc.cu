@@ -437,10 +437,11 @@ __global__ void __launch_bounds__(192, 1)
           }
           stage_bf16(stg, lane, 0, v0);
           stage_bf16(stg, lane, 4, v1);
+          // GELU of the pre-activation as stored (bf16), so a later recompute from it gives the same bits
 #pragma unroll
           for (int k = 0; k < 32; k++) {
-            v0[k] = gelu_tanh(v0[k]);
-            v1[k] = gelu_tanh(v1[k]);
+            v0[k] = gelu_tanh(__bfloat162float(__float2bfloat16_rn(v0[k])));
+            v1[k] = gelu_tanh(__bfloat162float(__float2bfloat16_rn(v1[k])));
           }
           stage_bf16(stg + STG, lane, 0, v0);
           stage_bf16(stg + STG, lane, 4, v1);

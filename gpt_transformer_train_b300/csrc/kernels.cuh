@@ -135,5 +135,10 @@ cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream
 
 template <typename T>
 cudaError_t gelu_forward(T* out, const T* in, long long n, cudaStream_t st);
+// y = (r - mean) * rstd * w + bias per row (the LayerNorm forward's last step
+// on a stored residual row and its stored statistics), rows x C
+template <typename T>
+cudaError_t layernorm_apply(T* y, const T* r, const float* mean, const float* rstd, const T* w, const T* bias,
+                            int rows, int C, cudaStream_t st);
 template <typename T>
 cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cudaStream_t st);

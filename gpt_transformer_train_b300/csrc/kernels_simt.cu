@@ -509,6 +509,42 @@ cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* r
   return launch_status(1);
 }
 
+// y = (r - mean) * rstd * w + bias from a stored residual row and its stored
+// statistics: the forward's last step, on the same stored values, for
+// activation recompute (same expression, same bits as the forward's y)
+template <typename T>
+__global__ void __launch_bounds__(256) layernorm_apply_kernel(T* __restrict__ y, const T* __restrict__ r,
+                                                              const float* __restrict__ mean,
+                                                              const float* __restrict__ rstd,
+                                                              const T* __restrict__ w, const T* __restrict__ bias,
+                                                              int rows, int C) {
+  pdl_enter();
+  constexpr int N = VecN<T>::n;
+  const int nvec = C / N;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)rows * nvec) return;
+  const int row = (int)(i / nvec), vi = (int)(i % nvec);
+  const float mu = mean[row], rs = rstd[row];
+  float x[N], wv[N], bv[N], o[N];
+  ld16_cs(r + (size_t)row * C + vi * N, x);
+  ld16(w + vi * N, wv);
+  ld16(bias + vi * N, bv);
+#pragma unroll
+  for (int k = 0; k < N; k++) o[k] = (x[k] - mu) * rs * wv[k] + bv[k];
+  st16(y + (size_t)row * C + vi * N, o);
+}
+
+template <typename T>
+cudaError_t layernorm_apply(T* y, const T* r, const float* mean, const float* rstd, const T* w, const T* bias,
+                            int rows, int C, cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  if (C % N || rows <= 0) return cudaErrorInvalidValue;
+  const long long n = (long long)rows * (C / N);
+  launch_k(layernorm_apply_kernel<T>, dim3((unsigned)cdiv(n, 256)), dim3(256), 0, st, y, r, mean, rstd, w, bias,
+           rows, C);
+  return launch_status(1);
+}
+
 // ============================================================================
 // Deterministic column reductions.  Producers write per-chunk partial sums
 // (a chunk = a fixed block of rows, summed in a fixed order); reduce_partials
@@ -1056,8 +1092,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
       } else {
         if (g.bias) v += to_f(((const T*)g.bias)[n]);
         if (g.epi == EPI_GELU) {
+          // GELU of the pre-activation as stored, so a later recompute from aux gives the same bits
           ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
-          v = gelu_f(v);
+          v = gelu_f(round_to<T>(v));
         }
         ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
       }
@@ -1747,6 +1784,8 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   template cudaError_t layernorm_backward<T>(float*, T*, const T*, const T*, const float*, const float*,  \
                                              const T*, int, int, int, float*, float*, float*, float*,     \
                                              cudaStream_t, int*);                                         \
+  template cudaError_t layernorm_apply<T>(T*, const T*, const float*, const float*, const T*, const T*, int,   \
+                                          int, cudaStream_t);                                                \
   template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t, int, long long,  \
                                  long long);                                                              \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \

@@ -90,6 +90,7 @@ int validate_config(const gpt2_config& c, const char** why) {
   } else {
     return *why = "precision must be GPT2_PRECISION_FP32 or GPT2_PRECISION_BF16", GPT2_ERR_INVALID_CONFIG;
   }
+  if (c.recompute < 0 || c.recompute > 2) return *why = "recompute must be 0, 1 or 2", GPT2_ERR_INVALID_CONFIG;
   return GPT2_OK;
 }
 
@@ -109,15 +110,19 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.m = take(pl.total * 4);
   b.v = take(pl.total * 4);
   b.pbf = c.precision == GPT2_PRECISION_BF16 ? take(pl.total * 2) : 0;
+  // recompute 2 keeps one LayerNorm output, 1 and 2 keep one GELU output and
+  // one layer's output gradients (the weight gradients then run in the layer loop)
+  const size_t n_ln = c.recompute >= 2 ? 1 : 2 * L + 1, n_gelu = c.recompute >= 1 ? 1 : L;
+  const size_t n_dlayer = c.recompute >= 1 ? 1 : L;
   b.resid = take((2 * L + 1) * BT * C * es);
-  b.ln = take((2 * L + 1) * BT * C * es);
+  b.ln = take(n_ln * BT * C * es);
   b.ln_mean = take((2 * L + 1) * BT * 4);
   b.ln_rstd = take((2 * L + 1) * BT * 4);
   b.qkv = take(L * BT * 3 * C * es);
   b.atty = take(L * BT * C * es);
   b.lse = take(L * BT * c.H * 4);
   b.fch = take(L * BT * 4 * C * es);
-  b.fchg = take(L * BT * 4 * C * es);
+  b.fchg = take(n_gelu * BT * 4 * C * es);
   b.proj = take(BT * C * es);
   b.logits = take(BT * (size_t)c.Vp * es);
   b.losses = take(BT * 4);
@@ -127,9 +132,9 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   // layers are taken together after the backward pass: the residual gradient
   // entering the fc projection and the attention projection ([L][2][BT][C]),
   // the fc output gradient ([L][BT][4C]) and the qkv gradient ([L][BT][3C])
-  b.dresc = take(L * 2 * BT * C * es);
-  b.dfch = take(L * BT * 4 * C * es);
-  b.dqkv = take(L * BT * 3 * C * es);
+  b.dresc = take(n_dlayer * 2 * BT * C * es);
+  b.dfch = take(n_dlayer * BT * 4 * C * es);
+  b.dqkv = take(n_dlayer * BT * 3 * C * es);
   b.dsmall = take(BT * C * es);
   b.attD = take(BT * c.H * 4);
   // dS blocks of the tensor-core attention backward (by shape alone, so the
@@ -138,16 +143,23 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   // the parameter-sum partials of all 2L+1 LayerNorm backwards (reduced
   // together after the layer loop), later the column-sum partials of all
   // layers' fc output gradients
-  b.partial = take(std::max((2 * L + 1) * ln_backward_partial_floats((int)BT, (int)C),
-                            L * colsum_partial_floats((int)BT, 4 * (int)C)) *
-                   sizeof(float));
+  // (with recompute the per-layer column sums use the space after the LayerNorm slots)
+  const size_t ln_part = (2 * L + 1) * ln_backward_partial_floats((int)BT, (int)C);
+  const size_t cs_part = n_dlayer * colsum_partial_floats((int)BT, 4 * (int)C);
+  b.partial = take((c.recompute >= 1 ? ln_part + cs_part : std::max(ln_part, cs_part)) * sizeof(float));
   b.keys = take(std::max(encoder_backward_scratch_bytes((int)BT), encoder_backward_fast_scratch_bytes((int)BT, (int)C)));
   // split-K workspace of the classifier weight gradient (bf16 mode)
   b.ws_floats = 0;
   if (c.precision == GPT2_PRECISION_BF16) {
     const int iBT = (int)BT, iC = (int)C;
-    // (the per-layer weight gradients run batched over the layers, unsplit)
+    // (without recompute the per-layer weight gradients run batched over the
+    // layers, unsplit; with it they run one layer at a time and may split K)
     b.ws_floats = gemm_tc_workspace_floats(c.Vp, iC, iBT, GPT2_NOMINAL_SMS);
+    if (c.recompute >= 1) {
+      const int shapes[4][2] = {{iC, 4 * iC}, {4 * iC, iC}, {iC, iC}, {3 * iC, iC}};
+      for (auto& sh : shapes)
+        b.ws_floats = std::max(b.ws_floats, gemm_tc_workspace_floats(sh[0], sh[1], iBT, GPT2_NOMINAL_SMS));
+    }
   }
   b.ws = take(std::max<size_t>(b.ws_floats, 1) * sizeof(float));
   b.gnorm = take((2 + grad_norm_scratch_floats()) * sizeof(float));  // norm, clip factor, chunk sums
@@ -178,14 +190,15 @@ struct Step {
     return m->at<float>(m->bl.grads) + m->pl.off[t] + layer * per_layer;
   }
   T* resid(size_t i) const { return m->at<T>(m->bl.resid) + i * BT * C; }
-  T* ln(size_t i) const { return m->at<T>(m->bl.ln) + i * BT * C; }
+  // LayerNorm output i (one buffer for all i under recompute 2)
+  T* ln(size_t i) const { return m->at<T>(m->bl.ln) + (c.recompute >= 2 ? 0 : i) * BT * C; }
   float* mean(size_t i) const { return m->at<float>(m->bl.ln_mean) + i * BT; }
   float* rstd(size_t i) const { return m->at<float>(m->bl.ln_rstd) + i * BT; }
   T* qkv(size_t l) const { return m->at<T>(m->bl.qkv) + l * BT * 3 * C; }
   T* atty(size_t l) const { return m->at<T>(m->bl.atty) + l * BT * C; }
   float* lse(size_t l) const { return m->at<float>(m->bl.lse) + l * BT * c.H; }
   T* fch(size_t l) const { return m->at<T>(m->bl.fch) + l * BT * 4 * C; }
-  T* fchg(size_t l) const { return m->at<T>(m->bl.fchg) + l * BT * 4 * C; }
+  T* fchg(size_t l) const { return m->at<T>(m->bl.fchg) + (c.recompute >= 1 ? 0 : l) * BT * 4 * C; }
   T* proj() const { return m->at<T>(m->bl.proj); }
   T* logits() const { return m->at<T>(m->bl.logits); }
   float* losses() const { return m->at<float>(m->bl.losses); }
@@ -193,9 +206,22 @@ struct Step {
   // operand copy of dres for the GEMMs (== dres in fp32 mode)
   // copy of the residual gradient that enters layer l's fc projection (k = 0)
   // or attention projection (k = 1)
-  T* dresc(size_t l, int k) const { return m->at<T>(m->bl.dresc) + (2 * l + k) * BT * C; }
-  T* dfch(size_t l) const { return m->at<T>(m->bl.dfch) + l * BT * 4 * C; }
-  T* dqkv(size_t l) const { return m->at<T>(m->bl.dqkv) + l * BT * 3 * C; }
+  // (one layer's worth under recompute >= 1)
+  size_t dl(size_t l) const { return c.recompute >= 1 ? 0 : l; }
+  T* dresc(size_t l, int k) const { return m->at<T>(m->bl.dresc) + (2 * dl(l) + k) * BT * C; }
+  T* dfch(size_t l) const { return m->at<T>(m->bl.dfch) + dl(l) * BT * 4 * C; }
+  T* dqkv(size_t l) const { return m->at<T>(m->bl.dqkv) + dl(l) * BT * 3 * C; }
+  // recompute: LayerNorm output i from the stored residual stream and statistics
+  // (the forward's arithmetic on the same stored values: the same bits)
+  cudaError_t ln_recompute(size_t i, const T* w, const T* b) {
+    if (c.recompute < 2) return cudaSuccess;
+    return layernorm_apply<T>(ln(i), resid(i), mean(i), rstd(i), w, b, m->BT, c.C, m->st);
+  }
+  // recompute: GELU of layer l's fc pre-activation
+  cudaError_t gelu_recompute(size_t l) {
+    if (c.recompute < 1) return cudaSuccess;
+    return gelu_forward<T>(fchg(l), fch(l), (long long)m->BT * 4 * c.C, m->st);
+  }
   T* dsmall() const { return m->at<T>(m->bl.dsmall); }
   int* flags() const { return m->at<int>(m->bl.flags); }
 
@@ -307,25 +333,38 @@ struct Step {
     size_t CC = C * C;
     float* part = m->at<float>(m->bl.partial);
     size_t f = 2 * L;
+    // recompute >= 1: weight gradients inside the layer loop, from one layer's
+    // recomputed GELU / LayerNorm outputs; else batched after the loop
+    const bool perlayer = c.recompute >= 1;
+    // every LayerNorm backward leaves its parameter-sum partials in its own
+    // slot (LN1 of layer l: 2l, LN2: 2l+1, final: 2L); they are reduced after
+    // the loop.  Per-layer column sums use the space after the slots.
+    const size_t lnslot = ln_backward_partial_floats(BTi, Ci);
+    float* cpart = part + (2 * L + 1) * lnslot;
+    int nch = 0;
     // classifier (tied wte): dlnf = dlogits . wte ; dwte += dlogits^T . lnf
     CK(m, linear_dgrad(dsmall(), logits(), W(GPT2_WTE), BTi, c.Vp, Ci));
+    CK(m, ln_recompute(f, W(GPT2_LNFW), W(GPT2_LNFB)));
     CK(m, linear_wgrad(G(GPT2_WTE), logits(), ln(f), BTi, c.Vp, Ci));
     // final LayerNorm; the column sums of the resulting dres are the bias
     // gradient of the last fc projection (its output gradient is dres)
-    // every LayerNorm backward leaves its parameter-sum partials in its own
-    // slot (LN1 of layer l: 2l, LN2: 2l+1, final: 2L); they are reduced after the loop
-    const size_t lnslot = ln_backward_partial_floats(BTi, Ci);
-    int nch = 0;
     CK(m, layernorm_backward<T>(dres(), dresc(L - 1, 0), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
                                 Ci, 0, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part + 2 * L * lnslot, st,
                                 &nch));
-    // the input-gradient chain, layer by layer; every weight gradient waits
-    // for the end (below), so its operands are kept per layer
     for (int l = Li - 1; l >= 0; l--) {
       // fc projection (+ GELU backward fused into its input-gradient GEMM)
       CK(m, linear_dgrad(dfch(l), dresc(l, 0), W(GPT2_FCPROJW, l, 4 * CC), BTi, Ci, 4 * Ci, fch(l)));
+      if (perlayer) {
+        CK(m, gelu_recompute(l));
+        CK(m, linear_wgrad(G(GPT2_FCPROJW, l, 4 * CC), dresc(l, 0), fchg(l), BTi, Ci, 4 * Ci));
+      }
       // fc
       CK(m, linear_dgrad(dsmall(), dfch(l), W(GPT2_FCW, l, 4 * CC), BTi, 4 * Ci, Ci));
+      if (perlayer) {
+        CK(m, ln_recompute(2 * l + 1, W(GPT2_LN2W, l, C), W(GPT2_LN2B, l, C)));
+        CK(m, linear_wgrad(G(GPT2_FCW, l, 4 * CC), dfch(l), ln(2 * l + 1), BTi, 4 * Ci, Ci));
+        CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dfch(l), BTi, 4 * Ci, 4 * Ci, cpart, st));
+      }
       // LN2 (+ residual gradient; its column sums give the attention-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), dresc(l, 1), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
                                   rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, G(GPT2_LN2W, l, C),
@@ -333,10 +372,16 @@ struct Step {
       // attention projection (its epilogue also forms the attention backward's D)
       bool d_ready = false;
       CK(m, attproj_dgrad(dsmall(), dresc(l, 1), W(GPT2_ATTPROJW, l, CC), atty(l), &d_ready));
+      if (perlayer) CK(m, linear_wgrad(G(GPT2_ATTPROJW, l, CC), dresc(l, 1), atty(l), BTi, Ci, Ci));
       // attention
       CK(m, attention_bwd(dqkv(l), dsmall(), qkv(l), atty(l), lse(l), d_ready));
       // qkv
       CK(m, linear_dgrad(dsmall(), dqkv(l), W(GPT2_QKVW, l, 3 * CC), BTi, 3 * Ci, Ci));
+      if (perlayer) {
+        CK(m, ln_recompute(2 * l, W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C)));
+        CK(m, linear_wgrad(G(GPT2_QKVW, l, 3 * CC), dqkv(l), ln(2 * l), BTi, 3 * Ci, Ci));
+        CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dqkv(l), BTi, 3 * Ci, 3 * Ci, cpart, st));
+      }
       // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), l > 0 ? dresc(l - 1, 0) : nullptr, dsmall(), resid(2 * l), mean(2 * l),
                                   rstd(2 * l), W(GPT2_LN1W, l, C), BTi, Ci, 1, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
@@ -352,15 +397,17 @@ struct Step {
       CK(m, reduce_partials(G(GPT2_LN1W, 1, C), G(GPT2_LN1B, 1, C), G(GPT2_FCPROJB), part + 2 * lnslot, nch, Ci, 3, st,
                             Li - 1, Ci, 2 * sl));
     CK(m, reduce_partials(G(GPT2_LN1W), G(GPT2_LN1B), nullptr, part, nch, Ci, 3, st));
-    // weight gradients of every layer, one batched product per weight type
-    const long long sBT = (long long)BTi * Ci;
-    CK(m, linear_wgrad_layers(G(GPT2_FCPROJW), dresc(0, 0), 2 * sBT, fchg(0), 4 * sBT, BTi, Ci, 4 * Ci));
-    CK(m, linear_wgrad_layers(G(GPT2_FCW), dfch(0), 4 * sBT, ln(1), 2 * sBT, BTi, 4 * Ci, Ci));
-    CK(m, linear_wgrad_layers(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, BTi, Ci, Ci));
-    CK(m, linear_wgrad_layers(G(GPT2_QKVW), dqkv(0), 3 * sBT, ln(0), 2 * sBT, BTi, 3 * Ci, Ci));
-    // bias gradients of the fc and qkv layers of every layer: column sums of their output gradients
-    CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT));
-    CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT));
+    if (!perlayer) {
+      // weight gradients of every layer, one batched product per weight type
+      const long long sBT = (long long)BTi * Ci;
+      CK(m, linear_wgrad_layers(G(GPT2_FCPROJW), dresc(0, 0), 2 * sBT, fchg(0), 4 * sBT, BTi, Ci, 4 * Ci));
+      CK(m, linear_wgrad_layers(G(GPT2_FCW), dfch(0), 4 * sBT, ln(1), 2 * sBT, BTi, 4 * Ci, Ci));
+      CK(m, linear_wgrad_layers(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, BTi, Ci, Ci));
+      CK(m, linear_wgrad_layers(G(GPT2_QKVW), dqkv(0), 3 * sBT, ln(0), 2 * sBT, BTi, 3 * Ci, Ci));
+      // bias gradients of the fc and qkv layers of every layer: column sums of their output gradients
+      CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT));
+      CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT));
+    }
     if (encoder_backward_fast_supported(BTi, Ci))
       CK(m, encoder_backward_fast(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
     else

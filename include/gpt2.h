@@ -62,9 +62,18 @@ enum {
  * Precision GPT2_PRECISION_BF16 needs C % 64 == 0, hd == 64, T % 128 == 0,
  * (B*T) % 128 == 0, Vp % 128 == 0; GPT2_PRECISION_FP32 needs C % 4 == 0 and
  * hd <= 128.  Both need C <= 2048, T <= max_T, B*T <= 32768, V <= 65535. */
+/* recompute: 0 keeps every activation the backward reads (fastest); 1 keeps
+ * only the fc pre-activation and recomputes GELU of it in the backward; 2
+ * also recomputes every LayerNorm output from the stored residual stream and
+ * statistics (the pages' activation-recompute option, "llm.c's Origin and the
+ * Future of LLM Compilers" [13:50]).  With recompute > 0 the weight gradients
+ * run inside the layer loop and only one layer's GELU / LayerNorm outputs and
+ * output gradients are held at a time, which shrinks the buffer; the forward
+ * results and the gradients are those of recompute 0. */
 typedef struct {
   int L, C, H, max_T, V, Vp, B, T;
   int precision;
+  int recompute;
 } gpt2_config;
 
 typedef struct gpt2 gpt2;  /* opaque handle; host memory owned by the library */

@@ -203,6 +203,49 @@ def test_graph_step_matches_direct_calls(g):
     assert outs[1][0][0] != outs[1][1][0]  # the second batch really was different
 
 
+@pytest.mark.parametrize("prec", [0, 1])
+def test_activation_recompute_modes(g, prec):
+    """recompute 1 (GELU) and 2 (also LayerNorm outputs) against recompute 0 on
+    the same weights and batch: the same forward bits; gradients within fp32
+    summation-order noise of mode 0 (its weight gradients run batched, the
+    recompute modes' layer by layer); modes 1 and 2 identical to the bit (the
+    recomputed LayerNorm output is the forward's, bit for bit); a smaller buffer
+    for each step up; the bf16 step also against the oracle."""
+    L, C, H, V, Vp, maxT, B, T = (TINY if prec == 0 else SMALL_BF16).values()
+    res = {}
+    for rc in (0, 1, 2):
+        cfg = g.make_config(L, C, H, V, Vp, maxT, B, T, prec, recompute=rc)
+        res.setdefault("bytes", []).append(g.required_bytes(cfg))
+        m = g.GPT2(cfg, 1234)
+        tok, tgt = zipf_tokens(B, T, V, 1234)
+        ttok, ttgt = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+        losses, grads = [], None
+        for step in (1, 2):
+            m.gpt2_zero_grad()
+            losses.append(m.gpt2_forward(ttok, ttgt))
+            m.gpt2_backward()
+            if step == 1:
+                grads = {n: m.gpt2_get_grads(n) for n in g.TENSORS}
+            m.gpt2_adamw_step(1e-3, 0.9, 0.95, 1e-8, 0.1, step)
+        res[rc] = (losses, grads)
+        m.close()
+    b0, b1, b2 = res["bytes"]
+    assert b2 < b1 < b0
+    assert res[0][0][0] == res[1][0][0] == res[2][0][0]  # step-1 forward: same bits
+    for n in g.TENSORS:
+        assert np.array_equal(res[1][1][n].view(np.uint32), res[2][1][n].view(np.uint32)), n
+        assert rel_l2(res[1][1][n], res[0][1][n]) <= 1e-5, n
+    assert abs(res[1][0][1] - res[0][0][1]) <= 1e-4 * abs(res[0][0][1])
+    if prec == 1:
+        ref = O.GPT2(O.Config(L, C, H, V, Vp, maxT), 1234, np.float32)
+        tok, tgt = zipf_tokens(B, T, V, 1234)
+        rloss = ref.forward(tok, tgt)
+        ref.backward()
+        assert abs(res[2][0][0] - rloss) <= 2e-2
+        for n in g.TENSORS:
+            assert rel_l2(res[2][1][n], ref.grads[n].reshape(-1)) <= 5e-2, n
+
+
 def test_error_paths_on_device(g):
     cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
     with pytest.raises(g.GPT2Error) as e:
