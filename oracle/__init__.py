@@ -10,5 +10,5 @@ from .gpt2 import (  # noqa: F401
     encoder_forward, encoder_backward, layernorm_forward, layernorm_backward,
     matmul_forward, matmul_backward, attention_forward, attention_backward,
     gelu_forward, gelu_backward, softmax_forward, crossentropy_forward,
-    crossentropy_softmax_backward, adamw_update, lr_schedule,
+    crossentropy_softmax_backward, adamw_update, lr_schedule, sample_token, generate,
 )

@@ -528,6 +528,48 @@ class GPT2:
         return norm
 
 
+def sample_token(logits_row, V, coin, temperature=1.0):
+    """The CPU trainer's sampler ("llm.c: GPT-2 training in plain C ...", §2
+    How the code works: the file ends with a sampler; §6 Reality check: it
+    keeps no KV cache, every new token runs the whole forward again): the
+    probabilities are the softmax of the first V logits (divided by the
+    temperature), and the token is the first index whose cumulative
+    probability exceeds the coin, a uniform number in [0, 1); the last index
+    when rounding leaves the total below the coin.  Temperature 0 (our
+    addition): the index of the largest logit, the lowest such index on ties.
+    Computed in float64."""
+    z = np.asarray(logits_row[:V], np.float64)
+    if temperature == 0:
+        return int(np.argmax(z))
+    z = z / temperature
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    cdf = 0.0
+    for i in range(V):
+        cdf += p[i]
+        if coin < cdf:
+            return i
+    return V - 1
+
+
+def generate(model, prompt, steps, coins, temperature=1.0):
+    """Tokens after `prompt` ([B][n]), the CPU trainer's way: for each new
+    token the whole forward runs over the sequence so far and the last
+    position's logits are sampled with coins[b][s] (see sample_token).
+    Returns (tokens [B][steps], logits [steps][B][Vp] of the sampled positions)."""
+    seq = np.array(prompt, np.int32)
+    B = seq.shape[0]
+    out, logs = [], []
+    for s in range(steps):
+        model.forward(seq)
+        last = model.cache["logits"][:, -1, :]
+        nxt = np.array([sample_token(last[b], model.cfg.V, coins[b][s], temperature) for b in range(B)], np.int32)
+        out.append(nxt)
+        logs.append(np.array(last))
+        seq = np.concatenate([seq, nxt[:, None]], axis=1)
+    return np.stack(out, 1), np.stack(logs, 0)
+
+
 def lr_schedule(max_lr, final_frac, warmup, total, step):
     """Learning rate at 0-based `step`: linear warmup to max_lr over `warmup`
     steps (step s gets max_lr (s + 1) / warmup), then cosine decay from max_lr

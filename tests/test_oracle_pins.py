@@ -452,3 +452,59 @@ def test_planted_mask_error_is_caught(monkeypatch):
         out, _ = G.attention_forward(qkv, 1)
     monkeypatch.undo()
     assert not np.allclose(out, _brute_attention(qkv, 1), atol=1e-6)
+
+
+# ---- sampler and generation (the CPU trainer's sampler, no KV cache) --------
+def test_sampler_two_token_closed_form():
+    """softmax([a, b]) = [1/(1+e^(b-a)), ...]: coins just below / above the
+    first probability pick token 0 / 1; the pads beyond V never count."""
+    z = np.array([0.3, -0.9, 50.0], np.float64)  # column 2 is a pad (V = 2)
+    p0 = 1.0 / (1.0 + math.exp(-0.9 - 0.3))
+    assert O.sample_token(z, 2, p0 - 1e-9) == 0
+    assert O.sample_token(z, 2, p0 + 1e-9) == 1
+    assert O.sample_token(z, 2, 0.0) == 0
+    assert O.sample_token(z, 2, 1.0 - 1e-12) == 1
+
+
+def test_sampler_stratified_coins_match_probabilities():
+    """Coins on a uniform grid of n points land on token i exactly
+    round-about n * p_i times (each interval of the CDF gets its share)."""
+    rng = np.random.default_rng(7)
+    V = 13
+    z = rng.normal(0, 2.0, V)
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    n = 20000
+    counts = np.bincount([O.sample_token(z, V, (k + 0.5) / n) for k in range(n)], minlength=V)
+    assert np.all(np.abs(counts - n * p) <= 1.0 + 1e-9)
+
+
+def test_sampler_temperature():
+    """Temperature 0 is argmax with the lowest index on ties; a tiny positive
+    temperature picks the maximum for any coin; temperature 2 equals
+    temperature 1 on logits halved."""
+    z = np.array([1.0, 3.0, 3.0, -2.0])
+    assert O.sample_token(z, 4, 0.7, 0.0) == 1
+    z2 = np.array([1.0, 3.5, 3.0, -2.0])
+    for coin in (0.0, 0.3, 0.999):
+        assert O.sample_token(z2, 4, coin, 1e-3) == 1
+        assert O.sample_token(z2, 4, coin, 2.0) == O.sample_token(z2 / 2.0, 4, coin, 1.0)
+
+
+def test_generate_recomputes_the_prefix_each_step():
+    """generate() samples from the last position's logits of a full forward
+    over the sequence so far: its first logits equal the prompt's last-position
+    logits, and each later one equals the full forward over prompt + the
+    tokens generated before it (causality: a longer forward leaves earlier
+    positions' logits unchanged)."""
+    cfg = O.Config(L=2, C=32, H=2, V=61, Vp=64, maxT=16)
+    m = O.GPT2(cfg, 5, np.float64)
+    prompt = np.random.default_rng(8).integers(0, 61, size=(2, 5)).astype(np.int32)
+    coins = np.random.default_rng(9).random((2, 4))
+    toks, logs = O.generate(m, prompt, 4, coins)
+    full = np.concatenate([prompt, toks], 1)
+    m.forward(full)
+    for s in range(4):
+        assert np.allclose(logs[s], m.cache["logits"][:, 4 + s, :], rtol=0, atol=1e-12)
+        for b in range(2):
+            assert toks[b, s] == O.sample_token(logs[s][b], 61, coins[b, s])
