@@ -57,6 +57,10 @@ _sigs = {
     "gpt2_get_grad_norm": (ctypes.c_int, [_P, _P]),
     "gpt2_lr_schedule": (_f, [_f, _f, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "gpt2_step_host": (ctypes.c_int, [_P, _P, _P, _f, _f, _f, _f, _f, ctypes.c_int, _P]),
+    "gpt2_infer_prefill": (ctypes.c_int, [_P, _P, ctypes.c_int]),
+    "gpt2_infer_step": (ctypes.c_int, [_P, _P, ctypes.c_int]),
+    "gpt2_sample": (ctypes.c_int, [_P, _f, _P, _P]),
+    "gpt2_get_infer_logits": (ctypes.c_int, [_P, _P]),
     "gpt2_get_params": (ctypes.c_int, [_P, ctypes.c_int, _P]),
     "gpt2_set_params": (ctypes.c_int, [_P, ctypes.c_int, _P]),
     "gpt2_get_grads": (ctypes.c_int, [_P, ctypes.c_int, _P]),
@@ -174,6 +178,22 @@ class GPT2:
         self._check(gpt2_step_host(self.h, _ptr(tokens_host), _ptr(targets_host), lr, b1, b2, eps, wd, t,
                                    loss.ctypes.data))
         return float(loss[0])
+
+    # inference with a KV cache
+    def gpt2_infer_prefill(self, tokens, n):
+        self._check(gpt2_infer_prefill(self.h, _ptr(tokens), n))
+
+    def gpt2_infer_step(self, next_tokens, pos):
+        self._check(gpt2_infer_step(self.h, _ptr(next_tokens), pos))
+
+    def gpt2_sample(self, temperature, coins, out_tokens):
+        self._check(gpt2_sample(self.h, temperature, _ptr(coins), _ptr(out_tokens)))
+
+    def gpt2_get_infer_logits(self):
+        c = self.cfg
+        out = np.empty(c.B * c.Vp, np.float32)
+        self._check(gpt2_get_infer_logits(self.h, out.ctypes.data))
+        return out.reshape(c.B, c.Vp)
 
     def numel(self, name):
         return tensor_numel(self.cfg, TENSORS.index(name))

@@ -135,6 +135,16 @@ cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream
 
 template <typename T>
 cudaError_t gelu_forward(T* out, const T* in, long long n, cudaStream_t st);
+// inference with a KV cache (the cache: qkv [B*Tmax][3C], row b*Tmax + t =
+// position t of sequence b): attention of position pos of every sequence over
+// keys 0..pos -> out [B][C]; and the sampler over the first V logits of each
+// row (temperature 0: argmax, lowest index on ties; else inverse CDF of
+// softmax(z / temperature) at coins[row]) -> out_tok [rows]
+template <typename T>
+cudaError_t decode_attention(T* out, const T* qkv, int B, int Tmax, int pos, int C, int H, cudaStream_t st);
+template <typename T>
+cudaError_t sample_tokens(int* out_tok, const T* logits, long long ld, int rows, int V, float temperature,
+                          const float* coins, cudaStream_t st);
 // y = (r - mean) * rstd * w + bias per row (the LayerNorm forward's last step
 // on a stored residual row and its stored statistics), rows x C
 template <typename T>

@@ -1590,6 +1590,176 @@ cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, i
   return launch_status(1);
 }
 
+// ============================================================================
+// inference with a KV cache: attention of one new position per sequence and
+// the sampler.  The cache is the qkv activation buffer [B*Tmax][3C]: row
+// b*Tmax + t holds q | k | v of position t of sequence b.
+// ============================================================================
+// One CTA per (b, h): scores q.k_t * scale for t = 0..pos (keys from the
+// cache), softmax, then the probability-weighted sum of v_t.  Threads take
+// keys t = tid, tid+256, ...; for P.V, group g = tid / hd of the 256 / hd
+// groups sums keys t = g, g+G, ... for dimension tid % hd, and the groups are
+// added in group order.  fp32 throughout.
+template <typename T>
+__global__ void __launch_bounds__(256) decode_attention_kernel(T* __restrict__ out, const T* __restrict__ qkv,
+                                                               int Tmax, int pos, int C, int H, float scale) {
+  pdl_enter();
+  constexpr int N = VecN<T>::n;
+  extern __shared__ float da_sh[];  // q[128] | red[32] | s[Tmax] | part[256]
+  float* q = da_sh;
+  float* red = q + 128;
+  float* s = red + 32;
+  float* part = s + Tmax;
+  const int b = blockIdx.x / H, h = blockIdx.x % H, hd = C / H, tid = threadIdx.x;
+  const size_t row0 = (size_t)b * Tmax;
+  for (int d = tid; d < hd; d += blockDim.x) q[d] = to_f(qkv[(row0 + pos) * 3 * C + h * hd + d]);
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int t = tid; t <= pos; t += blockDim.x) {
+    const T* kp = qkv + (row0 + t) * 3 * C + C + h * hd;
+    float a = 0.f;
+    for (int d = 0; d < hd; d += N) {
+      float k[N];
+      ld16(kp + d, k);
+#pragma unroll
+      for (int e = 0; e < N; e++) a = fmaf(q[d + e], k[e], a);
+    }
+    a *= scale;
+    s[t] = a;
+    mx = fmaxf(mx, a);
+  }
+  mx = warp_max(mx);
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); w++) mx = fmaxf(mx, red[w]);
+  __syncthreads();
+  float sum = 0.f;
+  for (int t = tid; t <= pos; t += blockDim.x) {
+    const float e = expf(s[t] - mx);
+    s[t] = e;
+    sum += e;
+  }
+  sum = warp_sum(sum);
+  if ((tid & 31) == 0) red[tid >> 5] = sum;
+  __syncthreads();  // (also: every s[t] written)
+  float l = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); w++) l += red[w];
+  const int G = blockDim.x / hd, g = tid / hd, d = tid % hd;
+  float acc = 0.f;
+  if (g < G)
+    for (int t = g; t <= pos; t += G) acc = fmaf(s[t], to_f(qkv[(row0 + t) * 3 * C + 2 * C + h * hd + d]), acc);
+  part[tid] = acc;
+  __syncthreads();
+  if (tid < hd) {
+    float o = 0.f;
+    for (int gg = 0; gg < G; gg++) o += part[gg * hd + tid];
+    out[(size_t)b * C + h * hd + tid] = from_f<T>(o / l);
+  }
+}
+
+template <typename T>
+cudaError_t decode_attention(T* out, const T* qkv, int B, int Tmax, int pos, int C, int H, cudaStream_t st) {
+  constexpr int N = VecN<T>::n;
+  const int hd = C / H;
+  if (B <= 0 || H <= 0 || C % H || hd > 128 || hd % N || pos < 0 || pos >= Tmax) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)(128 + 32 + Tmax + 256) * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(decode_attention_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  launch_k(decode_attention_kernel<T>, dim3((unsigned)(B * H)), dim3(256), smem, st, out, qkv, Tmax, pos, C, H,
+           1.0f / sqrtf((float)hd));
+  return launch_status(1);
+}
+
+// One CTA per row b: temperature 0 -> the index of the largest of the first V
+// logits (lowest index on ties); else the sampler's inverse CDF of
+// softmax(z / temperature) at coins[b]: thread t sums exp((z_i - max)/temp)
+// over its contiguous chunk of indices in order, the chunk sums are scanned
+// in thread order, and the thread whose chunk holds coin * total walks it to
+// the first index whose running sum exceeds that (V - 1 if none does).
+template <typename T>
+__global__ void __launch_bounds__(1024) sample_kernel(int* __restrict__ out_tok, const T* __restrict__ logits,
+                                                      long long ld, int V, float temperature,
+                                                      const float* __restrict__ coins) {
+  pdl_enter();
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  __shared__ float scan[1024];
+  __shared__ int found;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const T* z = logits + (size_t)b * ld;
+  // maximum (value, lowest index)
+  float best = -INFINITY;
+  int bi = V;
+  for (int i = tid; i < V; i += blockDim.x) {
+    const float v = to_f(z[i]);
+    if (v > best) best = v, bi = i;  // increasing i: the first maximum of this thread's indices
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) best = ov, bi = oi;
+  }
+  if (lane == 0) sv[w] = best, si[w] = bi;
+  __syncthreads();
+  best = sv[0];
+  bi = si[0];
+  for (int q = 1; q < (int)(blockDim.x >> 5); q++)
+    if (sv[q] > best || (sv[q] == best && si[q] < bi)) best = sv[q], bi = si[q];
+  if (temperature == 0.f) {
+    if (tid == 0) out_tok[b] = bi;
+    return;
+  }
+  const float inv_t = 1.0f / temperature;
+  const int chunk = (V + blockDim.x - 1) / blockDim.x;
+  const int c0 = tid * chunk, c1 = min(V, c0 + chunk);
+  float cs = 0.f;
+  for (int i = c0; i < c1; i++) cs += expf((to_f(z[i]) - best) * inv_t);
+  scan[tid] = cs;
+  __syncthreads();
+  // inclusive scan of the chunk sums in thread order (Hillis-Steele on shared memory)
+  for (int o = 1; o < (int)blockDim.x; o <<= 1) {
+    const float y = tid >= o ? scan[tid - o] : 0.f;
+    __syncthreads();
+    scan[tid] += y;
+    __syncthreads();
+  }
+  const float total = scan[blockDim.x - 1];
+  const float target = coins[b] * total;
+  const float before = tid > 0 ? scan[tid - 1] : 0.f;
+  // the chunk whose [start, end) holds the target; should rounding let two
+  // chunks claim it, the lower one wins
+  if (tid == 0) found = (int)blockDim.x;
+  __syncthreads();
+  if (c0 < c1 && target >= before && target < scan[tid]) atomicMin(&found, tid);
+  __syncthreads();
+  if (tid == found) {
+    float run = before;
+    int pick = c1 - 1;
+    for (int i = c0; i < c1; i++) {
+      run += expf((to_f(z[i]) - best) * inv_t);
+      if (target < run) {
+        pick = i;
+        break;
+      }
+    }
+    out_tok[b] = pick;
+  }
+  if (tid == 0 && found == (int)blockDim.x) out_tok[b] = V - 1;
+}
+
+template <typename T>
+cudaError_t sample_tokens(int* out_tok, const T* logits, long long ld, int rows, int V, float temperature,
+                          const float* coins, cudaStream_t st) {
+  if (rows <= 0 || V <= 0 || temperature < 0.f || (temperature > 0.f && !coins)) return cudaErrorInvalidValue;
+  launch_k(sample_kernel<T>, dim3((unsigned)rows), dim3(1024), 0, st, out_tok, logits, ld, V, temperature, coins);
+  return launch_status(1);
+}
+
 // mean of n per-position losses, one CTA, fixed summation order
 __global__ void mean_loss_kernel(float* loss, const float* __restrict__ losses, int n) {
   pdl_enter();
@@ -1786,6 +1956,9 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
                                              cudaStream_t, int*);                                         \
   template cudaError_t layernorm_apply<T>(T*, const T*, const float*, const float*, const T*, const T*, int,   \
                                           int, cudaStream_t);                                                \
+  template cudaError_t decode_attention<T>(T*, const T*, int, int, int, int, int, cudaStream_t);             \
+  template cudaError_t sample_tokens<T>(int*, const T*, long long, int, int, float, const float*,            \
+                                        cudaStream_t);                                                       \
   template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t, int, long long,  \
                                  long long);                                                              \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \

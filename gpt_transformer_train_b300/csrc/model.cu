@@ -24,6 +24,11 @@ extern unsigned long long gpt2_total_launches();
 
 struct gpt2 {
   gpt2_config cfg;
+  // inference: positions 0..cache_len-1 of every sequence are in the KV cache
+  // (the qkv activations); the last logits are B rows ld elements apart
+  int cache_len = 0;
+  size_t last_logits = 0;  // byte offset in the buffer
+  long long last_ld = 0;
   ParamLayout pl;
   BufferLayout bl;
   char* base = nullptr;
@@ -166,6 +171,10 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.flags = take(256);
   b.tok = take(BT * 4);
   b.tgt = take(BT * 4);
+  // inference with a KV cache, one new position per sequence: residual
+  // ping-pong, LayerNorm output, attention output, projection output (B x C
+  // each), fc pre-activation and GELU (B x 4C), logits (B x Vp), stats (2 x B fp32)
+  b.dec = take(((5 + 8) * (size_t)c.B * C + (size_t)c.B * c.Vp) * es + 2 * (size_t)c.B * 4);
   b.total = o;
   return b;
 }
@@ -223,6 +232,14 @@ struct Step {
     return gelu_forward<T>(fchg(l), fch(l), (long long)m->BT * 4 * c.C, m->st);
   }
   T* dsmall() const { return m->at<T>(m->bl.dsmall); }
+  // one-position inference scratch: k-th B x C slab (0, 1: residual, 2: LN out,
+  // 3: attention out, 4: projection out), fc pre-activation / GELU (B x 4C),
+  // logits (B x Vp), then the LayerNorm statistics
+  T* dec(int k) const { return m->at<T>(m->bl.dec) + (size_t)k * c.B * C; }
+  T* dec_fch() const { return dec(5); }
+  T* dec_fchg() const { return dec(9); }
+  T* dec_logits() const { return dec(13); }
+  float* dec_stats() const { return reinterpret_cast<float*>(dec_logits() + (size_t)c.B * c.Vp); }
   int* flags() const { return m->at<int>(m->bl.flags); }
 
   cudaError_t gemm(GemmArgs a) {
@@ -324,6 +341,45 @@ struct Step {
       CK(m, softmax_ce<T>(logits(), losses(), tgt, BTi, c.V, c.Vp, 1.0f / (float)BTi, 1, flags(), st));
       CK(m, mean_loss(m->at<float>(m->bl.loss), losses(), BTi, st));
     }
+    return GPT2_OK;
+  }
+
+  // One new position `pos` for every sequence, reading keys and values 0..pos
+  // from the KV cache and writing this position's q | k | v into it: the
+  // forward of one token per sequence (tok [B]), logits into dec_logits().
+  int decode(const int32_t* tok, int pos) {
+    cudaStream_t st = m->st;
+    const int Bi = c.B, Ci = c.C, Li = c.L;
+    const size_t CC = C * C;
+    T* x[2] = {dec(0), dec(1)};
+    T *lnb = dec(2), *att = dec(3), *prj = dec(4), *fh = dec_fch(), *fg = dec_fchg();
+    float *mu = dec_stats(), *rs = dec_stats() + Bi;
+    // x = wte[tok] + wpe[pos]: the encoder with one position, its wpe row pos
+    CK(m, encoder_forward<T>(x[0], tok, W(GPT2_WTE), W(GPT2_WPE) + (size_t)pos * C, Bi, 1, Ci, c.V, flags(), st));
+    int cur = 0;
+    for (int l = 0; l < Li; l++) {
+      if (l == 0) {
+        CK(m, residual_layernorm_forward<T>(nullptr, lnb, mu, rs, x[0], nullptr, W(GPT2_LN1W, l, C),
+                                            W(GPT2_LN1B, l, C), Bi, Ci, st));
+      } else {
+        CK(m, residual_layernorm_forward<T>(x[cur ^ 1], lnb, mu, rs, x[cur], prj, W(GPT2_LN1W, l, C),
+                                            W(GPT2_LN1B, l, C), Bi, Ci, st));
+        cur ^= 1;
+      }
+      // q | k | v of position pos straight into cache rows b*T + pos
+      GemmArgs a{lnb, C, 1, W(GPT2_QKVW, l, 3 * CC), C, 1, Bi, 3 * Ci, Ci, qkv(l) + (size_t)pos * 3 * C,
+                 (long long)c.T * 3 * C, W(GPT2_QKVB, l, 3 * C), nullptr, 0, EPI_STORE};
+      CK(m, gemm(a));
+      CK(m, decode_attention<T>(att, qkv(l), Bi, c.T, pos, Ci, c.H, st));
+      CK(m, linear_fwd(prj, att, W(GPT2_ATTPROJW, l, CC), W(GPT2_ATTPROJB, l, C), Bi, Ci, Ci));
+      CK(m, residual_layernorm_forward<T>(x[cur ^ 1], lnb, mu, rs, x[cur], prj, W(GPT2_LN2W, l, C),
+                                          W(GPT2_LN2B, l, C), Bi, Ci, st));
+      cur ^= 1;
+      CK(m, linear_fwd(fg, lnb, W(GPT2_FCW, l, 4 * CC), W(GPT2_FCB, l, 4 * C), Bi, 4 * Ci, Ci, fh));
+      CK(m, linear_fwd(prj, fg, W(GPT2_FCPROJW, l, 4 * CC), W(GPT2_FCPROJB, l, C), Bi, Ci, 4 * Ci));
+    }
+    CK(m, residual_layernorm_forward<T>(x[cur ^ 1], lnb, mu, rs, x[cur], prj, W(GPT2_LNFW), W(GPT2_LNFB), Bi, Ci, st));
+    CK(m, linear_fwd(dec_logits(), lnb, W(GPT2_WTE), nullptr, Bi, c.Vp, Ci));
     return GPT2_OK;
   }
 
@@ -507,8 +563,81 @@ int gpt2_forward(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_dev,
   m->logits_valid = rc == GPT2_OK && targets_dev == nullptr;
   m->loss_valid = m->have_targets;
   m->fwd_tokens = tokens_dev;
+  m->cache_len = 0;  // the qkv activations (the inference cache) now hold this batch
   if (rc) return rc;
   if (loss_host) return gpt2_get_loss(m, loss_host);
+  return GPT2_OK;
+}
+
+int gpt2_infer_prefill(gpt2* m, const int32_t* tokens_dev, int n) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!tokens_dev) FAIL(m, GPT2_ERR_INVALID_ARG, "tokens_dev is NULL");
+  if (n < 1 || n > m->cfg.T) FAIL(m, GPT2_ERR_INVALID_ARG, "prefill length %d outside 1..T=%d", n, m->cfg.T);
+  int rc = gpt2_forward(m, tokens_dev, nullptr, nullptr);
+  m->cache_len = 0;
+  if (rc) return rc;
+  const size_t es = m->cfg.precision == GPT2_PRECISION_BF16 ? 2 : 4;
+  m->cache_len = n;
+  m->last_logits = m->bl.logits + (size_t)(n - 1) * m->cfg.Vp * es;  // rows b*T + n-1
+  m->last_ld = (long long)m->cfg.T * m->cfg.Vp;
+  return GPT2_OK;
+}
+
+int gpt2_infer_step(gpt2* m, const int32_t* tokens_dev, int pos) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!tokens_dev) FAIL(m, GPT2_ERR_INVALID_ARG, "tokens_dev is NULL");
+  if (m->cache_len < 1) FAIL(m, GPT2_ERR_BAD_ORDER, "gpt2_infer_step needs gpt2_infer_prefill first");
+  if (pos != m->cache_len || pos >= m->cfg.T)
+    FAIL(m, GPT2_ERR_INVALID_ARG, "position %d: the cache holds %d positions of at most T=%d", pos, m->cache_len,
+         m->cfg.T);
+  int rc = m->cfg.precision == GPT2_PRECISION_BF16 ? Step<bf16>(m).decode(tokens_dev, pos)
+                                                   : Step<float>(m).decode(tokens_dev, pos);
+  m->have_targets = m->logits_valid = m->loss_valid = false;  // the training activations are overwritten
+  if (rc) {
+    m->cache_len = 0;
+    return rc;
+  }
+  m->cache_len = pos + 1;
+  m->last_logits = m->bl.dec + ((5 + 8) * (size_t)m->cfg.B * m->cfg.C) *
+                                   (m->cfg.precision == GPT2_PRECISION_BF16 ? 2 : 4);
+  m->last_ld = m->cfg.Vp;
+  return GPT2_OK;
+}
+
+int gpt2_sample(gpt2* m, float temperature, const float* coins_dev, int32_t* out_tokens_dev) {
+  if (!m) return GPT2_ERR_INVALID_ARG;
+  if (!out_tokens_dev || (temperature > 0.f && !coins_dev) || !(temperature >= 0.f))
+    FAIL(m, GPT2_ERR_INVALID_ARG, "sampling needs out_tokens_dev, a temperature >= 0 and coins_dev when it is > 0");
+  if (m->cache_len < 1) FAIL(m, GPT2_ERR_BAD_ORDER, "gpt2_sample needs gpt2_infer_prefill or gpt2_infer_step first");
+  if (m->cfg.precision == GPT2_PRECISION_BF16)
+    CK(m, sample_tokens<bf16>((int*)out_tokens_dev, m->at<bf16>(m->last_logits), m->last_ld, m->cfg.B, m->cfg.V,
+                              temperature, coins_dev, m->st));
+  else
+    CK(m, sample_tokens<float>((int*)out_tokens_dev, m->at<float>(m->last_logits), m->last_ld, m->cfg.B, m->cfg.V,
+                               temperature, coins_dev, m->st));
+  return GPT2_OK;
+}
+
+int gpt2_get_infer_logits(gpt2* m, float* host) {
+  if (!m || !host) return GPT2_ERR_INVALID_ARG;
+  if (m->cache_len < 1) FAIL(m, GPT2_ERR_BAD_ORDER, "no inference logits yet");
+  int rc = check_flags(m);
+  if (rc) return rc;
+  const size_t Vp = m->cfg.Vp;
+  if (m->cfg.precision == GPT2_PRECISION_BF16) {
+    std::vector<uint16_t> tmp((size_t)m->cfg.B * Vp);
+    CK(m, cudaMemcpy2DAsync(tmp.data(), Vp * 2, m->base + m->last_logits, (size_t)m->last_ld * 2, Vp * 2, m->cfg.B,
+                            cudaMemcpyDeviceToHost, m->st));
+    CK(m, cudaStreamSynchronize(m->st));
+    for (size_t i = 0; i < tmp.size(); i++) {
+      uint32_t u = (uint32_t)tmp[i] << 16;
+      memcpy(&host[i], &u, 4);
+    }
+  } else {
+    CK(m, cudaMemcpy2DAsync(host, Vp * 4, m->base + m->last_logits, (size_t)m->last_ld * 4, Vp * 4, m->cfg.B,
+                            cudaMemcpyDeviceToHost, m->st));
+    CK(m, cudaStreamSynchronize(m->st));
+  }
   return GPT2_OK;
 }
 
@@ -595,6 +724,7 @@ int gpt2_step_host(gpt2* m, const int32_t* tokens_host, const int32_t* targets_h
 }
 
 int gpt2_graph_step(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_dev) {
+  if (m) m->cache_len = 0;
   if (!m) return GPT2_ERR_INVALID_ARG;
   if (!tokens_dev || !targets_dev) FAIL(m, GPT2_ERR_INVALID_ARG, "tokens_dev and targets_dev are required");
   if (!m->st) FAIL(m, GPT2_ERR_INVALID_ARG, "graph capture needs a created stream, not the legacy default one");

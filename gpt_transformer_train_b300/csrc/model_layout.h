@@ -47,6 +47,7 @@ struct BufferLayout {
   size_t proj, logits, losses, loss;        // temporaries / classifier
   size_t dres, dresc, dfch, dqkv, dsmall;  // activation gradients (dresc, dfch, dqkv: per layer)
   size_t attD, attS, partial, keys, ws, ws_floats, gnorm, flags, tok, tgt;
+  size_t dec;                               // one-position inference scratch (see Step::dec_*)
   size_t total;
 };
 

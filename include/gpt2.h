@@ -155,6 +155,34 @@ float gpt2_lr_schedule(float max_lr, float final_frac, int warmup, int total, in
 int gpt2_step_host(gpt2* m, const int32_t* tokens_host, const int32_t* targets_host,
                    float lr, float b1, float b2, float eps, float wd, int t, float* loss_host);
 
+/* Inference with a KV cache (the pages' CPU sampler reruns the whole forward
+ * for every new token and keeps no cache: "llm.c: GPT-2 training in plain C
+ * ...", §6 Reality check; here the keys and values of earlier positions are
+ * kept).  The cache is the model's qkv activation buffer; any training
+ * forward replaces it, and the inference calls overwrite the training
+ * activations.
+ *   gpt2_infer_prefill: the forward over tokens_dev [B][T] (logits kept),
+ *     taking positions 0..n-1 as the prompt of every sequence (1 <= n <= T;
+ *     later positions of tokens_dev only need to hold valid token ids); the
+ *     logits of position n-1 become the last logits.
+ *   gpt2_infer_step: the forward of one new position pos (== the number of
+ *     positions cached, < T) of every sequence from next-token ids
+ *     tokens_dev [B] (device int32), reading keys and values 0..pos-1 from the
+ *     cache and adding position pos to it; its logits become the last logits.
+ *   gpt2_sample: one token per sequence from the last logits into
+ *     out_tokens_dev [B] (device int32): temperature 0 takes the largest of
+ *     the first V logits (lowest index on ties); a temperature > 0 takes the
+ *     first index whose cumulative softmax(logits / temperature) probability
+ *     exceeds coins_dev[b] (device float, uniform in [0, 1): the caller draws
+ *     them), the sampler of the pages' CPU trainer.
+ *   gpt2_get_infer_logits: the last logits as B x Vp host floats
+ *     (synchronises; reports a token out of range as GPT2_ERR_TOKEN_RANGE).
+ * Asynchronous on the model's stream except gpt2_get_infer_logits. */
+int gpt2_infer_prefill(gpt2* m, const int32_t* tokens_dev, int n);
+int gpt2_infer_step(gpt2* m, const int32_t* tokens_dev, int pos);
+int gpt2_sample(gpt2* m, float temperature, const float* coins_dev, int32_t* out_tokens_dev);
+int gpt2_get_infer_logits(gpt2* m, float* host);
+
 /* Host copies (synchronising).  tensor is a GPT2_* id; host holds
  * gpt2_tensor_numel() floats.  Logits: B*T*Vp floats, only after a forward
  * without targets.  Losses: B*T per-position losses of the last forward with
