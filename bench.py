@@ -356,6 +356,70 @@ def run_ours(args, w):
     return 0
 
 
+def run_decode(args, w):
+    """Generation with the KV cache: B sequences, a prompt of `prompt`
+    positions prefilled, then one new position per sequence per step (decode
+    forward + greedy sampling, the token feeding the next step).  value =
+    generated tokens per second over the timed steps; the roofline is HBM:
+    per step the bf16 weights of every matmul (block weights and the tied
+    classifier) and the cached keys and values of every layer are read once."""
+    import torch
+    import gpt_transformer_train_b300 as g
+    from synthetic import zipf_tokens
+    dev = torch.device("cuda", 0)
+    B, T, prompt = w["B"], w["T"], args.prompt
+    if prompt + args.warmup + args.steps > T:
+        raise SystemExit("prompt + warmup + steps must fit in T")
+    cfg = g.make_config(w["L"], w["C"], w["H"], w["V"], w["Vp"], w["maxT"], B, T, g.PRECISION_BF16)
+    stream = torch.cuda.Stream(dev)
+    m = g.GPT2(cfg, SEED, stream=stream)
+    tok, _ = zipf_tokens(B, T, w["V"], SEED)
+    ttok = torch.from_numpy(tok).to(dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    m.gpt2_infer_prefill(ttok, prompt)
+    m.gpt2_sample(0.0, None, nxt)
+    pos = prompt
+    for _ in range(args.warmup):
+        m.gpt2_infer_step(nxt, pos)
+        m.gpt2_sample(0.0, None, nxt)
+        pos += 1
+    torch.cuda.synchronize(dev)
+    clocks = Clocks(int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pos0 = pos
+    l0 = m.launch_count()
+    e0.record(stream)
+    for _ in range(args.steps):
+        m.gpt2_infer_step(nxt, pos)
+        m.gpt2_sample(0.0, None, nxt)
+        pos += 1
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    L, C, Vp = w["L"], w["C"], w["Vp"]
+    weight_bytes = 2 * (12 * L * C * C + Vp * C)
+    kv_bytes = sum(L * B * (p + 1) * 2 * C * 2 for p in range(pos0, pos)) / args.steps
+    step_bytes = weight_bytes + kv_bytes
+    peaks = load_peaks()
+    achieved = step_bytes * args.steps / (ms / 1e3) / 1e9
+    out = {"metric": f"GPT-2 {args.workload.upper()} decode tokens/s with a KV cache (B={B}, prompt {prompt}, greedy)",
+           "value": B * args.steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Zipf(1.1) prompt, seeded N(0,0.02) init)",
+           "config": {"workload": workload_name(args.workload, w) + f", decode positions {pos0}..{pos - 1}",
+                      "global_batch": B, "seq_len": T, "parallelism": "single GPU",
+                      "l2": "weights + KV cache read per step (up to 0.25 + 0.60 GB) exceed L2 in sum"},
+           "roofline": {"kernel": "decode step (all kernels)", "bound": "hbm", "achieved": achieved,
+                        "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                        "traffic": None, "bytes_per_step": step_bytes,
+                        "peak_source": f"{peaks['source']} HBM copy"},
+           "gpu_launches": m.launch_count() - l0, "clocks": clk}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -366,10 +430,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--recompute", type=int, default=0, choices=[0, 1, 2],
                     help="activation recompute level (0: keep all activations)")
+    ap.add_argument("--decode", action="store_true",
+                    help="time generation with the KV cache instead of the training step")
+    ap.add_argument("--prompt", type=int, default=512, help="--decode: prefilled positions")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.decode:
+        return run_decode(args, w)
     return run_ours(args, w)
 
 

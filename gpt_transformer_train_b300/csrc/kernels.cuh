@@ -38,6 +38,10 @@ struct GemmArgs {
   float* dvec; int dT, dH;  // EPI_ROWDOT only
 };
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
+// products with at most 32 rows (one position per sequence when decoding):
+// both operands K-major, EPI_STORE or EPI_GELU, A small enough for shared memory
+template <typename T> bool gemm_skinny_supported(const GemmArgs& a);
+template <typename T> cudaError_t gemm_skinny(const GemmArgs& a, cudaStream_t st);
 // tcgen05/TMA tensor-core path (bf16 operands); returns cudaErrorNotSupported
 // when the shape or layout is outside what the kernel handles.
 cudaError_t gemm_tc(const GemmArgs& a, int* flags, cudaStream_t st);

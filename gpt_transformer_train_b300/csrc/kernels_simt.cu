@@ -1122,6 +1122,176 @@ cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st) {
 }
 
 // ============================================================================
+// Products with few rows (M <= 32: one position per sequence when decoding):
+// D[m][n] = sum_k A[m][k] B[n][k] (+ bias, optionally GELU with aux), both
+// operands K-major.  Bound by the stream of B: A is copied to shared memory
+// once per CTA; each warp owns NC output columns and issues every 16-byte load
+// of those rows of B at once (lane l takes elements 8l.. of each of the KCH
+// 256-wide chunks; KCH = K / 256 for bf16), so one round trip serves the whole
+// row, then keeps one fp32 sum per (row m, column) and adds the 32 lanes'
+// sums by a shuffle tree.
+// ============================================================================
+constexpr int SKINNY_WARPS = 8;
+template <typename T, int MT, int KCH, int NC>
+__global__ void __launch_bounds__(32 * SKINNY_WARPS) gemm_skinny_kernel(GemmArgs g) {
+  pdl_enter();
+  constexpr int N = VecN<T>::n;
+  extern __shared__ __align__(16) unsigned char sk_raw[];
+  T* xs = reinterpret_cast<T*>(sk_raw);  // [M][K]
+  const int M = g.M, K = g.K, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const T* A = (const T*)g.A;
+  const T* Bw = (const T*)g.B;
+  const int ngroups = (g.N + NC - 1) / NC;
+  uint4 wr[NC][KCH];  // this warp's rows of B, all in flight at once
+  auto fetch = [&](int grp) {
+    const int n0 = grp * NC;
+#pragma unroll
+    for (int c = 0; c < NC; c++)
+#pragma unroll
+      for (int j = 0; j < KCH; j++)
+        wr[c][j] = n0 + c < g.N ? __ldcs(reinterpret_cast<const uint4*>(Bw + (size_t)(n0 + c) * g.ldb) + j * 32 + lane)
+                                : make_uint4(0u, 0u, 0u, 0u);
+  };
+  // the first group's B rows are requested before A is copied, so both round trips overlap
+  int grp = blockIdx.x * SKINNY_WARPS + w;
+  if (grp < ngroups) fetch(grp);
+  for (int i0 = threadIdx.x; i0 < M * (K / N); i0 += 4 * blockDim.x) {
+    uint4 t[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i = i0 + u * blockDim.x;
+      if (i < M * (K / N)) t[u] = reinterpret_cast<const uint4*>(A + (size_t)(i / (K / N)) * g.lda)[i % (K / N)];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int i = i0 + u * blockDim.x;
+      if (i < M * (K / N)) reinterpret_cast<uint4*>(xs + (size_t)(i / (K / N)) * K)[i % (K / N)] = t[u];
+    }
+  }
+  __syncthreads();
+  for (; grp < ngroups; grp += gridDim.x * SKINNY_WARPS) {
+    const int n0 = grp * NC;
+    if (grp != (int)(blockIdx.x * SKINNY_WARPS + w)) fetch(grp);
+    float acc[MT][NC];
+#pragma unroll
+    for (int m = 0; m < MT; m++)
+#pragma unroll
+      for (int c = 0; c < NC; c++) acc[m][c] = 0.f;
+#pragma unroll
+    for (int j = 0; j < KCH; j++) {
+      float wv[NC][N];
+#pragma unroll
+      for (int c = 0; c < NC; c++) {
+        if constexpr (N == 8) {
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&wr[c][j]);
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const float2 t = __bfloat1622float2(h[e]);
+            wv[c][2 * e] = t.x;
+            wv[c][2 * e + 1] = t.y;
+          }
+        } else {
+          const float* q = reinterpret_cast<const float*>(&wr[c][j]);
+#pragma unroll
+          for (int e = 0; e < N; e++) wv[c][e] = q[e];
+        }
+      }
+      const int k0 = (j * 32 + lane) * N;
+#pragma unroll
+      for (int m = 0; m < MT; m++) {
+        if (m < M) {
+          float xv[N];
+          ld16(xs + (size_t)m * K + k0, xv);
+#pragma unroll
+          for (int c = 0; c < NC; c++)
+#pragma unroll
+            for (int e = 0; e < N; e++) acc[m][c] = fmaf(xv[e], wv[c][e], acc[m][c]);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; m++) {
+      if (m < M) {
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+          const int n = n0 + c;
+          float v = warp_sum(acc[m][c]);
+          if (lane == (m * NC + c) % 32 && n < g.N) {
+            if (g.bias) v += to_f(((const T*)g.bias)[n]);
+            if (g.epi == EPI_GELU) {
+              ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
+              v = gelu_f(round_to<T>(v));
+            }
+            ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
+          }
+        }
+      }
+    }
+  }
+}
+
+// K in whole 32-lane chunks of 16 bytes, at most 12 of them (bf16: K = 256,
+// 512, ..., 3072; fp32: 128, ..., 1536)
+template <typename T>
+static int skinny_chunks(int K) {
+  constexpr int N = VecN<T>::n;
+  return K % (32 * N) ? 0 : K / (32 * N);
+}
+
+template <typename T>
+bool gemm_skinny_supported(const GemmArgs& a) {
+  auto al16 = [](const void* q) { return ((uintptr_t)q & 15) == 0; };
+  const int kch = skinny_chunks<T>(a.K);
+  return a.M >= 1 && a.M <= 32 && a.N >= 1 && kch >= 1 && kch <= 12 && a.a_kmajor && a.b_kmajor &&
+         a.batch <= 1 && (a.epi == EPI_STORE || (a.epi == EPI_GELU && a.aux)) && a.lda % VecN<T>::n == 0 &&
+         a.ldb % VecN<T>::n == 0 && al16(a.A) && al16(a.B) && (size_t)a.M * a.K * sizeof(T) <= 200 * 1024;
+}
+
+template <typename T, int MT, int KCH, int NC>
+static cudaError_t skinny_launch(const GemmArgs& a, size_t smem, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<T, MT, KCH, NC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int grid = (int)std::min<long long>(cdiv(cdiv(a.N, NC), SKINNY_WARPS), 8LL * tc_num_sms());
+  launch_k(gemm_skinny_kernel<T, MT, KCH, NC>, dim3(grid), dim3(32 * SKINNY_WARPS), smem, st, a);
+  return cudaSuccess;
+}
+
+template <typename T, int MT>
+static cudaError_t skinny_by_k(const GemmArgs& a, size_t smem, cudaStream_t st) {
+  switch (skinny_chunks<T>(a.K)) {  // two columns per warp while the registers allow
+    case 1: return skinny_launch<T, MT, 1, 2>(a, smem, st);
+    case 2: return skinny_launch<T, MT, 2, 2>(a, smem, st);
+    case 3: return skinny_launch<T, MT, 3, 2>(a, smem, st);
+    case 4: return skinny_launch<T, MT, 4, 2>(a, smem, st);
+    case 5: return skinny_launch<T, MT, 5, 1>(a, smem, st);
+    case 6: return skinny_launch<T, MT, 6, 1>(a, smem, st);
+    case 7: return skinny_launch<T, MT, 7, 1>(a, smem, st);
+    case 8: return skinny_launch<T, MT, 8, 1>(a, smem, st);
+    case 9: return skinny_launch<T, MT, 9, 1>(a, smem, st);
+    case 10: return skinny_launch<T, MT, 10, 1>(a, smem, st);
+    case 11: return skinny_launch<T, MT, 11, 1>(a, smem, st);
+    default: return skinny_launch<T, MT, 12, 1>(a, smem, st);
+  }
+}
+
+template <typename T>
+cudaError_t gemm_skinny(const GemmArgs& a, cudaStream_t st) {
+  if (!gemm_skinny_supported<T>(a)) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)a.M * a.K * sizeof(T);
+  cudaError_t e;
+  if (a.M <= 8) e = skinny_by_k<T, 8>(a, smem, st);
+  else if (a.M <= 16) e = skinny_by_k<T, 16>(a, smem, st);
+  else e = skinny_by_k<T, 32>(a, smem, st);
+  if (e != cudaSuccess) return e;
+  return launch_status(1);
+}
+
+// ============================================================================
 // SIMT causal attention (any head size <= 128).  Forward: one warp per query
 // row, keys in chunks of 32 (one key per lane), online max/sum, LSE saved.
 // Backward: D = rowsum(dO*O); a dQ pass per query row and a dK/dV pass per
@@ -1647,8 +1817,18 @@ __global__ void __launch_bounds__(256) decode_attention_kernel(T* __restrict__ o
   for (int w = 0; w < (int)(blockDim.x >> 5); w++) l += red[w];
   const int G = blockDim.x / hd, g = tid / hd, d = tid % hd;
   float acc = 0.f;
-  if (g < G)
-    for (int t = g; t <= pos; t += G) acc = fmaf(s[t], to_f(qkv[(row0 + t) * 3 * C + 2 * C + h * hd + d]), acc);
+  if (g < G) {
+    const T* vcol = qkv + row0 * 3 * C + 2 * C + h * hd + d;  // v_t[d] at vcol + t*3C
+    int t = g;
+    for (; t + 7 * G <= pos; t += 8 * G) {  // eight loads in flight, added in key order
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) v[u] = to_f(vcol[(size_t)(t + u * G) * 3 * C]);
+#pragma unroll
+      for (int u = 0; u < 8; u++) acc = fmaf(s[t + u * G], v[u], acc);
+    }
+    for (; t <= pos; t += G) acc = fmaf(s[t], to_f(vcol[(size_t)t * 3 * C]), acc);
+  }
   part[tid] = acc;
   __syncthreads();
   if (tid < hd) {
@@ -1694,9 +1874,16 @@ __global__ void __launch_bounds__(1024) sample_kernel(int* __restrict__ out_tok,
   // maximum (value, lowest index)
   float best = -INFINITY;
   int bi = V;
-  for (int i = tid; i < V; i += blockDim.x) {
-    const float v = to_f(z[i]);
-    if (v > best) best = v, bi = i;  // increasing i: the first maximum of this thread's indices
+  for (int i0 = tid; i0 < V; i0 += 8 * blockDim.x) {  // eight loads in flight, compared in index order
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int i = i0 + u * blockDim.x;
+      v[u] = i < V ? to_f(z[i]) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++)
+      if (v[u] > best) best = v[u], bi = i0 + u * blockDim.x;  // increasing index: the first maximum
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -1962,6 +2149,8 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t, int, long long,  \
                                  long long);                                                              \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \
+  template bool gemm_skinny_supported<T>(const GemmArgs&);                                                 \
+  template cudaError_t gemm_skinny<T>(const GemmArgs&, cudaStream_t);                                      \
   template cudaError_t attention_forward_simt<T>(T*, float*, const T*, int, int, int, int, cudaStream_t); \
   template cudaError_t attention_backward_simt<T>(T*, float*, const T*, const T*, const T*, const float*, \
                                                   int, int, int, int, cudaStream_t);                     \

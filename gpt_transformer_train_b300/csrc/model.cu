@@ -246,7 +246,11 @@ struct Step {
     bool rec = m->prof_on && m->prof_n < m->prof_flops.size();
     if (rec) cudaEventRecord(m->prof_ev[2 * m->prof_n], m->st);
     cudaError_t e;
-    if (c.precision == GPT2_PRECISION_BF16 && gemm_tc_supported(a)) e = gemm_tc(a, flags(), m->st);
+    // a few rows (decoding): the few-row kernel, except for very wide products
+    // (the classifier), which have enough tiles for the tensor cores
+    const bool tc_ok = c.precision == GPT2_PRECISION_BF16 && gemm_tc_supported(a);
+    if (gemm_skinny_supported<T>(a) && !(tc_ok && a.N >= 16384)) e = gemm_skinny<T>(a, m->st);
+    else if (tc_ok) e = gemm_tc(a, flags(), m->st);
     else e = gemm_simt<T>(a, m->st);
     if (rec) {
       cudaEventRecord(m->prof_ev[2 * m->prof_n + 1], m->st);

@@ -85,7 +85,11 @@ int gpt2_op_matmul(int dtype, const void* A, long long lda, int a_kmajor, const 
   if (workspace && ((uintptr_t)workspace & 15)) return GPT2_ERR_INVALID_ARG;
   GemmArgs a{A, lda, a_kmajor, B, ldb, b_kmajor, M, N, K, D, ldd, bias, aux, ldaux, epilogue,
              (float*)workspace, workspace ? workspace_bytes / sizeof(float) : 0};
-  if (path == 2 || (path == 0 && dtype == GPT2_PRECISION_BF16 && gemm_tc_supported(a))) {
+  // path 0 with at most 32 rows: the few-row SIMT kernel (as the decode step uses)
+  if (path == 0 && (dtype == GPT2_PRECISION_BF16 ? gemm_skinny_supported<bf16>(a) : gemm_skinny_supported<float>(a)))
+    return rc_of(dtype == GPT2_PRECISION_BF16 ? gemm_skinny<bf16>(a, ST(stream)) : gemm_skinny<float>(a, ST(stream)));
+  // (path 0 takes the tensor cores only with flags_dev, which their bounded waits report into)
+  if (path == 2 || (path == 0 && dtype == GPT2_PRECISION_BF16 && flags_dev && gemm_tc_supported(a))) {
     if (dtype != GPT2_PRECISION_BF16 || !flags_dev || !gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
     return rc_of(gemm_tc(a, flags_dev, ST(stream)));
   }

@@ -259,6 +259,26 @@ def test_matmul_simt_epilogues(ops, dt):
     assert rel_l2(host(F), acc + 1) < 1e-5
 
 
+@pytest.mark.parametrize("dt", ["fp32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(1, 200, 64), (7, 768, 768), (16, 2304, 768), (32, 768, 3072)])
+def test_matmul_few_rows(ops, dt, M, N, K):
+    """Products with at most 32 rows (the decode step's): path 0 takes the
+    few-row kernel; plain, +bias and +bias+GELU (pre-activation in aux)."""
+    A, B, bias = normal_array((M, K), 43), normal_array((N, K), 44, 0.05), normal_array((N,), 45)
+    tA, tB, tbias = dev(A, DT[dt]), dev(B, DT[dt]), dev(bias, DT[dt])
+    acc = host(tA).astype(np.float64) @ host(tB).astype(np.float64).T
+    tol = 1e-5 if dt == "fp32" else 2 ** -7
+    D = torch.empty(M, N, device="cuda", dtype=DT[dt])
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N)
+    assert rel_l2(host(D), acc) < tol
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias)
+    assert rel_l2(host(D), acc + host(tbias)) < tol
+    pre = torch.empty_like(D)
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias, aux=pre, ldaux=N, epilogue=ops.EPI_GELU)
+    assert rel_l2(host(pre), acc + host(tbias)) < tol
+    assert rel_l2(host(D), O.gelu_forward(host(pre).astype(np.float64))) < tol
+
+
 # ---- tensor-core (tcgen05/TMA) GEMM --------------------------------------
 # Row strides must be multiples of 8 bf16 (16 bytes) for TMA; M, N, K need
 # not be tile multiples (K=104, M=136, N=136/264 exercise the ragged edges).
