@@ -437,10 +437,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
 // the dQ kernel, a plain blocked product dQ = dS K over those blocks.
 // ============================================================================
 constexpr int DKV_STAGES = 3;            // Q/dO/lse/D ring of the dK/dV kernel
-constexpr int EW_WARPS = 8;              // elementwise warps of the dK/dV kernel
+constexpr int EW_WARPS = 16;             // elementwise warps of the dK/dV kernel
 constexpr int EW_COLS = 128 / (EW_WARPS / 4);  // columns of S each elementwise warp handles
-constexpr int BWD_THREADS = 64 + 32 * EW_WARPS;
-static_assert(EW_COLS == 64, "an elementwise warp's share of a dS block is one 32-row slice of one 64-wide half");
+constexpr int BWD_THREADS = 64 + 32 * EW_WARPS + 32;  // producer, MMA, elementwise warps, dS store warp
 
 // D[b][h][t] = sum over the head's 64 channels of dO * O: one thread per 8
 // channels, the 8 threads of a head added by a fixed shuffle tree.
@@ -608,9 +607,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 // ============================================================================
 // backward, dK and dV.  Persistent: items are (b, h, key tile), heaviest
 // first; per item the query tiles kt..nq-1 stream through a ring (Q, dO and
-// their lse and D).  Needs D from attn_rowdot_kernel; writes each dS^T tile
-// it forms to the dS block buffer for the dQ kernel (each elementwise warp
-// bulk-copies its own 4 KB slice: 32 key rows of one 64-query half).
+// their lse and D).  Needs D (from attn_rowdot_kernel or the producer of dO);
+// writes each dS^T tile it forms to the dS block buffer for the dQ kernel:
+// the last warp bulk-copies the whole 32 KB tile once the elementwise warps
+// have written it, and releases it when the copy has read it.
 // ============================================================================
 constexpr uint32_t BWD_QD = 2 * TILE + 1024;  // Q tile, dO tile, lse[128], D[128]
 constexpr size_t DKV_SMEM = 1024 + 2 * TILE + DKV_STAGES * BWD_QD + 2 * PTILE + 256;
@@ -634,7 +634,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t b_pfree = b_pfull + 8;   // dV/dK MMAs done reading them
   const uint32_t b_accfull = b_pfree + 8;
   const uint32_t b_accfree = b_accfull + 8;
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 + 2 * DKV_STAGES + 6);
+  const uint32_t b_dsfree = b_accfree + 8;  // dS^T tile copied out
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 + 2 * DKV_STAGES + 7);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -667,6 +668,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     mbar_init(b_pfree, 1);
     mbar_init(b_accfull, 1);
     mbar_init(b_accfree, EW_WARPS);
+    mbar_init(b_dsfree, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         g0 += it.nit;
       }
     }
-  } else {  // ---- elementwise warps: key row r (lane quarter q), query-column group cq
+  } else if (warp < 2 + EW_WARPS) {  // ---- elementwise warps: key row r (lane quarter q), query-column group cq
     const int q = warp & 3, cq = (warp - 2) >> 2;
     const int c0 = cq * EW_COLS;
     const uint32_t r = q * 32 + lane;
@@ -791,10 +793,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
 #pragma unroll
         for (int e = 0; e < EW_COLS; e++) dp[e] = sv[e] * (dp[e] - dq[e]);
-        if (nG > 0 && !mbar_wait_warp(b_pfree, (nG - 1) & 1, abort_flag)) { ok = false; break; }
-        // ... and this warp's copy of its previous dS^T slice has read it
-        if (lane == 0) bulk_wait_read();
-        __syncwarp();
+        // the P^T / dS^T tiles are free once the dV/dK MMAs have read them
+        // and the copy of the previous dS^T has read it
+        if (nG > 0 && (!mbar_wait_warp(b_pfree, (nG - 1) & 1, abort_flag) ||
+                       !mbar_wait_warp(b_dsfree, (nG - 1) & 1, abort_flag))) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < EW_COLS / 32; c++) {
           store_row32(sPT, r, c0 + 32 * c, *reinterpret_cast<float(*)[32]>(sv + 32 * c));
@@ -802,11 +804,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(b_pfull);
-          const uint32_t slice = (uint32_t)cq * TILE + (uint32_t)q * 32 * 128;
-          bulk_store(p.ds + ds_block(it.bh, nq, it.kt, it.kt + k) * PTILE + slice, sDST + slice, 32 * 128);
-        }
+        if (lane == 0) mbar_arrive(b_pfull);
         nG++;
       }
       if (!ok || !mbar_wait_warp(b_accfull, n & 1, abort_flag)) break;
@@ -832,6 +830,21 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                          p.scale);
       }
       g0 += it.nit;
+    }
+  } else {  // ---- the dS store warp: each finished dS^T tile to its block of the dS buffer
+    uint32_t nG = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      const Item it = item(i);
+      for (int k = 0; k < it.nit; k++, nG++) {
+        if (!mbar_wait_warp(b_pfull, nG & 1, abort_flag)) { ok = false; break; }
+        if (lane == 0) {
+          bulk_store(p.ds + ds_block(it.bh, nq, it.kt, it.kt + k) * PTILE, sDST, PTILE);
+          bulk_wait_read();
+          mbar_arrive(b_dsfree);
+        }
+        __syncwarp();
+      }
     }
     if (lane == 0) bulk_wait_all();
   }
