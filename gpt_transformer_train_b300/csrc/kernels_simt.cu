@@ -1737,11 +1737,127 @@ __global__ void __launch_bounds__(1024) softmax_ce_reg_kernel(T* __restrict__ lo
   }
 }
 
+// bf16 rows that fit in shared memory (Vp * 2 <= 110 KB): one CTA of 512
+// threads per row, two CTAs per SM.  The row is copied into shared memory with
+// cp.async (16 bytes a request, all in flight at once) and the three passes
+// (maximum, exp and sum, dlogits) read it there, so one CTA's copy overlaps the
+// other's passes.  exp(z - max) is kept in place as fp16, as in the register
+// kernel; same arithmetic, the reductions over 512 threads.
+constexpr int SCE_SMEM_THREADS = 512;
+__global__ void __launch_bounds__(SCE_SMEM_THREADS, 2)
+    softmax_ce_smem_kernel(bf16* __restrict__ logits, float* __restrict__ losses, const int* __restrict__ targets,
+                           int V, int Vp, float dloss, int write_grad, int* flags) {
+  pdl_enter();
+  constexpr int N = 8;
+  constexpr float L2E = 1.4426950408889634f;
+  constexpr int W = SCE_SMEM_THREADS / 32;
+  extern __shared__ __align__(16) unsigned char sce_row[];
+  __shared__ float red[2][W];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  bf16* z = logits + (size_t)blockIdx.x * Vp;
+  const int nvec = Vp / N;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sce_row);
+  for (int vi = tid; vi < nvec; vi += SCE_SMEM_THREADS)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + vi * 16), "l"(z + (size_t)vi * N)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  int tg = targets[blockIdx.x];
+  const bool bad = tg < 0 || tg >= V;
+  if (bad) tg = 0;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  uint4* row = reinterpret_cast<uint4*>(sce_row);
+  // row max over the first V columns
+  float m = -INFINITY;
+  for (int vi = tid; vi < nvec; vi += SCE_SMEM_THREADS) {
+    float f[N];
+    ld16(reinterpret_cast<const bf16*>(row + vi), f);
+    if (vi * N + N <= V) {
+#pragma unroll
+      for (int j = 0; j < N; j++) m = fmaxf(m, f[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < N; j++)
+        if (vi * N + j < V) m = fmaxf(m, f[j]);
+    }
+  }
+  const float zt = to_f(reinterpret_cast<const bf16*>(sce_row)[tg]);
+  m = warp_max(m);
+  if (lane == 0) red[0][w] = m;
+  __syncthreads();
+  m = red[0][0];
+#pragma unroll
+  for (int j = 1; j < W; j++) m = fmaxf(m, red[0][j]);
+  const float ml = m * L2E;
+  // exp(z - max) in place as fp16, and its sum
+  float s = 0.f;
+  for (int vi = tid; vi < nvec; vi += SCE_SMEM_THREADS) {
+    float f[N];
+    ld16(reinterpret_cast<const bf16*>(row + vi), f);
+    if (vi * N + N <= V) {
+#pragma unroll
+      for (int j = 0; j < N; j++) f[j] = fast_exp2(fmaf(f[j], L2E, -ml));
+    } else {
+#pragma unroll
+      for (int j = 0; j < N; j++) f[j] = vi * N + j < V ? fast_exp2(fmaf(f[j], L2E, -ml)) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < N; j++) s += f[j];
+    uint4 h;
+    __half2* hp = reinterpret_cast<__half2*>(&h);
+#pragma unroll
+    for (int j = 0; j < 4; j++) hp[j] = __floats2half2_rn(f[2 * j], f[2 * j + 1]);
+    row[vi] = h;
+  }
+  s = warp_sum(s);
+  if (lane == 0) red[1][w] = s;
+  __syncthreads();
+  s = red[1][0];
+#pragma unroll
+  for (int j = 1; j < W; j++) s += red[1][j];
+  if (tid == 0) {
+    if (bad) atomicOr(flags, FLAG_TARGET_RANGE);
+    losses[blockIdx.x] = m + logf(s) - zt;
+  }
+  if (!write_grad) return;
+  // the target's probability in fp32: p - 1 loses everything when p is near 1
+  const float g_tg = (fast_exp2(fmaf(zt, L2E, -ml)) / s - 1.f) * dloss;
+  const float scale = dloss / s;
+  for (int vi = tid; vi < nvec; vi += SCE_SMEM_THREADS) {
+    const uint4 h = row[vi];
+    const __half2* hp = reinterpret_cast<const __half2*>(&h);
+    float f[N];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float2 t = __half22float2(hp[j]);
+      f[2 * j] = t.x * scale;
+      f[2 * j + 1] = t.y * scale;
+    }
+    if (tg >= vi * N && tg < vi * N + N) f[tg - vi * N] = g_tg;
+    st16_cs(z + (size_t)vi * N, f);
+  }
+}
+
 template <typename T>
 cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,
                        float dloss, int write_grad, int* flags, cudaStream_t st) {
   constexpr int N = VecN<T>::n;
   if (Vp % N) return cudaErrorInvalidValue;
+  if constexpr (sizeof(T) == 2) {
+    const size_t smem = (size_t)Vp * 2;
+    if (smem <= 110 * 1024 && Vp >= 16384 && ((uintptr_t)logits & 15) == 0 && rows > 0) {
+      static bool attr = false;
+      if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(softmax_ce_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             110 * 1024);
+        if (e != cudaSuccess) return e;
+        attr = true;
+      }
+      launch_k(softmax_ce_smem_kernel, dim3(rows), dim3(SCE_SMEM_THREADS), smem, st, (bf16*)logits, losses, targets,
+               V, Vp, dloss, write_grad, flags);
+      return launch_status(1);
+    }
+  }
   const int vpt = (int)cdiv(Vp / N, 1024);
 #define SCE(K) launch_k(softmax_ce_reg_kernel<T, K>, dim3(rows), dim3(1024), 0, st, logits, losses, targets, V, Vp, dloss, write_grad, flags)
   switch (vpt) {
