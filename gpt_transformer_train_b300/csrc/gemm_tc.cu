@@ -77,6 +77,7 @@ struct TcParams {
   int batch;   // independent products, item z at depth z of every tensor map
   float* dvec;  // EPI_ROWDOT: the per-row, per-head dot products
   int dT, dH;
+  int acc_store;  // EPI_ACC_F32: split 0 stores its tile into D instead of adding it
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -373,7 +374,10 @@ __global__ void __launch_bounds__(192, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (sp == 0) tma_reduce_add_3d(&td, col0, rbase, z, buf);
+              if (sp == 0) {
+                if (p.acc_store) tma_store_3d(&td, col0, rbase, z, buf);
+                else tma_reduce_add_3d(&td, col0, rbase, z, buf);
+              }
               else tma_store_3d(&tx, col0, rbase, sp - 1, buf);  // workspace slot sp - 1
               bulk_commit();
             }
@@ -574,7 +578,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
   TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
-             (int)nb, g.dvec, g.dT, g.dH};
+             (int)nb, g.dvec, g.dT, g.dH, g.acc_store};
   const long long units = tiles * splits * (long long)nb;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(192);

@@ -36,6 +36,7 @@ struct GemmArgs {
   // bias, no K split
   int batch; long long sA, sB, sD, sAux;
   float* dvec; int dT, dH;  // EPI_ROWDOT only
+  int acc_store;            // EPI_ACC_F32: D = acc instead of D += acc (the first writer of a fresh gradient)
 };
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
 // products with at most 32 rows (one position per sequence when decoding):
@@ -56,15 +57,16 @@ template <typename T>
 cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, int B, int T_, int C,
                             int V, int* flags, cudaStream_t st);
 // dwte/dwpe += scatter of dres (fp32 [B*T][C]); keys: 2*pow2(B*T) uint32 scratch
+// (accumulate_wpe = 0: dwpe is overwritten instead of added to)
 cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
-                             int C, uint32_t* keys, cudaStream_t st);
+                             int C, uint32_t* keys, cudaStream_t st, int accumulate_wpe = 1);
 size_t encoder_backward_scratch_bytes(int BT);
 // the same with a larger scratch (BT <= 16384): radix-sorted keys and
 // fixed-size chunks of the per-token sums, so no CTA waits on a long run
 bool encoder_backward_fast_supported(int BT, int C);
 size_t encoder_backward_fast_scratch_bytes(int BT, int C);
 cudaError_t encoder_backward_fast(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_, int C,
-                                  void* scratch, cudaStream_t st);
+                                  void* scratch, cudaStream_t st, int accumulate_wpe = 1);
 
 template <typename T>
 cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* rstd, const T* a,
@@ -85,14 +87,15 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
 // out_o[z*sOut + c] += sum_k partial[z*sPart + (k*nout + o)*C + c] (sPart = 0:
 // nchunks*nout*C), chunks in a fixed order.
 cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
-                            int nout, cudaStream_t st, int nbatch = 1, long long sOut = 0, long long sPart = 0);
+                            int nout, cudaStream_t st, int nbatch = 1, long long sOut = 0, long long sPart = 0,
+                            int accumulate = 1);
 size_t ln_backward_partial_floats(int rows, int C);
 // out[c] += sum_rows X[r*ldx + c]; partial: colsum_partial_floats(rows, cols) floats.
 // nbatch > 1: the same for items z = 0..nbatch-1 at out + z*sOut, X + z*sX
 // (partial: nbatch times as many floats), in one pair of launches.
 template <typename T>
 cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st,
-                   int nbatch = 1, long long sOut = 0, long long sX = 0);
+                   int nbatch = 1, long long sOut = 0, long long sX = 0, int accumulate = 1);
 size_t colsum_partial_floats(int rows, int cols);
 int reduce_chunks(int rows);  // number of row chunks the reductions use
 

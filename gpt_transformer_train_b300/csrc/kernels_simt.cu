@@ -69,7 +69,8 @@ cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, 
 //   dwte[v] += sum over positions with token v, in increasing position order.
 // Positions are bucketed by a single-CTA bitonic sort of (token << 16 | pos).
 // ----------------------------------------------------------------------------
-__global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dres, int B, int T_, int C) {
+__global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restrict__ dres, int B, int T_, int C,
+                                int accumulate) {
   pdl_enter();
   int nvec = C / 4;
   long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -83,8 +84,8 @@ __global__ void wpe_grad_kernel(float* __restrict__ dwpe, const float* __restric
     for (int i = 0; i < 4; i++) s[i] += x[i];
   }
   float* dst = dwpe + (size_t)t * C + cv * 4;
-  float o[4];
-  ld16(dst, o);
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+  if (accumulate) ld16(dst, o);
 #pragma unroll
   for (int i = 0; i < 4; i++) o[i] += s[i];
   st16(dst, o);
@@ -192,12 +193,13 @@ __global__ void __launch_bounds__(32 * RUNS_WARPS) wte_grad_runs_kernel(float* _
 }
 
 cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
-                             int C, uint32_t* keys, cudaStream_t st) {  // the small-scratch form
+                             int C, uint32_t* keys, cudaStream_t st, int accumulate_wpe) {  // the small-scratch form
   int BT = B * T_;
   int n = pow2_at_least(BT);
   if (n > 32768) return cudaErrorInvalidValue;
   long long nv = (long long)T_ * (C / 4);
-  launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C);
+  launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C,
+           accumulate_wpe);
   size_t smem = (size_t)n * sizeof(uint32_t);
   static bool attr_set = false;
   if (!attr_set) {
@@ -383,13 +385,14 @@ __global__ void __launch_bounds__(128) wte_span_kernel(float* __restrict__ dwte,
 }
 
 cudaError_t encoder_backward_fast(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_, int C,
-                                  void* scratch, cudaStream_t st) {
+                                  void* scratch, cudaStream_t st, int accumulate_wpe) {
   const int BT = B * T_;
   if (!encoder_backward_fast_supported(BT, C)) return cudaErrorInvalidValue;
   uint32_t* keys = (uint32_t*)scratch;
   float* slots = (float*)((char*)scratch + fast_keys_bytes(BT));
   const long long nv = (long long)T_ * (C / 4);
-  launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C);
+  launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C,
+           accumulate_wpe);
   const size_t smem = ((size_t)2 * BT + 32 * 256) * sizeof(uint32_t);
   static bool attr = false;
   if (!attr) {
@@ -566,7 +569,8 @@ size_t colsum_partial_floats(int rows, int cols) { return (size_t)reduce_chunks(
 __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict__ out0, float* __restrict__ out1,
                                                               float* __restrict__ out2,
                                                               const float* __restrict__ partial, int nchunks,
-                                                              int C, int nout, long long sOut, long long sPart) {
+                                                              int C, int nout, long long sOut, long long sPart,
+                                                              int accumulate) {
   pdl_enter();
   __shared__ float sh[8][32];
   const int o = blockIdx.y;
@@ -597,17 +601,17 @@ __global__ void __launch_bounds__(256) reduce_partials_kernel(float* __restrict_
     float t = sh[0][lane];
 #pragma unroll
     for (int i = 1; i < 8; i++) t += sh[i][lane];
-    out[c] += t;
+    out[c] = accumulate ? out[c] + t : t;
   }
 }
 
 cudaError_t reduce_partials(float* out0, float* out1, float* out2, const float* partial, int nchunks, int C,
-                            int nout, cudaStream_t st, int nbatch, long long sOut, long long sPart) {
+                            int nout, cudaStream_t st, int nbatch, long long sOut, long long sPart, int accumulate) {
   if (nbatch < 1 || nbatch > 65535) return cudaErrorInvalidValue;
   if (sPart == 0) sPart = (long long)nchunks * nout * C;
   dim3 grid((unsigned)cdiv(C, 32), nout, nbatch);
   launch_k(reduce_partials_kernel, dim3(grid), dim3(256), 0, st, out0, out1, out2, partial, nchunks, C, nout, sOut,
-           sPart);
+           sPart, accumulate);
   return launch_status(1);
 }
 
@@ -997,7 +1001,7 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__
 
 template <typename T>
 cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, float* partial, cudaStream_t st,
-                   int nbatch, long long sOut, long long sX) {
+                   int nbatch, long long sOut, long long sX, int accumulate) {
   constexpr int N = VecN<T>::n;
   if (cols % N || ldx % N || nbatch < 1 || nbatch > 65535) return cudaErrorInvalidValue;
   const int nch = reduce_chunks(rows);
@@ -1006,7 +1010,7 @@ cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, fl
            sX);
   cudaError_t e = launch_status(1);
   if (e != cudaSuccess) return e;
-  return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st, nbatch, sOut);
+  return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st, nbatch, sOut, 0, accumulate);
 }
 
 // ============================================================================
@@ -1085,7 +1089,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
       float v = acc[i][j];
       if (g.epi == EPI_ACC_F32) {
         float* D = (float*)g.D;
-        D[(size_t)m * g.ldd + n] += v;
+        D[(size_t)m * g.ldd + n] = g.acc_store ? v : D[(size_t)m * g.ldd + n] + v;
       } else if (g.epi == EPI_GELU_BWD) {
         float h = to_f(((const T*)g.aux)[(size_t)m * g.ldaux + n]);
         ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v * gelu_grad_f(h));
@@ -1754,14 +1758,17 @@ __global__ void __launch_bounds__(SCE_SMEM_THREADS, 2)
   extern __shared__ __align__(16) unsigned char sce_row[];
   __shared__ float red[2][W];
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  bf16* z = logits + (size_t)blockIdx.x * Vp;
+  // rows from the last: the classifier GEMM wrote the last rows last (they are
+  // still in L2), and the input-gradient GEMM after this kernel starts from row 0
+  const int rowi = gridDim.x - 1 - blockIdx.x;
+  bf16* z = logits + (size_t)rowi * Vp;
   const int nvec = Vp / N;
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sce_row);
   for (int vi = tid; vi < nvec; vi += SCE_SMEM_THREADS)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sbase + vi * 16), "l"(z + (size_t)vi * N)
                  : "memory");
   asm volatile("cp.async.commit_group;" ::: "memory");
-  int tg = targets[blockIdx.x];
+  int tg = targets[rowi];
   const bool bad = tg < 0 || tg >= V;
   if (bad) tg = 0;
   asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -1817,7 +1824,7 @@ __global__ void __launch_bounds__(SCE_SMEM_THREADS, 2)
   for (int j = 1; j < W; j++) s += red[1][j];
   if (tid == 0) {
     if (bad) atomicOr(flags, FLAG_TARGET_RANGE);
-    losses[blockIdx.x] = m + logf(s) - zt;
+    losses[rowi] = m + logf(s) - zt;
   }
   if (!write_grad) return;
   // the target's probability in fp32: p - 1 loses everything when p is near 1
@@ -2263,7 +2270,7 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   template cudaError_t sample_tokens<T>(int*, const T*, long long, int, int, float, const float*,            \
                                         cudaStream_t);                                                       \
   template cudaError_t colsum<T>(float*, const T*, int, int, long long, float*, cudaStream_t, int, long long,  \
-                                 long long);                                                              \
+                                 long long, int);                                                         \
   template cudaError_t gemm_simt<T>(const GemmArgs&, cudaStream_t);                                       \
   template bool gemm_skinny_supported<T>(const GemmArgs&);                                                 \
   template cudaError_t gemm_skinny<T>(const GemmArgs&, cudaStream_t);                                      \

@@ -272,6 +272,7 @@ struct Step {
   cudaError_t linear_wgrad(float* dW, const T* dY, const T* X, int M, int N, int K) {
     GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32,
                m->at<float>(m->bl.ws), m->bl.ws_floats};
+    a.acc_store = fresh;
     return gemm(a);
   }
   // the same for every layer at once: item l reads dY + l*sY and X + l*sX and
@@ -280,6 +281,7 @@ struct Step {
                                   int K) {
     GemmArgs a{dY, N, 0, X, K, 0, N, K, M, dW, K, nullptr, nullptr, 0, EPI_ACC_F32, nullptr, 0,
                (int)c.L, sY, sX, (long long)N * K, 0};
+    a.acc_store = fresh;
     return gemm(a);
   }
 
@@ -387,7 +389,12 @@ struct Step {
     return GPT2_OK;
   }
 
-  int backward(const int32_t* tok) {
+  // fresh: the gradient buffer holds garbage and every gradient's first
+  // writer stores instead of adding (the graph step's backward, with no zero_grad)
+  int fresh = 0;
+  int backward(const int32_t* tok, bool fresh_grads = false) {
+    fresh = fresh_grads ? 1 : 0;
+    const int acc = fresh ? 0 : 1;
     cudaStream_t st = m->st;
     int Ci = c.C, Li = c.L, BTi = m->BT;
     size_t CC = C * C;
@@ -423,7 +430,7 @@ struct Step {
       if (perlayer) {
         CK(m, ln_recompute(2 * l + 1, W(GPT2_LN2W, l, C), W(GPT2_LN2B, l, C)));
         CK(m, linear_wgrad(G(GPT2_FCW, l, 4 * CC), dfch(l), ln(2 * l + 1), BTi, 4 * Ci, Ci));
-        CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dfch(l), BTi, 4 * Ci, 4 * Ci, cpart, st));
+        CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dfch(l), BTi, 4 * Ci, 4 * Ci, cpart, st, 1, 0, 0, acc));
       }
       // LN2 (+ residual gradient; its column sums give the attention-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), dresc(l, 1), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
@@ -440,7 +447,7 @@ struct Step {
       if (perlayer) {
         CK(m, ln_recompute(2 * l, W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C)));
         CK(m, linear_wgrad(G(GPT2_QKVW, l, 3 * CC), dqkv(l), ln(2 * l), BTi, 3 * Ci, Ci));
-        CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dqkv(l), BTi, 3 * Ci, 3 * Ci, cpart, st));
+        CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dqkv(l), BTi, 3 * Ci, 3 * Ci, cpart, st, 1, 0, 0, acc));
       }
       // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)
       CK(m, layernorm_backward<T>(dres(), l > 0 ? dresc(l - 1, 0) : nullptr, dsmall(), resid(2 * l), mean(2 * l),
@@ -451,12 +458,14 @@ struct Step {
     // all layers: final LN, every LN2 (one batched launch), LN1 of layers
     // 1..L-1 (one batched launch), LN1 of layer 0
     const long long sl = (long long)lnslot;
-    CK(m, reduce_partials(G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part + 2 * L * lnslot, nch, Ci, 3, st));
-    CK(m, reduce_partials(G(GPT2_LN2W), G(GPT2_LN2B), G(GPT2_ATTPROJB), part + lnslot, nch, Ci, 3, st, Li, Ci, 2 * sl));
+    CK(m, reduce_partials(G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part + 2 * L * lnslot, nch, Ci, 3, st,
+                          1, 0, 0, acc));
+    CK(m, reduce_partials(G(GPT2_LN2W), G(GPT2_LN2B), G(GPT2_ATTPROJB), part + lnslot, nch, Ci, 3, st, Li, Ci, 2 * sl,
+                          acc));
     if (Li > 1)
       CK(m, reduce_partials(G(GPT2_LN1W, 1, C), G(GPT2_LN1B, 1, C), G(GPT2_FCPROJB), part + 2 * lnslot, nch, Ci, 3, st,
-                            Li - 1, Ci, 2 * sl));
-    CK(m, reduce_partials(G(GPT2_LN1W), G(GPT2_LN1B), nullptr, part, nch, Ci, 3, st));
+                            Li - 1, Ci, 2 * sl, acc));
+    CK(m, reduce_partials(G(GPT2_LN1W), G(GPT2_LN1B), nullptr, part, nch, Ci, 3, st, 1, 0, 0, acc));
     if (!perlayer) {
       // weight gradients of every layer, one batched product per weight type
       const long long sBT = (long long)BTi * Ci;
@@ -465,13 +474,15 @@ struct Step {
       CK(m, linear_wgrad_layers(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, BTi, Ci, Ci));
       CK(m, linear_wgrad_layers(G(GPT2_QKVW), dqkv(0), 3 * sBT, ln(0), 2 * sBT, BTi, 3 * Ci, Ci));
       // bias gradients of the fc and qkv layers of every layer: column sums of their output gradients
-      CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT));
-      CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT));
+      CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT, acc));
+      CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT, acc));
     }
     if (encoder_backward_fast_supported(BTi, Ci))
-      CK(m, encoder_backward_fast(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
+      CK(m, encoder_backward_fast(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st,
+                                  acc));
     else
-      CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st));
+      CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st,
+                             acc));
     return GPT2_OK;
   }
 };
@@ -741,9 +752,14 @@ int gpt2_graph_step(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_d
     const bool prof = m->prof_on;
     m->prof_on = false;  // no event records inside the graph
     CK(m, cudaStreamBeginCapture(m->st, cudaStreamCaptureModeThreadLocal));
-    int rc = gpt2_zero_grad(m);
-    if (!rc) rc = gpt2_forward(m, tokens_dev, targets_dev, nullptr);
-    if (!rc) rc = gpt2_backward(m);
+    // zero_grad + forward + backward, the backward writing fresh gradients
+    // (every gradient's first writer stores), so no memset of the buffer runs
+    int rc = gpt2_forward(m, tokens_dev, targets_dev, nullptr);
+    if (!rc) {
+      rc = m->cfg.precision == GPT2_PRECISION_BF16 ? Step<bf16>(m).backward(m->fwd_tokens, true)
+                                                   : Step<float>(m).backward(m->fwd_tokens, true);
+      m->have_targets = false;
+    }
     cudaGraph_t graph = nullptr;
     cudaError_t e = cudaStreamEndCapture(m->st, &graph);
     m->prof_on = prof;
