@@ -1132,11 +1132,12 @@ cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st) {
 // once per CTA; each warp owns NC output columns and issues every 16-byte load
 // of those rows of B at once (lane l takes elements 8l.. of each of the KCH
 // 256-wide chunks; KCH = K / 256 for bf16), so one round trip serves the whole
-// row, then keeps one fp32 sum per (row m, column) and adds the 32 lanes'
+// row, then walks the rows m one at a time (a short loop body that stays in
+// the instruction cache), one fp32 sum per column, and adds the 32 lanes'
 // sums by a shuffle tree.
 // ============================================================================
 constexpr int SKINNY_WARPS = 8;
-template <typename T, int MT, int KCH, int NC>
+template <typename T, int KCH, int NC>
 __global__ void __launch_bounds__(32 * SKINNY_WARPS) gemm_skinny_kernel(GemmArgs g) {
   pdl_enter();
   constexpr int N = VecN<T>::n;
@@ -1176,66 +1177,51 @@ __global__ void __launch_bounds__(32 * SKINNY_WARPS) gemm_skinny_kernel(GemmArgs
   for (; grp < ngroups; grp += gridDim.x * SKINNY_WARPS) {
     const int n0 = grp * NC;
     if (grp != (int)(blockIdx.x * SKINNY_WARPS + w)) fetch(grp);
-    float acc[MT][NC];
+    for (int m = 0; m < M; m++) {
+      float acc[NC];
 #pragma unroll
-    for (int m = 0; m < MT; m++)
+      for (int c = 0; c < NC; c++) acc[c] = 0.f;
 #pragma unroll
-      for (int c = 0; c < NC; c++) acc[m][c] = 0.f;
-#pragma unroll
-    for (int j = 0; j < KCH; j++) {
-      float wv[NC][N];
-#pragma unroll
-      for (int c = 0; c < NC; c++) {
-        if constexpr (N == 8) {
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&wr[c][j]);
-#pragma unroll
-          for (int e = 0; e < 4; e++) {
-            const float2 t = __bfloat1622float2(h[e]);
-            wv[c][2 * e] = t.x;
-            wv[c][2 * e + 1] = t.y;
-          }
-        } else {
-          const float* q = reinterpret_cast<const float*>(&wr[c][j]);
-#pragma unroll
-          for (int e = 0; e < N; e++) wv[c][e] = q[e];
-        }
-      }
-      const int k0 = (j * 32 + lane) * N;
-#pragma unroll
-      for (int m = 0; m < MT; m++) {
-        if (m < M) {
-          float xv[N];
-          ld16(xs + (size_t)m * K + k0, xv);
-#pragma unroll
-          for (int c = 0; c < NC; c++)
-#pragma unroll
-            for (int e = 0; e < N; e++) acc[m][c] = fmaf(xv[e], wv[c][e], acc[m][c]);
-        }
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < MT; m++) {
-      if (m < M) {
+      for (int j = 0; j < KCH; j++) {
+        float xv[N];
+        ld16(xs + (size_t)m * K + (j * 32 + lane) * N, xv);
 #pragma unroll
         for (int c = 0; c < NC; c++) {
-          const int n = n0 + c;
-          float v = warp_sum(acc[m][c]);
-          if (lane == (m * NC + c) % 32 && n < g.N) {
-            if (g.bias) v += to_f(((const T*)g.bias)[n]);
-            if (g.epi == EPI_GELU) {
-              ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
-              v = gelu_f(round_to<T>(v));
+          float wv[N];
+          if constexpr (N == 8) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&wr[c][j]);
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              const float2 t = __bfloat1622float2(h[e]);
+              wv[2 * e] = t.x;
+              wv[2 * e + 1] = t.y;
             }
-            ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
+          } else {
+            const float* q = reinterpret_cast<const float*>(&wr[c][j]);
+#pragma unroll
+            for (int e = 0; e < N; e++) wv[e] = q[e];
           }
+#pragma unroll
+          for (int e = 0; e < N; e++) acc[c] = fmaf(xv[e], wv[e], acc[c]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < NC; c++) {
+        const int n = n0 + c;
+        float v = warp_sum(acc[c]);
+        if (lane == c && n < g.N) {
+          if (g.bias) v += to_f(((const T*)g.bias)[n]);
+          if (g.epi == EPI_GELU) {
+            ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
+            v = gelu_f(round_to<T>(v));
+          }
+          ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
         }
       }
     }
   }
 }
 
-// K in whole 32-lane chunks of 16 bytes, at most 12 of them (bf16: K = 256,
-// 512, ..., 3072; fp32: 128, ..., 1536)
 template <typename T>
 static int skinny_chunks(int K) {
   constexpr int N = VecN<T>::n;
@@ -1251,35 +1237,35 @@ bool gemm_skinny_supported(const GemmArgs& a) {
          a.ldb % VecN<T>::n == 0 && al16(a.A) && al16(a.B) && (size_t)a.M * a.K * sizeof(T) <= 200 * 1024;
 }
 
-template <typename T, int MT, int KCH, int NC>
+template <typename T, int KCH, int NC>
 static cudaError_t skinny_launch(const GemmArgs& a, size_t smem, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<T, MT, KCH, NC>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<T, KCH, NC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int grid = (int)std::min<long long>(cdiv(cdiv(a.N, NC), SKINNY_WARPS), 8LL * tc_num_sms());
-  launch_k(gemm_skinny_kernel<T, MT, KCH, NC>, dim3(grid), dim3(32 * SKINNY_WARPS), smem, st, a);
+  launch_k(gemm_skinny_kernel<T, KCH, NC>, dim3(grid), dim3(32 * SKINNY_WARPS), smem, st, a);
   return cudaSuccess;
 }
 
-template <typename T, int MT>
+template <typename T>
 static cudaError_t skinny_by_k(const GemmArgs& a, size_t smem, cudaStream_t st) {
   switch (skinny_chunks<T>(a.K)) {  // two columns per warp while the registers allow
-    case 1: return skinny_launch<T, MT, 1, 2>(a, smem, st);
-    case 2: return skinny_launch<T, MT, 2, 2>(a, smem, st);
-    case 3: return skinny_launch<T, MT, 3, 2>(a, smem, st);
-    case 4: return skinny_launch<T, MT, 4, 2>(a, smem, st);
-    case 5: return skinny_launch<T, MT, 5, 1>(a, smem, st);
-    case 6: return skinny_launch<T, MT, 6, 1>(a, smem, st);
-    case 7: return skinny_launch<T, MT, 7, 1>(a, smem, st);
-    case 8: return skinny_launch<T, MT, 8, 1>(a, smem, st);
-    case 9: return skinny_launch<T, MT, 9, 1>(a, smem, st);
-    case 10: return skinny_launch<T, MT, 10, 1>(a, smem, st);
-    case 11: return skinny_launch<T, MT, 11, 1>(a, smem, st);
-    default: return skinny_launch<T, MT, 12, 1>(a, smem, st);
+    case 1: return skinny_launch<T, 1, 2>(a, smem, st);
+    case 2: return skinny_launch<T, 2, 2>(a, smem, st);
+    case 3: return skinny_launch<T, 3, 2>(a, smem, st);
+    case 4: return skinny_launch<T, 4, 2>(a, smem, st);
+    case 5: return skinny_launch<T, 5, 1>(a, smem, st);
+    case 6: return skinny_launch<T, 6, 1>(a, smem, st);
+    case 7: return skinny_launch<T, 7, 1>(a, smem, st);
+    case 8: return skinny_launch<T, 8, 1>(a, smem, st);
+    case 9: return skinny_launch<T, 9, 1>(a, smem, st);
+    case 10: return skinny_launch<T, 10, 1>(a, smem, st);
+    case 11: return skinny_launch<T, 11, 1>(a, smem, st);
+    default: return skinny_launch<T, 12, 1>(a, smem, st);
   }
 }
 
@@ -1287,10 +1273,7 @@ template <typename T>
 cudaError_t gemm_skinny(const GemmArgs& a, cudaStream_t st) {
   if (!gemm_skinny_supported<T>(a)) return cudaErrorInvalidValue;
   const size_t smem = (size_t)a.M * a.K * sizeof(T);
-  cudaError_t e;
-  if (a.M <= 8) e = skinny_by_k<T, 8>(a, smem, st);
-  else if (a.M <= 16) e = skinny_by_k<T, 16>(a, smem, st);
-  else e = skinny_by_k<T, 32>(a, smem, st);
+  const cudaError_t e = skinny_by_k<T>(a, smem, st);
   if (e != cudaSuccess) return e;
   return launch_status(1);
 }
