@@ -56,17 +56,6 @@ using namespace tc;
 constexpr int BM = 128, BK = 64;
 constexpr uint32_t STG = 4096;  // one staging buffer: 32 rows x 128 B
 
-__device__ __forceinline__ float gelu_tanh(float x) {
-  float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.f + tanhf(u));
-}
-__device__ __forceinline__ float gelu_tanh_grad(float x) {
-  float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  float th = tanhf(u);
-  float du = 0.7978845608028654f * (1.f + 3.f * 0.044715f * x * x);
-  return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * du;
-}
-
 struct TcParams {
   int M, N, K;
   int a_mn, b_mn;
@@ -204,8 +193,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* bars = (uint64_t*)(stg_gen + 8 * STG);
   uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
-  uint32_t auxbar0 = smem_u32(bars + 2 * STAGES + 4);  // [4] GELU' input loads, one per epilogue warp
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * STAGES + 8);
+  uint32_t auxbar0 = smem_u32(bars + 2 * STAGES + 4);  // [8] aux tile loads, two per epilogue warp
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * STAGES + 12);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   const uint32_t ring = smem_u32(smem);
 
@@ -219,7 +208,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, 4 * CL);  // the epilogue warps of both CTAs of a pair
     }
-    for (int w = 0; w < 4; w++) mbar_init(auxbar0 + 8 * w, 1);
+    for (int w = 0; w < 8; w++) mbar_init(auxbar0 + 8 * w, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -341,8 +330,50 @@ __global__ void __launch_bounds__(192, 1)
     const int e = warp - 2;  // this warp's staging buffers and aux barrier
     const uint32_t stg = smem_u32(stg_gen) + e * 2 * STG;
     const uint8_t* stg_g = stg_gen + e * 2 * STG;
-    const uint32_t auxbar = auxbar0 + 8 * e;
-    uint32_t aux_phase = 0;
+    const uint32_t auxbar = auxbar0 + 16 * e;  // buffer b's loads complete on auxbar + 8 b
+    // epilogues that read an aux tile (GELU', ROWDOT): live chunk ci of this
+    // warp uses buffer ci & 1 (its aux tile in, its output written over it and
+    // stored from there); the next chunk's load is issued before this chunk's math
+    const bool aux_epi = p.epi == EPI_GELU_BWD || p.epi == EPI_ROWDOT;
+    // live chunk ci (of any epilogue but GELU) is staged in buffer ci & 1, so
+    // the store two chunks back is the last one that read it
+    uint32_t ci = 0;
+    int pending = -1;  // buffer with an aux load issued and not yet waited for
+    uint32_t pending_par = 0;
+    auto aux_issue = [&](int col, int row, int zz, uint32_t b) {  // lane 0
+      mbar_expect_tx(auxbar + 8 * b, STG);
+      tma_load_3d(stg + b * STG, &tx, col, row, zz, auxbar + 8 * b);
+    };
+    // the tile's bias: lane l holds columns 8l..8l+7 of it (16 bytes), the next
+    // tile's slice is loaded while this tile is processed
+    auto bias_slice = [&](int uu) {
+      uint4 r = make_uint4(0u, 0u, 0u, 0u);
+      if (p.bias && uu < units) {
+        const int col = ((uu % tiles) % num_n) * BN + 8 * lane;
+        if (8 * lane < BN && col < p.N) r = __ldg(reinterpret_cast<const uint4*>(p.bias + col));
+      }
+      return r;
+    };
+    uint4 bias_next = bias_slice(ustart);
+    // 32 bias values of columns c0..c0+31 of the tile into v
+    auto add_bias = [&](const uint4& bs, int c0, float (&v)[32]) {
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        uint4 w;
+        w.x = __shfl_sync(0xffffffffu, bs.x, c0 / 8 + g);
+        w.y = __shfl_sync(0xffffffffu, bs.y, c0 / 8 + g);
+        w.z = __shfl_sync(0xffffffffu, bs.z, c0 / 8 + g);
+        w.w = __shfl_sync(0xffffffffu, bs.w, c0 / 8 + g);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const float2 f = __bfloat1622float2(h[k]);
+          v[8 * g + 2 * k] += f.x;
+          v[8 * g + 2 * k + 1] += f.y;
+        }
+      }
+    };
+    bool prefetched = false;  // the next tile's first aux chunk is already on its way
     // the accumulator is free again: tell the CTA whose thread issues the MMAs
     auto release_acc = [&](uint32_t bar) {
       if (CL == 1) mbar_arrive(bar);
@@ -355,6 +386,18 @@ __global__ void __launch_bounds__(192, 1)
       const int rbase = m0 + q * 32;  // first row of this warp's slab
       const bool rows_in = rbase < p.M;
       const uint32_t a = j & 1, aph = (j >> 1) & 1;
+      const int nlive = rows_in ? min(BN / 64, (p.N - n0 + 63) / 64) : 0;  // live 64-column chunks
+      if (aux_epi && nlive > 0 && !prefetched) {  // the first chunk's aux tile, before the accumulator is ready
+        if (lane == 0) {
+          bulk_wait_read<1>();
+          aux_issue(n0, rbase, z, ci & 1);
+        }
+        pending = (int)(ci & 1);
+        pending_par = (ci >> 1) & 1;
+      }
+      prefetched = false;
+      const uint4 bias_cur = bias_next;
+      bias_next = bias_slice(u + ustep);
       // warp-uniform wait: tcgen05.ld below needs the whole warp converged
       if (!mbar_wait_warp(tfull0 + 8 * a, aph, abort_flag)) break;
       fence_after();
@@ -367,7 +410,7 @@ __global__ void __launch_bounds__(192, 1)
           tmem_ld32(tacc + c * 32, v);
           const int col0 = n0 + c * 32;
           if (rows_in && col0 < p.N) {
-            const uint32_t buf = stg + (c & 1) * STG;
+            const uint32_t buf = stg + (ci & 1) * STG;
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
             stage_f32(buf, lane, v);
@@ -381,6 +424,7 @@ __global__ void __launch_bounds__(192, 1)
               else tma_store_3d(&tx, col0, rbase, sp - 1, buf);  // workspace slot sp - 1
               bulk_commit();
             }
+            ci++;
           }
         }
         fence_before();
@@ -397,22 +441,13 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld32(tacc + cp * 64, v0);
         tmem_ld32(tacc + cp * 64 + 32, v1);
         if (!live) continue;
-        const uint32_t bo = stg + (cp & 1) * STG;  // output piece
+        const uint32_t bo = stg + (ci & 1) * STG;  // output piece
         if (p.epi == EPI_STORE) {
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
           if (p.bias) {
-#pragma unroll
-            for (int g = 0; g < 4; g++) {
-              float b0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, b1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-              if (col0 + 8 * g < p.N) ld16(p.bias + col0 + 8 * g, b0);
-              if (col0 + 32 + 8 * g < p.N) ld16(p.bias + col0 + 32 + 8 * g, b1);
-#pragma unroll
-              for (int k = 0; k < 8; k++) {
-                v0[8 * g + k] += b0[k];
-                v1[8 * g + k] += b1[k];
-              }
-            }
+            add_bias(bias_cur, cp * 64, v0);
+            add_bias(bias_cur, cp * 64 + 32, v1);
           }
           stage_bf16(bo, lane, 0, v0);
           stage_bf16(bo, lane, 4, v1);
@@ -422,72 +457,32 @@ __global__ void __launch_bounds__(192, 1)
             tma_store_3d(&td, col0, rbase, z, bo);
             bulk_commit();
           }
+          ci++;
         } else if (p.epi == EPI_GELU) {
-          // both buffers: pre-activation (aux) and GELU output
-          if (lane == 0) bulk_wait_read<0>();
+          // pre-activation (aux) from buffer 0 and GELU output from buffer 1,
+          // each store its own bulk group, so each buffer waits only for its own last store
+          if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
           if (p.bias) {
-#pragma unroll
-            for (int g = 0; g < 4; g++) {
-              float b0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, b1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-              if (col0 + 8 * g < p.N) ld16(p.bias + col0 + 8 * g, b0);
-              if (col0 + 32 + 8 * g < p.N) ld16(p.bias + col0 + 32 + 8 * g, b1);
-#pragma unroll
-              for (int k = 0; k < 8; k++) {
-                v0[8 * g + k] += b0[k];
-                v1[8 * g + k] += b1[k];
-              }
-            }
+            add_bias(bias_cur, cp * 64, v0);
+            add_bias(bias_cur, cp * 64 + 32, v1);
           }
           stage_bf16(stg, lane, 0, v0);
           stage_bf16(stg, lane, 4, v1);
-          // GELU of the pre-activation as stored (bf16), so a later recompute from it gives the same bits
-#pragma unroll
-          for (int k = 0; k < 32; k++) {
-            v0[k] = gelu_tanh(__bfloat162float(__float2bfloat16_rn(v0[k])));
-            v1[k] = gelu_tanh(__bfloat162float(__float2bfloat16_rn(v1[k])));
-          }
-          stage_bf16(stg + STG, lane, 0, v0);
-          stage_bf16(stg + STG, lane, 4, v1);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
             tma_store_3d(&tx, col0, rbase, z, stg);
-            tma_store_3d(&td, col0, rbase, z, stg + STG);
             bulk_commit();
           }
-        } else {  // EPI_GELU_BWD: D = acc * GELU'(aux); EPI_ROWDOT: D = acc and its dot with aux; aux tile by TMA
-          if (lane == 0) {
-            bulk_wait_read<0>();
-            mbar_expect_tx(auxbar, STG);
-            tma_load_3d(stg, &tx, col0, rbase, z, auxbar);
+          // GELU of the pre-activation as stored (bf16), so a later recompute from it gives the same bits
+#pragma unroll
+          for (int k = 0; k < 32; k++) {
+            v0[k] = gelu_fwd(__bfloat162float(__float2bfloat16_rn(v0[k])));
+            v1[k] = gelu_fwd(__bfloat162float(__float2bfloat16_rn(v1[k])));
           }
+          if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
-          if (!mbar_wait_warp(auxbar, aux_phase, abort_flag)) { ok = false; break; }
-          aux_phase ^= 1;
-          float hv[32];
-          if (p.epi == EPI_GELU_BWD) {
-            unstage_bf16(stg_g, lane, 0, hv);
-#pragma unroll
-            for (int k = 0; k < 32; k++) v0[k] *= gelu_tanh_grad(hv[k]);
-            unstage_bf16(stg_g, lane, 4, hv);
-#pragma unroll
-            for (int k = 0; k < 32; k++) v1[k] *= gelu_tanh_grad(hv[k]);
-          } else {
-            // the head's 64 columns: products of the stored (bf16) values with aux, in column order
-            float d = 0.f;
-            unstage_bf16(stg_g, lane, 0, hv);
-#pragma unroll
-            for (int k = 0; k < 32; k++) d = fmaf(__bfloat162float(__float2bfloat16_rn(v0[k])), hv[k], d);
-            unstage_bf16(stg_g, lane, 4, hv);
-#pragma unroll
-            for (int k = 0; k < 32; k++) d = fmaf(__bfloat162float(__float2bfloat16_rn(v1[k])), hv[k], d);
-            const int row = rbase + lane;
-            if (row < p.M) {
-              const int b = row / p.dT, t = row - b * p.dT;
-              p.dvec[((size_t)b * p.dH + col0 / 64) * p.dT + t] = d;
-            }
-          }
           stage_bf16(stg + STG, lane, 0, v0);
           stage_bf16(stg + STG, lane, 4, v1);
           fence_async_smem();
@@ -496,6 +491,70 @@ __global__ void __launch_bounds__(192, 1)
             tma_store_3d(&td, col0, rbase, z, stg + STG);
             bulk_commit();
           }
+        } else {  // EPI_GELU_BWD: D = acc * GELU'(aux); EPI_ROWDOT: D = acc and its dot with aux
+          const uint32_t b = ci & 1, buf = stg + b * STG;
+          const uint8_t* buf_g = stg_g + b * STG;
+          // the next live chunk's aux tile: this tile's next chunk, else the next tile's first
+          bool has_next = false;
+          int nx = col0 + 64, ny = rbase, nz = z;
+          if (cp + 1 < nlive) {
+            has_next = true;
+          } else if (u + ustep < units) {
+            const int u2 = u + ustep, t2 = u2 % tiles;
+            ny = tile_m0(t2) + q * 32;
+            nx = (t2 % num_n) * BN;
+            nz = u2 / (tiles * p.splits);
+            has_next = prefetched = ny < p.M;
+          }
+          if (has_next && lane == 0) {
+            bulk_wait_read<0>();  // the previous chunk's store has read the other buffer
+            aux_issue(nx, ny, nz, b ^ 1);
+          }
+          __syncwarp();
+          if (!mbar_wait_warp(auxbar + 8 * b, (ci >> 1) & 1, abort_flag)) {
+            if (has_next) mbar_settle(auxbar + 8 * (b ^ 1), ((ci + 1) >> 1) & 1);
+            pending = (int)b;
+            pending_par = (ci >> 1) & 1;
+            ok = false;
+            break;
+          }
+          pending = has_next ? (int)(b ^ 1) : -1;
+          pending_par = ((ci + 1) >> 1) & 1;
+          // each lane reads its row's aux values and writes its outputs over them
+          float hv[32];
+          if (p.epi == EPI_GELU_BWD) {
+            unstage_bf16(buf_g, lane, 0, hv);
+#pragma unroll
+            for (int k = 0; k < 32; k++) v0[k] *= gelu_bwd(hv[k]);
+            stage_bf16(buf, lane, 0, v0);
+            unstage_bf16(buf_g, lane, 4, hv);
+#pragma unroll
+            for (int k = 0; k < 32; k++) v1[k] *= gelu_bwd(hv[k]);
+            stage_bf16(buf, lane, 4, v1);
+          } else {
+            // the head's 64 columns: products of the stored (bf16) values with aux, in column order
+            float d = 0.f;
+            unstage_bf16(buf_g, lane, 0, hv);
+#pragma unroll
+            for (int k = 0; k < 32; k++) d = fmaf(__bfloat162float(__float2bfloat16_rn(v0[k])), hv[k], d);
+            stage_bf16(buf, lane, 0, v0);
+            unstage_bf16(buf_g, lane, 4, hv);
+#pragma unroll
+            for (int k = 0; k < 32; k++) d = fmaf(__bfloat162float(__float2bfloat16_rn(v1[k])), hv[k], d);
+            stage_bf16(buf, lane, 4, v1);
+            const int row = rbase + lane;
+            if (row < p.M) {
+              const int bb = row / p.dT, t = row - bb * p.dT;
+              p.dvec[((size_t)bb * p.dH + col0 / 64) * p.dT + t] = d;
+            }
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&td, col0, rbase, z, buf);
+            bulk_commit();
+          }
+          ci++;
         }
       }
       fence_before();
@@ -503,6 +562,8 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) release_acc(tempty0 + 8 * a);
       if (!ok) break;
     }
+    // an aux load cut short by an abort must land before the CTA exits
+    if (pending >= 0) mbar_settle(auxbar + 8 * pending, pending_par);
     // the staging buffers must stay valid until every store has read them
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
@@ -552,6 +613,7 @@ template <int BN, int STAGES, int CL>
 cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   constexpr size_t smem = smem_bytes<BN, STAGES, CL>();
   static_assert(smem <= 232448, "shared memory per CTA");
+  static_assert((2 * STAGES + 12) * 8 + 8 <= 256, "barriers, TMEM address and abort flag after the staging buffers");
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, CL>,
@@ -719,7 +781,7 @@ bool gemm_tc_supported(const GemmArgs& g) {
   if (g.epi == EPI_ROWDOT &&
       (!g.dvec || g.dT <= 0 || g.dH <= 0 || g.N != 64 * g.dH || g.M % g.dT || g.batch > 1 || g.bias))
     return false;
-  if (g.bias && !al16(g.bias)) return false;
+  if (g.bias && (!al16(g.bias) || (g.epi != EPI_STORE && g.epi != EPI_GELU))) return false;
   if (g.a_kmajor ? g.lda < g.K : g.lda < g.M) return false;
   if (g.b_kmajor ? g.ldb < g.K : g.ldb < g.N) return false;
   if (g.batch > 1) {

@@ -15,8 +15,6 @@
 #include <algorithm>
 
 #define LN_EPS 1e-5f
-#define GELU_SCALE 0.7978845608028654f   // sqrt(2/pi)
-#define GELU_CUBIC 0.044715f
 
 #include <atomic>
 static std::atomic<unsigned long long> g_launches{0};
@@ -1017,17 +1015,6 @@ cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, fl
 // SIMT GEMM (fp32 mode, and any shape the tensor-core path does not take)
 // 64x64 tile, BK 16, 256 threads, 4x4 per thread, fp32 accumulate.
 // ============================================================================
-__device__ __forceinline__ float gelu_f(float x) {
-  float u = GELU_SCALE * (x + GELU_CUBIC * x * x * x);
-  return 0.5f * x * (1.f + tanhf(u));
-}
-__device__ __forceinline__ float gelu_grad_f(float x) {
-  float u = GELU_SCALE * (x + GELU_CUBIC * x * x * x);
-  float th = tanhf(u);
-  float du = GELU_SCALE * (1.f + 3.f * GELU_CUBIC * x * x);
-  return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * du;
-}
-
 template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
   pdl_enter();
@@ -1092,13 +1079,13 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
         D[(size_t)m * g.ldd + n] = g.acc_store ? v : D[(size_t)m * g.ldd + n] + v;
       } else if (g.epi == EPI_GELU_BWD) {
         float h = to_f(((const T*)g.aux)[(size_t)m * g.ldaux + n]);
-        ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v * gelu_grad_f(h));
+        ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v * gelu_bwd(h));
       } else {
         if (g.bias) v += to_f(((const T*)g.bias)[n]);
         if (g.epi == EPI_GELU) {
           // GELU of the pre-activation as stored, so a later recompute from aux gives the same bits
           ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
-          v = gelu_f(round_to<T>(v));
+          v = gelu_fwd(round_to<T>(v));
         }
         ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
       }
@@ -1213,7 +1200,7 @@ __global__ void __launch_bounds__(32 * SKINNY_WARPS) gemm_skinny_kernel(GemmArgs
           if (g.bias) v += to_f(((const T*)g.bias)[n]);
           if (g.epi == EPI_GELU) {
             ((T*)g.aux)[(size_t)m * g.ldaux + n] = from_f<T>(v);
-            v = gelu_f(round_to<T>(v));
+            v = gelu_fwd(round_to<T>(v));
           }
           ((T*)g.D)[(size_t)m * g.ldd + n] = from_f<T>(v);
         }
@@ -2206,7 +2193,7 @@ __global__ void gelu_forward_kernel(T* __restrict__ out, const T* __restrict__ i
   float f[N];
   ld16_cs(in + i * N, f);
 #pragma unroll
-  for (int k = 0; k < N; k++) f[k] = gelu_f(f[k]);
+  for (int k = 0; k < N; k++) f[k] = gelu_fwd(f[k]);
   st16_cs(out + i * N, f);
 }
 template <typename T>
@@ -2220,7 +2207,7 @@ __global__ void gelu_backward_kernel(T* __restrict__ dinp, const T* __restrict__
   ld16_cs(inp + i * N, x);
   ld16_cs(dout + i * N, d);
 #pragma unroll
-  for (int k = 0; k < N; k++) d[k] *= gelu_grad_f(x[k]);
+  for (int k = 0; k < N; k++) d[k] *= gelu_bwd(x[k]);
   st16_cs(dinp + i * N, d);
 }
 template <typename T>

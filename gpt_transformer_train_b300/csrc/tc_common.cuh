@@ -61,6 +61,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
 }
+// a wait that ignores the abort flag, for copies still in flight when a CTA
+// gives up: it ends when the phase completes or after WAIT_NS
+__device__ __forceinline__ void mbar_settle(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = gtimer();
+  while (!mbar_try(bar, parity) && gtimer() - t0 < WAIT_NS) {
+  }
+}
 // the same wait taken by a whole warp (tcgen05.ld after it needs convergence)
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));

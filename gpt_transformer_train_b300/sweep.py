@@ -12,7 +12,9 @@ against the measured peaks (HBM copy GB/s, bf16 burst TFLOP/s).
 Kernel names: ln_fwd ln_bwd gelu_fwd gelu_bwd softmax_ce adamw encoder_fwd
 encoder_bwd attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096},
 gemm_<layer>_{fwd,dgrad,wgrad} for layer in qkv attproj fc fcproj classifier,
-and wgradL_<layer> (that weight gradient for 12 layers in one batched launch).
+gemmepi_fc_gelu, gemmepi_fcproj_gelubwd and gemmepi_attproj_rowdot (the fused
+epilogues as the step uses them), and wgradL_<layer> (that weight gradient for
+12 layers in one batched launch).
 """
 from __future__ import annotations
 
@@ -127,6 +129,25 @@ def make_case(name, ops):
         return (lambda: ops.gpt2_op_matmul_batched(L, dy, N, BT * N, 0, x, K, BT * K, 0, N, K, BT, dW, K, N * K,
                                                    epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC, flags_dev=fl),
                 2.0 * L * BT * N * K, "FLOP")
+    if name == "gemmepi_fc_gelu":  # fc forward: bias, pre-activation and GELU output written
+        N, K = GEMM_LAYERS["fc"]
+        W, b, x = randn((N, K), 22, std=0.02), randn((N,), 29), randn((BT, K), 23)
+        y, pre = torch.empty(BT, N, device="cuda", dtype=BF), torch.empty(BT, N, device="cuda", dtype=BF)
+        return (lambda: ops.gpt2_op_matmul(x, K, 1, W, K, 1, BT, N, K, y, N, bias=b, aux=pre, ldaux=N,
+                                           epilogue=ops.EPI_GELU, path=ops.PATH_TC, flags_dev=fl),
+                2.0 * BT * N * K, "FLOP")
+    if name == "gemmepi_fcproj_gelubwd":  # fc-projection input gradient times GELU' of the pre-activation
+        N, K = GEMM_LAYERS["fcproj"]
+        W, dy, pre = randn((N, K), 22, std=0.02), randn((BT, N), 24), randn((BT, K), 30)
+        dx = torch.empty(BT, K, device="cuda", dtype=BF)
+        return (lambda: ops.gpt2_op_matmul(dy, N, 1, W, K, 0, BT, K, N, dx, K, aux=pre, ldaux=K,
+                                           epilogue=ops.EPI_GELU_BWD, path=ops.PATH_TC, flags_dev=fl),
+                2.0 * BT * N * K, "FLOP")
+    if name == "gemmepi_attproj_rowdot":  # attention-projection input gradient and D = rowsum(dO * O)
+        W, dy, o = randn((C, C), 22, std=0.02), randn((BT, C), 24), randn((BT, C), 31)
+        dx, D = torch.empty(BT, C, device="cuda", dtype=BF), torch.empty(BT * H, device="cuda")
+        return (lambda: ops.gpt2_op_matmul_rowdot(dy, C, W, C, BT, C, C, dx, C, o, C, D, 1024, H, fl),
+                2.0 * BT * C * C, "FLOP")
     if name.startswith("gemm_"):
         _, layer, kind = name.split("_")
         N, K = GEMM_LAYERS[layer]
@@ -153,6 +174,7 @@ def make_case(name, ops):
 ALL = (["ln_fwd", "ln_bwd", "gelu_fwd", "gelu_bwd", "softmax_ce", "adamw", "encoder_fwd", "encoder_bwd"] +
        [f"attn_{d}_T{t}" for d in ("fwd", "bwd") for t in (256, 1024, 4096)] +
        [f"gemm_{l}_{k}" for l in GEMM_LAYERS for k in ("fwd", "dgrad", "wgrad")] +
+       ["gemmepi_fc_gelu", "gemmepi_fcproj_gelubwd", "gemmepi_attproj_rowdot"] +
        [f"wgradL_{l}" for l in ("qkv", "attproj", "fc", "fcproj")])
 
 
