@@ -9,7 +9,8 @@
 // (both K-major), dx = dy W (B MN-major) and dW = dy^T x (both MN-major)
 // without any transpose pass.  Accumulation is fp32 in TMEM.
 //
-// Structure (one CTA per SM, persistent over work units, 192 threads):
+// Structure (one CTA per SM, persistent over work units, 64 + 32 * EPI_WARPS
+// threads):
 //   warp 0      TMA producer: per k-block one 128x64 A box (or two 64x64
 //               boxes when MN-major) and the matching B boxes, 128-byte
 //               swizzle, into a STAGES-deep ring guarded by mbarriers.
@@ -17,8 +18,11 @@
 //               thread issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide
 //               k step; tcgen05.commit frees ring stages and, at the end
 //               of a unit, signals the epilogue.
-//   warps 2..5  epilogue, one 32-row slab each (the TMEM lane quarter the
-//               warp may access): tcgen05.ld 32 columns at a time, bias /
+//   warps 2..   EPI_WARPS = 4 or 8 epilogue warps: warp w takes the 32-row
+//               slab of the TMEM lane quarter it may access (w mod 4) and,
+//               with 8 warps, one half of the tile's columns, so two
+//               epilogue warps share each SM sub-partition and hide each
+//               other's latencies: tcgen05.ld 32 columns at a time, bias /
 //               GELU / GELU' in registers, the slab's 32 x 64 bf16 (or
 //               32 x 32 fp32) piece written to a 128-byte-swizzled staging
 //               buffer and sent out by one TMA store per piece; the fp32
@@ -33,7 +37,8 @@
 // CTA's 128 rows into its own TMEM.  Every SM then receives 32 KB of operands
 // per 64-deep k-block instead of 48 KB for the same work, which is what
 // bounds this kernel (operand delivery into the SM, not the tensor pipe),
-// and the ring gets 6 stages.  The odd CTA's TMA loads signal the even
+// and the ring gets 6 stages (5 with eight epilogue warps, whose staging
+// buffers take the room of one).  The odd CTA's TMA loads signal the even
 // CTA's "full" barrier; the MMA commit arrives on both CTAs' "empty" and
 // "accumulator full" barriers; both CTAs' epilogues arrive on the even CTA's
 // "accumulator empty" barrier.
@@ -69,7 +74,6 @@ struct TcParams {
   int acc_store;  // EPI_ACC_F32: split 0 stores its tile into D instead of adding it
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // shared::cluster address of the same shared variable in the even CTA of the pair
 __device__ __forceinline__ uint32_t leader_addr(uint32_t a) {
@@ -179,8 +183,8 @@ __device__ __forceinline__ void unstage_bf16(const uint8_t* buf, uint32_t r, uin
   }
 }
 
-template <int BN, int STAGES, int CL>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, int STAGES, int CL, int EPI_WARPS>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
                    const __grid_constant__ CUtensorMap td, const __grid_constant__ CUtensorMap tx, TcParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
@@ -189,12 +193,12 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* stg_gen = smem + STAGES * STAGE;  // 4 warps x 2 staging buffers
-  uint64_t* bars = (uint64_t*)(stg_gen + 8 * STG);
+  uint8_t* stg_gen = smem + STAGES * STAGE;  // EPI_WARPS warps x 2 staging buffers
+  uint64_t* bars = (uint64_t*)(stg_gen + 2 * EPI_WARPS * STG);
   uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   uint32_t tfull0 = smem_u32(bars + 2 * STAGES), tempty0 = smem_u32(bars + 2 * STAGES + 2);
-  uint32_t auxbar0 = smem_u32(bars + 2 * STAGES + 4);  // [8] aux tile loads, two per epilogue warp
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * STAGES + 12);
+  uint32_t auxbar0 = smem_u32(bars + 2 * STAGES + 4);  // aux tile loads, two per epilogue warp
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * STAGES + 4 + 2 * EPI_WARPS);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   const uint32_t ring = smem_u32(smem);
 
@@ -206,9 +210,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; a++) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4 * CL);  // the epilogue warps of both CTAs of a pair
+      mbar_init(tempty0 + 8 * a, EPI_WARPS * CL);  // the epilogue warps of both CTAs of a pair
     }
-    for (int w = 0; w < 8; w++) mbar_init(auxbar0 + 8 * w, 1);
+    for (int w = 0; w < 2 * EPI_WARPS; w++) mbar_init(auxbar0 + 8 * w, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -325,9 +329,11 @@ __global__ void __launch_bounds__(192, 1)
         else mma_commit_pair(tfull0 + 8 * a);
       }
     }
-  } else {  // ---- epilogue warps 2..5
+  } else {  // ---- epilogue warps 2 .. 1 + EPI_WARPS
+    constexpr int HALF = BN * 4 / EPI_WARPS;  // columns of the tile per epilogue warp
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int e = warp - 2;  // this warp's staging buffers and aux barrier
+    const int e = warp - 2;  // this warp's staging buffers and aux barriers
+    const int hc = (e >> 2) * HALF;  // first tile column of this warp's half
     const uint32_t stg = smem_u32(stg_gen) + e * 2 * STG;
     const uint8_t* stg_g = stg_gen + e * 2 * STG;
     const uint32_t auxbar = auxbar0 + 16 * e;  // buffer b's loads complete on auxbar + 8 b
@@ -386,11 +392,12 @@ __global__ void __launch_bounds__(192, 1)
       const int rbase = m0 + q * 32;  // first row of this warp's slab
       const bool rows_in = rbase < p.M;
       const uint32_t a = j & 1, aph = (j >> 1) & 1;
-      const int nlive = rows_in ? min(BN / 64, (p.N - n0 + 63) / 64) : 0;  // live 64-column chunks
+      // live 64-column chunks of this warp's half
+      const int nlive = rows_in && n0 + hc < p.N ? min(HALF / 64, (p.N - n0 - hc + 63) / 64) : 0;
       if (aux_epi && nlive > 0 && !prefetched) {  // the first chunk's aux tile, before the accumulator is ready
         if (lane == 0) {
           bulk_wait_read<1>();
-          aux_issue(n0, rbase, z, ci & 1);
+          aux_issue(n0 + hc, rbase, z, ci & 1);
         }
         pending = (int)(ci & 1);
         pending_par = (ci >> 1) & 1;
@@ -405,10 +412,10 @@ __global__ void __launch_bounds__(192, 1)
       if (p.epi == EPI_ACC_F32) {
         // split 0: D += tile (TMA reduce-add); split s > 0: workspace slot s - 1
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; c++) {
+        for (int c = 0; c < HALF / 32; c++) {
           float v[32];
-          tmem_ld32(tacc + c * 32, v);
-          const int col0 = n0 + c * 32;
+          tmem_ld32(tacc + hc + c * 32, v);
+          const int col0 = n0 + hc + c * 32;
           if (rows_in && col0 < p.N) {
             const uint32_t buf = stg + (ci & 1) * STG;
             if (lane == 0) bulk_wait_read<1>();
@@ -434,20 +441,21 @@ __global__ void __launch_bounds__(192, 1)
       }
       bool ok = true;
 #pragma unroll 1
-      for (int cp = 0; cp < BN / 64; cp++) {
-        const int col0 = n0 + cp * 64;
+      for (int cp = 0; cp < HALF / 64; cp++) {
+        const int tc0 = hc + cp * 64;  // first column of the chunk within the tile
+        const int col0 = n0 + tc0;
         const bool live = rows_in && col0 < p.N;
         float v0[32], v1[32];
-        tmem_ld32(tacc + cp * 64, v0);
-        tmem_ld32(tacc + cp * 64 + 32, v1);
+        tmem_ld32(tacc + tc0, v0);
+        tmem_ld32(tacc + tc0 + 32, v1);
         if (!live) continue;
         const uint32_t bo = stg + (ci & 1) * STG;  // output piece
         if (p.epi == EPI_STORE) {
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
           if (p.bias) {
-            add_bias(bias_cur, cp * 64, v0);
-            add_bias(bias_cur, cp * 64 + 32, v1);
+            add_bias(bias_cur, tc0, v0);
+            add_bias(bias_cur, tc0 + 32, v1);
           }
           stage_bf16(bo, lane, 0, v0);
           stage_bf16(bo, lane, 4, v1);
@@ -464,8 +472,8 @@ __global__ void __launch_bounds__(192, 1)
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
           if (p.bias) {
-            add_bias(bias_cur, cp * 64, v0);
-            add_bias(bias_cur, cp * 64 + 32, v1);
+            add_bias(bias_cur, tc0, v0);
+            add_bias(bias_cur, tc0 + 32, v1);
           }
           stage_bf16(stg, lane, 0, v0);
           stage_bf16(stg, lane, 4, v1);
@@ -502,9 +510,9 @@ __global__ void __launch_bounds__(192, 1)
           } else if (u + ustep < units) {
             const int u2 = u + ustep, t2 = u2 % tiles;
             ny = tile_m0(t2) + q * 32;
-            nx = (t2 % num_n) * BN;
+            nx = (t2 % num_n) * BN + hc;
             nz = u2 / (tiles * p.splits);
-            has_next = prefetched = ny < p.M;
+            has_next = prefetched = ny < p.M && nx < p.N;
           }
           if (has_next && lane == 0) {
             bulk_wait_read<0>();  // the previous chunk's store has read the other buffer
@@ -604,19 +612,21 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const v
                  uint64_t outer, uint64_t ld, uint64_t depth, uint64_t bstride, uint32_t box_inner,
                  uint32_t box_outer);
 
-template <int BN, int STAGES, int CL>
+template <int BN, int STAGES, int CL, int EPI_WARPS>
 constexpr size_t smem_bytes() {
-  return (size_t)STAGES * (BM * BK * 2 + (BN / CL) * BK * 2) + 8 * STG + 1024 + 256;
+  return (size_t)STAGES * (BM * BK * 2 + (BN / CL) * BK * 2) + 2 * EPI_WARPS * STG + 1024 + 512;
 }
 
-template <int BN, int STAGES, int CL>
+template <int BN, int STAGES, int CL, int EPI_WARPS>
 cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
-  constexpr size_t smem = smem_bytes<BN, STAGES, CL>();
+  constexpr size_t smem = smem_bytes<BN, STAGES, CL, EPI_WARPS>();
   static_assert(smem <= 232448, "shared memory per CTA");
-  static_assert((2 * STAGES + 12) * 8 + 8 <= 256, "barriers, TMEM address and abort flag after the staging buffers");
+  static_assert((2 * STAGES + 4 + 2 * EPI_WARPS) * 8 + 8 <= 512,
+                "barriers, TMEM address and abort flag after the staging buffers");
+  static_assert((BN * 4 / EPI_WARPS) % 64 == 0, "each epilogue warp takes whole 64-column chunks");
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, CL>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
@@ -643,7 +653,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
              (int)nb, g.dvec, g.dT, g.dH, g.acc_store};
   const long long units = tiles * splits * (long long)nb;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(64 + 32 * EPI_WARPS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[2];
@@ -658,7 +668,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
       cfg.attrs = at;
       cfg.numAttrs = 1;
       cfg.gridDim = dim3((unsigned)(slots * CL));
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_tc_kernel<BN, STAGES, CL>, &cfg) != cudaSuccess ||
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>, &cfg) != cudaSuccess ||
           max_clusters <= 0)
         max_clusters = (int)slots;
     }
@@ -679,7 +689,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
     at[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL>, ta, tb, td, tx, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>, ta, tb, td, tx, p);
 }
 
 }  // namespace
@@ -852,8 +862,16 @@ cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   // CTA pairs (cta_group::2) when there are enough row tiles to pair up, or for a split K
   const bool pair = mt >= 2 && (splits > 1 || mt * nt * nb >= sms);
   cudaError_t e;
-  if (wide) e = pair ? launch<256, 6, 2>(g, splits, flags, st) : launch<256, 4, 1>(g, 1, flags, st);
-  else e = pair ? launch<128, 8, 2>(g, splits, flags, st) : launch<128, 6, 1>(g, 1, flags, st);
+  // the GELU epilogues are bound by their arithmetic: eight epilogue warps (two
+  // per SM sub-partition, the ring one stage shorter to make room for their
+  // staging buffers); the others keep four warps and the deeper ring
+  // (measured on the 124M shapes: fc forward with GELU 100 -> 88 us, fc
+  // projection dgrad with GELU' 104 -> 90 us; plain epilogues 4-10% slower
+  // with eight warps)
+  const bool gelu = g.epi == EPI_GELU || g.epi == EPI_GELU_BWD;
+  if (wide && pair) e = gelu ? launch<256, 5, 2, 8>(g, splits, flags, st) : launch<256, 6, 2, 4>(g, splits, flags, st);
+  else if (wide) e = launch<256, 4, 1, 4>(g, 1, flags, st);
+  else e = pair ? launch<128, 8, 2, 4>(g, splits, flags, st) : launch<128, 6, 1, 4>(g, 1, flags, st);
   if (e != cudaSuccess || splits == 1) return e;
   gpt2_count_launches(1);
   const long long nv = (long long)g.M * (g.N / 4);
