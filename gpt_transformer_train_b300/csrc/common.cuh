@@ -58,22 +58,30 @@ template <typename T> __device__ __forceinline__ float round_to(float x) { retur
 
 // GELU in its tanh form, 0.5 x (1 + tanh u) with u = sqrt(2/pi) (x + 0.044715 x^3),
 // evaluated as x * sigmoid(2u): the same function, since 0.5 (1 + tanh u) =
-// 1 / (1 + exp(-2u)).  One exponential and one reciprocal, no branch, and no
-// cancellation for negative x.  Every GELU of the library (the GEMM epilogues,
-// the standalone and recompute kernels) goes through these two functions, so a
-// recomputed GELU reproduces the forward's bits.
+// 1 / (1 + exp(-2u)) = 1 / (1 + 2^(-2u log2 e)).  One base-2 exponential and
+// one reciprocal, no branch, and no cancellation for negative x.  Every GELU
+// of the library (the GEMM epilogues, the standalone and recompute kernels)
+// goes through these two functions, so a recomputed GELU reproduces the
+// forward's bits.
 constexpr float GELU_2U = 1.5957691216057308f;    // 2 sqrt(2/pi)
 constexpr float GELU_2U3 = 0.07135481627260025f;  // 2 sqrt(2/pi) * 0.044715
+constexpr float GELU_E1 = -2.302208198144325f;    // -2 sqrt(2/pi) log2(e)
+constexpr float GELU_E3 = -0.1029432395800235f;   // -2 sqrt(2/pi) * 0.044715 * log2(e)
+__device__ __forceinline__ float gelu_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float gelu_fwd(float x) {
-  const float u2 = x * fmaf(GELU_2U3, x * x, GELU_2U);
-  return __fdividef(x, 1.f + __expf(-u2));
+  const float e = gelu_exp2(x * fmaf(GELU_E3, x * x, GELU_E1));  // exp(-2u)
+  return __fdividef(x, 1.f + e);
 }
 // its derivative: s + x s (1 - s) d(2u)/dx with s = sigmoid(2u)
 __device__ __forceinline__ float gelu_bwd(float x) {
   const float x2 = x * x;
-  const float u2 = x * fmaf(GELU_2U3, x2, GELU_2U);
+  const float e = gelu_exp2(x * fmaf(GELU_E3, x2, GELU_E1));
   const float du2 = fmaf(3.f * GELU_2U3, x2, GELU_2U);
-  const float s = __fdividef(1.f, 1.f + __expf(-u2));
+  const float s = __fdividef(1.f, 1.f + e);
   return s * fmaf(x * du2, 1.f - s, 1.f);
 }
 
