@@ -121,14 +121,17 @@ int gpt2_zero_grad(gpt2* m);
  * (wte, wpe, qkvw, attprojw, fcw, fcprojw) only.  Refreshes the bf16 copy. */
 int gpt2_adamw_step(gpt2* m, float lr, float b1, float b2, float eps, float wd, int t);
 
-/* zero_grad + forward (with targets) + backward as ONE captured CUDA graph.
- * The first call captures the launches on the model's stream for these
- * token/target device pointers and instantiates the graph; later calls with
- * the same pointers replay it (one launch; the step's ~300 kernels run
- * without host gaps).  New pointers recapture.  The contents of the token
- * arrays are read at replay time.  Needs a created (non-default) stream;
- * run AdamW (and clipping) after it as usual.  Equivalent to
- * gpt2_zero_grad; gpt2_forward(tokens, targets, NULL); gpt2_backward. */
+/* Forward (with targets) + backward as ONE captured CUDA graph, the backward
+ * writing fresh gradients: the first writer of every gradient stores instead
+ * of adding, so no zero_grad memset runs and the previous gradients are
+ * overwritten.  The first call captures the launches on the model's stream
+ * for these token/target device pointers and instantiates the graph; later
+ * calls with the same pointers replay it (one launch; the step's ~200
+ * kernels run without host gaps).  New pointers recapture.  The contents of
+ * the token arrays are read at replay time.  Needs a created (non-default)
+ * stream; run AdamW (and clipping) after it as usual.  Equivalent to
+ * gpt2_zero_grad; gpt2_forward(tokens, targets, NULL); gpt2_backward, up to
+ * the sign of zero gradients (0 + x and x differ only there). */
 int gpt2_graph_step(gpt2* m, const int32_t* tokens_dev, const int32_t* targets_dev);
 
 /* Gradient-norm clipping, the step before AdamW (the llm.c tour names a
