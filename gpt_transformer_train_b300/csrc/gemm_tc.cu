@@ -72,6 +72,8 @@ struct TcParams {
   float* dvec;  // EPI_ROWDOT: the per-row, per-head dot products
   int dT, dH;
   int acc_store;  // EPI_ACC_F32: split 0 stores its tile into D instead of adding it
+  float* rowstats;  // EPI_STORE: per row and column tile, (max, sum of exp) of the stored values
+  int stats_cols;   // columns counted in rowstats
 };
 
 
@@ -179,6 +181,46 @@ __device__ __forceinline__ void round_stage_bf16(uint32_t buf, uint32_t r, uint3
     }
     st_shared_v4(buf + swz(r, ch0 + u), w[0], w[1], w[2], w[3]);
   }
+}
+// online row statistics over one 64-column chunk (v0: columns 0..31, v1:
+// 32..63; the first nval count): m = running maximum, s = sum of exp(x - m)
+__device__ __forceinline__ void chunk_stats(const float (&v0)[32], const float (&v1)[32], int nval, float& m,
+                                            float& s) {
+  constexpr float L2E = 1.4426950408889634f;
+  if (nval <= 0) return;
+  float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (nval >= 64) {
+#pragma unroll
+    for (int k = 0; k < 32; k++) {
+      c4[k & 3] = fmaxf(c4[k & 3], v0[k]);
+      c4[(k + 2) & 3] = fmaxf(c4[(k + 2) & 3], v1[k]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; k++) {
+      if (k < nval) c4[k & 3] = fmaxf(c4[k & 3], v0[k]);
+      if (32 + k < nval) c4[(k + 2) & 3] = fmaxf(c4[(k + 2) & 3], v1[k]);
+    }
+  }
+  const float mn = fmaxf(m, fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3])));
+  const float ml = mn * L2E;
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  if (nval >= 64) {
+#pragma unroll
+    for (int k = 0; k < 32; k++) {
+      s4[k & 3] += ex2(fmaf(v0[k], L2E, -ml));
+      s4[(k + 2) & 3] += ex2(fmaf(v1[k], L2E, -ml));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; k++) {
+      if (k < nval) s4[k & 3] += ex2(fmaf(v0[k], L2E, -ml));
+      if (32 + k < nval) s4[(k + 2) & 3] += ex2(fmaf(v1[k], L2E, -ml));
+    }
+  }
+  // the earlier chunks' sum moves to the new maximum (m = -inf at the first: factor 0)
+  s = s * ex2((m - mn) * L2E) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+  m = mn;
 }
 // 32 fp32 values (128 B) into row r of a staging buffer
 __device__ __forceinline__ void stage_f32(uint32_t buf, uint32_t r, const float (&v)[32]) {
@@ -424,6 +466,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       if (!mbar_wait_warp(tfull0 + 8 * a, aph, abort_flag)) break;
       fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + a * BN;
+      float st_m = -INFINITY, st_s = 0.f;  // rowstats of this lane's row over the tile
       if (p.epi == EPI_ACC_F32) {
         // split 0: D += tile (TMA reduce-add); split s > 0: workspace slot s - 1
 #pragma unroll 1
@@ -473,8 +516,15 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             add_bias(bias_cur, tc0, v0);
             add_bias(bias_cur, tc0 + 32, v1);
           }
-          stage_bf16(bo, lane, 0, v0);
-          stage_bf16(bo, lane, 4, v1);
+          if (p.rowstats) {
+            // the values as stored (bf16) enter the statistics
+            round_stage_bf16(bo, lane, 0, v0);
+            round_stage_bf16(bo, lane, 4, v1);
+            chunk_stats(v0, v1, p.stats_cols - col0, st_m, st_s);
+          } else {
+            stage_bf16(bo, lane, 0, v0);
+            stage_bf16(bo, lane, 4, v1);
+          }
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -588,6 +638,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       __syncwarp();
       if (lane == 0) release_acc(tempty0 + 8 * a);
       if (!ok) break;
+      if (p.rowstats && rows_in && rbase + lane < p.M)
+        *reinterpret_cast<float2*>(p.rowstats + ((size_t)(rbase + lane) * num_n + n0 / BN) * 2) =
+            make_float2(st_m, st_s);
     }
     // an aux load cut short by an abort must land before the CTA exits
     if (pending >= 0) mbar_settle(auxbar + 8 * pending, pending_par);
@@ -669,7 +722,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
   TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
-             (int)nb, g.dvec, g.dT, g.dH, g.acc_store};
+             (int)nb, g.dvec, g.dT, g.dH, g.acc_store, g.rowstats, g.stats_cols};
   const long long units = tiles * splits * (long long)nb;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(64 + 32 * EPI_WARPS);
@@ -811,6 +864,7 @@ bool gemm_tc_supported(const GemmArgs& g) {
       (!g.dvec || g.dT <= 0 || g.dH <= 0 || g.N != 64 * g.dH || g.M % g.dT || g.batch > 1 || g.bias))
     return false;
   if (g.bias && (!al16(g.bias) || (g.epi != EPI_STORE && g.epi != EPI_GELU))) return false;
+  if (g.rowstats && (g.epi != EPI_STORE || g.batch > 1 || g.stats_cols <= 0)) return false;
   if (g.a_kmajor ? g.lda < g.K : g.lda < g.M) return false;
   if (g.b_kmajor ? g.ldb < g.K : g.ldb < g.N) return false;
   if (g.batch > 1) {
@@ -868,10 +922,12 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(float* __restrict__ 
   }
 }
 
+int gemm_tc_stats_tiles(int N) { return N >= 512 ? (N + 255) / 256 : (N + 127) / 128; }
+
 cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;
   gpt2_count_launches(1);
-  const bool wide = g.N >= 512;  // 256-wide tiles (a ragged last column tile is clipped by TMA)
+  const bool wide = g.N >= 512;  // 256-wide tiles (a ragged last column tile is clipped by TMA); as gemm_tc_stats_tiles
   const int sms = tc_num_sms();
   const long long mt = (g.M + BM - 1) / BM, nt = (g.N + (wide ? 256 : 128) - 1) / (wide ? 256 : 128);
   const long long nb = g.batch > 1 ? g.batch : 1;

@@ -37,8 +37,18 @@ struct GemmArgs {
   int batch; long long sA, sB, sD, sAux;
   float* dvec; int dT, dH;  // EPI_ROWDOT only
   int acc_store;            // EPI_ACC_F32: D = acc instead of D += acc (the first writer of a fresh gradient)
+  // EPI_STORE on the tensor-core path (optional): per row and column tile n
+  // (gemm_tc_stats_tiles(N) tiles), the statistics of the stored (bf16)
+  // values of the columns < stats_cols: m = their maximum, s = the sum of
+  // exp(value - m), at rowstats[(row * tiles + n) * 2 + {0, 1}]
+  float* rowstats; int stats_cols;
 };
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
+int gemm_tc_stats_tiles(int N);  // column tiles of an N-wide tensor-core product
+// softmax + cross-entropy of bf16 logit rows from the per-tile statistics of
+// the classifier product (see GemmArgs::rowstats): loss and dlogits in place
+cudaError_t softmax_ce_from_stats(bf16* logits, float* losses, const int* targets, const float* rowstats, int tiles,
+                                  int rows, int V, int Vp, float dloss, int* flags, cudaStream_t st);
 // products with at most 32 rows (one position per sequence when decoding):
 // both operands K-major, EPI_STORE or EPI_GELU, A small enough for shared memory
 template <typename T> bool gemm_skinny_supported(const GemmArgs& a);

@@ -1815,6 +1815,93 @@ __global__ void __launch_bounds__(SCE_SMEM_THREADS, 2)
   }
 }
 
+// Softmax + cross-entropy from the classifier product's per-tile row
+// statistics (m_n, s_n) = (max, sum of exp(z - max)) over each 256-column
+// tile: M = max_n m_n, S = sum_n s_n exp(m_n - M) give the row's
+// log-sum-exp M + ln S, so the row itself is read once and written once
+// (dlogits in place), a plain stream at 256 threads per row.  Same outputs as
+// softmax_ce: loss = lse - z[target], dlogits = (softmax - onehot) * dloss
+// over the first V columns, 0 on the pads; the target's probability in fp32.
+constexpr int SCS_THREADS = 256;
+__global__ void __launch_bounds__(SCS_THREADS) softmax_ce_stats_kernel(
+    bf16* __restrict__ logits, float* __restrict__ losses, const int* __restrict__ targets,
+    const float* __restrict__ rowstats, int tiles, int V, int Vp, float dloss, int* flags) {
+  pdl_enter();
+  constexpr int N = 8;
+  constexpr float L2E = 1.4426950408889634f;
+  __shared__ float sh[3];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int row = blockIdx.x;
+  bf16* z = logits + (size_t)row * Vp;
+  int tg = targets[row];
+  const bool bad = tg < 0 || tg >= V;
+  if (bad) tg = 0;
+  if (tid < 32) {
+    // the tiles' statistics, combined in a fixed order (lane-strided, then a shuffle tree)
+    const float2* st = reinterpret_cast<const float2*>(rowstats) + (size_t)row * tiles;
+    float m = -INFINITY, sm = 0.f;
+    for (int i = lane; i < tiles; i += 32) {
+      const float2 t = st[i];
+      const float mn = fmaxf(m, t.x);
+      if (mn > -INFINITY) {
+        sm = sm * tc::ex2((m - mn) * L2E) + t.y * tc::ex2((t.x - mn) * L2E);
+        m = mn;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, off), s2 = __shfl_xor_sync(0xffffffffu, sm, off);
+      const float mn = fmaxf(m, m2);
+      if (mn > -INFINITY) {
+        sm = sm * tc::ex2((m - mn) * L2E) + s2 * tc::ex2((m2 - mn) * L2E);
+        m = mn;
+      }
+    }
+    if (lane == 0) {
+      sh[0] = m;
+      sh[1] = sm;
+      sh[2] = __bfloat162float(z[tg]);  // read before any thread overwrites the row
+    }
+  }
+  __syncthreads();
+  const float m = sh[0], sm = sh[1], zt = sh[2];
+  if (tid == 0) {
+    if (bad) atomicOr(flags, FLAG_TARGET_RANGE);
+    losses[row] = m + logf(sm) - zt;
+  }
+  const float ml = m * L2E, scale = dloss / sm;
+  // the target's probability in fp32: p - 1 loses everything when p is near 1
+  const float g_tg = (tc::ex2(fmaf(zt, L2E, -ml)) / sm - 1.f) * dloss;
+  const int nvec = Vp / N;
+  for (int v0 = tid; v0 < nvec; v0 += 4 * SCS_THREADS) {
+    uint4 r[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int vi = v0 + u * SCS_THREADS;
+      if (vi < nvec) r[u] = __ldcs(reinterpret_cast<const uint4*>(z) + vi);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int vi = v0 + u * SCS_THREADS;
+      if (vi >= nvec) break;
+      float f[N];
+      unpack_bf16x8(r[u], f);
+#pragma unroll
+      for (int j = 0; j < N; j++) f[j] = vi * N + j < V ? tc::ex2(fmaf(f[j], L2E, -ml)) * scale : 0.f;
+      if (tg >= vi * N && tg < vi * N + N) f[tg - vi * N] = g_tg;
+      st16_cs(z + (size_t)vi * N, f);
+    }
+  }
+}
+
+cudaError_t softmax_ce_from_stats(bf16* logits, float* losses, const int* targets, const float* rowstats, int tiles,
+                                  int rows, int V, int Vp, float dloss, int* flags, cudaStream_t st) {
+  if (rows <= 0 || tiles <= 0 || V <= 0 || Vp < V || Vp % 8 || ((uintptr_t)logits & 15)) return cudaErrorInvalidValue;
+  launch_k(softmax_ce_stats_kernel, dim3(rows), dim3(SCS_THREADS), 0, st, logits, losses, targets, rowstats, tiles, V,
+           Vp, dloss, flags);
+  return launch_status(1);
+}
+
 template <typename T>
 cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, int V, int Vp,
                        float dloss, int write_grad, int* flags, cudaStream_t st) {

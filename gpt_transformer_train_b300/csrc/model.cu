@@ -130,6 +130,9 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.fchg = take(n_gelu * BT * 4 * C * es);
   b.proj = take(BT * C * es);
   b.logits = take(BT * (size_t)c.Vp * es);
+  // per row and 256-column tile of the logits, (max, sum of exp) from the
+  // classifier product's epilogue (bf16 mode), read by the softmax
+  b.lstats = c.precision == GPT2_PRECISION_BF16 ? take(BT * (size_t)gemm_tc_stats_tiles(c.Vp) * 2 * 4) : 0;
   b.losses = take(BT * 4);
   b.loss = take(256);
   b.dres = take(BT * C * 4);
@@ -242,15 +245,21 @@ struct Step {
   float* dec_stats() const { return reinterpret_cast<float*>(dec_logits() + (size_t)c.B * c.Vp); }
   int* flags() const { return m->at<int>(m->bl.flags); }
 
+  // which kernel takes a product: 0 few-row, 1 tensor cores, 2 SIMT.  A few
+  // rows (decoding) go to the few-row kernel, except for very wide products
+  // (the classifier), which have enough tiles for the tensor cores
+  int gemm_path(const GemmArgs& a) const {
+    const bool tc_ok = c.precision == GPT2_PRECISION_BF16 && gemm_tc_supported(a);
+    if (gemm_skinny_supported<T>(a) && !(tc_ok && a.N >= 16384)) return 0;
+    return tc_ok ? 1 : 2;
+  }
   cudaError_t gemm(GemmArgs a) {
     bool rec = m->prof_on && m->prof_n < m->prof_flops.size();
     if (rec) cudaEventRecord(m->prof_ev[2 * m->prof_n], m->st);
     cudaError_t e;
-    // a few rows (decoding): the few-row kernel, except for very wide products
-    // (the classifier), which have enough tiles for the tensor cores
-    const bool tc_ok = c.precision == GPT2_PRECISION_BF16 && gemm_tc_supported(a);
-    if (gemm_skinny_supported<T>(a) && !(tc_ok && a.N >= 16384)) e = gemm_skinny<T>(a, m->st);
-    else if (tc_ok) e = gemm_tc(a, flags(), m->st);
+    const int path = gemm_path(a);
+    if (path == 0) e = gemm_skinny<T>(a, m->st);
+    else if (path == 1) e = gemm_tc(a, flags(), m->st);
     else e = gemm_simt<T>(a, m->st);
     if (rec) {
       cudaEventRecord(m->prof_ev[2 * m->prof_n + 1], m->st);
@@ -342,9 +351,21 @@ struct Step {
     size_t f = 2 * L;
     CK(m, residual_layernorm_forward<T>(resid(f), ln(f), mean(f), rstd(f), resid(f - 1), proj(), W(GPT2_LNFW),
                                         W(GPT2_LNFB), BTi, Ci, st));
-    CK(m, linear_fwd(logits(), ln(f), W(GPT2_WTE), nullptr, BTi, c.Vp, Ci));
+    // with targets on the tensor cores, the classifier's epilogue also takes
+    // each row's (max, sum of exp) per column tile, so the softmax reads the
+    // logits once
+    GemmArgs cls{ln(f), Ci, 1, W(GPT2_WTE), Ci, 1, BTi, c.Vp, Ci, logits(), c.Vp, nullptr, nullptr, c.Vp, EPI_STORE};
+    if (tgt && m->bl.lstats) {
+      cls.rowstats = m->at<float>(m->bl.lstats);
+      cls.stats_cols = c.V;
+      if (gemm_path(cls) != 1) cls.rowstats = nullptr;
+    }
+    CK(m, gemm(cls));
     if (tgt) {
-      CK(m, softmax_ce<T>(logits(), losses(), tgt, BTi, c.V, c.Vp, 1.0f / (float)BTi, 1, flags(), st));
+      if (cls.rowstats)
+        CK(m, softmax_ce_from_stats((bf16*)logits(), losses(), tgt, cls.rowstats, gemm_tc_stats_tiles(c.Vp), BTi, c.V,
+                                    c.Vp, 1.0f / (float)BTi, flags(), st));
+      else CK(m, softmax_ce<T>(logits(), losses(), tgt, BTi, c.V, c.Vp, 1.0f / (float)BTi, 1, flags(), st));
       CK(m, mean_loss(m->at<float>(m->bl.loss), losses(), BTi, st));
     }
     return GPT2_OK;

@@ -45,6 +45,7 @@ struct BufferLayout {
   size_t resid, ln, ln_mean, ln_rstd;       // [(2L+1)][BT][C], stats [(2L+1)][BT]
   size_t qkv, atty, lse, fch, fchg;         // per layer
   size_t proj, logits, losses, loss;        // temporaries / classifier
+  size_t lstats;                            // classifier per-tile row statistics (bf16 mode)
   size_t dres, dresc, dfch, dqkv, dsmall;  // activation gradients (dresc, dfch, dqkv: per layer)
   size_t attD, attS, partial, keys, ws, ws_floats, gnorm, flags, tok, tgt;
   size_t dec;                               // one-position inference scratch (see Step::dec_*)

@@ -126,6 +126,26 @@ int gpt2_op_matmul_rowdot(const void* dY, long long ldy, const void* W, long lon
   return rc_of(gemm_tc(a, flags_dev, ST(stream)));
 }
 
+int gpt2_op_logit_stats_tiles(int N) { return N > 0 ? gemm_tc_stats_tiles(N) : 0; }
+
+int gpt2_op_matmul_logit_stats(const void* A, long long lda, const void* B, long long ldb, int M, int N, int K,
+                               void* D, long long ldd, float* stats, int stats_cols, int* flags_dev, void* stream) {
+  if (!A || !B || !D || !stats || !flags_dev || M <= 0 || N <= 0 || K <= 0 || stats_cols <= 0)
+    return GPT2_ERR_INVALID_ARG;
+  GemmArgs a{A, lda, 1, B, ldb, 1, M, N, K, D, ldd, nullptr, nullptr, 0, EPI_STORE};
+  a.rowstats = stats;
+  a.stats_cols = stats_cols;
+  if (!gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
+  return rc_of(gemm_tc(a, flags_dev, ST(stream)));
+}
+
+int gpt2_op_softmax_crossentropy_stats(void* logits, float* losses, const int32_t* targets, const float* stats,
+                                       int rows, int V, int Vp, float dloss, int* flags_dev, void* stream) {
+  if (!logits || !losses || !targets || !stats || !flags_dev || rows <= 0 || V <= 0 || Vp < V) return GPT2_ERR_INVALID_ARG;
+  return rc_of(softmax_ce_from_stats((bf16*)logits, losses, targets, stats, gemm_tc_stats_tiles(Vp), rows, V, Vp,
+                                     dloss, flags_dev, ST(stream)));
+}
+
 int gpt2_op_attention_forward(int dtype, void* out, float* lse, const void* qkv, int B, int T, int C, int H, int path,
                               int* flags_dev, void* stream) {
   if (bad_dtype(dtype) || !out || !lse || !qkv || B <= 0 || T <= 0 || C <= 0 || H <= 0 || C % H) return GPT2_ERR_INVALID_ARG;

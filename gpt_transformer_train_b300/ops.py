@@ -30,6 +30,9 @@ _sigs = {
     "gpt2_op_attention_backward_scratch_bytes": (_sz, [_i, _i, _i]),
     "gpt2_op_attention_backward": (_i, [_i, _P, _P, _P, _P, _P, _i, _i, _i, _i, _i, _P, _P, _sz, _P]),
     "gpt2_op_softmax_crossentropy": (_i, [_i, _P, _P, _P, _i, _i, _i, _f, _i, _P, _P]),
+    "gpt2_op_logit_stats_tiles": (_i, [_i]),
+    "gpt2_op_matmul_logit_stats": (_i, [_P, _ll, _P, _ll, _i, _i, _i, _P, _ll, _P, _i, _P, _P]),
+    "gpt2_op_softmax_crossentropy_stats": (_i, [_P, _P, _P, _P, _i, _i, _i, _f, _P, _P]),
     "gpt2_op_adamw": (_i, [_P, _P, _P, _P, _P, _ll, _f, _f, _f, _f, _f, _i, _P, _P]),
     "gpt2_op_grad_norm_scratch_bytes": (_sz, []),
     "gpt2_op_grad_norm": (_i, [_P, _ll, _f, _P, _P, _sz, _P]),
@@ -149,6 +152,20 @@ def gpt2_op_attention_backward(dqkv, dout, qkv, out, lse, B, T, C, H, path=PATH_
 def gpt2_op_softmax_crossentropy(logits, losses, targets, rows, V, Vp, dloss, write_grad, flags_dev, stream=None):
     _ck(lib.gpt2_op_softmax_crossentropy(_dt(logits), _p(logits), _p(losses), _p(targets), rows, V, Vp, dloss,
                                          write_grad, _p(flags_dev), _s(stream)), "softmax_crossentropy")
+
+
+def gpt2_op_logit_stats_tiles(N):
+    return lib.gpt2_op_logit_stats_tiles(N)
+
+
+def gpt2_op_matmul_logit_stats(A, lda, B, ldb, M, N, K, D, ldd, stats, stats_cols, flags_dev, stream=None):
+    _ck(lib.gpt2_op_matmul_logit_stats(_p(A), lda, _p(B), ldb, M, N, K, _p(D), ldd, _p(stats), stats_cols,
+                                       _p(flags_dev), _s(stream)), "matmul_logit_stats")
+
+
+def gpt2_op_softmax_crossentropy_stats(logits, losses, targets, stats, rows, V, Vp, dloss, flags_dev, stream=None):
+    _ck(lib.gpt2_op_softmax_crossentropy_stats(_p(logits), _p(losses), _p(targets), _p(stats), rows, V, Vp, dloss,
+                                               _p(flags_dev), _s(stream)), "softmax_crossentropy_stats")
 
 
 def gpt2_op_adamw(p, g, m, v, p_bf16, lr, b1, b2, eps, wd, t, gscale=None, stream=None):

@@ -159,6 +159,24 @@ int gpt2_op_attention_backward(int dtype, void* dqkv, const void* dout, const vo
 int gpt2_op_softmax_crossentropy(int dtype, void* logits, float* losses, const int32_t* targets, int rows, int V,
                                  int Vp, float dloss, int write_grad, int* flags_dev, void* stream);
 
+/* The classifier's fused form (bf16, tensor cores): D[M][N] = A[M][K] . B[N][K]^T
+ * stored as bf16 (both operands K-major), and, per row and column tile n of
+ * gpt2_op_logit_stats_tiles(N), the statistics of the stored values of the
+ * columns < stats_cols: stats[(row * tiles + n) * 2] = their maximum m,
+ * stats[... + 1] = sum of exp(value - m) (m = -inf, sum 0 for a tile without
+ * such columns).  stats: M * tiles * 2 floats, caller-owned.
+ * gpt2_op_softmax_crossentropy_stats then gives the same losses and dlogits as
+ * gpt2_op_softmax_crossentropy (write_grad = 1) from D and those statistics,
+ * reading each row once: the row's log-sum-exp is M + ln S with M = max_n m_n,
+ * S = sum_n s_n exp(m_n - M).  Both need flags_dev (bounded waits report
+ * FLAG_TIMEOUT, a target outside [0, V) FLAG_TARGET_RANGE); INVALID_ARG when the
+ * shape or alignment is not supported (N % 8, 16-byte aligned pointers). */
+int gpt2_op_logit_stats_tiles(int N);
+int gpt2_op_matmul_logit_stats(const void* A, long long lda, const void* B, long long ldb, int M, int N, int K,
+                               void* D, long long ldd, float* stats, int stats_cols, int* flags_dev, void* stream);
+int gpt2_op_softmax_crossentropy_stats(void* logits, float* losses, const int32_t* targets, const float* stats,
+                                       int rows, int V, int Vp, float dloss, int* flags_dev, void* stream);
+
 /* AdamW on n floats (n % 4 == 0), bias-corrected at step t >= 1, decay wd;
  * p_bf16 (optional) receives the updated parameters rounded to bf16;
  * gscale_dev (optional, one device float): every gradient is multiplied by it

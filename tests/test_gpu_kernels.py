@@ -626,6 +626,52 @@ def test_softmax_crossentropy_many_rows(ops, write_grad):
     assert np.max(np.abs(got - rd)) < 2 ** -8 * dloss
 
 
+@pytest.mark.parametrize("rows,V,Vp,K", [(300, 50257, 50304, 64), (130, 700, 1024, 128), (257, 700, 768, 64)])
+def test_classifier_logit_stats_and_softmax(ops, rows, V, Vp, K):
+    """The classifier's fused form: logits by the tensor-core product with each
+    row's (max, sum of exp) per column tile taken in its epilogue from the
+    stored bf16 values, then softmax/CE from those statistics (one read of each
+    row), against numpy on the stored logits.  (130, 700, 1024): a last tile
+    with no column below V; (257, 700, 768): a tile cut by V."""
+    A, B = normal_array((rows, K), 170), normal_array((Vp, K), 171, 0.3)
+    tA, tB = dev(A, torch.bfloat16), dev(B, torch.bfloat16)
+    D = torch.empty(rows, Vp, device="cuda", dtype=torch.bfloat16)
+    tiles = ops.gpt2_op_logit_stats_tiles(Vp)
+    width = 256 if Vp >= 512 else 128
+    assert tiles == -(-Vp // width)
+    stats = torch.full((rows, tiles, 2), float("nan"), device="cuda")
+    fl = ops.flags()
+    ops.gpt2_op_matmul_logit_stats(tA, K, tB, K, rows, Vp, K, D, Vp, stats, V, fl)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    zs = host(D)
+    assert rel_l2(zs, host(tA) @ host(tB).T) < 2 ** -7
+    z = zs.astype(np.float64)
+    st = host(stats)
+    for n in range(tiles):
+        c0, c1 = n * width, min((n + 1) * width, V)
+        if c1 <= c0:
+            assert np.all(st[:, n, 0] == -np.inf) and np.all(st[:, n, 1] == 0)
+            continue
+        m = z[:, c0:c1].max(axis=1)
+        assert np.array_equal(st[:, n, 0], m.astype(np.float32))  # the max of stored values is exact
+        sref = np.exp(z[:, c0:c1] - m[:, None]).sum(axis=1)
+        assert np.max(np.abs(st[:, n, 1] / sref - 1)) < 1e-5
+    tgt = np.random.default_rng(172).integers(0, V, size=rows).astype(np.int32)
+    tgt[0] = V - 1
+    losses = torch.empty(rows, device="cuda")
+    dloss = 1.0 / rows
+    ops.gpt2_op_softmax_crossentropy_stats(D, losses, dev(tgt, torch.int32), stats, rows, V, Vp, dloss, fl)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    rl = O.crossentropy_forward(zs[None], tgt[None], V)[0]
+    assert np.max(np.abs(host(losses) - rl)) < 1e-4
+    rd = O.crossentropy_softmax_backward(O.softmax_forward(zs[None], V), tgt[None], np.full((1, rows), dloss))[0]
+    got = host(D)
+    assert np.all(got[:, V:] == 0)
+    assert np.max(np.abs(got - rd)) < 2 ** -8 * dloss
+
+
 def test_softmax_crossentropy_flags_bad_target_large_vocab(ops):
     z = dev(normal_array((3, 50304), 65), torch.bfloat16)
     fl = ops.flags()
