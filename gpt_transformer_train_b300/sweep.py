@@ -12,9 +12,10 @@ against the measured peaks (HBM copy GB/s, bf16 burst TFLOP/s).
 Kernel names: ln_fwd ln_bwd gelu_fwd gelu_bwd softmax_ce adamw encoder_fwd
 encoder_bwd attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096},
 gemm_<layer>_{fwd,dgrad,wgrad} for layer in qkv attproj fc fcproj classifier,
-gemmepi_fc_gelu, gemmepi_fcproj_gelubwd and gemmepi_attproj_rowdot (the fused
-epilogues as the step uses them), and wgradL_<layer> (that weight gradient for
-12 layers in one batched launch).
+gemmepi_fc_gelu, gemmepi_fcproj_gelubwd, gemmepi_attproj_rowdot and
+gemmepi_classifier_stats (the fused epilogues as the step uses them),
+softmax_ce_stats (the softmax/CE from the classifier's row statistics), and
+wgradL_<layer> (that weight gradient for 12 layers in one batched launch).
 """
 from __future__ import annotations
 
@@ -129,6 +130,20 @@ def make_case(name, ops):
         return (lambda: ops.gpt2_op_matmul_batched(L, dy, N, BT * N, 0, x, K, BT * K, 0, N, K, BT, dW, K, N * K,
                                                    epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC, flags_dev=fl),
                 2.0 * L * BT * N * K, "FLOP")
+    if name == "gemmepi_classifier_stats":  # classifier forward with the softmax's row statistics in its epilogue
+        W, x = randn((VP, C), 22, std=0.02), randn((BT, C), 23)
+        y = torch.empty(BT, VP, device="cuda", dtype=BF)
+        st = torch.empty(BT, ops.gpt2_op_logit_stats_tiles(VP), 2, device="cuda")
+        return (lambda: ops.gpt2_op_matmul_logit_stats(x, C, W, C, BT, VP, C, y, VP, st, V, fl), 2.0 * BT * VP * C, "FLOP")
+    if name == "softmax_ce_stats":  # softmax/CE from those statistics: logits read once, dlogits written once
+        W, x = randn((VP, C), 22, std=0.02), randn((BT, C), 23)
+        z = torch.empty(BT, VP, device="cuda", dtype=BF)
+        st = torch.empty(BT, ops.gpt2_op_logit_stats_tiles(VP), 2, device="cuda")
+        ops.gpt2_op_matmul_logit_stats(x, C, W, C, BT, VP, C, z, VP, st, V, fl)
+        tgt = torch.randint(0, V, (BT,), generator=torch.Generator().manual_seed(12), dtype=torch.int32).cuda()
+        losses = torch.empty(BT, device="cuda")
+        return (lambda: ops.gpt2_op_softmax_crossentropy_stats(z, losses, tgt, st, BT, V, VP, 1.0 / BT, fl),
+                2 * BT * VP * 2 + 8 * BT, "B")
     if name == "gemmepi_fc_gelu":  # fc forward: bias, pre-activation and GELU output written
         N, K = GEMM_LAYERS["fc"]
         W, b, x = randn((N, K), 22, std=0.02), randn((N,), 29), randn((BT, K), 23)
@@ -174,7 +189,8 @@ def make_case(name, ops):
 ALL = (["ln_fwd", "ln_bwd", "gelu_fwd", "gelu_bwd", "softmax_ce", "adamw", "encoder_fwd", "encoder_bwd"] +
        [f"attn_{d}_T{t}" for d in ("fwd", "bwd") for t in (256, 1024, 4096)] +
        [f"gemm_{l}_{k}" for l in GEMM_LAYERS for k in ("fwd", "dgrad", "wgrad")] +
-       ["gemmepi_fc_gelu", "gemmepi_fcproj_gelubwd", "gemmepi_attproj_rowdot"] +
+       ["gemmepi_fc_gelu", "gemmepi_fcproj_gelubwd", "gemmepi_attproj_rowdot", "gemmepi_classifier_stats",
+        "softmax_ce_stats"] +
        [f"wgradL_{l}" for l in ("qkv", "attproj", "fc", "fcproj")])
 
 
