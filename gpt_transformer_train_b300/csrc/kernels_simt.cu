@@ -1831,7 +1831,10 @@ __global__ void __launch_bounds__(SCS_THREADS) softmax_ce_stats_kernel(
   constexpr float L2E = 1.4426950408889634f;
   __shared__ float sh[3];
   const int tid = threadIdx.x, lane = tid & 31;
-  const int row = blockIdx.x;
+  // rows from the last: the classifier product wrote the last rows last (they
+  // are still in L2), and the input-gradient product after this kernel starts
+  // from row 0, which is then the most recently written
+  const int row = gridDim.x - 1 - blockIdx.x;
   bf16* z = logits + (size_t)row * Vp;
   int tg = targets[row];
   const bool bad = tg < 0 || tg >= V;
