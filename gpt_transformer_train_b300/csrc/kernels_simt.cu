@@ -1899,7 +1899,8 @@ __global__ void __launch_bounds__(SCS_THREADS) softmax_ce_stats_kernel(
 
 cudaError_t softmax_ce_from_stats(bf16* logits, float* losses, const int* targets, const float* rowstats, int tiles,
                                   int rows, int V, int Vp, float dloss, int* flags, cudaStream_t st) {
-  if (rows <= 0 || tiles <= 0 || V <= 0 || Vp < V || Vp % 8 || ((uintptr_t)logits & 15)) return cudaErrorInvalidValue;
+  if (rows <= 0 || tiles <= 0 || V <= 0 || Vp < V || Vp % 8 || ((uintptr_t)logits & 15) || ((uintptr_t)rowstats & 7))
+    return cudaErrorInvalidValue;
   launch_k(softmax_ce_stats_kernel, dim3(rows), dim3(SCS_THREADS), 0, st, logits, losses, targets, rowstats, tiles, V,
            Vp, dloss, flags);
   return launch_status(1);

@@ -130,7 +130,8 @@ int gpt2_op_logit_stats_tiles(int N) { return N > 0 ? gemm_tc_stats_tiles(N) : 0
 
 int gpt2_op_matmul_logit_stats(const void* A, long long lda, const void* B, long long ldb, int M, int N, int K,
                                void* D, long long ldd, float* stats, int stats_cols, int* flags_dev, void* stream) {
-  if (!A || !B || !D || !stats || !flags_dev || M <= 0 || N <= 0 || K <= 0 || stats_cols <= 0)
+  if (!A || !B || !D || !stats || !flags_dev || M <= 0 || N <= 0 || K <= 0 || stats_cols <= 0 ||
+      ((uintptr_t)stats & 7))
     return GPT2_ERR_INVALID_ARG;
   GemmArgs a{A, lda, 1, B, ldb, 1, M, N, K, D, ldd, nullptr, nullptr, 0, EPI_STORE};
   a.rowstats = stats;

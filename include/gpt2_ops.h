@@ -164,7 +164,7 @@ int gpt2_op_softmax_crossentropy(int dtype, void* logits, float* losses, const i
  * gpt2_op_logit_stats_tiles(N), the statistics of the stored values of the
  * columns < stats_cols: stats[(row * tiles + n) * 2] = their maximum m,
  * stats[... + 1] = sum of exp(value - m) (m = -inf, sum 0 for a tile without
- * such columns).  stats: M * tiles * 2 floats, caller-owned.
+ * such columns).  stats: M * tiles * 2 floats, 8-byte aligned, caller-owned.
  * gpt2_op_softmax_crossentropy_stats then gives the same losses and dlogits as
  * gpt2_op_softmax_crossentropy (write_grad = 1) from D and those statistics,
  * reading each row once: the row's log-sum-exp is M + ln S with M = max_n m_n,
