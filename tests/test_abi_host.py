@@ -121,3 +121,15 @@ def test_lr_schedule_matches_oracle(g):
         mine = g.lr_schedule(6e-4, 0.1, 10, 100, step)
         ref = O.lr_schedule(6e-4, 0.1, 10, 100, step)
         assert abs(mine - ref) <= 1e-6 * ref, (step, mine, ref)
+
+
+def test_logit_stats_tile_count(g):
+    """Column tiles of the row statistics: 256 wide from N = 512 up (the
+    tensor-core kernel's tile there), else 128; the last may be narrower."""
+    lib = ctypes.CDLL(g.LIB_PATH)
+    f = lib.gpt2_op_logit_stats_tiles
+    f.restype, f.argtypes = ctypes.c_int, [ctypes.c_int]
+    assert f(50304) == 197  # GPT-2's padded vocabulary: 196 full tiles and one of 128 columns
+    assert f(768) == 3 and f(1600) == 7 and f(512) == 2
+    assert f(384) == 3 and f(128) == 1 and f(8) == 1
+    assert f(0) == 0
