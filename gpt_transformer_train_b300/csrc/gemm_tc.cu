@@ -74,6 +74,10 @@ struct TcParams {
   int acc_store;  // EPI_ACC_F32: split 0 stores its tile into D instead of adding it
   float* rowstats;  // EPI_STORE: per row and column tile, (max, sum of exp) of the stored values
   int stats_cols;   // columns counted in rowstats
+  // a grouped launch (EPI_ACC_F32, no K split): after the first product's
+  // units come batch2 items of a second product with M2 rows and the same N
+  // and K, through the maps ta2, tb2, td2 (batch2 = 0: one product)
+  int M2, batch2;
 };
 
 
@@ -243,7 +247,9 @@ __device__ __forceinline__ void unstage_bf16(const uint8_t* buf, uint32_t r, uin
 template <int BN, int STAGES, int CL, int EPI_WARPS>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                   const __grid_constant__ CUtensorMap td, const __grid_constant__ CUtensorMap tx, TcParams p) {
+                   const __grid_constant__ CUtensorMap td, const __grid_constant__ CUtensorMap tx,
+                   const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb2,
+                   const __grid_constant__ CUtensorMap td2, TcParams p) {
   constexpr uint32_t A_BYTES = BM * BK * 2;
   constexpr uint32_t B_BYTES = (BN / CL) * BK * 2;  // this CTA's share of the B tile
   constexpr uint32_t STAGE = A_BYTES + B_BYTES;
@@ -294,8 +300,25 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   // a "tile" here is CL vertically adjacent 128-row tiles (one per CTA of the pair)
   const int tiles = ((p.M + CL * BM - 1) / (CL * BM)) * num_n;
   const int nk = (p.K + BK - 1) / BK;
-  // unit u: batch item u / (splits * tiles), split (u / tiles) % splits, tile u % tiles
-  const int units = tiles * p.splits * p.batch;
+  // unit u < units1: batch item u / (splits * tiles), split (u / tiles) % splits,
+  // tile u % tiles; the second product's units (grouped launch) follow
+  const int units1 = tiles * p.splits * p.batch;
+  const int tiles2 = ((p.M2 + CL * BM - 1) / (CL * BM)) * num_n;
+  const int units = units1 + tiles2 * p.batch2;
+  auto decode = [&](int u, int& pr, int& t, int& sp, int& z) {
+    if (u < units1) {
+      pr = 0;
+      t = u % tiles;
+      sp = (u / tiles) % p.splits;
+      z = u / (tiles * p.splits);
+    } else {
+      const int v = u - units1;
+      pr = 1;
+      t = v % tiles2;
+      sp = 0;
+      z = v / tiles2;
+    }
+  };
   auto kb_begin = [&](int sp) { return (int)((long long)nk * sp / p.splits); };
   const uint32_t crank = CL > 1 ? cluster_rank() : 0;
   const int ustart = (int)(blockIdx.x / CL), ustep = (int)(gridDim.x / CL);
@@ -305,7 +328,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     if (lane == 0) {  // ---- TMA producer
       uint32_t it = 0;
       for (int u = ustart; u < units; u += ustep) {
-        const int t = u % tiles, sp = (u / tiles) % p.splits, z = u / (tiles * p.splits);
+        int pr, t, sp, z;
+        decode(u, pr, t, sp, z);
+        const CUtensorMap* mA = pr ? &ta2 : &ta;
+        const CUtensorMap* mB = pr ? &tb2 : &tb;
         const int m0 = tile_m0(t), n0 = (t % num_n) * BN;
         bool ok = true;
         for (int kb = kb_begin(sp), kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
@@ -317,33 +343,33 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             const uint32_t fb = full0 + 8 * s;
             mbar_expect_tx(fb, STAGE);
             if (!p.a_mn) {
-              tma_load_3d(a_dst, &ta, k0, m0, z, fb);
+              tma_load_3d(a_dst, mA, k0, m0, z, fb);
             } else {
-              tma_load_3d(a_dst, &ta, m0, k0, z, fb);
-              tma_load_3d(a_dst + 8192, &ta, m0 + 64, k0, z, fb);
+              tma_load_3d(a_dst, mA, m0, k0, z, fb);
+              tma_load_3d(a_dst + 8192, mA, m0 + 64, k0, z, fb);
             }
             if (!p.b_mn) {
-              tma_load_3d(b_dst, &tb, k0, n0, z, fb);
+              tma_load_3d(b_dst, mB, k0, n0, z, fb);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; j++) tma_load_3d(b_dst + 8192 * j, &tb, n0 + 64 * j, k0, z, fb);
+              for (int j = 0; j < BN / 64; j++) tma_load_3d(b_dst + 8192 * j, mB, n0 + 64 * j, k0, z, fb);
             }
           } else {
             // both CTAs' loads complete on the even CTA's barrier, which expects all of them
             const uint32_t fb = leader_addr(full0 + 8 * s);
             if (crank == 0) mbar_expect_tx(full0 + 8 * s, 2 * STAGE);
             if (!p.a_mn) {
-              tma_load_3d_pair(a_dst, &ta, k0, m0, z, fb);
+              tma_load_3d_pair(a_dst, mA, k0, m0, z, fb);
             } else {
-              tma_load_3d_pair(a_dst, &ta, m0, k0, z, fb);
-              tma_load_3d_pair(a_dst + 8192, &ta, m0 + 64, k0, z, fb);
+              tma_load_3d_pair(a_dst, mA, m0, k0, z, fb);
+              tma_load_3d_pair(a_dst + 8192, mA, m0 + 64, k0, z, fb);
             }
             const int nb = n0 + (int)crank * (BN / 2);  // this CTA's half of the B tile
             if (!p.b_mn) {
-              tma_load_3d_pair(b_dst, &tb, k0, nb, z, fb);
+              tma_load_3d_pair(b_dst, mB, k0, nb, z, fb);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 128; j++) tma_load_3d_pair(b_dst + 8192 * j, &tb, nb + 64 * j, k0, z, fb);
+              for (int j = 0; j < BN / 128; j++) tma_load_3d_pair(b_dst + 8192 * j, mB, nb + 64 * j, k0, z, fb);
             }
           }
         }
@@ -365,7 +391,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
         fence_after();
         const uint32_t d = tmem + a * BN;
         bool ok = true;
-        const int sp = (u / tiles) % p.splits, kb0 = kb_begin(sp);
+        int pr, t, sp, z;
+        decode(u, pr, t, sp, z);
+        const int kb0 = kb_begin(sp);
         for (int kb = kb0, kb1 = kb_begin(sp + 1); kb < kb1; kb++, it++) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1;
           if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
@@ -444,10 +472,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     };
     uint32_t j = 0;
     for (int u = ustart; u < units; u += ustep, j++) {
-      const int t = u % tiles, sp = (u / tiles) % p.splits, z = u / (tiles * p.splits);
+      int pr, t, sp, z;
+      decode(u, pr, t, sp, z);
       const int m0 = tile_m0(t), n0 = (t % num_n) * BN;
       const int rbase = m0 + q * 32;  // first row of this warp's slab
-      const bool rows_in = rbase < p.M;
+      const bool rows_in = rbase < (pr ? p.M2 : p.M);
       const uint32_t a = j & 1, aph = (j >> 1) & 1;
       // live 64-column chunks of this warp's half
       const int nlive = rows_in && n0 + hc < p.N ? min(HALF / 64, (p.N - n0 - hc + 63) / 64) : 0;
@@ -483,8 +512,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             __syncwarp();
             if (lane == 0) {
               if (sp == 0) {
-                if (p.acc_store) tma_store_3d(&td, col0, rbase, z, buf);
-                else tma_reduce_add_3d(&td, col0, rbase, z, buf);
+                const CUtensorMap* mD = pr ? &td2 : &td;
+                if (p.acc_store) tma_store_3d(mD, col0, rbase, z, buf);
+                else tma_reduce_add_3d(mD, col0, rbase, z, buf);
               }
               else tma_store_3d(&tx, col0, rbase, sp - 1, buf);  // workspace slot sp - 1
               bulk_commit();
@@ -690,7 +720,7 @@ constexpr size_t smem_bytes() {
 }
 
 template <int BN, int STAGES, int CL, int EPI_WARPS>
-cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
+cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st, const GemmArgs* g2 = nullptr) {
   constexpr size_t smem = smem_bytes<BN, STAGES, CL, EPI_WARPS>();
   static_assert(smem <= 232448, "shared memory per CTA");
   static_assert((2 * STAGES + 4 + 2 * EPI_WARPS) * 8 + 8 <= 512,
@@ -718,12 +748,24 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
     ok = ok && make_map_3d(&tx, bf, 2, g.aux, g.N, g.M, g.ldaux, nb, g.sAux, 64, 32);
   else if (g.epi == EPI_ACC_F32 && splits > 1) ok = ok && tc_make_map_f32_3d(&tx, g.ws, g.N, g.M, splits - 1, 32, 32);
   else tx = td;
+  // the second product of a grouped launch (EPI_ACC_F32, same N, K and operand majors)
+  CUtensorMap ta2 = ta, tb2 = tb, td2 = td;
+  long long nb2 = 0;
+  if (g2) {
+    nb2 = g2->batch > 1 ? g2->batch : 1;
+    ok = ok && (g2->a_kmajor ? make_map_3d(&ta2, bf, 2, g2->A, g2->K, g2->M, g2->lda, nb2, g2->sA, 64, BM)
+                             : make_map_3d(&ta2, bf, 2, g2->A, g2->M, g2->K, g2->lda, nb2, g2->sA, 64, 64));
+    ok = ok && (g2->b_kmajor ? make_map_3d(&tb2, bf, 2, g2->B, g2->K, g2->N, g2->ldb, nb2, g2->sB, 64, BN / CL)
+                             : make_map_3d(&tb2, bf, 2, g2->B, g2->N, g2->K, g2->ldb, nb2, g2->sB, 64, 64));
+    ok = ok && make_map_3d(&td2, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g2->D, g2->N, g2->M, g2->ldd, nb2, g2->sD, 32, 32);
+  }
   if (!ok) return cudaErrorInvalidValue;
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
   TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
-             (int)nb, g.dvec, g.dT, g.dH, g.acc_store, g.rowstats, g.stats_cols};
-  const long long units = tiles * splits * (long long)nb;
+             (int)nb, g.dvec, g.dT, g.dH, g.acc_store, g.rowstats, g.stats_cols, g2 ? g2->M : 0, (int)nb2};
+  const long long tiles2 = g2 ? ((g2->M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN) : 0;
+  const long long units = tiles * splits * (long long)nb + tiles2 * nb2;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(64 + 32 * EPI_WARPS);
   cfg.dynamicSmemBytes = smem;
@@ -761,7 +803,7 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st) {
     at[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>, ta, tb, td, tx, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>, ta, tb, td, tx, ta2, tb2, td2, p);
 }
 
 }  // namespace
@@ -923,6 +965,28 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(float* __restrict__ 
 }
 
 int gemm_tc_stats_tiles(int N) { return N >= 512 ? (N + 255) / 256 : (N + 127) / 128; }
+
+// two fp32-accumulate products with the same N, K and operand majors in one
+// launch (the second's units after the first's), so the two share their last
+// partial wave; falls back to two launches when the pair of them would not
+// fill the CTA pairs or the shapes differ
+cudaError_t gemm_tc_grouped(const GemmArgs& a, const GemmArgs& b, int* flags, cudaStream_t st) {
+  if (!gemm_tc_supported(a) || !gemm_tc_supported(b)) return cudaErrorNotSupported;
+  const int sms = tc_num_sms();
+  auto row_tiles = [](const GemmArgs& g) { return (long long)(g.M + BM - 1) / BM; };
+  auto items = [](const GemmArgs& g) { return (long long)(g.batch > 1 ? g.batch : 1); };
+  const long long nt = (a.N + 255) / 256;
+  const bool same = a.epi == EPI_ACC_F32 && b.epi == EPI_ACC_F32 && a.N == b.N && a.K == b.K &&
+                    a.a_kmajor == b.a_kmajor && a.b_kmajor == b.b_kmajor && a.acc_store == b.acc_store && !a.bias &&
+                    !b.bias && a.N >= 512;
+  if (!same || row_tiles(a) < 2 || row_tiles(b) < 2 ||
+      (row_tiles(a) * items(a) + row_tiles(b) * items(b)) * nt < sms) {
+    cudaError_t e = gemm_tc(a, flags, st);
+    return e != cudaSuccess ? e : gemm_tc(b, flags, st);
+  }
+  gpt2_count_launches(1);
+  return launch<256, 6, 2, 4>(a, 1, flags, st, &b);
+}
 
 cudaError_t gemm_tc(const GemmArgs& g, int* flags, cudaStream_t st) {
   if (!gemm_tc_supported(g)) return cudaErrorNotSupported;

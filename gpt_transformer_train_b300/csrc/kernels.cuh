@@ -44,6 +44,9 @@ struct GemmArgs {
   float* rowstats; int stats_cols;
 };
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
+// two EPI_ACC_F32 products with the same N, K and operand majors as one launch
+// (the weight gradients of two weight types), or two launches when that does not pay
+cudaError_t gemm_tc_grouped(const GemmArgs& a, const GemmArgs& b, int* flags, cudaStream_t st);
 int gemm_tc_stats_tiles(int N);  // column tiles of an N-wide tensor-core product
 // softmax + cross-entropy of bf16 logit rows from the per-tile statistics of
 // the classifier product (see GemmArgs::rowstats): loss and dlogits in place

@@ -294,6 +294,30 @@ struct Step {
     return gemm(a);
   }
 
+  // two weight types' gradients for every layer (the same input width K and
+  // rows M = B*T), as one tensor-core launch when that fills the last wave better
+  cudaError_t linear_wgrad_layers_pair(float* dW1, const T* dY1, long long sY1, const T* X1, long long sX1, int N1,
+                                       float* dW2, const T* dY2, long long sY2, const T* X2, long long sX2, int N2,
+                                       int M, int K) {
+    GemmArgs a{dY1, N1, 0, X1, K, 0, N1, K, M, dW1, K, nullptr, nullptr, 0, EPI_ACC_F32, nullptr, 0,
+               (int)c.L, sY1, sX1, (long long)N1 * K, 0};
+    GemmArgs b{dY2, N2, 0, X2, K, 0, N2, K, M, dW2, K, nullptr, nullptr, 0, EPI_ACC_F32, nullptr, 0,
+               (int)c.L, sY2, sX2, (long long)N2 * K, 0};
+    a.acc_store = b.acc_store = fresh;
+    if (gemm_path(a) != 1 || gemm_path(b) != 1) {
+      cudaError_t e = gemm(a);
+      return e != cudaSuccess ? e : gemm(b);
+    }
+    const bool rec = m->prof_on && m->prof_n < m->prof_flops.size();
+    if (rec) cudaEventRecord(m->prof_ev[2 * m->prof_n], m->st);
+    cudaError_t e = gemm_tc_grouped(a, b, flags(), m->st);
+    if (rec) {
+      cudaEventRecord(m->prof_ev[2 * m->prof_n + 1], m->st);
+      m->prof_flops[m->prof_n++] = 2.0 * (double)(N1 + N2) * K * (double)M * c.L;
+    }
+    return e;
+  }
+
   // causal attention: tcgen05 flash kernels in bf16 mode, SIMT kernels in fp32 mode
   bool attention_on_tc() const {
     return c.precision == GPT2_PRECISION_BF16 && attention_tc_supported(c.B, c.T, c.C, c.H);
@@ -492,8 +516,9 @@ struct Step {
       const long long sBT = (long long)BTi * Ci;
       CK(m, linear_wgrad_layers(G(GPT2_FCPROJW), dresc(0, 0), 2 * sBT, fchg(0), 4 * sBT, BTi, Ci, 4 * Ci));
       CK(m, linear_wgrad_layers(G(GPT2_FCW), dfch(0), 4 * sBT, ln(1), 2 * sBT, BTi, 4 * Ci, Ci));
-      CK(m, linear_wgrad_layers(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, BTi, Ci, Ci));
-      CK(m, linear_wgrad_layers(G(GPT2_QKVW), dqkv(0), 3 * sBT, ln(0), 2 * sBT, BTi, 3 * Ci, Ci));
+      // attention projection and qkv together: 108 + 324 pair tiles at 124M share one last wave
+      CK(m, linear_wgrad_layers_pair(G(GPT2_ATTPROJW), dresc(0, 1), 2 * sBT, atty(0), sBT, Ci, G(GPT2_QKVW), dqkv(0),
+                                     3 * sBT, ln(0), 2 * sBT, 3 * Ci, BTi, Ci));
       // bias gradients of the fc and qkv layers of every layer: column sums of their output gradients
       CK(m, colsum<T>(G(GPT2_FCB), dfch(0), BTi, 4 * Ci, 4 * Ci, part, st, Li, 4 * Ci, 4 * sBT, acc));
       CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT, acc));

@@ -152,6 +152,26 @@ def test_bf16_small_forward_backward_and_curve(g):
     assert rcurve[-1] < rcurve[0]
 
 
+WIDE_BF16 = dict(L=3, C=768, H=12, V=1000, Vp=1024, maxT=128, B=2, T=128)
+
+
+def test_bf16_wide_step_gradients(g):
+    """C = 768 with few tokens: the weight gradients of the attention
+    projection and qkv go out as one grouped tensor-core launch (their pair
+    tiles together fill more than one wave); every gradient against the oracle."""
+    cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **WIDE_BF16, prec=1, dtype=np.float32)
+    m.gpt2_zero_grad()
+    ref.zero_grad()
+    loss = m.gpt2_forward(ttok, ttgt)
+    rloss = ref.forward(tok, tgt)
+    m.gpt2_backward()
+    ref.backward()
+    assert abs(loss - rloss) <= 2e-2
+    for n in g.TENSORS:
+        e = rel_l2(m.gpt2_get_grads(n), ref.grads[n].reshape(-1))
+        assert e <= 5e-2, (n, e)
+
+
 def test_bf16_step_host_matches_device_calls(g):
     cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **SMALL_BF16, prec=1)
     cfg2, m2, _, _, _, _, _ = _setup(g, **SMALL_BF16, prec=1)
