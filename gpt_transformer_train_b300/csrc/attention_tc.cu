@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return kernel_smem_attr(kernel, (int)bytes);
 }
 
 }  // namespace
@@ -875,11 +875,9 @@ cudaError_t attention_forward_tc(bf16* out, float* lse, const bf16* qkv, int B, 
                                  cudaStream_t st) {
   if (!attention_tc_supported(B, T, C, H) || !flags) return cudaErrorNotSupported;
   if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15)) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
+  {
     cudaError_t e = set_smem(attn_fwd_tc_kernel, FWD_SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   CUtensorMap tq;
   if (!tc_make_map(&tq, qkv, 3 * (uint64_t)C, (uint64_t)B * T, 3 * (uint64_t)C, HD, 128)) return cudaErrorInvalidValue;
@@ -905,12 +903,10 @@ cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16*
   if (((uintptr_t)qkv & 15) || ((uintptr_t)out & 15) || ((uintptr_t)dout & 15) || ((uintptr_t)dqkv & 15) ||
       ((uintptr_t)lse & 15) || ((uintptr_t)Dbuf & 15) || !dS || ((uintptr_t)dS & 15))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
+  {
     cudaError_t e = set_smem(attn_bwd_dq_tc_kernel, DQ_SMEM);
     if (e == cudaSuccess) e = set_smem(attn_bwd_dkv_tc_kernel, DKV_SMEM);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   CUtensorMap tq, td;
   if (!tc_make_map(&tq, qkv, 3 * (uint64_t)C, (uint64_t)B * T, 3 * (uint64_t)C, HD, 128) ||

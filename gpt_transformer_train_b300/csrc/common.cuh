@@ -43,6 +43,17 @@ inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  Function attributes are per device, so the library keeps
+// one record per (kernel, device) under a lock and calls
+// cudaFuncSetAttribute once for each; the first failure is returned (and
+// retried on the next call).
+cudaError_t kernel_smem_attr(const void* kernel, int bytes);
+template <typename... KArgs>
+inline cudaError_t kernel_smem_attr(void (*kernel)(KArgs...), int bytes) {
+  return kernel_smem_attr(reinterpret_cast<const void*>(kernel), bytes);
+}
+
 // elements per 16-byte word
 template <typename T> struct VecN;
 template <> struct VecN<float> { static constexpr int n = 4; };

@@ -726,12 +726,9 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st, c
   static_assert((2 * STAGES + 4 + 2 * EPI_WARPS) * 8 + 8 <= 512,
                 "barriers, TMEM address and abort flag after the staging buffers");
   static_assert((BN * 4 / EPI_WARPS) % 64 == 0, "each epilogue warp takes whole 64-column chunks");
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  {
+    cudaError_t e = kernel_smem_attr(gemm_tc_kernel<BN, STAGES, CL, EPI_WARPS>, (int)smem);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   // every operand map is 3-D: depth = batch items, g.sX elements apart
   CUtensorMap ta, tb, td, tx;

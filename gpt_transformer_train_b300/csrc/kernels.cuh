@@ -69,17 +69,19 @@ bool gemm_tc_supported(const GemmArgs& a);
 template <typename T>
 cudaError_t encoder_forward(T* out, const int* tok, const T* wte, const T* wpe, int B, int T_, int C,
                             int V, int* flags, cudaStream_t st);
-// dwte/dwpe += scatter of dres (fp32 [B*T][C]); keys: 2*pow2(B*T) uint32 scratch
-// (accumulate_wpe = 0: dwpe is overwritten instead of added to)
+// dwte/dwpe += scatter of dres (fp32 [B*T][C]); keys: pow2(B*T) uint32 keys of
+// scratch (accumulate_wpe = 0: dwpe is overwritten instead of added to).
+// Positions whose token is outside [0, V) (V <= 65535) add nothing to dwte and
+// OR FLAG_TOKEN_RANGE into *flags (flags may be null).
 cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
-                             int C, uint32_t* keys, cudaStream_t st, int accumulate_wpe = 1);
+                             int C, int V, int* flags, uint32_t* keys, cudaStream_t st, int accumulate_wpe = 1);
 size_t encoder_backward_scratch_bytes(int BT);
 // the same with a larger scratch (BT <= 16384): radix-sorted keys and
 // fixed-size chunks of the per-token sums, so no CTA waits on a long run
 bool encoder_backward_fast_supported(int BT, int C);
 size_t encoder_backward_fast_scratch_bytes(int BT, int C);
 cudaError_t encoder_backward_fast(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_, int C,
-                                  void* scratch, cudaStream_t st, int accumulate_wpe = 1);
+                                  int V, int* flags, void* scratch, cudaStream_t st, int accumulate_wpe = 1);
 
 template <typename T>
 cudaError_t residual_layernorm_forward(T* resid_out, T* y, float* mean, float* rstd, const T* a,

@@ -17,6 +17,24 @@
 #define LN_EPS 1e-5f
 
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
+cudaError_t kernel_smem_attr(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> bytes set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({kernel, dev});
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[{kernel, dev}] = bytes;
+  return e;
+}
+
 static std::atomic<unsigned long long> g_launches{0};
 void gpt2_count_launches(int n) { g_launches += (unsigned long long)(long long)n; }
 unsigned long long gpt2_total_launches() { return g_launches.load(); }
@@ -96,12 +114,25 @@ static inline int pow2_at_least(int n) {
 }
 size_t encoder_backward_scratch_bytes(int BT) { return (size_t)pow2_at_least(BT) * sizeof(uint32_t); }
 
+// The sort key of position i: (token << 16) | i.  A token outside [0, V)
+// (V <= 65535) gets the token field BAD_TOKEN, which sorts after every real
+// token and is never scattered into dwte; it raises FLAG_TOKEN_RANGE.
+constexpr uint32_t BAD_TOKEN = 0xFFFFu;
+__device__ __forceinline__ uint32_t sort_key(const int* tok, int i, int V, int* flags) {
+  const int v = tok[i];
+  if (v < 0 || v >= V) {
+    if (flags) atomicOr(flags, FLAG_TOKEN_RANGE);
+    return (BAD_TOKEN << 16) | (uint32_t)i;
+  }
+  return ((uint32_t)v << 16) | (uint32_t)i;
+}
+
 // one CTA sorts n (power of two, <= 32768) keys in shared memory
-__global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restrict__ tok, int BT, int n) {
+__global__ void bitonic_sort_keys_kernel(uint32_t* keys_out, const int* __restrict__ tok, int BT, int n, int V,
+                                         int* flags) {
   pdl_enter();
   extern __shared__ uint32_t sk[];
-  for (int i = threadIdx.x; i < n; i += blockDim.x)
-    sk[i] = i < BT ? (((uint32_t)tok[i] & 0xFFFFu) << 16) | (uint32_t)i : 0xFFFFFFFFu;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) sk[i] = i < BT ? sort_key(tok, i, V, flags) : 0xFFFFFFFFu;
   __syncthreads();
   for (int k = 2; k <= n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
@@ -135,7 +166,7 @@ __global__ void __launch_bounds__(32 * RUNS_WARPS) wte_grad_runs_kernel(float* _
   __shared__ float4 part[RUNS_WARPS][32];
   const int i = blockIdx.x;
   const uint32_t tk = keys[i] >> 16;
-  if (i > 0 && (keys[i - 1] >> 16) == tk) return;
+  if (tk == BAD_TOKEN || (i > 0 && (keys[i - 1] >> 16) == tk)) return;
   int lo = i + 1, hi = BT;  // first entry past the run
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -191,20 +222,18 @@ __global__ void __launch_bounds__(32 * RUNS_WARPS) wte_grad_runs_kernel(float* _
 }
 
 cudaError_t encoder_backward(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_,
-                             int C, uint32_t* keys, cudaStream_t st, int accumulate_wpe) {  // the small-scratch form
+                             int C, int V, int* flags, uint32_t* keys, cudaStream_t st,
+                             int accumulate_wpe) {  // the small-scratch form
   int BT = B * T_;
   int n = pow2_at_least(BT);
-  if (n > 32768) return cudaErrorInvalidValue;
+  if (n > 32768 || V <= 0 || V > (int)BAD_TOKEN) return cudaErrorInvalidValue;
   long long nv = (long long)T_ * (C / 4);
   launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C,
            accumulate_wpe);
   size_t smem = (size_t)n * sizeof(uint32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(bitonic_sort_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768 * 4);
-    attr_set = true;
-  }
-  launch_k(bitonic_sort_keys_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT, n);
+  cudaError_t ea = kernel_smem_attr(bitonic_sort_keys_kernel, 32768 * 4);
+  if (ea != cudaSuccess) return ea;
+  launch_k(bitonic_sort_keys_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT, n, V, flags);
   launch_k(wte_grad_runs_kernel, dim3((unsigned)BT, (unsigned)cdiv(C / 4, 32)), dim3(256), 0, st, dwte, dres, keys, BT, C);
   return launch_status(3);
 }
@@ -232,7 +261,8 @@ size_t encoder_backward_fast_scratch_bytes(int BT, int C) {
 bool encoder_backward_fast_supported(int BT, int C) { return BT > 0 && BT <= RADIX_MAX && C % 4 == 0; }
 
 __global__ void __launch_bounds__(1024) radix_sort_tokens_kernel(uint32_t* __restrict__ keys_out,
-                                                                 const int* __restrict__ tok, int BT) {
+                                                                 const int* __restrict__ tok, int BT, int V,
+                                                                 int* flags) {
   pdl_enter();
   extern __shared__ uint32_t rs_sh[];
   uint32_t* bufA = rs_sh;
@@ -241,7 +271,7 @@ __global__ void __launch_bounds__(1024) radix_sort_tokens_kernel(uint32_t* __res
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int seg = ((BT + 31) / 32 + 31) & ~31;  // keys per warp, a multiple of 32
   const unsigned lt = (1u << lane) - 1u;
-  for (int i = threadIdx.x; i < BT; i += blockDim.x) bufA[i] = (((uint32_t)tok[i] & 0xFFFFu) << 16) | (uint32_t)i;
+  for (int i = threadIdx.x; i < BT; i += blockDim.x) bufA[i] = sort_key(tok, i, V, flags);
   for (int pass = 0; pass < 2; pass++) {
     const int shift = 16 + 8 * pass;
     const uint32_t* src = pass == 0 ? bufA : bufB;
@@ -334,7 +364,7 @@ __global__ void __launch_bounds__(128) wte_chunk_kernel(float* __restrict__ dwte
       if (e == e1 - 1 || tok_at(e + 1) != t) {  // end of a segment
         const bool run_start = seg_first > e0 || tok_at(e0 - 1) != t;
         const bool run_end = tok_at(e + 1) != t;
-        if (on) {
+        if (on && t != BAD_TOKEN) {
           if (run_start && run_end) {
             float4* dst = reinterpret_cast<float4*>(dwte + (size_t)t * C) + cv;
             float4 o = *dst;
@@ -358,7 +388,7 @@ __global__ void __launch_bounds__(128) wte_span_kernel(float* __restrict__ dwte,
   pdl_enter();
   const int c = blockIdx.x, e0 = c * WTE_CH, e1 = min(BT, e0 + WTE_CH);
   const uint32_t tk = keys[e1 - 1] >> 16;
-  if (e1 >= BT || (keys[e1] >> 16) != tk) return;  // the chunk's last run ends here
+  if (tk == BAD_TOKEN || e1 >= BT || (keys[e1] >> 16) != tk) return;  // the chunk's last run ends here
   int s = e1 - 1;
   while (s > e0 && (keys[s - 1] >> 16) == tk) s--;
   if (s == e0 && e0 > 0 && (keys[e0 - 1] >> 16) == tk) return;  // the run started in an earlier chunk
@@ -383,23 +413,20 @@ __global__ void __launch_bounds__(128) wte_span_kernel(float* __restrict__ dwte,
 }
 
 cudaError_t encoder_backward_fast(float* dwte, float* dwpe, const float* dres, const int* tok, int B, int T_, int C,
-                                  void* scratch, cudaStream_t st, int accumulate_wpe) {
+                                  int V, int* flags, void* scratch, cudaStream_t st, int accumulate_wpe) {
   const int BT = B * T_;
-  if (!encoder_backward_fast_supported(BT, C)) return cudaErrorInvalidValue;
+  if (!encoder_backward_fast_supported(BT, C) || V <= 0 || V > (int)BAD_TOKEN) return cudaErrorInvalidValue;
   uint32_t* keys = (uint32_t*)scratch;
   float* slots = (float*)((char*)scratch + fast_keys_bytes(BT));
   const long long nv = (long long)T_ * (C / 4);
   launch_k(wpe_grad_kernel, dim3((unsigned)cdiv(nv, 256)), dim3(256), 0, st, dwpe, dres, B, T_, C,
            accumulate_wpe);
   const size_t smem = ((size_t)2 * BT + 32 * 256) * sizeof(uint32_t);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(radix_sort_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(((size_t)2 * RADIX_MAX + 32 * 256) * sizeof(uint32_t)));
+  {
+    cudaError_t e = kernel_smem_attr(radix_sort_tokens_kernel, (int)(((size_t)2 * RADIX_MAX + 32 * 256) * sizeof(uint32_t)));
     if (e != cudaSuccess) return e;
-    attr = true;
   }
-  launch_k(radix_sort_tokens_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT);
+  launch_k(radix_sort_tokens_kernel, dim3(1), dim3(1024), smem, st, keys, tok, BT, V, flags);
   const dim3 grid((unsigned)cdiv(BT, WTE_CH), (unsigned)cdiv(C / 4, 128));
   launch_k(wte_chunk_kernel, grid, dim3(128), 0, st, dwte, dres, keys, slots, BT, C);
   launch_k(wte_span_kernel, grid, dim3(128), 0, st, dwte, keys, slots, BT, C);
@@ -876,18 +903,14 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
   if (sums && (!dw || !db || !partial)) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)cdiv(rows, 8 * LNB_RPW);
   const size_t smem = sums ? (size_t)8 * 3 * C * sizeof(float) : 0;
-  static bool attr[2] = {false, false};
-  if (sums && !attr[sizeof(T) == 2]) {
+  if (sums) {
     const int mx = 8 * 3 * 2048 * (int)sizeof(float);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(layernorm_backward_kernel<T, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    attr[sizeof(T) == 2] = true;
+    for (auto k : {layernorm_backward_kernel<T, 1>, layernorm_backward_kernel<T, 2>, layernorm_backward_kernel<T, 3>,
+                   layernorm_backward_kernel<T, 4>, layernorm_backward_kernel<T, 6>, layernorm_backward_kernel<T, 8>,
+                   layernorm_backward_kernel<T, 12>, layernorm_backward_kernel<T, 16>}) {
+      cudaError_t e = kernel_smem_attr(k, mx);
+      if (e != cudaSuccess) return e;
+    }
   }
   float* part = sums ? partial : nullptr;
   const int rsum = dres_sum != nullptr;
@@ -897,15 +920,13 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
       const int pgrid = std::min(tc_num_sms(), reduce_chunks(rows));
       const int rpw = (int)cdiv(rows, (long long)pgrid * LNBP_WARPS);
       const size_t psmem = sums ? (size_t)LNBP_WARPS * 3 * C * sizeof(float) : 0;
-      static bool pattr = false;
-      if (!pattr) {
+      {
         const int mx = LNBP_WARPS * 3 * 1024 * (int)sizeof(float);
         for (auto k : {layernorm_backward_pipe_kernel<1>, layernorm_backward_pipe_kernel<2>,
                        layernorm_backward_pipe_kernel<3>, layernorm_backward_pipe_kernel<4>}) {
-          cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+          cudaError_t e = kernel_smem_attr(k, mx);
           if (e != cudaSuccess) return e;
         }
-        pattr = true;
       }
 #define LNBP(NVv)                                                                                            \
   launch_k(layernorm_backward_pipe_kernel<NVv>, dim3(pgrid), dim3(32 * LNBP_WARPS), psmem, st, dres,          \
@@ -1226,12 +1247,9 @@ bool gemm_skinny_supported(const GemmArgs& a) {
 
 template <typename T, int KCH, int NC>
 static cudaError_t skinny_launch(const GemmArgs& a, size_t smem, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<T, KCH, NC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  {
+    cudaError_t e = kernel_smem_attr(gemm_skinny_kernel<T, KCH, NC>, 200 * 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int grid = (int)std::min<long long>(cdiv(cdiv(a.N, NC), SKINNY_WARPS), 8LL * tc_num_sms());
   launch_k(gemm_skinny_kernel<T, KCH, NC>, dim3(grid), dim3(32 * SKINNY_WARPS), smem, st, a);
@@ -1914,12 +1932,9 @@ cudaError_t softmax_ce(T* logits, float* losses, const int* targets, int rows, i
   if constexpr (sizeof(T) == 2) {
     const size_t smem = (size_t)Vp * 2;
     if (smem <= 110 * 1024 && Vp >= 16384 && ((uintptr_t)logits & 15) == 0 && rows > 0) {
-      static bool attr = false;
-      if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(softmax_ce_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             110 * 1024);
+      {
+        cudaError_t e = kernel_smem_attr(softmax_ce_smem_kernel, 110 * 1024);
         if (e != cudaSuccess) return e;
-        attr = true;
       }
       launch_k(softmax_ce_smem_kernel, dim3(rows), dim3(SCE_SMEM_THREADS), smem, st, (bf16*)logits, losses, targets,
                V, Vp, dloss, write_grad, flags);
@@ -2029,8 +2044,7 @@ cudaError_t decode_attention(T* out, const T* qkv, int B, int Tmax, int pos, int
   if (B <= 0 || H <= 0 || C % H || hd > 128 || hd % N || pos < 0 || pos >= Tmax) return cudaErrorInvalidValue;
   const size_t smem = (size_t)(128 + 32 + Tmax + 256) * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attention_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = kernel_smem_attr(decode_attention_kernel<T>, (int)smem);
     if (e != cudaSuccess) return e;
   }
   launch_k(decode_attention_kernel<T>, dim3((unsigned)(B * H)), dim3(256), smem, st, out, qkv, Tmax, pos, C, H,

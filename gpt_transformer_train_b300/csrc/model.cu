@@ -524,11 +524,11 @@ struct Step {
       CK(m, colsum<T>(G(GPT2_QKVB), dqkv(0), BTi, 3 * Ci, 3 * Ci, part, st, Li, 3 * Ci, 3 * sBT, acc));
     }
     if (encoder_backward_fast_supported(BTi, Ci))
-      CK(m, encoder_backward_fast(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st,
-                                  acc));
+      CK(m, encoder_backward_fast(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, c.V, flags(),
+                                  m->at<uint32_t>(m->bl.keys), st, acc));
     else
-      CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, m->at<uint32_t>(m->bl.keys), st,
-                             acc));
+      CK(m, encoder_backward(G(GPT2_WTE), G(GPT2_WPE), dres(), tok, c.B, c.T, Ci, c.V, flags(),
+                             m->at<uint32_t>(m->bl.keys), st, acc));
     return GPT2_OK;
   }
 };

@@ -15,6 +15,8 @@
 // first call made on that device.  The sort kernel writes every key slot it
 // later reads, so nothing needs clearing between calls; calls that overlap
 // on the GPU (two streams, or two threads) share the array and race.
+// Tokens outside [0, V) are sorted past every real token and never scattered
+// (dwte is indexed only by checked tokens); they raise FLAG_TOKEN_RANGE.
 #include <mutex>
 
 #include "../../include/gpt2_ops.h"
@@ -42,12 +44,13 @@ uint32_t* keys_on_current_device() {
 }  // namespace
 
 extern "C" int gpt2_op_encoder_backward_noalloc(float* dwte, float* dwpe, const float* dres, const int32_t* tokens,
-                                                int B, int T, int C, void* stream) {
+                                                int B, int T, int C, int V, int* flags_dev, void* stream) {
   if (!dwte || !dwpe || !dres || !tokens || B <= 0 || T <= 0 || C <= 0 || C % 4) return GPT2_ERR_INVALID_ARG;
+  if (V <= 0 || V > 65535) return GPT2_ERR_INVALID_ARG;
   // the keys of B*T positions, padded to a power of two, must fit the array
   if ((long long)B * T > GPT2_NOALLOC_MAX_TOKENS) return GPT2_ERR_BUFFER_TOO_SMALL;
   uint32_t* keys = keys_on_current_device();
   if (!keys) return GPT2_ERR_CUDA;
-  cudaError_t e = encoder_backward(dwte, dwpe, dres, tokens, B, T, C, keys, (cudaStream_t)stream);
+  cudaError_t e = encoder_backward(dwte, dwpe, dres, tokens, B, T, C, V, flags_dev, keys, (cudaStream_t)stream);
   return e == cudaSuccess ? GPT2_OK : (e == cudaErrorInvalidValue ? GPT2_ERR_INVALID_ARG : GPT2_ERR_CUDA);
 }

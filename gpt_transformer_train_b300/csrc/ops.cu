@@ -31,12 +31,13 @@ size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T, int C) {
 }
 
 int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B, int T, int C,
-                             void* scratch, size_t scratch_bytes, void* stream) {
+                             int V, int* flags_dev, void* scratch, size_t scratch_bytes, void* stream) {
   if (!dwte || !dwpe || !dres || !tokens || !scratch || B <= 0 || T <= 0 || C <= 0 || C % 4) return GPT2_ERR_INVALID_ARG;
+  if (V <= 0 || V > 65535) return GPT2_ERR_INVALID_ARG;
   if ((long long)B * T > 32768 || scratch_bytes < gpt2_op_encoder_backward_scratch_bytes(B, T, C)) return GPT2_ERR_INVALID_ARG;
   if (encoder_backward_fast_supported(B * T, C))
-    return rc_of(encoder_backward_fast(dwte, dwpe, dres, tokens, B, T, C, scratch, ST(stream)));
-  return rc_of(encoder_backward(dwte, dwpe, dres, tokens, B, T, C, (uint32_t*)scratch, ST(stream)));
+    return rc_of(encoder_backward_fast(dwte, dwpe, dres, tokens, B, T, C, V, flags_dev, scratch, ST(stream)));
+  return rc_of(encoder_backward(dwte, dwpe, dres, tokens, B, T, C, V, flags_dev, (uint32_t*)scratch, ST(stream)));
 }
 
 int gpt2_op_residual_layernorm_forward(int dtype, void* resid_out, void* y, float* mean, float* rstd, const void* a,

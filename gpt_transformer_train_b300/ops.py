@@ -16,8 +16,8 @@ _P, _i, _ll, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.
 _sigs = {
     "gpt2_op_encoder_forward": (_i, [_i, _P, _P, _P, _P, _i, _i, _i, _i, _P, _P]),
     "gpt2_op_encoder_backward_scratch_bytes": (_sz, [_i, _i, _i]),
-    "gpt2_op_encoder_backward": (_i, [_P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
-    "gpt2_op_encoder_backward_noalloc": (_i, [_P, _P, _P, _P, _i, _i, _i, _P]),
+    "gpt2_op_encoder_backward": (_i, [_P, _P, _P, _P, _i, _i, _i, _i, _P, _P, _sz, _P]),
+    "gpt2_op_encoder_backward_noalloc": (_i, [_P, _P, _P, _P, _i, _i, _i, _i, _P, _P]),
     "gpt2_op_residual_layernorm_forward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _P]),
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
@@ -83,17 +83,22 @@ def gpt2_op_encoder_forward(out, tokens, wte, wpe, B, T, C, V, flags_dev, stream
                                     _s(stream)), "encoder_forward")
 
 
-def gpt2_op_encoder_backward(dwte, dwpe, dres, tokens, B, T, C, stream=None):
+def gpt2_op_encoder_backward(dwte, dwpe, dres, tokens, B, T, C, V=None, flags_dev=None, stream=None):
+    """V defaults to the row count of dwte."""
     n = lib.gpt2_op_encoder_backward_scratch_bytes(B, T, C)
     sc = _scratch(n, dres.device)
-    _ck(lib.gpt2_op_encoder_backward(_p(dwte), _p(dwpe), _p(dres), _p(tokens), B, T, C, _p(sc), sc.numel(),
-                                     _s(stream)), "encoder_backward")
+    V = dwte.shape[0] if V is None else V
+    _ck(lib.gpt2_op_encoder_backward(_p(dwte), _p(dwpe), _p(dres), _p(tokens), B, T, C, V, _p(flags_dev), _p(sc),
+                                     sc.numel(), _s(stream)), "encoder_backward")
 
 
-def gpt2_op_encoder_backward_noalloc(dwte, dwpe, dres, tokens, B, T, C, stream=None):
+def gpt2_op_encoder_backward_noalloc(dwte, dwpe, dres, tokens, B, T, C, V=None, flags_dev=None, stream=None):
     """Encoder backward whose scratch is a library-owned static device array
-    (no allocation by the library or here); returns the C status code."""
-    return lib.gpt2_op_encoder_backward_noalloc(_p(dwte), _p(dwpe), _p(dres), _p(tokens), B, T, C, _s(stream))
+    (no allocation by the library or here); returns the C status code.
+    V defaults to the row count of dwte."""
+    V = dwte.shape[0] if V is None else V
+    return lib.gpt2_op_encoder_backward_noalloc(_p(dwte), _p(dwpe), _p(dres), _p(tokens), B, T, C, V,
+                                                _p(flags_dev), _s(stream))
 
 
 def gpt2_op_residual_layernorm_forward(resid_out, y, mean, rstd, a, b, w, bias, rows, C, stream=None):

@@ -43,14 +43,17 @@ int gpt2_op_encoder_forward(int dtype, void* out, const int32_t* tokens, const v
                             int B, int T, int C, int V, int* flags_dev, void* stream);
 
 /* dwpe[t] += sum_b dres[b,t];  dwte[v] += sum of dres rows with token v, in a
- * fixed order (deterministic).  dres: float [B*T][C].  With B*T <= 16384 the
- * positions are grouped by a radix sort on the token and each token's sum is
- * taken over fixed chunks of the sorted positions (chunk partials added in
- * chunk order); otherwise a bitonic sort and one sum per token in position
- * order.  scratch: gpt2_op_encoder_backward_scratch_bytes(B, T, C) bytes. */
+ * fixed order (deterministic).  dres: float [B*T][C]; dwte: [V][C].  With
+ * B*T <= 16384 the positions are grouped by a radix sort on the token and
+ * each token's sum is taken over fixed chunks of the sorted positions (chunk
+ * partials added in chunk order); otherwise a bitonic sort and one sum per
+ * token in position order.  A position whose token is outside [0, V) adds
+ * nothing to dwte (its dwpe term still counts) and ORs 1 into *flags_dev
+ * (flags_dev may be NULL).  1 <= V <= 65535.
+ * scratch: gpt2_op_encoder_backward_scratch_bytes(B, T, C) bytes. */
 size_t gpt2_op_encoder_backward_scratch_bytes(int B, int T, int C);
 int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B, int T,
-                             int C, void* scratch, size_t scratch_bytes, void* stream);
+                             int C, int V, int* flags_dev, void* scratch, size_t scratch_bytes, void* stream);
 
 /* The same encoder backward without a scratch argument, for callers that
  * cannot allocate device memory: code running inside a host program that owns
@@ -64,12 +67,13 @@ int gpt2_op_encoder_backward(float* dwte, float* dwpe, const float* dres, const 
  * device, so make that first call before capturing any stream on it.  Calls
  * share the array: calls that overlap on the GPU race, and each call rewrites
  * every key slot it reads, so no state carries over between calls.
+ * Tokens are range-checked as in gpt2_op_encoder_backward (V, flags_dev).
  * Returns GPT2_ERR_BUFFER_TOO_SMALL when B*T exceeds GPT2_NOALLOC_MAX_TOKENS,
- * GPT2_ERR_INVALID_ARG for bad pointers or C % 4 != 0, GPT2_ERR_CUDA if the
- * array's address cannot be obtained or a launch fails. */
+ * GPT2_ERR_INVALID_ARG for bad pointers, C % 4 != 0 or V outside [1, 65535],
+ * GPT2_ERR_CUDA if the array's address cannot be obtained or a launch fails. */
 #define GPT2_NOALLOC_MAX_TOKENS 32768
 int gpt2_op_encoder_backward_noalloc(float* dwte, float* dwpe, const float* dres, const int32_t* tokens, int B,
-                                     int T, int C, void* stream);
+                                     int T, int C, int V, int* flags_dev, void* stream);
 
 /* r = a + b (b may be NULL: r = a, resid_out unused); y = (r - mean)*rstd*w + bias,
  * rstd = 1/sqrt(biased var + 1e-5); rows x C. */

@@ -110,6 +110,27 @@ def test_encoder_backward_deterministic_scatter(ops, B, T, C):
     assert np.array_equal(host(outs[0][1]).astype(np.float32), O.encoder_backward(dres, tok, V, T + 3)[1])
 
 
+@pytest.mark.parametrize("B,T", [(2, 100), (17, 1000)])
+def test_encoder_backward_out_of_range_tokens(ops, B, T):
+    """Both sort forms (radix up to 16384 positions, bitonic above): tokens
+    -1, V and V + 5 add nothing to dwte and raise the token flag; dwte has
+    65536 rows of which the first V are passed, the rest a guard band."""
+    C, V = 64, 500
+    tok, _ = zipf_tokens(B, T, V, 31)
+    tok[0, 3], tok[1, 50], tok[-1, -1] = -1, V + 5, V
+    good = ((tok >= 0) & (tok < V)).reshape(-1)
+    dres = normal_array((B * T, C), 32)
+    base = normal_array((65536, C), 33)
+    w, p, fl = dev(base), torch.zeros(T, C, device="cuda"), ops.flags()
+    ops.gpt2_op_encoder_backward(w, p, dev(dres), dev(tok, torch.int32), B, T, C, V=V, flags_dev=fl)
+    torch.cuda.synchronize()
+    assert fl[0].item() & 1
+    assert torch.equal(w[V:], dev(base[V:]))
+    ref = base[:V].astype(np.float64)
+    np.add.at(ref, tok.reshape(-1)[good], dres.astype(np.float64)[good])
+    assert np.max(np.abs(host(w[:V]) - ref)) < 1e-4
+
+
 @pytest.mark.parametrize("pattern", ["one_token", "blocks_of_32", "blocks_of_33", "ascending"])
 def test_encoder_backward_run_patterns(ops, pattern):
     """Token runs that fill whole sorted chunks, end exactly on a chunk
