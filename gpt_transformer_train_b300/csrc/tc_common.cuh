@@ -46,7 +46,8 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  Returns false when the
 // CTA's abort flag is set or when the wait has run for WAIT_NS (it then sets
 // the flag, so every other role of the CTA stops too).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = WAIT_NS) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; it++) {
     if (mbar_try(bar, parity)) return true;
@@ -54,7 +55,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       if (*abort_flag) return false;
       uint64_t now = gtimer();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > WAIT_NS) {
+      else if (now - t0 > limit_ns) {
         *abort_flag = 1;
         return false;
       }

@@ -40,6 +40,7 @@ _sigs = {
     "gpt2_op_gelu_backward": (_i, [_i, _P, _P, _P, _ll, _P]),
     "gpt2_op_colsum_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_colsum": (_i, [_i, _P, _P, _i, _i, _ll, _P, _sz, _P]),
+    "gpt2_op_wait_probe": (_i, [_i, _P, _P]),
 }
 for _n, (_r, _a) in _sigs.items():
     _fn = getattr(lib, _n)
@@ -196,3 +197,9 @@ def gpt2_op_colsum(out, X, rows, cols, ldx, stream=None):
     n = lib.gpt2_op_colsum_scratch_bytes(rows, cols)
     sc = _scratch(n, X.device)
     _ck(lib.gpt2_op_colsum(_dt(X), _p(out), _p(X), rows, cols, ldx, _p(sc), sc.numel(), _s(stream)), "colsum")
+
+
+def gpt2_op_wait_probe(limit_us, flags_dev, stream=None):
+    """Run the bounded-wait failure path on purpose; returns the C status code
+    (GPT2_ERR_TIMEOUT, -8, is the expected outcome)."""
+    return lib.gpt2_op_wait_probe(limit_us, _p(flags_dev), _s(stream))

@@ -207,6 +207,21 @@ size_t gpt2_op_colsum_scratch_bytes(int rows, int cols);
 int gpt2_op_colsum(int dtype, float* out, const void* X, int rows, int cols, long long ldx, void* scratch,
                    size_t scratch_bytes, void* stream);
 
+/* Check of the failure path of the tensor-core kernels' bounded waits (the
+ * llm.c tour's detail graph keeps long runs observable with an outlier
+ * detector; here a kernel that stops making progress must report it instead
+ * of hanging the GPU).  Launches one CTA that allocates tensor memory and
+ * waits on an mbarrier that nothing signals: one warp gives up after limit_us
+ * microseconds (1 .. 1000000) and raises the CTA's abort flag, the other warp
+ * (on the kernels' default limit) stops on that flag, the tensor memory is
+ * freed and FLAG_TIMEOUT (4) is ORed into *flags_dev -- the path every
+ * GEMM and attention kernel takes when a wait runs out.  Synchronises the
+ * stream and returns GPT2_ERR_TIMEOUT when the flag is set (the expected
+ * outcome), GPT2_OK if not, GPT2_ERR_INVALID_ARG for a bad limit, a NULL
+ * flags_dev or no tensor-core device, GPT2_ERR_CUDA if the launch fails.
+ * The device stays usable afterwards. */
+int gpt2_op_wait_probe(int limit_us, int* flags_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -182,18 +182,28 @@ def init_params(cfg: Config, seed: int, dtype=np.float32) -> dict:
     std_proj = 0.02 / math.sqrt(2.0 * cfg.L)
     params = {}
     off = 0
+
+    def normal_block(first, count, s):
+        # elements first .. first+count-1 of the stream, scaled and rounded,
+        # drawn a block at a time (each element depends only on its index)
+        a = np.empty(count, dtype=np.float32)
+        step = 1 << 22
+        for b in range(0, count, step):
+            e = min(count, b + step)
+            z = standard_normal_at(seed, np.arange(first + b, first + e, dtype=np.uint64))
+            a[b:e] = (z * s).astype(np.float32)
+        return a
+
     for name, shape in param_shapes(cfg):
         n = int(np.prod(shape))
         if name in ("wte", "wpe", "qkvw", "fcw", "attprojw", "fcprojw"):
             s = std_proj if name in ("attprojw", "fcprojw") else std
             if name == "wte":
                 nd = cfg.V * cfg.C
-                z = standard_normal_at(seed, np.arange(off, off + nd, dtype=np.uint64))
                 a = np.zeros(n, dtype=np.float32)
-                a[:nd] = (z * s).astype(np.float32)
+                a[:nd] = normal_block(off, nd, s)
             else:
-                z = standard_normal_at(seed, np.arange(off, off + n, dtype=np.uint64))
-                a = (z * s).astype(np.float32)
+                a = normal_block(off, n, s)
         elif name in ("ln1w", "ln2w", "lnfw"):
             a = np.ones(n, dtype=np.float32)
         else:

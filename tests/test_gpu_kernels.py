@@ -4,7 +4,9 @@ ragged sizes (rows not multiples of the tile, odd channel counts).
 
 Tolerances: fp32 kernels against the float64 oracle at 1e-5 relative (sum
 order only); bf16 kernels at the bf16 rounding scale, 2^-8 relative per
-stored element, with reductions done in fp32.
+stored element, with reductions done in fp32.  The tensor-core GEMM and
+attention kernels are also held to element-wise bounds (tests/parity.py): a
+single wrong element or tile fails them, which a norm would not show.
 """
 import math
 
@@ -13,6 +15,7 @@ import pytest
 import torch
 
 import oracle as O
+from parity import (check, gemm_ref, gemm_bound, gelu_bound, gelu_bwd_bound, attention_bounds, U8)
 from synthetic import normal_array, zipf_tokens
 
 pytestmark = pytest.mark.gpu
@@ -238,12 +241,6 @@ def test_layernorm_backward_overwrite(ops, rows, C):
 
 
 # ---------------------------------------------------------------------------
-def _gemm_ref(A, B, akm, bkm, M, N, K):
-    Am = A.reshape(M, K) if akm else A.reshape(K, M).T
-    Bn = B.reshape(N, K) if bkm else B.reshape(K, N).T
-    return Am @ Bn.T
-
-
 @pytest.mark.parametrize("dt", ["fp32", "bf16"])
 @pytest.mark.parametrize("akm,bkm", [(1, 1), (1, 0), (0, 0), (0, 1)])
 @pytest.mark.parametrize("M,N,K", [(65, 33, 17), (128, 192, 64), (200, 70, 300)])
@@ -253,7 +250,7 @@ def test_matmul_simt_layouts(ops, dt, akm, bkm, M, N, K):
     tA, tB = dev(A, DT[dt]), dev(B, DT[dt])
     D = torch.empty(M, N, device="cuda", dtype=DT[dt])
     ops.gpt2_op_matmul(tA, K if akm else M, akm, tB, K if bkm else N, bkm, M, N, K, D, N, path=ops.PATH_SIMT)
-    ref = _gemm_ref(host(tA), host(tB), akm, bkm, M, N, K)
+    ref, _ = gemm_ref(host(tA), host(tB), akm, bkm, M, N, K)
     tol = 1e-5 if dt == "fp32" else 2 ** -7
     assert rel_l2(host(D), ref) < tol
 
@@ -319,9 +316,10 @@ def test_matmul_tc_layouts(ops, akm, bkm, M, N, K):
     fl = ops.flags()
     ops.gpt2_op_matmul(tA, K if akm else M, akm, tB, K if bkm else N, bkm, M, N, K, D, N, path=ops.PATH_TC,
                        flags_dev=fl)
-    ref = _gemm_ref(host(tA), host(tB), akm, bkm, M, N, K)
+    ref, absprod = gemm_ref(host(tA), host(tB), akm, bkm, M, N, K)
     assert fl.sum().item() == 0
     assert rel_l2(host(D), ref) < 2 ** -7
+    check(host(D), ref, gemm_bound(ref, absprod), "D")
 
 
 # (12800, 400, 136): more tiles than CTA pairs, and edge tiles with an odd
@@ -331,23 +329,31 @@ def test_matmul_tc_layouts(ops, akm, bkm, M, N, K):
 def test_matmul_tc_epilogues(ops, M, N, K):
     A, B, bias = normal_array((M, K), 140), normal_array((N, K), 141), normal_array((N,), 142)
     tA, tB, tbias = dev(A, torch.bfloat16), dev(B, torch.bfloat16), dev(bias, torch.bfloat16)
-    acc = host(tA) @ host(tB).T
+    acc, absprod = gemm_ref(host(tA), host(tB), 1, 1, M, N, K)
+    hb = host(tbias)
     fl = ops.flags()
     D = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
     ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias, path=ops.PATH_TC, flags_dev=fl)
-    assert rel_l2(host(D), acc + host(tbias)) < 2 ** -7
+    assert rel_l2(host(D), acc + hb) < 2 ** -7
+    check(host(D), acc + hb, gemm_bound(acc + hb, absprod + np.abs(hb)), "D + bias")
     pre = torch.empty_like(D)
     ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, bias=tbias, aux=pre, ldaux=N, epilogue=ops.EPI_GELU,
                        path=ops.PATH_TC, flags_dev=fl)
-    assert rel_l2(host(pre), acc + host(tbias)) < 2 ** -7
-    assert rel_l2(host(D), O.gelu_forward(acc + host(tbias))) < 2 ** -7
+    assert rel_l2(host(pre), acc + hb) < 2 ** -7
+    assert rel_l2(host(D), O.gelu_forward(acc + hb)) < 2 ** -7
+    check(host(pre), acc + hb, gemm_bound(acc + hb, absprod + np.abs(hb)), "pre-activation")
+    g_ref = O.gelu_forward(host(pre))  # GELU of the stored pre-activation
+    check(host(D), g_ref, gelu_bound(g_ref, host(pre)), "GELU")
     D2 = torch.empty_like(D)
     ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D2, N, aux=pre, ldaux=N, epilogue=ops.EPI_GELU_BWD,
                        path=ops.PATH_TC, flags_dev=fl)
-    assert rel_l2(host(D2), O.gelu_backward(host(pre), acc)) < 2 ** -7
+    ref2 = O.gelu_backward(host(pre), acc)
+    assert rel_l2(host(D2), ref2) < 2 ** -7
+    check(host(D2), ref2, gelu_bwd_bound(ref2, acc, absprod, host(pre)), "acc * GELU'")
     F = dev(np.full((M, N), 0.25, np.float32))
     ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, F, N, epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC, flags_dev=fl)
     assert rel_l2(host(F), acc + 0.25) < 2e-5
+    check(host(F), acc + 0.25, gemm_bound(acc + 0.25, absprod, bf16_out=False), "F += acc")
     assert fl.sum().item() == 0
 
 
@@ -361,8 +367,10 @@ def test_matmul_tc_weight_gradient_pattern(ops):
     fl = ops.flags()
     ops.gpt2_op_matmul(tdy, N, 0, tx, K, 0, N, K, BT, dW, K, epilogue=ops.EPI_ACC_F32, path=ops.PATH_TC,
                        flags_dev=fl)
-    ref = W0 + host(tdy).T @ host(tx)
+    acc, absprod = gemm_ref(host(tdy), host(tx), 0, 0, N, K, BT)
+    ref = W0 + acc
     assert rel_l2(host(dW), ref) < 2e-5
+    check(host(dW), ref, gemm_bound(ref, absprod, bf16_out=False), "dW")
     assert fl.sum().item() == 0
 
 
@@ -387,8 +395,10 @@ def test_matmul_tc_split_k_weight_gradient(ops, BT, N, K):
     torch.cuda.synchronize()
     assert fl.sum().item() == 0
     assert torch.equal(outs[0], outs[1])
-    ref = W0.astype(np.float64) + host(tdy).T @ host(tx)
+    acc, absprod = gemm_ref(host(tdy), host(tx), 0, 0, N, K, BT)
+    ref = W0.astype(np.float64) + acc
     assert rel_l2(host(outs[0]), ref) < 2e-5
+    check(host(outs[0]), ref, gemm_bound(ref, absprod, bf16_out=False), "split-K dW")
 
 
 @pytest.mark.parametrize("path", ["tc", "simt"])
@@ -423,6 +433,8 @@ def test_matmul_batched_weight_gradient(ops, path, batch, BT, N, K, gap):
         Xz = hx[z * sX:z * sX + BT * K].reshape(BT, K).astype(np.float64)
         ref = W0[z * sW:z * sW + N * K].reshape(N, K) + Y.T @ Xz
         assert rel_l2(got[z * sW:z * sW + N * K].reshape(N, K), ref) < 2e-5, z
+        check(got[z * sW:z * sW + N * K].reshape(N, K), ref,
+              gemm_bound(ref, np.abs(Y).T @ np.abs(Xz), bf16_out=False), f"item {z}")
         # the gap rows between items are untouched
         assert np.array_equal(got[z * sW + N * K:(z + 1) * sW], W0[z * sW + N * K:(z + 1) * sW])
 
@@ -441,10 +453,15 @@ def test_matmul_rowdot_epilogue(ops, B, T, H, N):
     ops.gpt2_op_matmul_rowdot(tdy, N, tw, K, M, N, K, dX, K, to, K, D, T, H, fl)
     torch.cuda.synchronize()
     assert fl.sum().item() == 0
-    assert rel_l2(host(dX), host(tdy) @ host(tw)) < 2 ** -7
+    ref, absprod = gemm_ref(host(tdy), host(tw), 1, 0, M, K, N)
+    assert rel_l2(host(dX), ref) < 2 ** -7
+    check(host(dX), ref, gemm_bound(ref, absprod), "dX")
     x = host(dX).astype(np.float64).reshape(B, T, H, 64)
-    rD = (x * host(to).astype(np.float64).reshape(B, T, H, 64)).sum(-1).transpose(0, 2, 1)
+    o = host(to).astype(np.float64).reshape(B, T, H, 64)
+    rD = (x * o).sum(-1).transpose(0, 2, 1)
     assert np.max(np.abs(host(D).reshape(B, H, T) - rD)) < 1e-4 * max(1.0, np.abs(rD).max())
+    # D from the stored dX: an fp32 sum of 64 products per head
+    check(host(D).reshape(B, H, T), rD, 2.0 ** -20 * np.abs(x * o).sum(-1).transpose(0, 2, 1), "D")
 
 
 @pytest.mark.parametrize("epi", ["store", "gelu_bwd"])
@@ -466,9 +483,11 @@ def test_matmul_batched_bf16_epilogues(ops, epi):
     assert fl.sum().item() == 0
     hA, hB, got = host(tA), host(tB), host(D)
     for z in range(batch):
-        acc = hA[z] @ hB[z].T
+        acc, absprod = gemm_ref(hA[z], hB[z], 1, 1, M, N, K)
         ref = acc if epi == "store" else O.gelu_backward(host(pre)[z], acc)
         assert rel_l2(got[z], ref) < 2 ** -7, z
+        bound = gemm_bound(ref, absprod) if epi == "store" else gelu_bwd_bound(ref, acc, absprod, host(pre)[z])
+        check(got[z], ref, bound, f"item {z}")
 
 
 # ---------------------------------------------------------------------------
@@ -552,6 +571,17 @@ def test_attention_tc_against_oracle(ops, B, T, C, H, sigma):
     for part in range(3):
         a = host(dq).reshape(B, T, 3 * C)[..., part * C:(part + 1) * C]
         assert rel_l2(a, rd[..., part * C:(part + 1) * C]) < 2e-2, part
+    _check_attention_elementwise(qs, dos, host(out).reshape(B, T, C), host(dq).reshape(B, T, 3 * C), H)
+
+
+def _check_attention_elementwise(qs, dos, o, dqkv, H):
+    """O, dQ, dK, dV of the tensor-core kernels element by element against the
+    float64 oracle, within the bounds of tests/parity.py."""
+    C = qs.shape[-1] // 3
+    bd = attention_bounds(qs, dos, o, H)
+    check(o, *bd["out"], "O")
+    for part, name in enumerate(("dq", "dk", "dv")):
+        check(dqkv[..., part * C:(part + 1) * C], *bd[name], name)
 
 
 def test_attention_tc_deterministic(ops):
@@ -582,6 +612,30 @@ def test_attention_tc_full_size_sampled_heads(ops):
         rd = O.attention_backward(dos[b:b + 1, :, h * hd:(h + 1) * hd], sq, att, 1)
         for p in range(3):
             assert rel_l2(dq_all[b:b + 1, :, cols[p]], rd[..., p * hd:(p + 1) * hd]) < 2e-2, (b, h, p)
+        _check_attention_elementwise(sq, dos[b:b + 1, :, h * hd:(h + 1) * hd], o_all[b:b + 1, :, h * hd:(h + 1) * hd],
+                                     np.concatenate([dq_all[b:b + 1, :, c] for c in cols], -1), 1)
+
+
+@pytest.mark.parametrize("B,T", [(8, 2048), (4, 4096)])
+def test_attention_tc_long_context(ops, B, T):
+    """Long sequences at the 124M head layout (C=768, H=12) with the token
+    count of the per-kernel sweep (B*T = 16384): many key tiles per query
+    row, the online rescaling over up to 32 tiles, and the dS block buffer of
+    a 32-tile triangle.  Sampled (batch, head) pairs against the oracle,
+    element by element."""
+    C, H = 768, 12
+    hd = C // H
+    qkv = normal_array((B, T, 3 * C), 76)
+    dout = normal_array((B, T, C), 77)
+    tq, tdo, out, lse, dq, D = _attention_tc(ops, qkv, dout, B, T, C, H)
+    qs, dos = host(tq), host(tdo)
+    o_all, dq_all, lse_all = host(out).reshape(B, T, C), host(dq).reshape(B, T, 3 * C), host(lse).reshape(B, H, T)
+    for b, h in [(0, 0), (B - 1, 7)]:
+        cols = [slice(p * C + h * hd, p * C + (h + 1) * hd) for p in range(3)]
+        sq = np.concatenate([qs[b:b + 1, :, c] for c in cols], -1)
+        assert np.max(np.abs(lse_all[b, h] - _lse_ref(sq, 1, T, hd, 1)[0, 0])) < 2e-3
+        _check_attention_elementwise(sq, dos[b:b + 1, :, h * hd:(h + 1) * hd], o_all[b:b + 1, :, h * hd:(h + 1) * hd],
+                                     np.concatenate([dq_all[b:b + 1, :, c] for c in cols], -1), 1)
 
 
 def test_attention_tc_path_rejects_unsupported(ops):
@@ -667,6 +721,8 @@ def test_classifier_logit_stats_and_softmax(ops, rows, V, Vp, K):
     assert fl.sum().item() == 0
     zs = host(D)
     assert rel_l2(zs, host(tA) @ host(tB).T) < 2 ** -7
+    ref, absprod = gemm_ref(host(tA), host(tB), 1, 1, rows, Vp, K)
+    check(zs, ref, gemm_bound(ref, absprod), "logits")
     z = zs.astype(np.float64)
     st = host(stats)
     for n in range(tiles):
@@ -786,3 +842,30 @@ def test_colsum(ops, dt, rows, cols, ldx):
     out = dev(np.ones(cols, np.float32))
     ops.gpt2_op_colsum(out, tX, rows, cols, ldx)
     assert rel_l2(host(out), host(tX)[:, :cols].sum(0) + 1) < 1e-5
+
+
+# ---------------------------------------------------------------------------
+def test_bounded_wait_times_out_and_device_recovers(ops):
+    """The tensor-core kernels' failure path, run on purpose: a CTA holding
+    tensor memory waits on an mbarrier nothing signals; the wait gives up
+    after the 5 ms limit, the CTA frees its tensor memory and sets the timeout
+    flag, and the call reports GPT2_ERR_TIMEOUT.  A tensor-core GEMM right
+    after it on the same device gives the right result."""
+    import time
+    fl = ops.flags()
+    t0 = time.perf_counter()
+    rc = ops.gpt2_op_wait_probe(5000, fl)
+    dt = time.perf_counter() - t0
+    assert rc == -8
+    assert fl[0].item() & 4
+    assert 0.004 < dt < 5.0
+    M, N, K = 256, 256, 128
+    A, B = normal_array((M, K), 190), normal_array((N, K), 191)
+    tA, tB = dev(A, torch.bfloat16), dev(B, torch.bfloat16)
+    D = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    fl2 = ops.flags()
+    ops.gpt2_op_matmul(tA, K, 1, tB, K, 1, M, N, K, D, N, path=ops.PATH_TC, flags_dev=fl2)
+    torch.cuda.synchronize()
+    assert fl2.sum().item() == 0
+    ref, absprod = gemm_ref(host(tA), host(tB), 1, 1, M, N, K)
+    check(host(D), ref, gemm_bound(ref, absprod), "D after the timeout")
