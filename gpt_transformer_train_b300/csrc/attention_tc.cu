@@ -17,17 +17,12 @@
 // to tcgen05.mma as the A operand.  Accumulators live in TMEM.
 //
 // Forward (persistent: one CTA per SM walks the work items, an item being a
-// pair of 128-row query tiles of one (b, h); 576 threads): warp 0 issues TMA
-// (both Q tiles once, then K/V tiles through a ring), one thread of warp 1
-// issues S = Q K^T and O += P V (M=128, K=16 per instruction), warps 2-9 run
-// the online softmax of query tile 0 and warps 10-17 that of tile 1: two
-// warps share each row, one per 64-column half, and combine row maxima and
-// sums through shared memory.  The two tiles share
-// every K/V tile, and their softmax phases interleave on the tensor core.
-// Each softmax warp reads its 128 scores with four TMEM loads and one wait,
-// then releases the S accumulator at once, so the next Q K^T runs while it
-// computes the exponentials; O accumulates in TMEM
-// (rescaled in place only when a row's maximum jumps by more than 2^8).
+// pair of 128-row query tiles of one (b, h); 320 threads): warp 0 issues TMA,
+// one thread of warp 1 issues S = Q K^T and O += P [V | 1], and two softmax
+// warpgroups (one per query tile) hold one score row per thread.  P goes
+// back into TMEM over its own scores and is the A operand of the P V product,
+// whose B operand is V extended by a block of ones, so the row sums come out
+// of the tensor core beside O.  See attn_fwd_tc_kernel.
 //
 // Backward: two persistent kernels, so that no gradient is accumulated with
 // atomics (the result is deterministic).  The dQ kernel walks the key tiles of one
@@ -102,6 +97,14 @@ __device__ __forceinline__ float exp2_poly(float x) {
   const float q = fmaf(fmaf(fmaf(0.0550089069f, f, 0.242210984f), f, 0.693282962f), f, 1.f);
   return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
 }
+// (a0, a1) * b + (c, c) on the packed fp32 pipe: two FMAs in one instruction
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %5};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -124,7 +127,15 @@ struct AttnParams {
 // ============================================================================
 // forward
 // ============================================================================
-// 32 lanes x 32 consecutive fp32 columns into TMEM (the inverse of tmem_ld32)
+// TMEM accesses of one warp: 32 lanes x N consecutive 32-bit columns
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -135,23 +146,95 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, float& v) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  v = __uint_as_float(r);
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // 32 lanes x 128 consecutive fp32 columns, four loads in flight, one wait
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
 #pragma unroll
   for (int c = 0; c < 4; c++) tmem_ld32_async(taddr + 32 * c, *reinterpret_cast<float(*)[32]>(v + 32 * c));
   tmem_wait_ld();
 }
+// O (+)= P V with P read from TMEM (A operand, M=128 x K=16 per instruction:
+// 8 columns of packed bf16 pairs) and V from shared memory
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+constexpr int FWD_POLY = 16;  // one exponential in this many columns from the FMA-pipe polynomial
+// The probabilities of one 128-wide score row (TMEM lane r of the warp's
+// quarter, columns tS..tS+127): read 64 columns at a time, p = 2^(s sl2 -
+// m_ref), packed to bf16 pairs and written over the first 64 columns (behind
+// every read of the pass, so no score is overwritten before it is read).  One
+// exponential in FWD_POLY comes from the FMA-pipe polynomial, the rest from
+// the MUFU unit.  DIAG: the diagonal block, columns past the row masked to 0.
+template <bool DIAG>
+__device__ __forceinline__ void fwd_probs(uint32_t tS, uint32_t r, float sl2, float m_ref) {
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    float sv[64];
+    tmem_ld32_async(tS + 64 * h, *reinterpret_cast<float(*)[32]>(sv));
+    tmem_ld32_async(tS + 64 * h + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const int lc = 32 * c + e, col = 64 * h + lc;
+        float x0, x1;
+        ffma2(x0, x1, sv[lc], sv[lc + 1], sl2, -m_ref);
+        if (!DIAG) {
+          x0 = (col % FWD_POLY) == FWD_POLY - 2 ? exp2_poly(x0) : ex2(x0);
+          x1 = ex2(x1);
+        } else {
+          x0 = col > (int)r ? 0.f : ex2(x0);
+          x1 = col + 1 > (int)r ? 0.f : ex2(x1);
+        }
+        pk[e >> 1] = pack_bf16(x0, x1);
+      }
+      tmem_st16(tS + 32 * h + 16 * c, pk);
+    }
+  }
+}
 
 // Online softmax with a lazily rescaled accumulator: the probabilities of a
-// row are taken against a reference max m_ref; O (in TMEM) and the row sum l
-// are only rescaled when a new block's max exceeds m_ref by more than
-// RESCALE_LOG2 (then P stays <= 2^RESCALE_LOG2, harmless in fp32 and bf16).
-// The result is the same softmax: every term and l share one reference.
+// row are taken against a reference max m_ref; O (in TMEM) is only rescaled
+// when a new block's max exceeds m_ref by more than RESCALE_LOG2 (then P
+// stays <= 2^RESCALE_LOG2, harmless in fp32 and bf16).  The result is the
+// same softmax: every term and the row sum share one reference.
+//
+// Forward kernel layout (persistent, one CTA per SM, 320 threads): an item is
+// a pair of 128-row query tiles of one (b, h); warp 0 issues TMA (both Q tiles,
+// then K/V tiles through a ring), one thread of warp 1 issues the MMAs, warps
+// 2-5 run the softmax of query tile 0 and warps 6-9 that of tile 1, one
+// thread per query row with the whole 128-wide score row in registers.  Per
+// key block j and tile t:
+//   S_t = Q_t K_j^T                  (TMEM columns 128 t .. 128 t + 127)
+//   P_t = exp2(S_t sl2 - m_ref)      written as bf16 back over the first 64
+//                                     columns of S_t (no shared-memory trip)
+//   O_t += P_t [V_j | 1]             A = P_t from TMEM, B = V_j and a block of
+//                                     ones from shared memory: N = 80, so
+//                                     column 64 of O_t accumulates the row
+//                                     sum of the same bf16 P (free)
+// and S_t of block j+1 is issued right behind that P V (the tensor core takes
+// them in order, so it reads P_t before overwriting it).  The two tiles'
+// softmax phases interleave: one tile's exponentials overlap the other's MMAs.
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr int FWD_STAGES = 3;
 constexpr uint32_t FWD_KV = 2 * TILE;  // K tile then V tile
-constexpr size_t FWD_SMEM = 1024 + 2 * TILE + FWD_STAGES * FWD_KV + 2 * PTILE + 256 + (2 * 2 * 2 + 2 * 2) * 128 * 4;
-constexpr int FWD_THREADS = 64 + 32 * 16;  // producer, MMA, 16 softmax warps
+constexpr int FWD_ON = 80;             // P V width: 64 value columns + the row-sum column (+ 15 unused)
+constexpr size_t FWD_SMEM = 1024 + 2 * TILE + FWD_STAGES * FWD_KV + TILE + 256;
+constexpr int FWD_THREADS = 64 + 32 * 8;  // producer, MMA, two softmax warpgroups
 
 // Persistent: each CTA takes work items blockIdx.x, blockIdx.x + gridDim.x, ...
 // (item = one pair of query tiles of one (b, h), heaviest first).  Every
@@ -162,21 +245,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sQ = smem_u32(smem);                  // 2 query tiles
   const uint32_t sKV = sQ + 2 * TILE;                  // ring of K/V tiles
-  const uint32_t sP = sKV + FWD_STAGES * FWD_KV;       // P tile of each query tile (128 x 128)
-  uint64_t* bars = (uint64_t*)(smem + 2 * TILE + FWD_STAGES * FWD_KV + 2 * PTILE);
+  const uint32_t sOnes = sKV + FWD_STAGES * FWD_KV;    // 128 x 64 bf16 ones: the row-sum columns of V
+  uint64_t* bars = (uint64_t*)(smem + 2 * TILE + FWD_STAGES * FWD_KV + TILE);
   const uint32_t b_qfull = smem_u32(bars), b_qempty = b_qfull + 8;
   const uint32_t b_kvfull = b_qempty + 8, b_kvempty = b_kvfull + 8 * FWD_STAGES;
   const uint32_t b_sfull = b_kvempty + 8 * FWD_STAGES;  // [2] S of tile t computed
-  const uint32_t b_sfree = b_sfull + 16;                // [2] S of tile t read by its softmax warps
-  const uint32_t b_pfull = b_sfree + 16;                // [2] P of tile t written
-  const uint32_t b_pempty = b_pfull + 16;               // [2] P V of tile t done with it (O updated)
-  const uint32_t b_ofree = b_pempty + 16;               // [2] finished O of tile t read out
-  uint32_t* tmem_holder = (uint32_t*)(bars + 2 + 2 * FWD_STAGES + 10);
+  const uint32_t b_pfull = b_sfull + 16;                // [2] P of tile t written (4 warps)
+  const uint32_t b_pvdone = b_pfull + 16;               // [2] a P V of tile t completed
+  const uint32_t b_ofree = b_pvdone + 16;               // [2] finished O of tile t read out (4 warps)
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 + 2 * FWD_STAGES + 8);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
-  // row statistics exchanged between the two warps that share a row:
-  // red[block parity][tile][half][row] (maxima), then lsum[tile][half][row]
-  float* red = (float*)(smem + 2 * TILE + FWD_STAGES * FWD_KV + 2 * PTILE + 256);
-  float* lsum = red + 2 * 2 * 2 * 128;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = p.T / 128, npair = (nq + 1) / 2;
@@ -205,14 +283,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
     }
     for (int t = 0; t < 2; t++) {
       mbar_init(b_sfull + 8 * t, 1);
-      mbar_init(b_sfree + 8 * t, 8);
-      mbar_init(b_ofree + 8 * t, 8);
-      mbar_init(b_pfull + 8 * t, 8);
-      mbar_init(b_pempty + 8 * t, 1);
+      mbar_init(b_pfull + 8 * t, 4);
+      mbar_init(b_pvdone + 8 * t, 1);
+      mbar_init(b_ofree + 8 * t, 4);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // the ones block (bf16 1.0 everywhere, so its swizzle does not matter)
+  for (uint32_t o = threadIdx.x * 16; o < TILE; o += FWD_THREADS * 16) st_shared_v4(sOnes + o, 0x3f803f80u, 0x3f803f80u,
+                                                                                        0x3f803f80u, 0x3f803f80u);
+  fence_async_smem();
   if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
   if (warp == 0 && lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tqkv) : "memory");
   fence_before();
@@ -220,7 +301,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
   fence_after();
   const uint32_t tmem = *tmem_holder;
   pdl_enter();  // global memory only from here on
-  // TMEM columns: S of tile t at 128 t, O of tile t at 256 + 64 t
+  // TMEM columns: S (and P) of tile t at 128 t, O of tile t at 256 + 128 t (80 wide)
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer
@@ -245,45 +326,42 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ---- MMA issuer
-      constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);  // S = Q K^T
-      constexpr uint32_t ID_O = idesc_bf16(128, HD, 0, 1);   // O += P V (V is MN-major)
-      uint32_t g0 = 0, n = 0;                 // K/V blocks before this item, items so far
-      uint32_t nS[2] = {0, 0}, nP[2] = {0, 0}, nO[2] = {0, 0};  // per tile: S issued, P V issued, items
-      int kv_ready = -1;                      // highest K/V block known loaded (global index)
+      constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);     // S = Q K^T
+      constexpr uint32_t ID_O = idesc_bf16(128, FWD_ON, 0, 1);  // O += P [V | 1] (V is MN-major)
+      uint32_t g0 = 0, n = 0;                                   // K/V blocks before this item, items so far
+      uint32_t nP[2] = {0, 0}, nO[2] = {0, 0};                  // per tile: P blocks consumed, items finished
+      int kv_ready = -1;                                        // highest K/V block known loaded (global index)
       bool ok = true;
       for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
         const Item it = item(i);
+        const int last_t = it.two ? 1 : 0;
         auto active = [&](int t, int j) { return t == 0 ? j <= it.qt0 : (it.two && j <= it.qt0 + 1); };
         auto wait_kv = [&](int j) {
           const int gj = (int)g0 + j;
           if (kv_ready >= gj) return true;
           if (!mbar_wait(b_kvfull + 8 * (gj % FWD_STAGES), (gj / FWD_STAGES) & 1, abort_flag)) return false;
           kv_ready = gj;
-          fence_after();
           return true;
         };
-        // S of tile t for block j; S of the tile must have been read out first
         auto issue_s = [&](int t, int j) {
-          if (nS[t] > 0 && !mbar_wait(b_sfree + 8 * t, (nS[t] - 1) & 1, abort_flag)) return false;
           if (!wait_kv(j)) return false;
           fence_after();
           const uint32_t k = sKV + ((g0 + j) % FWD_STAGES) * FWD_KV, q = sQ + t * TILE;
 #pragma unroll
           for (int kk = 0; kk < HD / 16; kk++) mma_bf16(tmem + 128 * t, desc_k(q, kk), desc_k(k, kk), ID_S, kk > 0);
           mma_commit(b_sfull + 8 * t);
-          nS[t]++;
+          // the item's last Q K^T: the Q tiles may be reloaded once it completes
+          if (t == last_t && j == it.nkv - 1) mma_commit(b_qempty);
           return true;
         };
         if (!mbar_wait(b_qfull, n & 1, abort_flag)) break;
         fence_after();
         ok = issue_s(0, 0) && (!active(1, 0) || issue_s(1, 0));
-        if (ok && it.nkv == 1) mma_commit(b_qempty);
         for (int j = 0; ok && j < it.nkv; j++) {
-          // next scores first: S of tile t is free as soon as its softmax warps have read it
-          for (int t = 0; t < 2 && ok; t++)
-            if (j + 1 < it.nkv && active(t, j + 1)) ok = issue_s(t, j + 1);
-          if (ok && j + 2 == it.nkv) mma_commit(b_qempty);  // the item's last Q K^T is issued
           const uint32_t v = sKV + ((g0 + j) % FWD_STAGES) * FWD_KV + TILE;
+          // V and the ones block are one MN-major operand of N = 80 columns:
+          // the ones sit at a fixed distance after this stage's V tile
+          const uint32_t lbo = sOnes - v;
           for (int t = 0; t < 2 && ok; t++) {
             if (!active(t, j)) continue;
             if (!mbar_wait(b_pfull + 8 * t, nP[t] & 1, abort_flag)) { ok = false; break; }
@@ -293,12 +371,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
               break;
             }
             fence_after();
-            const uint32_t pt = sP + t * PTILE;
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; kk++)
-              mma_bf16(tmem + 256 + HD * t, desc_k128(pt, kk), desc_mn(v, kk), ID_O, (j | kk) > 0);
-            mma_commit(b_pempty + 8 * t);
+              mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, sdesc(v + kk * 2048, lbo, 1024), ID_O,
+                          (j | kk) > 0);
+            mma_commit(b_pvdone + 8 * t);
             nP[t]++;
+            // the next scores of this tile, behind the P V that reads P from the same columns
+            if (active(t, j + 1) && !issue_s(t, j + 1)) { ok = false; break; }
           }
           if (ok) mma_commit(b_kvempty + 8 * ((g0 + j) % FWD_STAGES));
         }
@@ -307,118 +387,88 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
         g0 += it.nkv;
       }
     }
-  } else {  // ---- softmax warps: tile t, TMEM lane quarter q, column half hf; one row per thread pair
-    const int wt = warp - 2;
-    const int t = wt >> 3, hf = (wt >> 2) & 1, q = warp & 3;
-    const uint32_t r = q * 32 + lane;             // row inside the tile
+  } else {  // ---- softmax warps: tile t, TMEM lane quarter q; one query row per thread
+    const int t = (warp - 2) >> 2, q = warp & 3;
+    const uint32_t r = q * 32 + lane;  // row inside the tile
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
-    const uint32_t tS = tmem + lrow + 128 * t + 64 * hf, tO = tmem + lrow + 256 + HD * t + 32 * hf;
-    const int bar_id = 1 + 4 * t + q;             // named barrier of the two warps sharing these rows
-    float* my_red = red + (t * 2 + hf) * 128 + r;
-    const float* peer_red = red + (t * 2 + (hf ^ 1)) * 128 + r;
-    uint32_t nS = 0, nP = 0;                      // S blocks consumed, P blocks produced
+    const uint32_t tS = tmem + lrow + 128 * t, tO = tmem + lrow + 256 + 128 * t;
+    uint32_t nS = 0, nPV = 0;  // S blocks consumed; P V products of this tile before the current item
     bool ok = true;
     for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
       const Item it = item(i);
       const int qt = it.qt0 + t;
-      if (qt >= nq) continue;                     // this item has no tile t
-      float m_ref = -INFINITY, l = 0.f;
+      if (qt >= nq) continue;  // this item has no tile t
+      float m_ref = -INFINITY;
       for (int j = 0; j <= qt; j++) {
         if (!mbar_wait_warp(b_sfull + 8 * t, nS & 1, abort_flag)) { ok = false; break; }
-        fence_after();
-        float sv[64];
-        tmem_ld32_async(tS, *reinterpret_cast<float(*)[32]>(sv));
-        tmem_ld32_async(tS + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
-        tmem_wait_ld();
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_sfree + 8 * t);  // the MMA may overwrite S now
-        const int c0 = 64 * hf;                      // first column of this half
-        const bool diag = j == qt;
-        // row maximum: four independent chains, then the partner half through shared memory
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (!diag) {
-#pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            m4[0] = max3(m4[0], sv[c], sv[c + 1]);
-            m4[1] = max3(m4[1], sv[c + 2], sv[c + 3]);
-            m4[2] = max3(m4[2], sv[c + 4], sv[c + 5]);
-            m4[3] = max3(m4[3], sv[c + 6], sv[c + 7]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c++)
-            if (c0 + c <= (int)r) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
-        }
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        float* slot = my_red + (nS & 1) * 512;
-        *slot = mx;
-        asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
-        mx = fmaxf(mx, peer_red[(nS & 1) * 512]) * p.sl2;
         nS++;
-        // move the reference when this block's max runs too far above it; O and
-        // l are rescaled below, once the probabilities no longer need registers
-        const bool need = j > 0 && mx > m_ref + RESCALE_LOG2;
-        const float m_old = j == 0 ? mx : m_ref;
-        if (j == 0 || need) m_ref = mx;
-        // the P tile is free, and O holds every earlier block, once the previous P V is done
-        const uint32_t pt = sP + t * PTILE;
-        if (nP >= 1 && !mbar_wait_warp(b_pempty + 8 * t, (nP - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
         fence_after();
-        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool diag = j == qt;
+        float mx;
+        {  // pass 1: the row maximum over the valid columns (c <= r on the diagonal block)
+          float sv[128];
+          tmem_ld128(tS, sv);
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (!diag) {
 #pragma unroll
-        for (int c = 0; c < 2; c++) {
-          float(&pv)[32] = *reinterpret_cast<float(*)[32]>(sv + 32 * c);  // probabilities overwrite the scores
+            for (int c = 0; c < 128; c += 8) {
+              m4[0] = max3(m4[0], sv[c], sv[c + 1]);
+              m4[1] = max3(m4[1], sv[c + 2], sv[c + 3]);
+              m4[2] = max3(m4[2], sv[c + 4], sv[c + 5]);
+              m4[3] = max3(m4[3], sv[c + 6], sv[c + 7]);
+            }
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; e++) {
-            const float x = fmaf(pv[e], p.sl2, -m_ref);
-            pv[e] = (e & 3) == 3 ? exp2_poly(x) : ex2(x);
+            for (int c = 0; c < 128; c++)
+              if (c <= (int)r) m4[c & 3] = fmaxf(m4[c & 3], sv[c]);
           }
-          if (diag) {
-#pragma unroll
-            for (int e = 0; e < 32; e++)
-              if (c0 + 32 * c + e > (int)r) pv[e] = 0.f;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; e++) rs4[e & 3] += pv[e];
-          store_row32(pt, r, c0 + 32 * c, pv);
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.sl2;
         }
+        // move the reference when this block's max runs too far above it
+        const bool need = j > 0 && mx > m_ref + RESCALE_LOG2;
+        const float m_old = m_ref;
+        if (j == 0 || need) m_ref = mx;
+        // pass 2: the scores again, 64 columns at a time; probabilities packed
+        // to bf16 pairs over the first 64 columns of S
+        if (!diag) fwd_probs<false>(tS, r, p.sl2, m_ref);
+        else fwd_probs<true>(tS, r, p.sl2, m_ref);
         if (__any_sync(0xffffffffu, need)) {
+          // O holds blocks 0 .. j-1 once the previous P V has completed
+          if (!mbar_wait_warp(b_pvdone + 8 * t, (nPV + j - 1) & 1, abort_flag)) { ok = false; break; }
+          fence_after();
           const float alpha = need ? ex2(m_old - m_ref) : 1.f;
           float ov[32];
-          tmem_ld32(tO, ov);
 #pragma unroll
-          for (int e = 0; e < 32; e++) ov[e] *= alpha;
-          tmem_st32(tO, ov);
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          l *= alpha;
+          for (int c = 0; c < 3; c++) {  // 64 value columns and the row sum (column 64)
+            tmem_ld32(tO + 32 * c, ov);
+#pragma unroll
+            for (int e = 0; e < 32; e++) ov[e] *= alpha;
+            tmem_st32(tO + 32 * c, ov);
+          }
         }
-        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        tmem_wait_st();
         fence_before();
-        fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_pfull + 8 * t);
-        nP++;
       }
       if (!ok) break;
-      // the row sum is split over the two halves
-      lsum[(t * 2 + hf) * 128 + r] = l;
-      // the item's last P V completes the accumulator
-      if (!mbar_wait_warp(b_pempty + 8 * t, (nP - 1) & 1, abort_flag)) break;
+      // the item's last P V completes the accumulator and the row sum
+      if (!mbar_wait_warp(b_pvdone + 8 * t, (nPV + qt) & 1, abort_flag)) break;
+      nPV += qt + 1;
       fence_after();
-      float o[32];
-      tmem_ld32(tO, o);
+      float o[64], lt;
+      tmem_ld32_async(tO, *reinterpret_cast<float(*)[32]>(o));
+      tmem_ld32_async(tO + 32, *reinterpret_cast<float(*)[32]>(o + 32));
+      tmem_ld1(tO + 64, lt);
+      tmem_wait_ld();
       fence_before();
-      asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");  // both halves stored l and read O
+      __syncwarp();
       if (lane == 0) mbar_arrive(b_ofree + 8 * t);  // the next item may overwrite O
-      const float lt = l + lsum[(t * 2 + (hf ^ 1)) * 128 + r];
-      bf16* dst = p.out + (size_t)(it.row0 + qt * 128 + r) * p.C + it.h * HD + 32 * hf;
-      store_global32(dst, o, 1.f / lt);
-      if (hf == 0) p.lse[((size_t)it.b * p.H + it.h) * p.T + qt * 128 + r] = (m_ref + log2f(lt)) * LN2;
-      // lsum is rewritten by the next item only after both halves pass the next block's barrier
+      bf16* dst = p.out + (size_t)(it.row0 + qt * 128 + r) * p.C + it.h * HD;
+      const float inv = 1.f / lt;
+      store_global32(dst, *reinterpret_cast<float(*)[32]>(o), inv);
+      store_global32(dst + 32, *reinterpret_cast<float(*)[32]>(o + 32), inv);
+      p.lse[((size_t)it.b * p.H + it.h) * p.T + qt * 128 + r] = (m_ref + log2f(lt)) * LN2;
     }
   }
   fence_before();

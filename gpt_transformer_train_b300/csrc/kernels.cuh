@@ -96,6 +96,16 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
                                const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
                                float* db, float* dres_sum, float* partial, cudaStream_t st,
                                int* deferred_chunks = nullptr);
+// The same with the residual gradient passed along in its own type RT (the
+// activation type in the training step, float in fp32 mode):
+//   rout = (rin ? rin : 0) + dx; rcopy (T) and rf32 (float) optional copies of
+//   the new value (before rounding to RT); rout may be null when rf32 is given;
+//   rin may equal rout.  RT = bf16 only with T = bf16.
+template <typename T, typename RT>
+cudaError_t layernorm_backward_rg(RT* rout, const RT* rin, T* rcopy, float* rf32, const T* dy, const T* x,
+                                  const float* mean, const float* rstd, const T* w, int rows, int C, float* dw,
+                                  float* db, float* dres_sum, float* partial, cudaStream_t st,
+                                  int* deferred_chunks = nullptr);
 // With deferred_chunks, layernorm_backward only writes its per-chunk partial
 // sums (partial[chunk][3][C]) and stores the chunk count there; the sums are
 // added later by reduce_partials, possibly for several calls at once:

@@ -670,12 +670,28 @@ __device__ __forceinline__ void block_column_sum(float (&acc)[NV][N], float* sh,
 // the block adds the eight slices in warp order into partial[block][3][C] for
 // dw, db and the bias gradient of the projection whose output gradient dres is.
 // ============================================================================
+// The residual gradient passes from rin to rout in its own type RT (float,
+// or the activation type: the training step's bf16 form):
+//   rout = (rin ? rin : 0) + dx, rcopy (optional, T) and rf32 (optional,
+//   float) receive the same new value; rout may be null when rf32 is given,
+//   and rin may equal rout (in place).
 constexpr int LNB_RPW = 8;
-template <typename T, int NV>
+// 8 consecutive values of a residual-gradient row, as floats
+__device__ __forceinline__ void ld8(const float* p, float (&f)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p)), b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const bf16* p, float (&f)[8]) { ld16_cs(p, f); }
+__device__ __forceinline__ void st8(float* p, const float (&f)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+__device__ __forceinline__ void st8(bf16* p, const float (&f)[8]) { st16(p, f); }
+template <typename T, typename RT, int NV>
 __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kernel(
-    float* __restrict__ dres, T* __restrict__ dres_c, const T* __restrict__ dy, const T* __restrict__ x,
-    const float* __restrict__ mean, const float* __restrict__ rstd, const T* __restrict__ w, int rows, int C,
-    int accumulate, float* __restrict__ partial, int want_rsum) {
+    RT* rout, const RT* rin, T* __restrict__ rcopy, float* __restrict__ rf32, const T* __restrict__ dy,
+    const T* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd, const T* __restrict__ w,
+    int rows, int C, float* __restrict__ partial, int want_rsum) {
   pdl_enter();
   constexpr int N = VecN<T>::n;
   extern __shared__ float lnb_sh[];  // [8 warps][3][N][nvec] when partial
@@ -703,11 +719,21 @@ __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kerne
         ld16(w + vi * N, wv);
         // the incoming residual gradient, fetched with the row rather than after the reductions
 #pragma unroll
-        for (int k = 0; k < N; k += 4) {
-          float a4[4] = {0.f, 0.f, 0.f, 0.f};
-          if (accumulate) ld16_cs(dres + (size_t)row * C + vi * N + k, a4);
+        for (int k = 0; k < N; k++) acc_in[i][k] = 0.f;
+        if (rin) {
+          if constexpr (sizeof(RT) == 4) {
 #pragma unroll
-          for (int u = 0; u < 4; u++) acc_in[i][k + u] = a4[u];
+            for (int k = 0; k < N; k += 4) {
+              float a4[4];
+              ld16_cs(reinterpret_cast<const float*>(rin) + (size_t)row * C + vi * N + k, a4);
+#pragma unroll
+              for (int u = 0; u < 4; u++) acc_in[i][k + u] = a4[u];
+            }
+          } else {
+            static_assert(sizeof(RT) == 4 || N == 8, "a bf16 residual gradient goes with bf16 rows");
+            ld16_cs(reinterpret_cast<const bf16*>(rin) + (size_t)row * C + vi * N,
+                    *reinterpret_cast<float(*)[8]>(acc_in[i]));
+          }
         }
 #pragma unroll
         for (int k = 0; k < N; k++) {
@@ -734,13 +760,26 @@ __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kerne
         float o[N];
 #pragma unroll
         for (int k = 0; k < N; k++) o[k] = acc_in[i][k] + (dn[i][k] - s1 - xh[i][k] * s2) * rs;
-        float* dst = dres + (size_t)row * C + vi * N;
+        if (rout) {
+          if constexpr (sizeof(RT) == 4) {
+            float* dst = reinterpret_cast<float*>(rout) + (size_t)row * C + vi * N;
 #pragma unroll
-        for (int k = 0; k < N; k += 4) {
-          float r4[4] = {o[k], o[k + 1], o[k + 2], o[k + 3]};
-          st16(dst + k, r4);
+            for (int k = 0; k < N; k += 4) {
+              float r4[4] = {o[k], o[k + 1], o[k + 2], o[k + 3]};
+              st16(dst + k, r4);
+            }
+          } else {
+            st16(reinterpret_cast<T*>(rout) + (size_t)row * C + vi * N, o);
+          }
         }
-        if (dres_c) st16(dres_c + (size_t)row * C + vi * N, o);
+        if (rcopy) st16(rcopy + (size_t)row * C + vi * N, o);
+        if (rf32) {
+#pragma unroll
+          for (int k = 0; k < N; k += 4) {
+            float r4[4] = {o[k], o[k + 1], o[k + 2], o[k + 3]};
+            st16(rf32 + (size_t)row * C + vi * N + k, r4);
+          }
+        }
         if (partial && want_rsum) {
 #pragma unroll
           for (int k = 0; k < N; k++) acc[(2 * N + k) * nvec + vi] += o[k];
@@ -790,11 +829,11 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
     f[2 * i + 1] = t.y;
   }
 }
-template <int NV>
+template <typename RT, int NV>
 __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_kernel(
-    float* __restrict__ dres, bf16* __restrict__ dres_c, const bf16* __restrict__ dy, const bf16* __restrict__ x,
-    const float* __restrict__ mean, const float* __restrict__ rstd, const bf16* __restrict__ w, int rows, int C,
-    int accumulate, float* __restrict__ partial, int want_rsum, int rpw) {
+    RT* rout, const RT* rin, bf16* __restrict__ rcopy, float* __restrict__ rf32, const bf16* __restrict__ dy,
+    const bf16* __restrict__ x, const float* __restrict__ mean, const float* __restrict__ rstd,
+    const bf16* __restrict__ w, int rows, int C, float* __restrict__ partial, int want_rsum, int rpw) {
   pdl_enter();
   constexpr int N = 8;
   extern __shared__ float lnb_sh[];  // [LNBP_WARPS][3][N][nvec] when partial
@@ -820,16 +859,13 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
     }
     if (row + 1 < r1) lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)(row + 1) * C, lane, nvec);
     const float mu = mean[row], rs = rstd[row];
-    float4 din[NV][2];
+    float din[NV][N];
 #pragma unroll
     for (int i = 0; i < NV; i++) {
       const int vi = lane + i * 32;
-      din[i][0] = din[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (accumulate && vi < nvec) {
-        const float4* src = reinterpret_cast<const float4*>(dres + (size_t)row * C) + 2 * vi;
-        din[i][0] = __ldcs(src);
-        din[i][1] = __ldcs(src + 1);
-      }
+#pragma unroll
+      for (int k = 0; k < N; k++) din[i][k] = 0.f;
+      if (rin && vi < nvec) ld8(rin + (size_t)row * C + vi * N, din[i]);
     }
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
@@ -862,17 +898,14 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
         unpack_bf16x8(cdy[i], dv);
         unpack_bf16x8(cx[i], xv);
         unpack_bf16x8(wv[i], ww);
-        const float a[N] = {din[i][0].x, din[i][0].y, din[i][0].z, din[i][0].w,
-                            din[i][1].x, din[i][1].y, din[i][1].z, din[i][1].w};
 #pragma unroll
         for (int k = 0; k < N; k++) {
           const float xh = (xv[k] - mu) * rs, dn = dv[k] * ww[k];
-          o[k] = a[k] + (dn - s1 - xh * s2) * rs;
+          o[k] = din[i][k] + (dn - s1 - xh * s2) * rs;
         }
-        float4* dst = reinterpret_cast<float4*>(dres + (size_t)row * C) + 2 * vi;
-        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-        if (dres_c) st16(dres_c + (size_t)row * C + vi * N, o);
+        if (rout) st8(rout + (size_t)row * C + vi * N, o);
+        if (rcopy) st16(rcopy + (size_t)row * C + vi * N, o);
+        if (rf32) st8(rf32 + (size_t)row * C + vi * N, o);
         if (partial && want_rsum) {
 #pragma unroll
           for (int k = 0; k < N; k++) acc[(2 * N + k) * nvec + vi] += o[k];
@@ -893,10 +926,12 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
   }
 }
 
-template <typename T>
-cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
-                               const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
-                               float* db, float* dres_sum, float* partial, cudaStream_t st, int* deferred_chunks) {
+template <typename T, typename RT>
+cudaError_t layernorm_backward_rg(RT* rout, const RT* rin, T* rcopy, float* rf32, const T* dy, const T* x,
+                                  const float* mean, const float* rstd, const T* w, int rows, int C, float* dw,
+                                  float* db, float* dres_sum, float* partial, cudaStream_t st, int* deferred_chunks) {
+  static_assert(sizeof(RT) == 4 || sizeof(T) == 2, "a bf16 residual gradient goes with bf16 rows");
+  if (!rout && !rf32) return cudaErrorInvalidValue;
   constexpr int N = VecN<T>::n;
   const int nvec = C / N;
   const bool sums = dw || db || dres_sum;
@@ -905,9 +940,10 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
   const size_t smem = sums ? (size_t)8 * 3 * C * sizeof(float) : 0;
   if (sums) {
     const int mx = 8 * 3 * 2048 * (int)sizeof(float);
-    for (auto k : {layernorm_backward_kernel<T, 1>, layernorm_backward_kernel<T, 2>, layernorm_backward_kernel<T, 3>,
-                   layernorm_backward_kernel<T, 4>, layernorm_backward_kernel<T, 6>, layernorm_backward_kernel<T, 8>,
-                   layernorm_backward_kernel<T, 12>, layernorm_backward_kernel<T, 16>}) {
+    for (auto k : {layernorm_backward_kernel<T, RT, 1>, layernorm_backward_kernel<T, RT, 2>,
+                   layernorm_backward_kernel<T, RT, 3>, layernorm_backward_kernel<T, RT, 4>,
+                   layernorm_backward_kernel<T, RT, 6>, layernorm_backward_kernel<T, RT, 8>,
+                   layernorm_backward_kernel<T, RT, 12>, layernorm_backward_kernel<T, RT, 16>}) {
       cudaError_t e = kernel_smem_attr(k, mx);
       if (e != cudaSuccess) return e;
     }
@@ -915,23 +951,24 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
   float* part = sums ? partial : nullptr;
   const int rsum = dres_sum != nullptr;
   if constexpr (sizeof(T) == 2) {
-    if (nvec <= 128 && ((uintptr_t)dres & 15) == 0 && ((uintptr_t)w & 15) == 0) {
+    if (nvec <= 128 && ((uintptr_t)rout & 15) == 0 && ((uintptr_t)rin & 15) == 0 && ((uintptr_t)rf32 & 15) == 0 &&
+        ((uintptr_t)w & 15) == 0) {
       // one CTA per SM, never more CTAs than the partial buffer has chunks
       const int pgrid = std::min(tc_num_sms(), reduce_chunks(rows));
       const int rpw = (int)cdiv(rows, (long long)pgrid * LNBP_WARPS);
       const size_t psmem = sums ? (size_t)LNBP_WARPS * 3 * C * sizeof(float) : 0;
       {
         const int mx = LNBP_WARPS * 3 * 1024 * (int)sizeof(float);
-        for (auto k : {layernorm_backward_pipe_kernel<1>, layernorm_backward_pipe_kernel<2>,
-                       layernorm_backward_pipe_kernel<3>, layernorm_backward_pipe_kernel<4>}) {
+        for (auto k : {layernorm_backward_pipe_kernel<RT, 1>, layernorm_backward_pipe_kernel<RT, 2>,
+                       layernorm_backward_pipe_kernel<RT, 3>, layernorm_backward_pipe_kernel<RT, 4>}) {
           cudaError_t e = kernel_smem_attr(k, mx);
           if (e != cudaSuccess) return e;
         }
       }
 #define LNBP(NVv)                                                                                            \
-  launch_k(layernorm_backward_pipe_kernel<NVv>, dim3(pgrid), dim3(32 * LNBP_WARPS), psmem, st, dres,          \
-           (bf16*)dres_c, (const bf16*)dy, (const bf16*)x, mean, rstd, (const bf16*)w, rows, C, accumulate, \
-           part, rsum, rpw)
+  launch_k(layernorm_backward_pipe_kernel<RT, NVv>, dim3(pgrid), dim3(32 * LNBP_WARPS), psmem, st, rout, rin,     \
+           (bf16*)rcopy, rf32, (const bf16*)dy, (const bf16*)x, mean, rstd, (const bf16*)w, rows, C, part, rsum, \
+           rpw)
       if (nvec <= 32) LNBP(1);
       else if (nvec <= 64) LNBP(2);
       else if (nvec <= 96) LNBP(3);
@@ -946,8 +983,9 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
       return reduce_partials(dw, db, dres_sum, partial, pgrid, C, 3, st);
     }
   }
-#define LNB(NVv) launch_k(layernorm_backward_kernel<T, NVv>, dim3(grid), dim3(256), smem, st, dres, dres_c, dy, x, mean, rstd, w, rows, \
-                                                                            C, accumulate, part, rsum)
+#define LNB(NVv)                                                                                              \
+  launch_k(layernorm_backward_kernel<T, RT, NVv>, dim3(grid), dim3(256), smem, st, rout, rin, rcopy, rf32, dy, x, \
+           mean, rstd, w, rows, C, part, rsum)
   if (nvec <= 32) LNB(1);
   else if (nvec <= 64) LNB(2);
   else if (nvec <= 96) LNB(3);
@@ -966,6 +1004,14 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
     return cudaSuccess;
   }
   return reduce_partials(dw, db, dres_sum, partial, (int)grid, C, 3, st);
+}
+
+template <typename T>
+cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, const float* mean,
+                               const float* rstd, const T* w, int rows, int C, int accumulate, float* dw,
+                               float* db, float* dres_sum, float* partial, cudaStream_t st, int* deferred_chunks) {
+  return layernorm_backward_rg<T, float>(dres, accumulate ? dres : nullptr, dres_c, nullptr, dy, x, mean, rstd, w,
+                                         rows, C, dw, db, dres_sum, partial, st, deferred_chunks);
 }
 
 // ============================================================================
@@ -2289,44 +2335,63 @@ cudaError_t convert_f32_bf16(bf16* out, const float* in, long long n, cudaStream
 // ============================================================================
 // standalone GELU forward/backward (128-bit streaming)
 // ============================================================================
+// GELU over a flat array: a block covers 256 * GELU_U consecutive 16-byte
+// words, each thread GELU_U of them 256 words apart, and every thread issues
+// all its loads before any arithmetic, so that enough bytes are in flight per
+// SM to stream at the copy rate.
+constexpr int GELU_U = 4;
 template <typename T>
-__global__ void gelu_forward_kernel(T* __restrict__ out, const T* __restrict__ in, long long nvec) {
+__global__ void __launch_bounds__(256) gelu_forward_kernel(T* __restrict__ out, const T* __restrict__ in,
+                                                           long long nvec) {
   pdl_enter();
   constexpr int N = VecN<T>::n;
-  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= nvec) return;
-  float f[N];
-  ld16_cs(in + i * N, f);
+  const long long base = (long long)blockIdx.x * 256 * GELU_U + threadIdx.x;
+  float f[GELU_U][N];
 #pragma unroll
-  for (int k = 0; k < N; k++) f[k] = gelu_fwd(f[k]);
-  st16_cs(out + i * N, f);
+  for (int u = 0; u < GELU_U; u++)
+    if (base + u * 256 < nvec) ld16_cs(in + (base + u * 256) * N, f[u]);
+#pragma unroll
+  for (int u = 0; u < GELU_U; u++) {
+    if (base + u * 256 >= nvec) break;
+#pragma unroll
+    for (int k = 0; k < N; k++) f[u][k] = gelu_fwd(f[u][k]);
+    st16_cs(out + (base + u * 256) * N, f[u]);
+  }
 }
 template <typename T>
-__global__ void gelu_backward_kernel(T* __restrict__ dinp, const T* __restrict__ inp, const T* __restrict__ dout,
-                                     long long nvec) {
+__global__ void __launch_bounds__(256) gelu_backward_kernel(T* __restrict__ dinp, const T* __restrict__ inp,
+                                                            const T* __restrict__ dout, long long nvec) {
   pdl_enter();
   constexpr int N = VecN<T>::n;
-  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= nvec) return;
-  float x[N], d[N];
-  ld16_cs(inp + i * N, x);
-  ld16_cs(dout + i * N, d);
+  const long long base = (long long)blockIdx.x * 256 * GELU_U + threadIdx.x;
+  float x[GELU_U][N], d[GELU_U][N];
 #pragma unroll
-  for (int k = 0; k < N; k++) d[k] *= gelu_bwd(x[k]);
-  st16_cs(dinp + i * N, d);
+  for (int u = 0; u < GELU_U; u++)
+    if (base + u * 256 < nvec) {
+      ld16_cs(inp + (base + u * 256) * N, x[u]);
+      ld16_cs(dout + (base + u * 256) * N, d[u]);
+    }
+#pragma unroll
+  for (int u = 0; u < GELU_U; u++) {
+    if (base + u * 256 >= nvec) break;
+#pragma unroll
+    for (int k = 0; k < N; k++) d[u][k] *= gelu_bwd(x[u][k]);
+    st16_cs(dinp + (base + u * 256) * N, d[u]);
+  }
 }
 template <typename T>
 cudaError_t gelu_forward(T* out, const T* in, long long n, cudaStream_t st) {
   constexpr int N = VecN<T>::n;
   if (n % N) return cudaErrorInvalidValue;
-  launch_k(gelu_forward_kernel<T>, dim3((unsigned)cdiv(n / N, 256)), dim3(256), 0, st, out, in, n / N);
+  launch_k(gelu_forward_kernel<T>, dim3((unsigned)cdiv(n / N, 256 * GELU_U)), dim3(256), 0, st, out, in, n / N);
   return launch_status(1);
 }
 template <typename T>
 cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cudaStream_t st) {
   constexpr int N = VecN<T>::n;
   if (n % N) return cudaErrorInvalidValue;
-  launch_k(gelu_backward_kernel<T>, dim3((unsigned)cdiv(n / N, 256)), dim3(256), 0, st, dinp, inp, dout, n / N);
+  launch_k(gelu_backward_kernel<T>, dim3((unsigned)cdiv(n / N, 256 * GELU_U)), dim3(256), 0, st, dinp, inp, dout,
+           n / N);
   return launch_status(1);
 }
 
@@ -2358,3 +2423,9 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   template cudaError_t gelu_backward<T>(T*, const T*, const T*, long long, cudaStream_t);
 INST(float)
 INST(bf16)
+template cudaError_t layernorm_backward_rg<float, float>(float*, const float*, float*, float*, const float*,
+                                                         const float*, const float*, const float*, const float*, int,
+                                                         int, float*, float*, float*, float*, cudaStream_t, int*);
+template cudaError_t layernorm_backward_rg<bf16, bf16>(bf16*, const bf16*, bf16*, float*, const bf16*, const bf16*,
+                                                       const float*, const float*, const bf16*, int, int, float*,
+                                                       float*, float*, float*, cudaStream_t, int*);

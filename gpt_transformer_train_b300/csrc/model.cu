@@ -458,11 +458,15 @@ struct Step {
     CK(m, linear_dgrad(dsmall(), logits(), W(GPT2_WTE), BTi, c.Vp, Ci));
     CK(m, ln_recompute(f, W(GPT2_LNFW), W(GPT2_LNFB)));
     CK(m, linear_wgrad(G(GPT2_WTE), logits(), ln(f), BTi, c.Vp, Ci));
-    // final LayerNorm; the column sums of the resulting dres are the bias
-    // gradient of the last fc projection (its output gradient is dres)
-    CK(m, layernorm_backward<T>(dres(), dresc(L - 1, 0), dsmall(), resid(f), mean(f), rstd(f), W(GPT2_LNFW), BTi,
-                                Ci, 0, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C), part + 2 * L * lnslot, st,
-                                &nch));
+    // The residual gradient runs backwards through the LayerNorm backwards in
+    // the activation type, from one kept slot to the next: dresc(l, 0) enters
+    // layer l's fc projection, dresc(l, 1) its attention projection; the
+    // last one (into the embeddings) is written in fp32 to dres().
+    // final LayerNorm; the column sums of the resulting residual gradient are
+    // the bias gradient of the last fc projection (whose output gradient it is)
+    CK(m, (layernorm_backward_rg<T, T>(dresc(L - 1, 0), nullptr, nullptr, nullptr, dsmall(), resid(f), mean(f), rstd(f),
+                                      W(GPT2_LNFW), BTi, Ci, G(GPT2_LNFW), G(GPT2_LNFB), G(GPT2_FCPROJB, L - 1, C),
+                                      part + 2 * L * lnslot, st, &nch)));
     for (int l = Li - 1; l >= 0; l--) {
       // fc projection (+ GELU backward fused into its input-gradient GEMM)
       CK(m, linear_dgrad(dfch(l), dresc(l, 0), W(GPT2_FCPROJW, l, 4 * CC), BTi, Ci, 4 * Ci, fch(l)));
@@ -478,9 +482,10 @@ struct Step {
         CK(m, colsum<T>(G(GPT2_FCB, l, 4 * C), dfch(l), BTi, 4 * Ci, 4 * Ci, cpart, st, 1, 0, 0, acc));
       }
       // LN2 (+ residual gradient; its column sums give the attention-projection bias gradient)
-      CK(m, layernorm_backward<T>(dres(), dresc(l, 1), dsmall(), resid(2 * l + 1), mean(2 * l + 1),
-                                  rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci, 1, G(GPT2_LN2W, l, C),
-                                  G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C), part + (2 * l + 1) * lnslot, st, &nch));
+      CK(m, (layernorm_backward_rg<T, T>(dresc(l, 1), dresc(l, 0), nullptr, nullptr, dsmall(), resid(2 * l + 1),
+                                        mean(2 * l + 1), rstd(2 * l + 1), W(GPT2_LN2W, l, C), BTi, Ci,
+                                        G(GPT2_LN2W, l, C), G(GPT2_LN2B, l, C), G(GPT2_ATTPROJB, l, C),
+                                        part + (2 * l + 1) * lnslot, st, &nch)));
       // attention projection (its epilogue also forms the attention backward's D)
       bool d_ready = false;
       CK(m, attproj_dgrad(dsmall(), dresc(l, 1), W(GPT2_ATTPROJW, l, CC), atty(l), &d_ready));
@@ -495,9 +500,10 @@ struct Step {
         CK(m, colsum<T>(G(GPT2_QKVB, l, 3 * C), dqkv(l), BTi, 3 * Ci, 3 * Ci, cpart, st, 1, 0, 0, acc));
       }
       // LN1 (+ residual gradient; its column sums give the previous block's fc-projection bias gradient)
-      CK(m, layernorm_backward<T>(dres(), l > 0 ? dresc(l - 1, 0) : nullptr, dsmall(), resid(2 * l), mean(2 * l),
-                                  rstd(2 * l), W(GPT2_LN1W, l, C), BTi, Ci, 1, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
-                                  l > 0 ? G(GPT2_FCPROJB, l - 1, C) : nullptr, part + 2 * l * lnslot, st, &nch));
+      CK(m, (layernorm_backward_rg<T, T>(l > 0 ? dresc(l - 1, 0) : nullptr, dresc(l, 1), nullptr,
+                                        l > 0 ? nullptr : dres(), dsmall(), resid(2 * l), mean(2 * l), rstd(2 * l),
+                                        W(GPT2_LN1W, l, C), BTi, Ci, G(GPT2_LN1W, l, C), G(GPT2_LN1B, l, C),
+                                        l > 0 ? G(GPT2_FCPROJB, l - 1, C) : nullptr, part + 2 * l * lnslot, st, &nch)));
     }
     // LayerNorm weight / bias sums and the projection biases they give, for
     // all layers: final LN, every LN2 (one batched launch), LN1 of layers

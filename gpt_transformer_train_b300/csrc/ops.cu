@@ -72,6 +72,28 @@ int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void*
                                          (const float*)w, rows, C, accumulate, dw, db, dres_sum, part, ST(stream)));
 }
 
+int gpt2_op_layernorm_backward_rg(int dtype, void* dres_out, const void* dres_in, float* dres_f32, const void* dy,
+                                  const void* x, const float* mean, const float* rstd, const void* w, float* dw,
+                                  float* db, float* dres_sum, int rows, int C, void* scratch, size_t scratch_bytes,
+                                  void* stream) {
+  if (bad_dtype(dtype) || (!dres_out && !dres_f32) || !dy || !x || !mean || !rstd || !w || rows <= 0 || C <= 0)
+    return GPT2_ERR_INVALID_ARG;
+  if (C % (dtype ? 8 : 4) || C > 2048) return GPT2_ERR_INVALID_ARG;
+  for (const void* q : {(const void*)dres_out, dres_in, (const void*)dres_f32, dy, x, w})
+    if (!aligned16(q)) return GPT2_ERR_INVALID_ARG;
+  const bool sums = dw || db || dres_sum;
+  if (sums && (!dw || !db || !scratch || scratch_bytes < gpt2_op_layernorm_backward_scratch_bytes(rows, C)))
+    return GPT2_ERR_INVALID_ARG;
+  float* part = sums ? (float*)scratch : nullptr;
+  if (dtype == GPT2_PRECISION_BF16)
+    return rc_of(layernorm_backward_rg<bf16, bf16>((bf16*)dres_out, (const bf16*)dres_in, nullptr, dres_f32,
+                                                   (const bf16*)dy, (const bf16*)x, mean, rstd, (const bf16*)w, rows,
+                                                   C, dw, db, dres_sum, part, ST(stream)));
+  return rc_of(layernorm_backward_rg<float, float>((float*)dres_out, (const float*)dres_in, nullptr, dres_f32,
+                                                   (const float*)dy, (const float*)x, mean, rstd, (const float*)w,
+                                                   rows, C, dw, db, dres_sum, part, ST(stream)));
+}
+
 size_t gpt2_op_matmul_workspace_bytes(int M, int N, int K, int epilogue) {
   if (M <= 0 || N <= 0 || K <= 0 || epilogue != EPI_ACC_F32) return 0;
   return gemm_tc_workspace_floats(M, N, K, GPT2_NOMINAL_SMS) * sizeof(float);

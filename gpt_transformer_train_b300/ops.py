@@ -21,6 +21,7 @@ _sigs = {
     "gpt2_op_residual_layernorm_forward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _P]),
     "gpt2_op_layernorm_backward_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_layernorm_backward": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P, _sz, _P]),
+    "gpt2_op_layernorm_backward_rg": (_i, [_i, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _i, _i, _P, _sz, _P]),
     "gpt2_op_matmul_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "gpt2_op_matmul": (_i, [_i, _P, _ll, _i, _P, _ll, _i, _i, _i, _i, _P, _ll, _P, _P, _ll, _i, _i, _P, _P, _sz, _P]),
     "gpt2_op_matmul_rowdot": (_i, [_P, _ll, _P, _ll, _i, _i, _i, _P, _ll, _P, _ll, _P, _i, _i, _P, _P]),
@@ -114,6 +115,15 @@ def gpt2_op_layernorm_backward(dres, dres_c, dy, x, mean, rstd, w, dw, db, rows,
     _ck(lib.gpt2_op_layernorm_backward(_dt(dy), _p(dres), _p(dres_c), _p(dy), _p(x), _p(mean), _p(rstd), _p(w),
                                        _p(dw), _p(db), _p(dres_sum), rows, C, accumulate, _p(sc), sc.numel(),
                                        _s(stream)), "layernorm_backward")
+
+
+def gpt2_op_layernorm_backward_rg(dres_out, dres_in, dres_f32, dy, x, mean, rstd, w, dw, db, rows, C, stream=None,
+                                  dres_sum=None):
+    n = lib.gpt2_op_layernorm_backward_scratch_bytes(rows, C)
+    sc = _scratch(n, dy.device)
+    _ck(lib.gpt2_op_layernorm_backward_rg(_dt(dy), _p(dres_out), _p(dres_in), _p(dres_f32), _p(dy), _p(x), _p(mean),
+                                          _p(rstd), _p(w), _p(dw), _p(db), _p(dres_sum), rows, C, _p(sc), sc.numel(),
+                                          _s(stream)), "layernorm_backward_rg")
 
 
 def gemm_workspace(M, N, K, epilogue=EPI_ACC_F32, device="cuda"):

@@ -9,7 +9,7 @@ against the measured peaks (HBM copy GB/s, bf16 burst TFLOP/s).
 
   python -m gpt_transformer_train_b300.sweep [--kernel NAME ...] [--reps N] [--warmup N]
 
-Kernel names: ln_fwd ln_bwd gelu_fwd gelu_bwd softmax_ce adamw encoder_fwd
+Kernel names: ln_fwd ln_bwd ln_bwd_f32res gelu_fwd gelu_bwd softmax_ce adamw encoder_fwd
 encoder_bwd attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096},
 gemm_<layer>_{fwd,dgrad,wgrad} for layer in qkv attproj fc fcproj classifier,
 gemmepi_fc_gelu, gemmepi_fcproj_gelubwd, gemmepi_attproj_rowdot and
@@ -61,7 +61,16 @@ def make_case(name, ops):
         mean, rstd = torch.empty(BT, device="cuda"), torch.empty(BT, device="cuda")
         return (lambda: ops.gpt2_op_residual_layernorm_forward(r, y, mean, rstd, a, b, w, bias, BT, C),
                 4 * BT * C * 2 + 8 * BT, "B")
-    if name == "ln_bwd":
+    if name == "ln_bwd":  # the step's form: the residual gradient passed along in bf16
+        dy, x, w = randn((BT, C), 5), randn((BT, C), 6), randn((C,), 7)
+        mean, rstd = torch.zeros(BT, device="cuda"), torch.ones(BT, device="cuda")
+        rin, rout = randn((BT, C), 8), torch.empty(BT, C, device="cuda", dtype=BF)
+        dw, db, rsum = torch.zeros(C, device="cuda"), torch.zeros(C, device="cuda"), torch.zeros(C, device="cuda")
+        # dy, x, incoming residual gradient read; new residual gradient written (bf16); stats read
+        return (lambda: ops.gpt2_op_layernorm_backward_rg(rout, rin, None, dy, x, mean, rstd, w, dw, db, BT, C,
+                                                          dres_sum=rsum),
+                BT * C * (2 + 2 + 2 + 2) + 8 * BT, "B")
+    if name == "ln_bwd_f32res":  # fp32 residual gradient in place plus a bf16 copy
         dy, x, w = randn((BT, C), 5), randn((BT, C), 6), randn((C,), 7)
         mean, rstd = torch.zeros(BT, device="cuda"), torch.ones(BT, device="cuda")
         dres = randn((BT, C), 8, torch.float32)

@@ -93,6 +93,20 @@ int gpt2_op_layernorm_backward(int dtype, float* dres, void* dres_c, const void*
                                float* dres_sum, int rows, int C, int accumulate, void* scratch,
                                size_t scratch_bytes, void* stream);
 
+/* The LayerNorm backward as the training step runs it: the residual gradient
+ * passed from one layer to the next in the activation dtype (bf16 in the bf16
+ * step, float in the fp32 step) instead of an fp32 accumulator plus a copy.
+ * dres_out = (dres_in ? dres_in : 0) + dx, both [rows][C] in dtype (dres_in
+ * NULL: no incoming gradient; dres_in == dres_out: in place); dres_f32
+ * (optional) receives the new value in float, before rounding to dtype
+ * (dres_out may then be NULL).  dw, db, dres_sum and scratch as for
+ * gpt2_op_layernorm_backward, dres_sum taking the column sums of the new value
+ * before rounding.  Pointers 16-byte aligned. */
+int gpt2_op_layernorm_backward_rg(int dtype, void* dres_out, const void* dres_in, float* dres_f32, const void* dy,
+                                  const void* x, const float* mean, const float* rstd, const void* w, float* dw,
+                                  float* db, float* dres_sum, int rows, int C, void* scratch, size_t scratch_bytes,
+                                  void* stream);
+
 /* D(m,n) = sum_k A(m,k) B(n,k) then an epilogue:
  *   A(m,k) = a_kmajor ? A[m*lda+k] : A[k*lda+m];  B(n,k) = b_kmajor ? B[n*ldb+k] : B[k*ldb+n]
  *   epilogue 0: D = acc (+bias[n])          1: aux = acc + bias[n], D = GELU_tanh(aux)

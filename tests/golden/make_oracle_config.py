@@ -13,8 +13,9 @@ Configs (tokens: Zipf(1.1) over V = 50257 from seed 1234, B*(T+1) drawn and
 shifted by one; weights from seed 1234; same as the device side):
   350m  L=24 C=1024 H=16 B=8   -> tests/golden/oracle_350m.npz
   1.6b  L=48 C=1600 H=25 B=8   -> tests/golden/oracle_1p6b.npz
-  124m  L=12 C=768  H=12 B=16  -> tests/golden/oracle_124m_logits.npz (logits
-        rows only; the rest of the 124M step is in oracle_124m.npz)
+  124m  L=12 C=768  H=12 B=16  -> tests/golden/oracle_124m_logits.npz (forward
+        only: logits rows and pos_scale; the rest of the 124M step is in
+        oracle_124m.npz)
 
 Stores:
   loss          []          mean loss of the step
@@ -23,9 +24,13 @@ Stores:
   logit_rows    [R, Vp]     the oracle's logits at those positions
   logit_bound   [R, Vp]     sum over channels of |lnf[b,t,c] * wte[v,c]| (the
                             magnitude scale of each logit's dot product)
+  pos_scale     [B*T]       per position, that scale at the target logit plus
+                            its softmax-weighted mean over the vocabulary (the
+                            magnitude scale of the position's loss, lse - z_t)
   grad_idx_<n>, grad_val_<n>, grad_norm_<n>   as in oracle_124m.npz
 
 Usage: python tests/golden/make_oracle_config.py 350m|1.6b|124m
+(The 124m run stores the logit rows of the first two sequences only.)
 1.6b needs about 35 GB of RAM and a quarter of an hour on an 8-core host.
 """
 import os
@@ -63,23 +68,31 @@ def main():
     m.m = m.v = None  # no update is taken: the moments are not needed
     print(f"init {time.time() - t0:.1f}s", flush=True)
     out = {"logit_pos": [], "logit_rows": [], "logit_bound": []}
-    losses = []
-    seqs = range(2) if logits_only else range(B)
-    for b in seqs:
+    losses, scales = [], []
+    abs_wte = np.abs(m.params["wte"])
+    for b in range(B):
         t0 = time.time()
         loss = m.forward(tok[b:b + 1], tgt[b:b + 1])
-        t = logit_position(b)
-        lnf = m.cache["lnf"][0, t].astype(np.float64)
-        out["logit_pos"].append((b, t))
-        out["logit_rows"].append(m.cache["logits"][0, t].astype(np.float32))
-        out["logit_bound"].append((np.abs(m.params["wte"].astype(np.float64)) @ np.abs(lnf)).astype(np.float32))
+        if not logits_only or b < 2:
+            t = logit_position(b)
+            lnf = m.cache["lnf"][0, t].astype(np.float64)
+            out["logit_pos"].append((b, t))
+            out["logit_rows"].append(m.cache["logits"][0, t].astype(np.float32))
+            out["logit_bound"].append((np.abs(m.params["wte"].astype(np.float64)) @ np.abs(lnf)).astype(np.float32))
         losses.append(m.cache["losses"].reshape(-1).astype(np.float32))
+        # per position: sum_c |lnf_c wte_vc| at the target and softmax-weighted over v < V
+        S = np.abs(m.cache["lnf"][0]) @ abs_wte.T
+        probs = O.softmax_forward(m.cache["logits"][0], cfg.V)
+        s_t = np.take_along_axis(S, tgt[b][:, None].astype(np.int64), axis=1)[:, 0]
+        scales.append((s_t + (probs * S).sum(axis=1)).astype(np.float32))
+        del S, probs
         if not logits_only:
             m.backward()
         m.cache = None
         print(f"sequence {b}: loss {loss:.6f} ({time.time() - t0:.1f}s)", flush=True)
     for k in ("logit_pos", "logit_rows", "logit_bound"):
         out[k] = np.array(out[k])
+    out["pos_scale"] = np.concatenate(scales)
     if not logits_only:
         out["pos_losses"] = np.concatenate(losses)
         out["loss"] = np.float64(np.mean(out["pos_losses"].astype(np.float64)))

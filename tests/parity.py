@@ -21,7 +21,9 @@ The constants are written once here; the design notes list them.
 """
 from __future__ import annotations
 
+import json
 import math
+import os
 
 import numpy as np
 
@@ -48,7 +50,13 @@ def check(got, ref, bound, what=""):
         i = np.unravel_index(np.argmax(ratio), ratio.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of bound; worst at {i}: "
                              f"got {got[i]!r}, ref {ref[i]!r}, bound {bound[i]!r} (ratio {ratio[i]:.3g})")
-    return float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    worst = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    log = os.environ.get("GPT2_PARITY_LOG")
+    if log:  # margin record: the largest |got - ref| / bound of each check
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", ""), "what": what,
+                                "n": int(err.size), "max_ratio": worst}) + "\n")
+    return worst
 
 
 def gemm_ref(A, B, akm, bkm, M, N, K):
@@ -128,3 +136,12 @@ def logits_bound(ref, absdot):
     bf16 activations upstream each move the dot product by at most a few
     2^-8 of that sum)."""
     return U8 * np.abs(ref) + C_LOGITS * U8 * absdot
+
+
+def loss_bound(ref, pos_scale):
+    """Per-position cross-entropy lse - z_target of the bf16 model against the
+    oracle: its own output scale plus the logits allowance taken at the
+    position's magnitude scale (sum_c |lnf_c wte_vc| at the target plus its
+    softmax-weighted mean over the vocabulary, stored with the oracle's
+    values)."""
+    return U8 * np.abs(ref) + C_LOGITS * U8 * pos_scale
