@@ -36,7 +36,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 
 class gpt2_config(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int) for n in ("L", "C", "H", "max_T", "V", "Vp", "B", "T", "precision", "recompute")]
+    _fields_ = [(n, ctypes.c_int) for n in ("L", "C", "H", "max_T", "V", "Vp", "B", "T", "precision", "recompute",
+                                            "ln_fold")]
 
 
 _P = ctypes.c_void_p
@@ -97,8 +98,8 @@ def _ptr(a):
     return a.data_ptr()  # torch tensor
 
 
-def make_config(L, C, H, V, Vp, max_T, B, T, precision=PRECISION_BF16, recompute=0):
-    return gpt2_config(L, C, H, max_T, V, Vp, B, T, precision, recompute)
+def make_config(L, C, H, V, Vp, max_T, B, T, precision=PRECISION_BF16, recompute=0, ln_fold=0):
+    return gpt2_config(L, C, H, max_T, V, Vp, B, T, precision, recompute, ln_fold)
 
 
 def num_parameters(cfg):

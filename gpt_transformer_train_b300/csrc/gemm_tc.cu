@@ -78,6 +78,8 @@ struct TcParams {
   // units come batch2 items of a second product with M2 rows and the same N
   // and K, through the maps ta2, tb2, td2 (batch2 = 0: one product)
   int M2, batch2;
+  // EPI_STORE / EPI_GELU: the LayerNorm of A folded in (GemmArgs::ln_*)
+  const float* ln_mean; const float* ln_rstd; const float* ln_s; const float* ln_c;
 };
 
 
@@ -464,6 +466,22 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
         }
       }
     };
+    // LayerNorm folded into the product: 32 accumulator columns c0.. (tile
+    // columns, global column col0) of this lane's row to
+    // rstd * (acc - mean * s[n]) + c[n]; s and c are read as broadcast float4s
+    auto apply_fold = [&](float (&v)[32], int col0, float mu, float rs) {
+#pragma unroll
+      for (int g = 0; g < 8; g++) {
+        if (col0 + 4 * g < p.N) {
+          const float4 sv = __ldg(reinterpret_cast<const float4*>(p.ln_s + col0) + g);
+          const float4 cv = __ldg(reinterpret_cast<const float4*>(p.ln_c + col0) + g);
+          v[4 * g] = fmaf(rs, fmaf(-mu, sv.x, v[4 * g]), cv.x);
+          v[4 * g + 1] = fmaf(rs, fmaf(-mu, sv.y, v[4 * g + 1]), cv.y);
+          v[4 * g + 2] = fmaf(rs, fmaf(-mu, sv.z, v[4 * g + 2]), cv.z);
+          v[4 * g + 3] = fmaf(rs, fmaf(-mu, sv.w, v[4 * g + 3]), cv.w);
+        }
+      }
+    };
     bool prefetched = false;  // the next tile's first aux chunk is already on its way
     // the accumulator is free again: tell the CTA whose thread issues the MMAs
     auto release_acc = [&](uint32_t bar) {
@@ -496,6 +514,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + a * BN;
       float st_m = -INFINITY, st_s = 0.f;  // rowstats of this lane's row over the tile
+      // this lane's row statistics when the LayerNorm is folded in
+      float ln_mu = 0.f, ln_rs = 0.f;
+      if (p.ln_mean && rows_in && rbase + lane < p.M) {
+        ln_mu = __ldg(p.ln_mean + rbase + lane);
+        ln_rs = __ldg(p.ln_rstd + rbase + lane);
+      }
       if (p.epi == EPI_ACC_F32) {
         // split 0: D += tile (TMA reduce-add); split s > 0: workspace slot s - 1
 #pragma unroll 1
@@ -545,6 +569,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           if (p.bias) {
             add_bias(bias_cur, tc0, v0);
             add_bias(bias_cur, tc0 + 32, v1);
+          } else if (p.ln_mean) {
+            apply_fold(v0, col0, ln_mu, ln_rs);
+            apply_fold(v1, col0 + 32, ln_mu, ln_rs);
           }
           if (p.rowstats) {
             // the values as stored (bf16) enter the statistics
@@ -572,6 +599,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           if (p.bias) {
             add_bias(bias_cur, tc0, v0);
             add_bias(bias_cur, tc0 + 32, v1);
+          } else if (p.ln_mean) {
+            apply_fold(v0, col0, ln_mu, ln_rs);
+            apply_fold(v1, col0 + 32, ln_mu, ln_rs);
           }
           // the pre-activation as stored (bf16) is what GELU takes, so a later
           // recompute from it gives the same bits
@@ -760,7 +790,8 @@ cudaError_t launch(const GemmArgs& g, int splits, int* flags, cudaStream_t st, c
   const int sms = tc_num_sms();
   const long long tiles = ((g.M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN);
   TcParams p{g.M, g.N, g.K, g.a_kmajor ? 0 : 1, g.b_kmajor ? 0 : 1, g.epi, (const bf16*)g.bias, flags, splits,
-             (int)nb, g.dvec, g.dT, g.dH, g.acc_store, g.rowstats, g.stats_cols, g2 ? g2->M : 0, (int)nb2};
+             (int)nb, g.dvec, g.dT, g.dH, g.acc_store, g.rowstats, g.stats_cols, g2 ? g2->M : 0, (int)nb2,
+             g.ln_mean, g.ln_rstd, g.ln_s, g.ln_c};
   const long long tiles2 = g2 ? ((g2->M + CL * BM - 1) / (CL * BM)) * (long long)((g.N + BN - 1) / BN) : 0;
   const long long units = tiles * splits * (long long)nb + tiles2 * nb2;
   cudaLaunchConfig_t cfg = {};
@@ -904,6 +935,10 @@ bool gemm_tc_supported(const GemmArgs& g) {
     return false;
   if (g.bias && (!al16(g.bias) || (g.epi != EPI_STORE && g.epi != EPI_GELU))) return false;
   if (g.rowstats && (g.epi != EPI_STORE || g.batch > 1 || g.stats_cols <= 0)) return false;
+  if (g.ln_mean || g.ln_rstd || g.ln_s || g.ln_c) {
+    if (!g.ln_mean || !g.ln_rstd || !g.ln_s || !g.ln_c || !al16(g.ln_s) || !al16(g.ln_c)) return false;
+    if ((g.epi != EPI_STORE && g.epi != EPI_GELU) || g.bias || g.rowstats || g.batch > 1 || !g.a_kmajor) return false;
+  }
   if (g.a_kmajor ? g.lda < g.K : g.lda < g.M) return false;
   if (g.b_kmajor ? g.ldb < g.K : g.ldb < g.N) return false;
   if (g.batch > 1) {

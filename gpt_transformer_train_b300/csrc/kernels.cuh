@@ -42,7 +42,22 @@ struct GemmArgs {
   // values of the columns < stats_cols: m = their maximum, s = the sum of
   // exp(value - m), at rowstats[(row * tiles + n) * 2 + {0, 1}]
   float* rowstats; int stats_cols;
+  // EPI_STORE / EPI_GELU on the tensor-core path (optional, no bias): the
+  // LayerNorm of A folded into the product.  A is the LayerNorm's input r,
+  // B the weight with the LayerNorm gain folded in (W' = W diag(gamma)); the
+  // epilogue takes acc = r . W'^T to ln_rstd[m] * (acc - ln_mean[m] * ln_s[n]) +
+  // ln_c[n], which is LN(r) . W^T + b with ln_s[n] = sum_k W'[n][k] and
+  // ln_c[n] = b[n] + sum_k beta[k] W[n][k] (see lnfold_weights)
+  const float* ln_mean; const float* ln_rstd; const float* ln_s; const float* ln_c;
 };
+// The folded weights of lnfold GEMMs, for `items` stacked weights of N x K:
+// Wf = bf16(W diag(gamma)) (row-major [N][K]), s[n] = sum_k of Wf[n][k] as
+// stored, c[n] = bias[n] + sum_k beta[k] W[n][k]; item z reads W + z*N*K,
+// gamma/beta + z*K, bias + z*N and writes Wf + z*N*K, s/c + z*N.  K % 8 == 0.
+// out_rows (default N): rows between items in Wf, s and c (items interleaved
+// with other weights' rows)
+cudaError_t lnfold_weights(bf16* Wf, float* s, float* c, const float* W, const float* gamma, const float* beta,
+                           const float* bias, int items, int N, int K, cudaStream_t st, long long out_rows = 0);
 template <typename T> cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st);
 // two EPI_ACC_F32 products with the same N, K and operand majors as one launch
 // (the weight gradients of two weight types), or two launches when that does not pay

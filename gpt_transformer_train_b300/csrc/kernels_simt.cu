@@ -497,16 +497,18 @@ __global__ void __launch_bounds__(256) residual_layernorm_forward_kernel(
     }
     var = warp_sum(var) / (float)C;
     const float rs = 1.0f / sqrtf(var + LN_EPS);
+    if (y) {  // (no y: only the statistics, for a product that folds the LayerNorm in)
 #pragma unroll
-    for (int i = 0; i < NV; i++) {
-      const int vi = lane + i * 32;
-      if (vi < nvec) {
-        float wv[N], bv[N], o[N];
-        ld16(w + vi * N, wv);
-        ld16(bias + vi * N, bv);
+      for (int i = 0; i < NV; i++) {
+        const int vi = lane + i * 32;
+        if (vi < nvec) {
+          float wv[N], bv[N], o[N];
+          ld16(w + vi * N, wv);
+          ld16(bias + vi * N, bv);
 #pragma unroll
-        for (int k = 0; k < N; k++) o[k] = (x[q][i][k] - mu) * rs * wv[k] + bv[k];
-        st16(y + (size_t)row * C + vi * N, o);
+          for (int k = 0; k < N; k++) o[k] = (x[q][i][k] - mu) * rs * wv[k] + bv[k];
+          st16(y + (size_t)row * C + vi * N, o);
+        }
       }
     }
     if (lane == 0) {
@@ -1163,6 +1165,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs g) {
 template <typename T>
 cudaError_t gemm_simt(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaErrorInvalidValue;
+  if (a.ln_mean) return cudaErrorNotSupported;  // the folded LayerNorm is a tensor-core epilogue
   dim3 grid((unsigned)cdiv(a.N, 64), (unsigned)cdiv(a.M, 64));
   const int nb = a.batch > 1 ? a.batch : 1;
   if (nb > 1 && a.bias) return cudaErrorInvalidValue;
@@ -1286,7 +1289,7 @@ template <typename T>
 bool gemm_skinny_supported(const GemmArgs& a) {
   auto al16 = [](const void* q) { return ((uintptr_t)q & 15) == 0; };
   const int kch = skinny_chunks<T>(a.K);
-  return a.M >= 1 && a.M <= 32 && a.N >= 1 && kch >= 1 && kch <= 12 && a.a_kmajor && a.b_kmajor &&
+  return a.M >= 1 && a.M <= 32 && a.N >= 1 && kch >= 1 && kch <= 12 && a.a_kmajor && a.b_kmajor && !a.ln_mean &&
          a.batch <= 1 && (a.epi == EPI_STORE || (a.epi == EPI_GELU && a.aux)) && a.lda % VecN<T>::n == 0 &&
          a.ldb % VecN<T>::n == 0 && al16(a.A) && al16(a.B) && (size_t)a.M * a.K * sizeof(T) <= 200 * 1024;
 }
@@ -2392,6 +2395,62 @@ cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cud
   if (n % N) return cudaErrorInvalidValue;
   launch_k(gelu_backward_kernel<T>, dim3((unsigned)cdiv(n / N, 256 * GELU_U)), dim3(256), 0, st, dinp, inp, dout,
            n / N);
+  return launch_status(1);
+}
+
+// ============================================================================
+// LayerNorm folded into the next product: one warp per weight row n of one
+// stacked item; Wf[n][k] = bf16(W[n][k] gamma[k]), s[n] = sum of Wf[n][k] (as
+// stored), c[n] = bias[n] + sum_k beta[k] W[n][k], lanes over k in 8-wide
+// groups, the sums added by a fixed shuffle tree (deterministic).
+// ============================================================================
+__global__ void __launch_bounds__(256) lnfold_weights_kernel(bf16* __restrict__ Wf, float* __restrict__ s,
+                                                             float* __restrict__ c, const float* __restrict__ W,
+                                                             const float* __restrict__ gamma,
+                                                             const float* __restrict__ beta,
+                                                             const float* __restrict__ bias, int items, int N, int K,
+                                                             long long out_rows) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)items * N) return;
+  const int z = (int)(row / N), n = (int)(row % N);
+  const long long orow = (long long)z * out_rows + n;  // the row in Wf, s, c
+  const float* w = W + (size_t)row * K;
+  const float* g = gamma + (size_t)z * K;
+  const float* be = beta + (size_t)z * K;
+  float ss = 0.f, cc = 0.f;
+  for (int k = 8 * lane; k < K; k += 256) {
+    float wv[8], gv[8], bv[8];
+    ld16(w + k, *reinterpret_cast<float(*)[4]>(wv));
+    ld16(w + k + 4, *reinterpret_cast<float(*)[4]>(wv + 4));
+    ld16(g + k, *reinterpret_cast<float(*)[4]>(gv));
+    ld16(g + k + 4, *reinterpret_cast<float(*)[4]>(gv + 4));
+    ld16(be + k, *reinterpret_cast<float(*)[4]>(bv));
+    ld16(be + k + 4, *reinterpret_cast<float(*)[4]>(bv + 4));
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      o[e] = round_to<bf16>(wv[e] * gv[e]);
+      ss += o[e];
+      cc = fmaf(bv[e], wv[e], cc);
+    }
+    st16(Wf + (size_t)orow * K + k, o);
+  }
+  ss = warp_sum(ss);
+  cc = warp_sum(cc);
+  if (lane == 0) {
+    s[orow] = ss;
+    c[orow] = (bias ? bias[(size_t)z * N + n] : 0.f) + cc;
+  }
+}
+
+cudaError_t lnfold_weights(bf16* Wf, float* s, float* c, const float* W, const float* gamma, const float* beta,
+                           const float* bias, int items, int N, int K, cudaStream_t st, long long out_rows) {
+  if (items <= 0 || N <= 0 || K <= 0 || K % 8) return cudaErrorInvalidValue;
+  if (out_rows <= 0) out_rows = N;
+  launch_k(lnfold_weights_kernel, dim3((unsigned)cdiv((long long)items * N, 8)), dim3(256), 0, st, Wf, s, c, W, gamma,
+           beta, bias, items, N, K, out_rows);
   return launch_status(1);
 }
 

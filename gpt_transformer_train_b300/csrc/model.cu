@@ -96,6 +96,9 @@ int validate_config(const gpt2_config& c, const char** why) {
     return *why = "precision must be GPT2_PRECISION_FP32 or GPT2_PRECISION_BF16", GPT2_ERR_INVALID_CONFIG;
   }
   if (c.recompute < 0 || c.recompute > 2) return *why = "recompute must be 0, 1 or 2", GPT2_ERR_INVALID_CONFIG;
+  if (c.ln_fold < 0 || c.ln_fold > 1) return *why = "ln_fold must be 0 or 1", GPT2_ERR_INVALID_CONFIG;
+  if (c.ln_fold && (c.precision != GPT2_PRECISION_BF16 || c.recompute != 2))
+    return *why = "ln_fold needs bf16 precision and recompute 2", GPT2_ERR_INVALID_CONFIG;
   return GPT2_OK;
 }
 
@@ -178,6 +181,11 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   // ping-pong, LayerNorm output, attention output, projection output (B x C
   // each), fc pre-activation and GELU (B x 4C), logits (B x Vp), stats (2 x B fp32)
   b.dec = take(((5 + 8) * (size_t)c.B * C + (size_t)c.B * c.Vp) * es + 2 * (size_t)c.B * 4);
+  // ln_fold: per layer the qkv (3C rows) then the fc (4C rows) weight with
+  // the LayerNorm gain folded in, and their column sums s, c
+  b.wfold = c.ln_fold ? take(L * 7 * C * C * 2) : 0;
+  b.fold_s = c.ln_fold ? take(L * 7 * C * 4) : 0;
+  b.fold_c = c.ln_fold ? take(L * 7 * C * 4) : 0;
   b.total = o;
   return b;
 }
@@ -266,6 +274,24 @@ struct Step {
       m->prof_flops[m->prof_n++] = 2.0 * a.M * a.N * (double)a.K * (a.batch > 1 ? a.batch : 1);
     }
     return e;
+  }
+  // fp32 master copy of a parameter tensor
+  const float* P(int t) const { return m->at<float>(m->bl.params) + m->pl.off[t]; }
+  // ln_fold: layer l's folded qkv (k = 0) or fc (k = 1) weight and its sums
+  size_t fold_row(size_t l, int k) const { return l * 7 * C + (k ? 3 * C : 0); }
+  bf16* wfold(size_t l, int k) const { return m->at<bf16>(m->bl.wfold) + fold_row(l, k) * C; }
+  float* fold_s(size_t l, int k) const { return m->at<float>(m->bl.fold_s) + fold_row(l, k); }
+  float* fold_c(size_t l, int k) const { return m->at<float>(m->bl.fold_c) + fold_row(l, k); }
+  // out[BT][N] = LayerNorm i (of resid(i)) . W^T + b with the LayerNorm folded
+  // into the product (layer l's qkv for k = 0, fc with GELU for k = 1)
+  cudaError_t linear_fwd_folded(T* out, size_t i, size_t l, int k, int N, T* aux) {
+    GemmArgs a{resid(i), (long long)C, 1, wfold(l, k), (long long)C, 1, m->BT, N, (int)C, out, N, nullptr, aux, N,
+               aux ? EPI_GELU : EPI_STORE};
+    a.ln_mean = mean(i);
+    a.ln_rstd = rstd(i);
+    a.ln_s = fold_s(l, k);
+    a.ln_c = fold_c(l, k);
+    return gemm(a);
   }
   // out[M][N] = X[M][K] . W[N][K]^T (+ bias), optionally with GELU (aux = pre-activation)
   cudaError_t linear_fwd(T* out, const T* X, const T* Wt, const T* bias, int M, int N, int K, T* aux = nullptr) {
@@ -357,19 +383,33 @@ struct Step {
     int B = c.B, T_ = c.T, Ci = c.C, Li = c.L, BTi = m->BT;
     size_t CC = C * C;
     CK(m, encoder_forward<T>(resid(0), tok, W(GPT2_WTE), W(GPT2_WPE), B, T_, Ci, c.V, flags(), st));
+    const bool fold = c.ln_fold != 0;
+    if (fold) {  // this step's weights with the LayerNorm gains folded in
+      CK(m, lnfold_weights(wfold(0, 0), fold_s(0, 0), fold_c(0, 0), P(GPT2_QKVW), P(GPT2_LN1W), P(GPT2_LN1B),
+                           P(GPT2_QKVB), Li, 3 * Ci, Ci, st, 7 * C));
+      CK(m, lnfold_weights(wfold(0, 1), fold_s(0, 1), fold_c(0, 1), P(GPT2_FCW), P(GPT2_LN2W), P(GPT2_LN2B),
+                           P(GPT2_FCB), Li, 4 * Ci, Ci, st, 7 * C));
+    }
     for (int l = 0; l < Li; l++) {
+      // with the fold only the residual stream and the statistics are written
       if (l == 0)
-        CK(m, residual_layernorm_forward<T>(nullptr, ln(0), mean(0), rstd(0), resid(0), nullptr,
+        CK(m, residual_layernorm_forward<T>(nullptr, fold ? nullptr : ln(0), mean(0), rstd(0), resid(0), nullptr,
                                             W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C), BTi, Ci, st));
       else
-        CK(m, residual_layernorm_forward<T>(resid(2 * l), ln(2 * l), mean(2 * l), rstd(2 * l), resid(2 * l - 1),
-                                            proj(), W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C), BTi, Ci, st));
-      CK(m, linear_fwd(qkv(l), ln(2 * l), W(GPT2_QKVW, l, 3 * CC), W(GPT2_QKVB, l, 3 * C), BTi, 3 * Ci, Ci));
+        CK(m, residual_layernorm_forward<T>(resid(2 * l), fold ? nullptr : ln(2 * l), mean(2 * l), rstd(2 * l),
+                                            resid(2 * l - 1), proj(), W(GPT2_LN1W, l, C), W(GPT2_LN1B, l, C), BTi,
+                                            Ci, st));
+      if (fold) CK(m, linear_fwd_folded(qkv(l), 2 * l, l, 0, 3 * Ci, nullptr));
+      else CK(m, linear_fwd(qkv(l), ln(2 * l), W(GPT2_QKVW, l, 3 * CC), W(GPT2_QKVB, l, 3 * C), BTi, 3 * Ci, Ci));
       CK(m, attention_fwd(atty(l), lse(l), qkv(l)));
       CK(m, linear_fwd(proj(), atty(l), W(GPT2_ATTPROJW, l, CC), W(GPT2_ATTPROJB, l, C), BTi, Ci, Ci));
-      CK(m, residual_layernorm_forward<T>(resid(2 * l + 1), ln(2 * l + 1), mean(2 * l + 1), rstd(2 * l + 1),
-                                          resid(2 * l), proj(), W(GPT2_LN2W, l, C), W(GPT2_LN2B, l, C), BTi, Ci, st));
-      CK(m, linear_fwd(fchg(l), ln(2 * l + 1), W(GPT2_FCW, l, 4 * CC), W(GPT2_FCB, l, 4 * C), BTi, 4 * Ci, Ci, fch(l)));
+      CK(m, residual_layernorm_forward<T>(resid(2 * l + 1), fold ? nullptr : ln(2 * l + 1), mean(2 * l + 1),
+                                          rstd(2 * l + 1), resid(2 * l), proj(), W(GPT2_LN2W, l, C), W(GPT2_LN2B, l, C),
+                                          BTi, Ci, st));
+      if (fold) CK(m, linear_fwd_folded(fchg(l), 2 * l + 1, l, 1, 4 * Ci, fch(l)));
+      else
+        CK(m, linear_fwd(fchg(l), ln(2 * l + 1), W(GPT2_FCW, l, 4 * CC), W(GPT2_FCB, l, 4 * C), BTi, 4 * Ci, Ci,
+                         fch(l)));
       CK(m, linear_fwd(proj(), fchg(l), W(GPT2_FCPROJW, l, 4 * CC), W(GPT2_FCPROJB, l, C), BTi, Ci, 4 * Ci));
     }
     size_t f = 2 * L;

@@ -94,6 +94,28 @@ int gpt2_op_layernorm_backward_rg(int dtype, void* dres_out, const void* dres_in
                                                    rows, C, dw, db, dres_sum, part, ST(stream)));
 }
 
+int gpt2_op_lnfold_weights(void* Wf, float* s, float* c, const float* W, const float* gamma, const float* beta,
+                           const float* bias, int items, int N, int K, void* stream) {
+  if (!Wf || !s || !c || !W || !gamma || !beta || items <= 0 || N <= 0 || K <= 0 || K % 8) return GPT2_ERR_INVALID_ARG;
+  for (const void* q : {(const void*)Wf, (const void*)W, (const void*)gamma, (const void*)beta})
+    if (!aligned16(q)) return GPT2_ERR_INVALID_ARG;
+  return rc_of(lnfold_weights((bf16*)Wf, s, c, W, gamma, beta, bias, items, N, K, ST(stream)));
+}
+
+int gpt2_op_matmul_lnfold(const void* R, long long ldr, const float* mean, const float* rstd, const void* Wf,
+                          long long ldw, const float* s, const float* c, int M, int N, int K, void* D, long long ldd,
+                          void* aux, long long ldaux, int* flags_dev, void* stream) {
+  if (!R || !mean || !rstd || !Wf || !s || !c || !D || !flags_dev || M <= 0 || N <= 0 || K <= 0)
+    return GPT2_ERR_INVALID_ARG;
+  GemmArgs a{R, ldr, 1, Wf, ldw, 1, M, N, K, D, ldd, nullptr, aux, ldaux, aux ? EPI_GELU : EPI_STORE};
+  a.ln_mean = mean;
+  a.ln_rstd = rstd;
+  a.ln_s = s;
+  a.ln_c = c;
+  if (!gemm_tc_supported(a)) return GPT2_ERR_INVALID_ARG;
+  return rc_of(gemm_tc(a, flags_dev, ST(stream)));
+}
+
 size_t gpt2_op_matmul_workspace_bytes(int M, int N, int K, int epilogue) {
   if (M <= 0 || N <= 0 || K <= 0 || epilogue != EPI_ACC_F32) return 0;
   return gemm_tc_workspace_floats(M, N, K, GPT2_NOMINAL_SMS) * sizeof(float);

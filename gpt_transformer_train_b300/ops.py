@@ -42,6 +42,8 @@ _sigs = {
     "gpt2_op_colsum_scratch_bytes": (_sz, [_i, _i]),
     "gpt2_op_colsum": (_i, [_i, _P, _P, _i, _i, _ll, _P, _sz, _P]),
     "gpt2_op_wait_probe": (_i, [_i, _P, _P]),
+    "gpt2_op_lnfold_weights": (_i, [_P, _P, _P, _P, _P, _P, _P, _i, _i, _i, _P]),
+    "gpt2_op_matmul_lnfold": (_i, [_P, _ll, _P, _P, _P, _ll, _P, _P, _i, _i, _i, _P, _ll, _P, _ll, _P, _P]),
 }
 for _n, (_r, _a) in _sigs.items():
     _fn = getattr(lib, _n)
@@ -213,3 +215,14 @@ def gpt2_op_wait_probe(limit_us, flags_dev, stream=None):
     """Run the bounded-wait failure path on purpose; returns the C status code
     (GPT2_ERR_TIMEOUT, -8, is the expected outcome)."""
     return lib.gpt2_op_wait_probe(limit_us, _p(flags_dev), _s(stream))
+
+
+def gpt2_op_lnfold_weights(Wf, s, c, W, gamma, beta, bias, items, N, K, stream=None):
+    _ck(lib.gpt2_op_lnfold_weights(_p(Wf), _p(s), _p(c), _p(W), _p(gamma), _p(beta), _p(bias), items, N, K,
+                                   _s(stream)), "lnfold_weights")
+
+
+def gpt2_op_matmul_lnfold(R, ldr, mean, rstd, Wf, ldw, s, c, M, N, K, D, ldd, aux=None, ldaux=0, flags_dev=None,
+                          stream=None):
+    _ck(lib.gpt2_op_matmul_lnfold(_p(R), ldr, _p(mean), _p(rstd), _p(Wf), ldw, _p(s), _p(c), M, N, K, _p(D), ldd,
+                                  _p(aux), ldaux, _p(flags_dev), _s(stream)), "matmul_lnfold")

@@ -70,10 +70,20 @@ enum {
  * run inside the layer loop and only one layer's GELU / LayerNorm outputs and
  * output gradients are held at a time, which shrinks the buffer; the forward
  * results and the gradients are those of recompute 0. */
+/* ln_fold (bf16 with recompute 2 only): the LayerNorms in front of the qkv
+ * and fc products are folded into those products (the pages' fused LayerNorm
+ * -> matmul, [13:50]): each step first forms W diag(gamma) (bf16) and the two
+ * per-output-column sums the fold needs, the LayerNorm kernels then write
+ * only the residual stream and its statistics, and the qkv and fc products
+ * run on the residual stream and normalise in their epilogue
+ * (gpt2_op_matmul_lnfold).  With recompute 2 the backward rebuilds the
+ * LayerNorm outputs it needs anyway, so no normalised activation is written
+ * in the forward.  0 = off. */
 typedef struct {
   int L, C, H, max_T, V, Vp, B, T;
   int precision;
   int recompute;
+  int ln_fold;
 } gpt2_config;
 
 typedef struct gpt2 gpt2;  /* opaque handle; host memory owned by the library */

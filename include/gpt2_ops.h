@@ -149,6 +149,30 @@ int gpt2_op_matmul_rowdot(const void* dY, long long ldy, const void* W, long lon
                           long long ldx, const void* O, long long ldo, float* D, int T, int H, int* flags_dev,
                           void* stream);
 
+/* The LayerNorm in front of a product folded into it (the pages' fused
+ * LayerNorm -> matmul, "llm.c's Origin and the Future of LLM Compilers",
+ * [13:50] Avengers Assemble).  Since LN(r) = (r - mean) rstd gamma + beta per
+ * row, LN(r) W^T + b = rstd (r W'^T - mean s) + c with W' = W diag(gamma),
+ * s[n] = sum_k W'[n][k], c[n] = b[n] + sum_k beta[k] W[n][k]: the product runs
+ * on the LayerNorm's input r itself and its epilogue applies the row's
+ * statistics, so no normalised copy of r is written or read.
+ *   gpt2_op_lnfold_weights: Wf (bf16 [N][K]) = W diag(gamma) rounded, s[n] the
+ *     sum of Wf's row as stored, c[n] = bias[n] + sum_k beta[k] W[n][k] (fp32),
+ *     for `items` stacked weights (item z: W + z*N*K, gamma/beta + z*K,
+ *     bias + z*N, outputs likewise); W, gamma, beta fp32; bias may be NULL.
+ *     K % 8 == 0, pointers 16-byte aligned.
+ *   gpt2_op_matmul_lnfold: D[m][n] = rstd[m] (sum_k R[m][k] Wf[n][k] -
+ *     mean[m] s[n]) + c[n] stored bf16 (R [M][ldr] the LayerNorm input, bf16;
+ *     mean/rstd its row statistics); with aux non-NULL the GELU form: aux =
+ *     that value (bf16), D = GELU(aux).  Tensor cores only: INVALID_ARG when
+ *     the shape is outside what they handle (N % 8, 16-byte aligned rows).
+ *     flags_dev: a bounded wait that runs out ORs 4 into it. */
+int gpt2_op_lnfold_weights(void* Wf, float* s, float* c, const float* W, const float* gamma, const float* beta,
+                           const float* bias, int items, int N, int K, void* stream);
+int gpt2_op_matmul_lnfold(const void* R, long long ldr, const float* mean, const float* rstd, const void* Wf,
+                          long long ldw, const float* s, const float* c, int M, int N, int K, void* D, long long ldd,
+                          void* aux, long long ldaux, int* flags_dev, void* stream);
+
 /* Causal multi-head attention over qkv [B*T][3C] (columns Q | K | V, head h uses
  * columns h*hd..h*hd+hd-1 of each); out [B*T][C]; lse [B][H][T] = log sum exp of
  * the scaled scores q.k/sqrt(hd) over t2 <= t (the attention layer and its

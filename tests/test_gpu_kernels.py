@@ -496,6 +496,54 @@ def test_matmul_rowdot_epilogue(ops, B, T, H, N):
     check(host(D).reshape(B, H, T), rD, 2.0 ** -20 * np.abs(x * o).sum(-1).transpose(0, 2, 1), "D")
 
 
+@pytest.mark.parametrize("M,N,K,gelu", [(384, 2304, 768, False), (256 + 136, 3072, 768, True), (200, 136, 64, False)])
+def test_matmul_layernorm_folded(ops, M, N, K, gelu):
+    """LayerNorm folded into the next product: the weight fold (W gamma in
+    bf16, the column sums s and c) and the product on the LayerNorm's input
+    with the normalisation in the epilogue, against the oracle's LayerNorm
+    followed by the oracle's matmul (and GELU), element by element.  Rows
+    with a large common offset check the mean term's cancellation."""
+    r = normal_array((M, K), 180, 1.0) + normal_array((M, 1), 181, 3.0)
+    gamma, beta = normal_array((K,), 182, 0.2) + 1, normal_array((K,), 183, 0.1)
+    W, b = normal_array((N, K), 184, 0.02), normal_array((N,), 185, 0.1)
+    tr = dev(r, torch.bfloat16)
+    rs_ = host(tr)
+    y_ln = torch.empty(M, K, device="cuda", dtype=torch.bfloat16)
+    mean, rstd = torch.empty(M, device="cuda"), torch.empty(M, device="cuda")
+    ops.gpt2_op_residual_layernorm_forward(None, y_ln, mean, rstd, tr, None, dev(gamma, torch.bfloat16),
+                                           dev(beta, torch.bfloat16), M, K)
+    Wf = torch.empty(N, K, device="cuda", dtype=torch.bfloat16)
+    sv, cv = torch.empty(N, device="cuda"), torch.empty(N, device="cuda")
+    ops.gpt2_op_lnfold_weights(Wf, sv, cv, dev(W), dev(gamma), dev(beta), dev(b), 1, N, K)
+    # the fold against its definition (bf16 product, sums of the stored values)
+    wf = host(Wf)
+    assert np.array_equal(wf.astype(np.float32), host(dev(W * gamma[None, :], torch.bfloat16)).astype(np.float32))
+    assert np.allclose(host(sv), wf.sum(1), rtol=1e-5, atol=1e-5)
+    assert np.allclose(host(cv), b + W.astype(np.float64) @ beta, rtol=1e-5, atol=1e-6)
+    D = torch.full((M, N), float("nan"), device="cuda", dtype=torch.bfloat16)
+    pre = torch.empty(M, N, device="cuda", dtype=torch.bfloat16) if gelu else None
+    fl = ops.flags()
+    ops.gpt2_op_matmul_lnfold(tr, K, mean, rstd, Wf, K, sv, cv, M, N, K, D, N, aux=pre, ldaux=N if gelu else 0,
+                              flags_dev=fl)
+    torch.cuda.synchronize()
+    assert fl.sum().item() == 0
+    y, _, _ = O.layernorm_forward(rs_, gamma.astype(np.float64), beta.astype(np.float64))
+    ref = O.matmul_forward(y, W.astype(np.float64), b.astype(np.float64))
+    # output rounding; the bf16 weight fold (2^-8 of sum |xhat gamma W|); fp32
+    # accumulation over the raw rows and the mean term (ACC of their magnitudes)
+    xhat = (rs_ - rs_.mean(1, keepdims=True)) / np.sqrt(rs_.var(1, keepdims=True) + 1e-5)
+    fold_scale = np.abs(xhat) @ np.abs(W * gamma[None, :]).T
+    raw = (np.abs(rs_) @ np.abs(wf).T + np.abs(rs_.mean(1, keepdims=True)) * np.abs(wf).sum(1)[None, :]) / \
+        np.sqrt(rs_.var(1, keepdims=True) + 1e-5)
+    bound = U8 * np.abs(ref) + 2 * U8 * fold_scale + 2 ** -16 * raw
+    if not gelu:
+        check(host(D), ref, bound, "folded product")
+    else:
+        check(host(pre), ref, bound, "folded pre-activation")
+        g_ref = O.gelu_forward(host(pre))
+        check(host(D), g_ref, gelu_bound(g_ref, host(pre)), "GELU of the folded pre-activation")
+
+
 @pytest.mark.parametrize("epi", ["store", "gelu_bwd"])
 def test_matmul_batched_bf16_epilogues(ops, epi):
     """Batched K-major products with bf16 output (and the GELU' epilogue with a

@@ -310,6 +310,42 @@ def test_activation_recompute_modes(g, prec):
             assert rel_l2(res[2][1][n], ref.grads[n].reshape(-1)) <= 5e-2, n
 
 
+@pytest.mark.parametrize("dims", ["small", "wide"])
+def test_ln_fold_step(g, dims):
+    """ln_fold (recompute 2): the LayerNorms before the qkv and fc products
+    folded into them.  Two steps against the same model without the fold
+    (same weights, batch and recompute mode: loss and every gradient within
+    bf16 rounding of each other) and the first step against the oracle."""
+    d = SMALL_BF16 if dims == "small" else WIDE_BF16
+    L, C, H, V, Vp, maxT, B, T = d.values()
+    tok, tgt = zipf_tokens(B, T, V, 1234)
+    ttok, ttgt = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+    res = {}
+    for fold in (0, 1):
+        m = g.GPT2(g.make_config(L, C, H, V, Vp, maxT, B, T, 1, recompute=2, ln_fold=fold), 1234)
+        out = []
+        for step in (1, 2):
+            m.gpt2_zero_grad()
+            loss = m.gpt2_forward(ttok, ttgt)
+            m.gpt2_backward()
+            out.append((loss, {n: m.gpt2_get_grads(n) for n in g.TENSORS}))
+            m.gpt2_adamw_step(1e-3, 0.9, 0.95, 1e-8, 0.1, step)
+        res[fold] = out
+        m.close()
+    for step in range(2):
+        assert abs(res[1][step][0] - res[0][step][0]) <= 2e-2, step
+        for n in g.TENSORS:
+            assert rel_l2(res[1][step][1][n], res[0][step][1][n]) <= 5e-2, (step, n)
+    ref = O.GPT2(O.Config(L, C, H, V, Vp, maxT), 1234, np.float32)
+    rloss = ref.forward(tok, tgt)
+    ref.backward()
+    assert abs(res[1][0][0] - rloss) <= 2e-2
+    for n in g.TENSORS:
+        assert rel_l2(res[1][0][1][n], ref.grads[n].reshape(-1)) <= 5e-2, n
+    with pytest.raises(g.GPT2Error):  # the fold needs recompute 2
+        g.GPT2(g.make_config(L, C, H, V, Vp, maxT, B, T, 1, recompute=0, ln_fold=1), 1234)
+
+
 def test_error_paths_on_device(g):
     cfg, m, ref, tok, tgt, ttok, ttgt = _setup(g, **TINY, prec=0)
     with pytest.raises(g.GPT2Error) as e:
