@@ -105,6 +105,28 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
+// packed fp32 pairs: (a0, a1) op (b0, b1), one instruction for two lanes' worth
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "sub.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -828,21 +850,33 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // lse and D of this stage's 128 queries (bulk-loaded with the Q tile)
         const uint32_t gk = g0 + k;
         if (!mbar_wait_warp(b_qfull + 8 * (gk % DKV_STAGES), (gk / DKV_STAGES) & 1, abort_flag)) { ok = false; break; }
-        const float* lq = (const float*)(ring_gen + (gk % DKV_STAGES) * BWD_QD + 2 * TILE) + c0;
-        const float* dq = lq + 128;
-        const bool diag = k == 0;  // query tile == key tile
+        // this group's 32 queries' lse and D (four floats per shared-memory load)
+        const float4* lq4 = reinterpret_cast<const float4*>(ring_gen + (gk % DKV_STAGES) * BWD_QD + 2 * TILE) + c0 / 4;
+        const float4* dq4 = lq4 + 32;
+        // P^T = 2^(S^T sl2 - lse log2 e) and dS^T = P^T (dP^T - D), on packed fp32 pairs
 #pragma unroll
-        for (int e = 0; e < EW_COLS; e++) {
-          const float x = fmaf(sv[e], p.sl2, -lq[e] * LOG2E);
-          sv[e] = (e & 3) == 3 ? exp2_poly(x) : ex2(x);
+        for (int g = 0; g < EW_COLS / 4; g++) {
+          const float4 lv = lq4[g], dv = dq4[g];
+          float n0, n1, n2, n3;
+          mul2(n0, n1, lv.x, lv.y, -LOG2E, -LOG2E);
+          mul2(n2, n3, lv.z, lv.w, -LOG2E, -LOG2E);
+          float x0, x1, x2, x3;
+          fma2(x0, x1, sv[4 * g], sv[4 * g + 1], p.sl2, p.sl2, n0, n1);
+          fma2(x2, x3, sv[4 * g + 2], sv[4 * g + 3], p.sl2, p.sl2, n2, n3);
+          sv[4 * g] = (g & 3) == 3 ? exp2_poly(x0) : ex2(x0);  // one exponential in 16 on the FMA pipe
+          sv[4 * g + 1] = ex2(x1);
+          sv[4 * g + 2] = ex2(x2);
+          sv[4 * g + 3] = ex2(x3);
+          sub2(dp[4 * g], dp[4 * g + 1], dp[4 * g], dp[4 * g + 1], dv.x, dv.y);
+          sub2(dp[4 * g + 2], dp[4 * g + 3], dp[4 * g + 2], dp[4 * g + 3], dv.z, dv.w);
         }
-        if (diag) {
+        if (k == 0) {  // the diagonal tile: a key after its query gets P = 0
 #pragma unroll
           for (int e = 0; e < EW_COLS; e++)
-            if ((int)r > c0 + e) sv[e] = 0.f;  // key after query
+            if ((int)r > c0 + e) sv[e] = 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < EW_COLS; e++) dp[e] = sv[e] * (dp[e] - dq[e]);
+        for (int e = 0; e < EW_COLS; e += 2) mul2(dp[e], dp[e + 1], sv[e], sv[e + 1], dp[e], dp[e + 1]);
         // the P^T / dS^T tiles are free once the dV/dK MMAs have read them
         // and the copy of the previous dS^T has read it
         if (nG > 0 && (!mbar_wait_warp(b_pfree, (nG - 1) & 1, abort_flag) ||
