@@ -831,6 +831,41 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
     f[2 * i + 1] = t.y;
   }
 }
+// packed fp32 pairs (one instruction for two values)
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 x, y, z, w;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 x, y, w;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 x, y, w;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "add.rn.f32x2 w, x, y;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// 8 bf16 values of a 16-byte word as four float pairs
+__device__ __forceinline__ void unpack_bf16x8_2(const uint4& v, float2 (&f)[4]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; i++) f[i] = __bfloat1622float2(h[i]);
+}
+// The per-warp column sums live in shared memory as [3][C] (dw, db, new
+// residual gradient), each lane updating its own 8 columns with two 16-byte
+// read-modify-writes per array, so the slices are in the layout of the
+// partial buffer.  All arithmetic on packed fp32 pairs.
 template <typename RT, int NV>
 __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_kernel(
     RT* rout, const RT* rin, bf16* __restrict__ rcopy, float* __restrict__ rf32, const bf16* __restrict__ dy,
@@ -838,12 +873,12 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
     const bf16* __restrict__ w, int rows, int C, float* __restrict__ partial, int want_rsum, int rpw) {
   pdl_enter();
   constexpr int N = 8;
-  extern __shared__ float lnb_sh[];  // [LNBP_WARPS][3][N][nvec] when partial
+  extern __shared__ float lnb_sh[];  // [LNBP_WARPS][3][C] when partial
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = C / N;
   float* acc = lnb_sh + (size_t)warp * 3 * C;
   if (partial)
-    for (int c = lane; c < 3 * C; c += 32) acc[c] = 0.f;
+    for (int c = 4 * lane; c < 3 * C; c += 128) *reinterpret_cast<float4*>(acc + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   uint4 wv[NV];
 #pragma unroll
   for (int i = 0; i < NV; i++)
@@ -861,56 +896,87 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
     }
     if (row + 1 < r1) lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)(row + 1) * C, lane, nvec);
     const float mu = mean[row], rs = rstd[row];
+    const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-mu * rs, -mu * rs);
+    // the incoming residual gradient: fetched with the row, or (the widest
+    // rows, to keep registers free) after the first pass
     float din[NV][N];
+    auto load_din = [&]() {
 #pragma unroll
-    for (int i = 0; i < NV; i++) {
-      const int vi = lane + i * 32;
+      for (int i = 0; i < NV; i++) {
+        const int vi = lane + i * 32;
 #pragma unroll
-      for (int k = 0; k < N; k++) din[i][k] = 0.f;
-      if (rin && vi < nvec) ld8(rin + (size_t)row * C + vi * N, din[i]);
-    }
-    float s1 = 0.f, s2 = 0.f;
+        for (int k = 0; k < N; k++) din[i][k] = 0.f;
+        if (rin && vi < nvec) ld8(rin + (size_t)row * C + vi * N, din[i]);
+      }
+    };
+    if constexpr (NV < 4) load_din();
+    float2 s1 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < NV; i++) {
       const int vi = lane + i * 32;
       if (vi < nvec) {
-        float dv[N], xv[N], ww[N];
-        unpack_bf16x8(cdy[i], dv);
-        unpack_bf16x8(cx[i], xv);
-        unpack_bf16x8(wv[i], ww);
+        float2 dv[4], xv[4], ww[4];
+        unpack_bf16x8_2(cdy[i], dv);
+        unpack_bf16x8_2(cx[i], xv);
+        unpack_bf16x8_2(wv[i], ww);
+        float2 xh[4];
 #pragma unroll
-        for (int k = 0; k < N; k++) {
-          const float xh = (xv[k] - mu) * rs, dn = dv[k] * ww[k];
-          s1 += dn;
-          s2 += dn * xh;
-          if (partial) {
-            acc[k * nvec + vi] += dv[k] * xh;
-            acc[(N + k) * nvec + vi] += dv[k];
+        for (int k = 0; k < 4; k++) {
+          xh[k] = f2_fma(xv[k], rs2, nmr);
+          const float2 dn = f2_mul(dv[k], ww[k]);
+          s1 = f2_add(s1, dn);
+          s2 = f2_fma(dn, xh[k], s2);
+        }
+        if (partial) {
+          float4* aw = reinterpret_cast<float4*>(acc + vi * N);
+          float4* ab = reinterpret_cast<float4*>(acc + C + vi * N);
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            float4 a = aw[h], b = ab[h];
+            const float2 lo = f2_fma(dv[2 * h], xh[2 * h], make_float2(a.x, a.y));
+            const float2 hi = f2_fma(dv[2 * h + 1], xh[2 * h + 1], make_float2(a.z, a.w));
+            const float2 blo = f2_add(dv[2 * h], make_float2(b.x, b.y));
+            const float2 bhi = f2_add(dv[2 * h + 1], make_float2(b.z, b.w));
+            aw[h] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            ab[h] = make_float4(blo.x, blo.y, bhi.x, bhi.y);
           }
         }
       }
     }
-    s1 = warp_sum(s1) / (float)C;
-    s2 = warp_sum(s2) / (float)C;
+    if constexpr (NV >= 4) load_din();
+    const float m1 = -warp_sum(s1.x + s1.y) / (float)C;
+    const float m2 = -warp_sum(s2.x + s2.y) / (float)C;
+    const float2 m1v = make_float2(m1, m1), m2v = make_float2(m2, m2);
 #pragma unroll
     for (int i = 0; i < NV; i++) {
       const int vi = lane + i * 32;
       if (vi < nvec) {
-        float dv[N], xv[N], ww[N], o[N];
-        unpack_bf16x8(cdy[i], dv);
-        unpack_bf16x8(cx[i], xv);
-        unpack_bf16x8(wv[i], ww);
+        float2 dv[4], xv[4], ww[4];
+        unpack_bf16x8_2(cdy[i], dv);
+        unpack_bf16x8_2(cx[i], xv);
+        unpack_bf16x8_2(wv[i], ww);
+        float o[N];
 #pragma unroll
-        for (int k = 0; k < N; k++) {
-          const float xh = (xv[k] - mu) * rs, dn = dv[k] * ww[k];
-          o[k] = din[i][k] + (dn - s1 - xh * s2) * rs;
+        for (int k = 0; k < 4; k++) {
+          // o = din + (dn - mean(dn) - xhat * mean(dn xhat)) * rstd
+          const float2 xh = f2_fma(xv[k], rs2, nmr);
+          const float2 t = f2_fma(xh, m2v, f2_add(f2_mul(dv[k], ww[k]), m1v));
+          const float2 ov = f2_fma(t, rs2, make_float2(din[i][2 * k], din[i][2 * k + 1]));
+          o[2 * k] = ov.x;
+          o[2 * k + 1] = ov.y;
         }
         if (rout) st8(rout + (size_t)row * C + vi * N, o);
         if (rcopy) st16(rcopy + (size_t)row * C + vi * N, o);
         if (rf32) st8(rf32 + (size_t)row * C + vi * N, o);
         if (partial && want_rsum) {
+          float4* ar = reinterpret_cast<float4*>(acc + 2 * C + vi * N);
 #pragma unroll
-          for (int k = 0; k < N; k++) acc[(2 * N + k) * nvec + vi] += o[k];
+          for (int h = 0; h < 2; h++) {
+            const float4 a = ar[h];
+            const float2 lo = f2_add(make_float2(o[4 * h], o[4 * h + 1]), make_float2(a.x, a.y));
+            const float2 hi = f2_add(make_float2(o[4 * h + 2], o[4 * h + 3]), make_float2(a.z, a.w));
+            ar[h] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
         }
       }
     }
@@ -919,12 +985,14 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
   __syncthreads();
   float* dst = partial + (size_t)blockIdx.x * 3 * C;
   const int nc = want_rsum ? 3 * C : 2 * C;
-  for (int idx = threadIdx.x; idx < nc; idx += blockDim.x) {
-    const int a = idx / C, rem = idx - a * C, k = rem / nvec, vi = rem - k * nvec;
-    float t = lnb_sh[idx];
+  for (int idx = 4 * threadIdx.x; idx < nc; idx += 4 * blockDim.x) {
+    float4 t = *reinterpret_cast<const float4*>(lnb_sh + idx);
 #pragma unroll
-    for (int q = 1; q < LNBP_WARPS; q++) t += lnb_sh[(size_t)q * 3 * C + idx];
-    dst[a * C + vi * N + k] = t;
+    for (int q = 1; q < LNBP_WARPS; q++) {
+      const float4 u = *reinterpret_cast<const float4*>(lnb_sh + (size_t)q * 3 * C + idx);
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    *reinterpret_cast<float4*>(dst + idx) = t;
   }
 }
 
