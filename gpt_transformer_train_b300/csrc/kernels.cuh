@@ -199,3 +199,12 @@ cudaError_t layernorm_apply(T* y, const T* r, const float* mean, const float* rs
                             int rows, int C, cudaStream_t st);
 template <typename T>
 cudaError_t gelu_backward(T* dinp, const T* inp, const T* dout, long long n, cudaStream_t st);
+// One decoding position through every transformer block in one cooperative
+// launch (bf16): w = the [L]-stacked bf16 weights ln1w, ln1b, qkvw, qkvb, apw,
+// apb, ln2w, ln2b, fcw, fcb, fpw, fpb; qkv the KV cache ([L][B*Tmax][3C]);
+// x0 [B][C] holds the embedded rows on entry and the last block's residual on
+// return; x1 [B][C], att [B][C], h [B][4C] scratch; bar 4 bytes (zeroed
+// here).  A grid barrier that waits too long raises FLAG_TIMEOUT in flags.
+bool decode_layers_supported(int B, int C, int H, int Tmax);
+cudaError_t decode_layers(const bf16* const* w, bf16* qkv, bf16* x0, bf16* x1, bf16* att, bf16* h, unsigned* bar,
+                          int* flags, int L, int B, int C, int H, int Tmax, int pos, cudaStream_t st);

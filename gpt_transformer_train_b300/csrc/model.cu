@@ -186,6 +186,7 @@ BufferLayout buffer_layout(const gpt2_config& c) {
   b.wfold = c.ln_fold ? take(L * 7 * C * C * 2) : 0;
   b.fold_s = c.ln_fold ? take(L * 7 * C * 4) : 0;
   b.fold_c = c.ln_fold ? take(L * 7 * C * 4) : 0;
+  b.decbar = take(256);
   b.total = o;
   return b;
 }
@@ -447,6 +448,20 @@ struct Step {
     float *mu = dec_stats(), *rs = dec_stats() + Bi;
     // x = wte[tok] + wpe[pos]: the encoder with one position, its wpe row pos
     CK(m, encoder_forward<T>(x[0], tok, W(GPT2_WTE), W(GPT2_WPE) + (size_t)pos * C, Bi, 1, Ci, c.V, flags(), st));
+    if constexpr (sizeof(T) == 2) {
+      if (decode_layers_supported(Bi, Ci, c.H, c.T)) {
+        // every block in one cooperative launch; the residual comes back in x[0]
+        const bf16* w[12] = {W(GPT2_LN1W), W(GPT2_LN1B), W(GPT2_QKVW), W(GPT2_QKVB), W(GPT2_ATTPROJW),
+                             W(GPT2_ATTPROJB), W(GPT2_LN2W), W(GPT2_LN2B), W(GPT2_FCW), W(GPT2_FCB),
+                             W(GPT2_FCPROJW), W(GPT2_FCPROJB)};
+        CK(m, decode_layers(w, qkv(0), x[0], x[1], att, fg, m->at<unsigned>(m->bl.decbar), flags(), Li, Bi, Ci, c.H,
+                            c.T, pos, st));
+        CK(m, residual_layernorm_forward<T>(nullptr, lnb, mu, rs, x[0], nullptr, W(GPT2_LNFW), W(GPT2_LNFB), Bi, Ci,
+                                            st));
+        CK(m, linear_fwd(dec_logits(), lnb, W(GPT2_WTE), nullptr, Bi, c.Vp, Ci));
+        return GPT2_OK;
+      }
+    }
     int cur = 0;
     for (int l = 0; l < Li; l++) {
       if (l == 0) {

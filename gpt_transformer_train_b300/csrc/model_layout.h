@@ -50,6 +50,7 @@ struct BufferLayout {
   size_t attD, attS, partial, keys, ws, ws_floats, gnorm, flags, tok, tgt;
   size_t dec;                               // one-position inference scratch (see Step::dec_*)
   size_t wfold, fold_s, fold_c;             // ln_fold: folded qkv | fc weights [L][7C][C] bf16, their sums [L][7C]
+  size_t decbar;                            // grid-barrier counter of the one-launch decode step
   size_t total;
 };
 
