@@ -162,14 +162,17 @@ def blas_threads():
 # ---------------------------------------------------------------------------
 # CPU oracle timing (bench's reference arm and cpu_baseline leg)
 # ---------------------------------------------------------------------------
-def oracle_sample(w):
+def oracle_sample(w, full=False):
+    """The oracle's training step on the host cores: one sequence of
+    CPU_SAMPLE_T tokens, or (full) the whole B x T batch of the workload."""
     import oracle as O
     from synthetic import normal_array, zipf_tokens
     cfg = O.Config(w["L"], w["C"], w["H"], w["V"], w["Vp"], w["maxT"])
     # synthetic weights of the right shapes (timing does not depend on values)
     params = {n: normal_array(s, 100 + i, 0.02) for i, (n, s) in enumerate(O.param_shapes(cfg))}
     ref = O.GPT2(cfg, params=params, dtype=np.float32)
-    tok, tgt = zipf_tokens(1, CPU_SAMPLE_T, w["V"], SEED)
+    nb, nt = (w["B"], w["T"]) if full else (1, CPU_SAMPLE_T)
+    tok, tgt = zipf_tokens(nb, nt, w["V"], SEED)
     cores = blas_threads()
     state = {"t": 0}
 
@@ -182,27 +185,28 @@ def oracle_sample(w):
         ref.adamw_step(LR, B1, B2, EPS, WD, state["t"])
         return time.perf_counter() - t0
 
-    sample = (f"one sequence of {CPU_SAMPLE_T} tokens (B=1) of the same model, fp32 forward+backward+AdamW, "
-              f"numpy/OpenBLAS on {cores} threads")
-    return step, cores, sample
+    what = f"the full batch (B={nb}, T={nt})" if full else f"one sequence of {CPU_SAMPLE_T} tokens (B=1)"
+    sample = f"{what} of the same model, fp32 forward+backward+AdamW, numpy/OpenBLAS on {cores} threads"
+    return step, cores, sample, nb * nt
 
 
 def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    step, cores, sample = oracle_sample(w)
+    step, cores, sample, ntok = oracle_sample(w, args.oracle_full_step)
     for _ in range(args.warmup):
         step()
     times = [step() for _ in range(args.steps)]
     tot = sum(times)
-    value = CPU_SAMPLE_T * args.steps / tot
+    value = ntok * args.steps / tot
     line = {"impl": "reference", "metric": metric_name(args.workload, w), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (Zipf(1.1) tokens, N(0,0.02) weights)",
             "config": {"workload": workload_name(args.workload, w) + f"; CPU sample: {sample}",
-                       "global_batch": 1, "seq_len": CPU_SAMPLE_T, "parallelism": "host cores"},
+                       "global_batch": ntok // (w["T"] if args.oracle_full_step else CPU_SAMPLE_T),
+                       "seq_len": w["T"] if args.oracle_full_step else CPU_SAMPLE_T, "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -354,9 +358,9 @@ def run_ours(args, w):
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         del m
         torch.cuda.empty_cache()
-        stepf, cores, sample = oracle_sample(w)
+        stepf, cores, sample, ntok = oracle_sample(w)
         dt = stepf()
-        out["cpu_baseline"] = {"value": CPU_SAMPLE_T / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+        out["cpu_baseline"] = {"value": ntok / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                "sample": sample}
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -417,7 +421,9 @@ def run_decode(args, w):
            "value": B * args.steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (Zipf(1.1) prompt, seeded N(0,0.02) init)",
-           "config": {"workload": workload_name(args.workload, w) + f", decode positions {pos0}..{pos - 1}",
+           "config": {"workload": (f"GPT-2 {args.workload.upper()} decode (L={w['L']}, C={w['C']}, H={w['H']}, "
+                                   f"V={w['V']}->{w['Vp']}), B={B}, bf16 weights and KV cache, "
+                                   f"positions {pos0}..{pos - 1}"),
                       "global_batch": B, "seq_len": T, "parallelism": "single GPU",
                       "l2": "weights + KV cache read per step (up to 0.25 + 0.60 GB) exceed L2 in sum"},
            "roofline": {"kernel": "decode step (all kernels)", "bound": "hbm", "achieved": achieved,
@@ -439,6 +445,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--recompute", type=int, default=0, choices=[0, 1, 2],
                     help="activation recompute level (0: keep all activations)")
+    ap.add_argument("--oracle-full-step", action="store_true",
+                    help="--impl reference: time the oracle on the workload's whole B x T batch (minutes per step "
+                         "at 124M) instead of one sequence")
     ap.add_argument("--ln-fold", action="store_true",
                     help="fold the LayerNorms before the qkv and fc products into them (needs --recompute 2)")
     ap.add_argument("--decode", action="store_true",

@@ -34,6 +34,13 @@
 //
 // Every mbarrier wait is bounded; on expiry the CTA raises FLAG_TIMEOUT,
 // stops, frees its TMEM and returns.
+#include <map>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
+
 #include "kernels.cuh"
 #include "tc_common.cuh"
 
@@ -146,6 +153,31 @@ struct AttnParams {
   uint8_t* ds;        // backward: dS blocks (see ds_block)
 };
 
+// Which work items each persistent CTA takes.  The items of a kernel differ in
+// length (a causal query tile of index qt spans qt + 1 key tiles), so taking
+// items i = blockIdx.x, blockIdx.x + gridDim.x, ... left the busiest CTA 10-15%
+// above the mean at T = 1024.  The host assigns the items, heaviest first, each
+// to the CTA with the least work so far (longest-processing-time first, lowest
+// index on ties): every CTA then ends within one item of the mean.  The table
+// is a pure function of the shape and travels as a kernel parameter, so a
+// captured launch replays it unchanged.  n = 0: more items or CTAs than the
+// table holds; the kernels then stride over the items.
+constexpr int SCHED_MAX_ITEMS = 4096;
+constexpr int SCHED_MAX_CTAS = 256;
+struct AttnSched {
+  int n;                                 // items in the table (0: stride over them)
+  uint16_t first[SCHED_MAX_CTAS + 1];    // CTA c takes item[first[c] .. first[c + 1] - 1], in order
+  uint16_t item[SCHED_MAX_ITEMS];
+};
+
+__device__ __forceinline__ int sched_count(const AttnSched& s, int n_items) {
+  if (s.n) return s.first[blockIdx.x + 1] - s.first[blockIdx.x];
+  return n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+}
+__device__ __forceinline__ int sched_item(const AttnSched& s, int k) {
+  return s.n ? (int)s.item[s.first[blockIdx.x] + k] : (int)blockIdx.x + k * (int)gridDim.x;
+}
+
 // ============================================================================
 // forward
 // ============================================================================
@@ -173,6 +205,9 @@ __device__ __forceinline__ void tmem_ld1(uint32_t taddr, float& v) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
   v = __uint_as_float(r);
 }
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v)) : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // 32 lanes x 128 consecutive fp32 columns, four loads in flight, one wait
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
@@ -193,14 +228,42 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 }
 
 constexpr int FWD_POLY = 16;  // one exponential in this many columns from the FMA-pipe polynomial
-// The probabilities of one 128-wide score row (TMEM lane r of the warp's
-// quarter, columns tS..tS+127): read 64 columns at a time, p = 2^(s sl2 -
-// m_ref), packed to bf16 pairs and written over the first 64 columns (behind
-// every read of the pass, so no score is overwritten before it is read).  One
-// exponential in FWD_POLY comes from the FMA-pipe polynomial, the rest from
-// the MUFU unit.  DIAG: the diagonal block, columns past the row masked to 0.
+constexpr float RESCALE_LOG2 = 8.f;
+// P of one block in TMEM, as the A operand of O += P [V | 1]: 64 columns of
+// packed bf16 pairs, keys 0..63 in the 32 columns at tP0 (beside O, which
+// leaves them free) and keys 64..127 over the first 32 columns of S (whose
+// scores of keys 0..63 have been read by then).
+
+// 32 probabilities p = 2^(x) of columns col0 .. col0 + 31 from x = s sl2 -
+// m_ref, packed into 16 bf16 pairs; m2 tracks the maximum of x.  One
+// exponential in FWD_POLY from the FMA-pipe polynomial (none on the diagonal
+// block, whose keys after the query get x = -inf, p = 0).
 template <bool DIAG>
-__device__ __forceinline__ void fwd_probs(uint32_t tS, uint32_t r, float sl2, float m_ref) {
+__device__ __forceinline__ void fwd_chunk(const float* sv, int col0, uint32_t r, float sl2, float m_ref, float (&m2)[2],
+                                          uint32_t* pk) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const int col = col0 + e;
+    float x0, x1;
+    ffma2(x0, x1, sv[e], sv[e + 1], sl2, -m_ref);
+    if (DIAG) {
+      if (col > (int)r) x0 = -INFINITY;
+      if (col + 1 > (int)r) x1 = -INFINITY;
+    }
+    m2[(e >> 1) & 1] = max3(m2[(e >> 1) & 1], x0, x1);
+    if (!DIAG && (col % FWD_POLY) == FWD_POLY - 2) x0 = exp2_poly(x0);
+    else x0 = ex2(x0);
+    x1 = ex2(x1);
+    pk[e >> 1] = pack_bf16(x0, x1);
+  }
+}
+
+// The probabilities of one 128-wide score row (TMEM lane r of the warp's
+// quarter, scores at tS) against the reference m_ref, read 64 columns at a
+// time and written to the P layout above.
+template <bool DIAG>
+__device__ __forceinline__ void fwd_probs(uint32_t tS, uint32_t tP0, uint32_t r, float sl2, float m_ref) {
+  float m2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int h = 0; h < 2; h++) {
     float sv[64];
@@ -210,23 +273,49 @@ __device__ __forceinline__ void fwd_probs(uint32_t tS, uint32_t r, float sl2, fl
 #pragma unroll
     for (int c = 0; c < 2; c++) {
       uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const int lc = 32 * c + e, col = 64 * h + lc;
-        float x0, x1;
-        ffma2(x0, x1, sv[lc], sv[lc + 1], sl2, -m_ref);
-        if (!DIAG) {
-          x0 = (col % FWD_POLY) == FWD_POLY - 2 ? exp2_poly(x0) : ex2(x0);
-          x1 = ex2(x1);
-        } else {
-          x0 = col > (int)r ? 0.f : ex2(x0);
-          x1 = col + 1 > (int)r ? 0.f : ex2(x1);
-        }
-        pk[e >> 1] = pack_bf16(x0, x1);
-      }
-      tmem_st16(tS + 32 * h + 16 * c, pk);
+      fwd_chunk<DIAG>(sv + 32 * c, 64 * h + 32 * c, r, sl2, m_ref, m2, pk);
+      tmem_st16((h ? tS : tP0) + 16 * c, pk);
     }
   }
+}
+
+// The same probabilities in one read of the scores, for a block after the
+// first below the diagonal: the row's maximum is tracked while p is taken against the current
+// reference.  Keys 0..63 are written at once (to tP0, which leaves the scores
+// intact); keys 64..127 stay in registers and are written only when no row of
+// the warp has run more than RESCALE_LOG2 above its reference.  Otherwise
+// false is returned with the scores untouched (fwd_probs then redoes the
+// block); mrel = max over the valid columns of s sl2 - m_ref for this row.
+__device__ __forceinline__ bool fwd_probs_once(uint32_t tS, uint32_t tP0, uint32_t r, float sl2, float m_ref,
+                                               float& mrel) {
+  float m2[2] = {-INFINITY, -INFINITY};
+  {
+    float sv[64];
+    tmem_ld32_async(tS, *reinterpret_cast<float(*)[32]>(sv));
+    tmem_ld32_async(tS + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+      uint32_t pk[16];
+      fwd_chunk<false>(sv + 32 * c, 32 * c, r, sl2, m_ref, m2, pk);
+      tmem_st16(tP0 + 16 * c, pk);
+    }
+  }
+  uint32_t pk[32];
+  {
+    float a[32], b[32];
+    tmem_ld32_async(tS + 64, a);
+    tmem_wait_ld();
+    tmem_ld32_async(tS + 96, b);  // in flight while keys 64..95 are worked
+    fwd_chunk<false>(a, 64, r, sl2, m_ref, m2, pk);
+    tmem_wait_ld();
+    fwd_chunk<false>(b, 96, r, sl2, m_ref, m2, pk + 16);
+  }
+  mrel = fmaxf(m2[0], m2[1]);
+  if (!__all_sync(0xffffffffu, !(mrel > RESCALE_LOG2))) return false;
+  tmem_st16(tS, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+  tmem_st16(tS + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+  return true;
 }
 
 // Online softmax with a lazily rescaled accumulator: the probabilities of a
@@ -242,8 +331,10 @@ __device__ __forceinline__ void fwd_probs(uint32_t tS, uint32_t r, float sl2, fl
 // thread per query row with the whole 128-wide score row in registers.  Per
 // key block j and tile t:
 //   S_t = Q_t K_j^T                  (TMEM columns 128 t .. 128 t + 127)
-//   P_t = exp2(S_t sl2 - m_ref)      written as bf16 back over the first 64
-//                                     columns of S_t (no shared-memory trip)
+//   P_t = exp2(S_t sl2 - m_ref)      written as bf16 pairs into TMEM (keys
+//                                     0..63 beside O_t, keys 64..127 over the
+//                                     first 32 columns of S_t; no shared-memory
+//                                     trip)
 //   O_t += P_t [V_j | 1]             A = P_t from TMEM, B = V_j and a block of
 //                                     ones from shared memory: N = 80, so
 //                                     column 64 of O_t accumulates the row
@@ -251,18 +342,35 @@ __device__ __forceinline__ void fwd_probs(uint32_t tS, uint32_t r, float sl2, fl
 // and S_t of block j+1 is issued right behind that P V (the tensor core takes
 // them in order, so it reads P_t before overwriting it).  The two tiles'
 // softmax phases interleave: one tile's exponentials overlap the other's MMAs.
-constexpr float RESCALE_LOG2 = 8.f;
+// O *= alpha for this thread's row: the 64 value columns and the row sum
+// (column 64); the columns after it hold P (see FWD_P0) and stay as they are
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+  float ov[32], l;
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+    tmem_ld32(tO + 32 * c, ov);
+#pragma unroll
+    for (int e = 0; e < 32; e++) ov[e] *= alpha;
+    tmem_st32(tO + 32 * c, ov);
+  }
+  tmem_ld1(tO + 64, l);
+  tmem_wait_ld();
+  tmem_st1(tO + 64, l * alpha);
+}
+
 constexpr int FWD_STAGES = 3;
 constexpr uint32_t FWD_KV = 2 * TILE;  // K tile then V tile
 constexpr int FWD_ON = 80;             // P V width: 64 value columns + the row-sum column (+ 15 unused)
+constexpr uint32_t FWD_P0 = 256 + FWD_ON;  // P of keys 0..63, relative to the tile's S columns (beside O)
 constexpr size_t FWD_SMEM = 1024 + 2 * TILE + FWD_STAGES * FWD_KV + TILE + 256;
 constexpr int FWD_THREADS = 64 + 32 * 8;  // producer, MMA, two softmax warpgroups
 
-// Persistent: each CTA takes work items blockIdx.x, blockIdx.x + gridDim.x, ...
-// (item = one pair of query tiles of one (b, h), heaviest first).  Every
+// Persistent: each CTA takes the work items its schedule table lists (item =
+// one pair of query tiles of one (b, h); item indices run heaviest first).  Every
 // barrier phase is tracked by a running counter across items, so the next
 // item's Q load, first Q K^T and K/V loads overlap the tail of the current one.
-__global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tqkv, AttnParams p) {
+__global__ void __launch_bounds__(FWD_THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tqkv, AttnParams p, const __grid_constant__ AttnSched sch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sQ = smem_u32(smem);                  // 2 query tiles
@@ -282,6 +390,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
   const int nq = p.T / 128, npair = (nq + 1) / 2;
   const int BH = p.B * p.H;
   const int n_items = BH * npair;
+  const int n_mine = sched_count(sch, n_items);
   struct Item { int qt0, nkv, b, h, row0; bool two; };
   auto item = [&](int i) {
     Item it;
@@ -323,13 +432,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
   fence_after();
   const uint32_t tmem = *tmem_holder;
   pdl_enter();  // global memory only from here on
-  // TMEM columns: S (and P) of tile t at 128 t, O of tile t at 256 + 128 t (80 wide)
+  // TMEM columns: S of tile t at 128 t, O of tile t at 256 + 128 t (80 wide), P of tile t:
+  // keys 0..63 at 336 + 128 t (32 columns), keys 64..127 at 128 t (32 columns)
 
   if (warp == 0) {
     if (lane == 0) {  // ---- TMA producer
       uint32_t g = 0, n = 0;  // K/V blocks and items loaded so far
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
+      for (int ki = 0; ok && ki < n_mine; ki++, n++) {
+        const int i = sched_item(sch, ki);
         const Item it = item(i);
         // the Q tiles are free once the previous item's last Q K^T has completed
         if (!mbar_wait(b_qempty, (n & 1) ^ 1, abort_flag)) break;
@@ -354,7 +465,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
       uint32_t nP[2] = {0, 0}, nO[2] = {0, 0};                  // per tile: P blocks consumed, items finished
       int kv_ready = -1;                                        // highest K/V block known loaded (global index)
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
+      for (int ki = 0; ok && ki < n_mine; ki++, n++) {
+        const int i = sched_item(sch, ki);
         const Item it = item(i);
         const int last_t = it.two ? 1 : 0;
         auto active = [&](int t, int j) { return t == 0 ? j <= it.qt0 : (it.two && j <= it.qt0 + 1); };
@@ -395,7 +507,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
             fence_after();
 #pragma unroll
             for (int kk = 0; kk < 128 / 16; kk++)
-              mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, sdesc(v + kk * 2048, lbo, 1024), ID_O,
+              mma_bf16_ts(tmem + 256 + 128 * t, tmem + 128 * t + (kk < 4 ? FWD_P0 + 8 * kk : 8 * (kk - 4)),
+                          sdesc(v + kk * 2048, lbo, 1024), ID_O,
                           (j | kk) > 0);
             mma_commit(b_pvdone + 8 * t);
             nP[t]++;
@@ -413,10 +526,11 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
     const int t = (warp - 2) >> 2, q = warp & 3;
     const uint32_t r = q * 32 + lane;  // row inside the tile
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
-    const uint32_t tS = tmem + lrow + 128 * t, tO = tmem + lrow + 256 + 128 * t;
+    const uint32_t tS = tmem + lrow + 128 * t, tO = tmem + lrow + 256 + 128 * t, tP0 = tS + FWD_P0;
     uint32_t nS = 0, nPV = 0;  // S blocks consumed; P V products of this tile before the current item
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    for (int ki = 0; ok && ki < n_mine; ki++) {
+      const int i = sched_item(sch, ki);
       const Item it = item(i);
       const int qt = it.qt0 + t;
       if (qt >= nq) continue;  // this item has no tile t
@@ -426,6 +540,28 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
         nS++;
         fence_after();
         const bool diag = j == qt;
+        if (j > 0 && !diag) {
+          // one read of the scores against the current reference; a row that
+          // ran too far above it moves the reference, and the block is redone
+          float mrel;
+          if (!fwd_probs_once(tS, tP0, r, p.sl2, m_ref, mrel)) {
+            const bool need = mrel > RESCALE_LOG2;
+            const float m_old = m_ref;
+            if (need) m_ref += mrel;
+            tmem_wait_st();  // the first half's stores land before they are redone
+            fwd_probs<false>(tS, tP0, r, p.sl2, m_ref);
+            // O holds blocks 0 .. j-1 once the previous P V has completed
+            if (!mbar_wait_warp(b_pvdone + 8 * t, (nPV + j - 1) & 1, abort_flag)) { ok = false; break; }
+            fence_after();
+            rescale_o(tO, need ? ex2(m_old - m_ref) : 1.f);
+          }
+          tmem_wait_st();
+          fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_pfull + 8 * t);
+          continue;
+        }
+        // the first and the diagonal block: two reads of the scores
         float mx;
         {  // pass 1: the row maximum over the valid columns (c <= r on the diagonal block)
           float sv[128];
@@ -450,23 +586,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) attn_fwd_tc_kernel(const __gri
         const bool need = j > 0 && mx > m_ref + RESCALE_LOG2;
         const float m_old = m_ref;
         if (j == 0 || need) m_ref = mx;
-        // pass 2: the scores again, 64 columns at a time; probabilities packed
-        // to bf16 pairs over the first 64 columns of S
-        if (!diag) fwd_probs<false>(tS, r, p.sl2, m_ref);
-        else fwd_probs<true>(tS, r, p.sl2, m_ref);
+        // pass 2: the scores again, 64 columns at a time, into P
+        if (!diag) fwd_probs<false>(tS, tP0, r, p.sl2, m_ref);
+        else fwd_probs<true>(tS, tP0, r, p.sl2, m_ref);
         if (__any_sync(0xffffffffu, need)) {
           // O holds blocks 0 .. j-1 once the previous P V has completed
           if (!mbar_wait_warp(b_pvdone + 8 * t, (nPV + j - 1) & 1, abort_flag)) { ok = false; break; }
           fence_after();
-          const float alpha = need ? ex2(m_old - m_ref) : 1.f;
-          float ov[32];
-#pragma unroll
-          for (int c = 0; c < 3; c++) {  // 64 value columns and the row sum (column 64)
-            tmem_ld32(tO + 32 * c, ov);
-#pragma unroll
-            for (int e = 0; e < 32; e++) ov[e] *= alpha;
-            tmem_st32(tO + 32 * c, ov);
-          }
+          rescale_o(tO, need ? ex2(m_old - m_ref) : 1.f);
         }
         tmem_wait_st();
         fence_before();
@@ -567,7 +694,8 @@ constexpr int DQ_THREADS = 64 + 32 * 4;      // producer, MMA, 4 read-out warps
 constexpr size_t DQ_SMEM = 1024 + DQ_STAGES * DQ_STAGE + 256;
 
 __global__ void __launch_bounds__(DQ_THREADS, 1)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const uint8_t* __restrict__ ds, AttnParams p) {
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const uint8_t* __restrict__ ds, AttnParams p,
+                          const __grid_constant__ AttnSched sch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t ring = smem_u32(smem);
@@ -581,6 +709,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = p.T / 128, BH = p.B * p.H;
   const int n_items = BH * nq;
+  const int n_mine = sched_count(sch, n_items);
   auto item_qt = [&](int i) { return nq - 1 - i / BH; };  // heaviest tiles first
 
   if (threadIdx.x == 0) {
@@ -608,7 +737,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+      for (int ki = 0; ok && ki < n_mine; ki++) {
+        const int i = sched_item(sch, ki);
         const int qt = item_qt(i), bh = i % BH, h = bh % p.H, row0 = (bh / p.H) * p.T;
         for (int kt = 0; kt <= qt; kt++, g++) {
           const uint32_t s = g % DQ_STAGES, ph = (g / DQ_STAGES) & 1;
@@ -627,7 +757,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       constexpr uint32_t ID_DQ = idesc_bf16(128, HD, 1, 1);
       uint32_t g = 0, n = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
+      for (int ki = 0; ok && ki < n_mine; ki++, n++) {
+        const int i = sched_item(sch, ki);
         const int qt = item_qt(i);
         const uint32_t a = n & 1, acc = tmem + 64 * a;
         if (!mbar_wait(b_accfree + 8 * a, ((n >> 1) & 1) ^ 1, abort_flag)) break;
@@ -649,7 +780,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const int q = warp & 3;
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
     uint32_t n = 0;
-    for (int i = blockIdx.x; i < n_items; i += gridDim.x, n++) {
+    for (int ki = 0; ki < n_mine; ki++, n++) {
+      const int i = sched_item(sch, ki);
       const int qt = item_qt(i), bh = i % BH, h = bh % p.H, row0 = (bh / p.H) * p.T;
       const uint32_t a = n & 1;
       if (!mbar_wait_warp(b_accfull + 8 * a, (n >> 1) & 1, abort_flag)) break;
@@ -689,7 +821,7 @@ constexpr size_t DKV_SMEM = 1024 + 2 * TILE + DKV_STAGES * BWD_QD + 2 * PTILE + 
 
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
-                           AttnParams p) {
+                           AttnParams p, const __grid_constant__ AttnSched sch) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sK = smem_u32(smem), sV = sK + TILE;
@@ -713,6 +845,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq = p.T / 128, BH = p.B * p.H;
   const int n_items = BH * nq;
+  const int n_mine = sched_count(sch, n_items);
   struct Item { int kt, nit, bh, b, h, row0; size_t sbase; };
   auto item = [&](int i) {
     Item it;
@@ -760,7 +893,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (lane == 0) {
       uint32_t g = 0, n = 0;
       bool ok = true;
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
+      for (int ki = 0; ok && ki < n_mine; ki++, n++) {
+        const int i = sched_item(sch, ki);
         const Item it = item(i);
         if (!mbar_wait(b_kvempty, (n & 1) ^ 1, abort_flag)) break;
         mbar_expect_tx(b_kvfull, 2 * TILE);
@@ -801,7 +935,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         nG++;
         return true;
       };
-      for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
+      for (int ki = 0; ok && ki < n_mine; ki++, n++) {
+        const int i = sched_item(sch, ki);
         const Item it = item(i);
         if (!mbar_wait(b_kvfull, n & 1, abort_flag)) break;
         for (int k = 0; ok && k < it.nit; k++) {
@@ -831,7 +966,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint32_t lrow = (uint32_t)(q * 32) << 16;
     uint32_t g0 = 0, n = 0, nS = 0, nG = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x, n++) {
+    for (int ki = 0; ok && ki < n_mine; ki++, n++) {
+      const int i = sched_item(sch, ki);
       const Item it = item(i);
       for (int k = 0; k < it.nit; k++) {
         if (!mbar_wait_warp(b_sfull, nS & 1, abort_flag)) { ok = false; break; }
@@ -918,7 +1054,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   } else {  // ---- the dS store warp: each finished dS^T tile to its block of the dS buffer
     uint32_t nG = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < n_items; i += gridDim.x) {
+    for (int ki = 0; ok && ki < n_mine; ki++) {
+      const int i = sched_item(sch, ki);
       const Item it = item(i);
       for (int k = 0; k < it.nit; k++, nG++) {
         if (!mbar_wait_warp(b_pfull, nG & 1, abort_flag)) { ok = false; break; }
@@ -947,6 +1084,51 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return kernel_smem_attr(kernel, (int)bytes);
 }
 
+// The schedule table of one kernel at one shape (see AttnSched).  kind 0: the
+// forward (item i = pair of query tiles qt0, qt0 + 1 with qt0 = 2 (npair - 1 -
+// i / BH): qt0 + 1 + qt0 + 2 key tiles); kind 1: dK/dV (key tile kt = i / BH:
+// nq - kt query tiles); kind 2: dQ (query tile qt = nq - 1 - i / BH: qt + 1 key
+// tiles).  Built once per (kind, BH, nq, grid) and kept.
+const AttnSched& attn_schedule(int kind, int BH, int nq, int grid) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int>, std::unique_ptr<AttnSched>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto& slot = cache[std::make_tuple(kind, BH, nq, grid)];
+  if (slot) return *slot;
+  slot.reset(new AttnSched());
+  AttnSched& s = *slot;
+  const int npair = (nq + 1) / 2;
+  const long long n_items = (long long)BH * (kind == 0 ? npair : nq);
+  s.n = 0;
+  if (n_items <= 0 || n_items > SCHED_MAX_ITEMS || grid <= 0 || grid > SCHED_MAX_CTAS) return s;
+  auto weight = [&](int i) -> long long {
+    const int cls = i / BH;
+    if (kind == 0) {
+      const int qt0 = 2 * (npair - 1 - cls);
+      return qt0 + 1 + (qt0 + 1 < nq ? qt0 + 2 : 0);
+    }
+    if (kind == 1) return nq - cls;
+    return nq - cls;  // dQ: qt + 1 with qt = nq - 1 - cls
+  };
+  using Slot = std::pair<long long, int>;  // (work so far, CTA)
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> pq;
+  for (int c = 0; c < grid; c++) pq.push({0, c});
+  std::vector<int> owner((size_t)n_items), count((size_t)grid, 0);
+  for (int i = 0; i < (int)n_items; i++) {
+    const Slot top = pq.top();
+    pq.pop();
+    owner[i] = top.second;
+    count[top.second]++;
+    pq.push({top.first + weight(i), top.second});
+  }
+  s.first[0] = 0;
+  for (int c = 0; c < grid; c++) s.first[c + 1] = (uint16_t)(s.first[c] + count[c]);
+  std::vector<int> pos(s.first, s.first + grid);
+  for (int i = 0; i < (int)n_items; i++) s.item[pos[owner[i]]++] = (uint16_t)i;
+  s.n = (int)n_items;
+  return s;
+}
+
 }  // namespace
 
 bool attention_tc_supported(int B, int T, int C, int H) {
@@ -970,7 +1152,9 @@ cudaError_t attention_forward_tc(bf16* out, float* lse, const bf16* qkv, int B, 
   const long long items = (long long)B * H * npair;
   const int sms = tc_num_sms();
   gpt2_count_launches(1);
-  launch_k(attn_fwd_tc_kernel, dim3((unsigned)(items < sms ? items : sms)), dim3(FWD_THREADS), FWD_SMEM, st, tq, p);
+  const int grid = (int)(items < sms ? items : sms);
+  const AttnSched& sch = attn_schedule(0, B * H, T / 128, grid);
+  launch_k(attn_fwd_tc_kernel, dim3((unsigned)grid), dim3(FWD_THREADS), FWD_SMEM, st, tq, p, sch);
   return cudaGetLastError();
 }
 
@@ -1009,9 +1193,11 @@ cudaError_t attention_backward_tc(bf16* dqkv, float* Dbuf, void* dS, const bf16*
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  launch_k(attn_bwd_dkv_tc_kernel, dim3(grid), dim3(BWD_THREADS), DKV_SMEM, st, tq, td, p);
+  launch_k(attn_bwd_dkv_tc_kernel, dim3(grid), dim3(BWD_THREADS), DKV_SMEM, st, tq, td, p,
+           attn_schedule(1, B * H, T / 128, (int)grid));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  launch_k(attn_bwd_dq_tc_kernel, dim3(grid), dim3(DQ_THREADS), DQ_SMEM, st, tq, (const uint8_t*)dS, p);
+  launch_k(attn_bwd_dq_tc_kernel, dim3(grid), dim3(DQ_THREADS), DQ_SMEM, st, tq, (const uint8_t*)dS, p,
+           attn_schedule(2, B * H, T / 128, (int)grid));
   return cudaGetLastError();
 }

@@ -35,6 +35,8 @@ ACC = 2.0 ** -16      # fp32 accumulation allowance per unit of sum |a b|
 C_ATT_FWD = 2.0       # attention forward: P in bf16 + exponentials
 C_ATT_BWD = 4.0       # attention backward: P, dS in bf16, D from the stored output
 C_LOGITS = 4.0        # whole-model logits: bf16 weight copy + bf16 activations upstream
+TINY = 2.0 ** -126    # fp32 exponentials flush to zero (or clamp) below the smallest normal
+SUB = 2.0 ** -133     # bf16 subnormal step: the absolute rounding floor of a bf16 output
 
 
 def check(got, ref, bound, what=""):
@@ -96,6 +98,11 @@ def attention_bounds(qkv, dout, o_kernel, H):
       dk:   U8 |dK| + C_ATT_BWD U8 s sum_i E_ij |Q_i|
     with s = 1/sqrt(hd) and E_ij = P_ij (|dP_ij| + |D_i| + sum_d |dO_id O_id|),
     the magnitude of dS_ij = P_ij (dP_ij - D_i) and of its rounding sources.
+    Each also gets the underflow floor of fp32 exponentials: a probability
+    below 2^-126 comes out as 0 or 2^-126, so every causal term may be off by
+    TINY (out: TINY sum_j |V_j|, dv: TINY sum_i |dO_i|, dq/dk: C_ATT_BWD TINY s
+    sum (|dP_ij| + |D_i|) |K_j| (|Q_i|)), and the bf16 subnormal step SUB.
+    These matter only where the scores span more than 2^126 within a row.
     """
     qkv = np.asarray(qkv, np.float64)
     dout = np.asarray(dout, np.float64)
@@ -117,10 +124,12 @@ def attention_bounds(qkv, dout, o_kernel, H):
     dP = do @ v.transpose(0, 1, 3, 2)
     D = (do * heads(ro)).sum(-1)
     E = att * (np.abs(dP) + np.abs(D)[..., None] + (np.abs(do) * np.abs(ok)).sum(-1)[..., None])
-    out_b = U8 * np.abs(ro) + C_ATT_FWD * U8 * merge(att @ np.abs(v))
-    dv_b = C_ATT_FWD * U8 * merge(att.transpose(0, 1, 3, 2) @ np.abs(do))
-    dq_b = C_ATT_BWD * U8 * s * merge(E @ np.abs(k))
-    dk_b = C_ATT_BWD * U8 * s * merge(E.transpose(0, 1, 3, 2) @ np.abs(q))
+    causal = np.tril(np.ones((T, T)))
+    F = causal * (np.abs(dP) + np.abs(D)[..., None])
+    out_b = U8 * np.abs(ro) + C_ATT_FWD * U8 * merge(att @ np.abs(v)) + TINY * merge(causal @ np.abs(v)) + SUB
+    dv_b = C_ATT_FWD * U8 * merge(att.transpose(0, 1, 3, 2) @ np.abs(do)) + TINY * merge(causal.T @ np.abs(do)) + SUB
+    dq_b = C_ATT_BWD * s * merge((U8 * E + TINY * F) @ np.abs(k)) + SUB
+    dk_b = C_ATT_BWD * s * merge((U8 * E + TINY * F).transpose(0, 1, 3, 2) @ np.abs(q)) + SUB
     rq, rk, rv = rd[..., :C], rd[..., C:2 * C], rd[..., 2 * C:]
     return {
         "out": (ro, out_b),

@@ -661,6 +661,25 @@ def test_attention_tc_against_oracle(ops, B, T, C, H, sigma):
     _check_attention_elementwise(qs, dos, host(out).reshape(B, T, C), host(dq).reshape(B, T, 3 * C), H)
 
 
+@pytest.mark.parametrize("growth", [1.25, 1.8])
+def test_attention_tc_growing_scores(ops, growth):
+    """Keys scaled by growth^(key tile): the scores of each later key tile run
+    further above the earlier ones, so rows keep moving their softmax
+    reference after the first tile (growth 1.8: about half the rows of a
+    tile, 1.25: a few rows of some warps and none of others), through the path that
+    redoes a tile's probabilities and rescales the accumulator.  Element-wise
+    against the oracle."""
+    B, T, C, H = 2, 1024, 128, 2
+    qkv = normal_array((B, T, 3 * C), 78)
+    scale = growth ** (np.arange(T) // 128)
+    qkv[:, :, C:2 * C] *= scale[None, :, None].astype(np.float32)
+    dout = normal_array((B, T, C), 79)
+    tq, tdo, out, lse, dq, D = _attention_tc(ops, qkv, dout, B, T, C, H)
+    qs, dos = host(tq), host(tdo)
+    assert np.max(np.abs(host(lse).reshape(B, H, T) - _lse_ref(qs, B, T, C, H))) < LSE_TOL
+    _check_attention_elementwise(qs, dos, host(out).reshape(B, T, C), host(dq).reshape(B, T, 3 * C), H)
+
+
 def _check_attention_elementwise(qs, dos, o, dqkv, H):
     """O, dQ, dK, dV of the tensor-core kernels element by element against the
     float64 oracle, within the bounds of tests/parity.py."""
