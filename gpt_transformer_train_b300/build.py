@@ -61,7 +61,7 @@ def build(force=False, verbose=False):
         results = list(ex.map(lambda s: _compile(s, verbose), todo))
     failed = [(s, out) for s, rc, out in results if rc != 0]
     for s, rc, out in results:
-        if verbose or rc != 0:
+        if out.strip():  # errors, warnings, and with verbose the ptxas report
             sys.stderr.write(out)
     if failed:
         raise RuntimeError("nvcc failed building " + ", ".join(os.path.basename(s) for s, _ in failed))

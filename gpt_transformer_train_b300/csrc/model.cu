@@ -473,8 +473,8 @@ struct Step {
         cur ^= 1;
       }
       // q | k | v of position pos straight into cache rows b*T + pos
-      GemmArgs a{lnb, C, 1, W(GPT2_QKVW, l, 3 * CC), C, 1, Bi, 3 * Ci, Ci, qkv(l) + (size_t)pos * 3 * C,
-                 (long long)c.T * 3 * C, W(GPT2_QKVB, l, 3 * C), nullptr, 0, EPI_STORE};
+      GemmArgs a{lnb, (long long)C, 1, W(GPT2_QKVW, l, 3 * CC), (long long)C, 1, Bi, 3 * Ci, Ci,
+                 qkv(l) + (size_t)pos * 3 * C, (long long)c.T * 3 * Ci, W(GPT2_QKVB, l, 3 * C), nullptr, 0, EPI_STORE};
       CK(m, gemm(a));
       CK(m, decode_attention<T>(att, qkv(l), Bi, c.T, pos, Ci, c.H, st));
       CK(m, linear_fwd(prj, att, W(GPT2_ATTPROJW, l, CC), W(GPT2_ATTPROJB, l, C), Bi, Ci, Ci));
