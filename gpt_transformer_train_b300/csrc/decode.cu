@@ -65,6 +65,20 @@ __device__ __forceinline__ float ldcg_bf16(const bf16* p) {
   const unsigned short u = __ldcg(reinterpret_cast<const unsigned short*>(p));
   return __uint_as_float((unsigned)u << 16);
 }
+// shared memory at the start of the kernel's dynamic area: the staged operand
+// rows of the products ([NB][4C] bf16) and, in the attention phase of a head
+// of size 64, the values of every cached position ([Tmax][64] bf16)
+__host__ __device__ inline size_t decode_region0(int NB, int C, int Tmax) {
+  const size_t a = (size_t)NB * 4 * C * sizeof(bf16), b = (size_t)Tmax * 64 * sizeof(bf16);
+  return a > b ? a : b;
+}
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -136,37 +150,47 @@ __device__ void ln_rows(bf16* out, const bf16* x, const bf16* w, const bf16* b, 
 
 // y[b][n] = sum_k X[b][k] W[n][k] for the columns n of this CTA's range
 // [n0, n1): X [B][K] in shared memory (bf16; rows B..NB-1 are not used), W
-// [N][K] row-major bf16.  Warp w takes columns n0 + w, n0 + w + 16, ...; lane
-// l takes k = 8 l + 256 j, issuing the loads of up to DOT_VEC of its 16-byte
-// words of the weight row before any arithmetic (the weights stream from HBM:
-// enough bytes must be in flight), and keeps one partial sum per sequence of
-// a group of DOT_GROUP; each sequence's partials are added by a fixed shuffle
-// tree and lane b of the group stores it through epi(b, n, value).
-constexpr int DOT_VEC = 4;
+// [N][K] row-major bf16.  The work is cut into units of one column and one
+// part of its k range: when the CTA has fewer columns than warps, each
+// column's k range is split into S parts so that every warp streams weights
+// (the weights come from HBM: enough bytes must be in flight).  In a unit,
+// lane l takes k = 8 l + 256 j over the part's chunks j, issuing the loads
+// of up to DOT_VEC of its 16-byte words before any arithmetic, and keeps one
+// partial sum per sequence of a group of DOT_GROUP; each sequence's partials
+// are added by a fixed shuffle tree into `red` (S * (n1 - n0) * B floats of
+// shared memory); then the parts of each column are added in part order and
+// each sum goes out through epi(b, n, value).  Called by every thread of the
+// CTA (it synchronises the CTA).
+constexpr int DOT_VEC = 3;
 constexpr int DOT_GROUP = 8;  // sequences whose partial sums are live at once
 template <int NB, typename Epi>
-__device__ void dot_columns(const bf16* X, const bf16* W, int K, int n0, int n1, int B, Epi epi) {
+__device__ void dot_columns(const bf16* X, const bf16* W, int K, int n0, int n1, int B, float* red, Epi epi) {
   constexpr int G = NB < DOT_GROUP ? NB : DOT_GROUP;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int n = n0 + warp; n < n1; n += DEC_WARPS) {
+  const int ncol = n1 - n0, nch = (K + 255) / 256;
+  int S = ncol > 0 ? DEC_WARPS / ncol : 1;
+  S = S < 1 ? 1 : (S > nch ? nch : S);
+  for (int u = warp; u < ncol * S; u += DEC_WARPS) {
+    const int n = n0 + u / S, part = u % S;
+    const int j0 = part * nch / S, j1 = (part + 1) * nch / S;
     const bf16* wr = W + (size_t)n * K;
     for (int b0 = 0; b0 < B; b0 += G) {  // (a second group re-reads the row from L1)
       float acc[G];
 #pragma unroll
       for (int b = 0; b < G; b++) acc[b] = 0.f;
-      for (int k0 = 0; k0 < K; k0 += 256 * DOT_VEC) {
+      for (int jb = j0; jb < j1; jb += DOT_VEC) {
         uint4 wq[DOT_VEC];
 #pragma unroll
-        for (int j = 0; j < DOT_VEC; j++) {
-          const int k = k0 + 8 * lane + 256 * j;
-          if (k < K) wq[j] = __ldg(reinterpret_cast<const uint4*>(wr + k));
+        for (int v = 0; v < DOT_VEC; v++) {
+          const int k = 256 * (jb + v) + 8 * lane;
+          if (jb + v < j1 && k < K) wq[v] = __ldg(reinterpret_cast<const uint4*>(wr + k));
         }
 #pragma unroll
-        for (int j = 0; j < DOT_VEC; j++) {
-          const int k = k0 + 8 * lane + 256 * j;
-          if (k < K) {
+        for (int v = 0; v < DOT_VEC; v++) {
+          const int k = 256 * (jb + v) + 8 * lane;
+          if (jb + v < j1 && k < K) {
             float wv[8];
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&wq[j]);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&wq[v]);
 #pragma unroll
             for (int i = 0; i < 4; i++) {
               const float2 t = __bfloat1622float2(h2[i]);
@@ -183,13 +207,20 @@ __device__ void dot_columns(const bf16* X, const bf16* W, int K, int n0, int n1,
           }
         }
       }
-      // each sequence's partial sums across the lanes by a fixed tree; lane b stores it
+      // each sequence's partial sums across the lanes by a fixed tree
 #pragma unroll
       for (int b = 0; b < G; b++) acc[b] = warp_sum(acc[b]);
 #pragma unroll
       for (int b = 0; b < G; b++)
-        if (lane == b && b0 + b < B) epi(b0 + b, n, acc[b]);
+        if (lane == b && b0 + b < B) red[((size_t)part * ncol + (n - n0)) * B + b0 + b] = acc[b];
     }
+  }
+  __syncthreads();
+  // the parts of each column, added in part order
+  for (int e = threadIdx.x; e < ncol * B; e += DEC_THREADS) {
+    float v = red[e];
+    for (int q = 1; q < S; q++) v += red[(size_t)q * ncol * B + e];
+    epi(e % B, n0 + e / B, v);
   }
 }
 
@@ -199,7 +230,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
   __shared__ int sh_abort;
   __shared__ float red[DEC_WARPS];
   bf16* xs = reinterpret_cast<bf16*>(dec_sh);  // [B][max(C, 4C)] staged operand rows
-  float* sc = reinterpret_cast<float*>(dec_sh + (size_t)NB * 4 * p.C * sizeof(bf16));  // attention scores [Tmax]
+  float* sc = reinterpret_cast<float*>(dec_sh + decode_region0(NB, p.C, p.Tmax));  // attention scores [Tmax]
   if (threadIdx.x == 0) sh_abort = 0;
   __syncthreads();
   const int C = p.C, B = p.B, hd = C / p.H;
@@ -210,6 +241,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
     a = min(N, cta * per);
     b = min(N, a + per);
   };
+  float* red_dot = sc + p.Tmax;  // part sums of dot_columns (the attention's partial rows otherwise)
   unsigned nbar = 0;
   bf16 *x = p.x0, *xn = p.x1;
   for (int l = 0; l < p.L; l++) {
@@ -222,13 +254,103 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
       int n0, n1;
       range(3 * C, n0, n1);
       const bf16* bias = p.qkvb + (size_t)l * C3;
-      dot_columns<NB>(xs, p.qkvw + (size_t)l * C3 * C, C, n0, n1, B, [&](int b, int n, float v) {
+      dot_columns<NB>(xs, p.qkvw + (size_t)l * C3 * C, C, n0, n1, B, red_dot, [&](int b, int n, float v) {
         cache[((size_t)b * p.Tmax + p.pos) * C3 + n] = __float2bfloat16_rn(v + __bfloat162float(bias[n]));
       });
     }
     if (!grid_barrier(p.bar, ++nbar, p.flags, &sh_abort)) return;
     // ---- B: attention of position pos, one (sequence, head) per CTA at a time
-    for (int bh = cta; bh < B * p.H; bh += ncta) {
+    // Head size 64 (every GPT-2 size): the values of keys 0..pos are copied
+    // into shared memory (cp.async) while the scores are formed, eight
+    // threads per key (one 16-byte piece of the key each, the loads of four
+    // keys in flight at once); P V then reads the values from shared memory.
+    for (int bh = cta; hd == 64 && bh < B * p.H; bh += ncta) {
+      const int b = bh / p.H, hh = bh % p.H, nk = p.pos + 1;
+      const bf16* base = cache + (size_t)b * p.Tmax * C3 + hh * 64;
+      bf16* vs = reinterpret_cast<bf16*>(dec_sh);  // [nk][64]
+      float* part = sc + p.Tmax;                   // [8][64] partial output rows, then q [64]
+      float* qf = part + DEC_THREADS * 8 - 64;
+      for (int c = threadIdx.x; c < nk * 8; c += DEC_THREADS)
+        cp_async16(vs + 8 * c, base + 2 * C + (size_t)(c >> 3) * C3 + 8 * (c & 7));
+      if (threadIdx.x < 64) qf[threadIdx.x] = ldcg_bf16(base + (size_t)p.pos * C3 + threadIdx.x) * p.scale;
+      __syncthreads();
+      const int cc = threadIdx.x & 7, kg = threadIdx.x >> 3;  // piece of the key, first key
+      float qv[8];
+#pragma unroll
+      for (int e = 0; e < 8; e++) qv[e] = qf[8 * cc + e];
+      float mx = -INFINITY;
+      constexpr int KB = 4;  // keys of a thread whose loads are in flight at once
+      // the batch loop is the same for every lane (the shuffles below need the
+      // whole warp): lane groups past the last key compute nothing
+      for (int tb = 0; tb < nk; tb += KB * (DEC_THREADS / 8)) {
+        const int t0 = tb + kg;
+        uint4 kw[KB];
+#pragma unroll
+        for (int u = 0; u < KB; u++) {
+          const int t = t0 + u * (DEC_THREADS / 8);
+          if (t < nk) kw[u] = __ldcg(reinterpret_cast<const uint4*>(base + (size_t)t * C3 + C) + cc);
+        }
+#pragma unroll
+        for (int u = 0; u < KB; u++) {
+          const int t = t0 + u * (DEC_THREADS / 8);
+          float a = 0.f;
+          if (t < nk) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kw[u]);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+              const float2 f = __bfloat1622float2(h2[i]);
+              a = fmaf(qv[2 * i], f.x, a);
+              a = fmaf(qv[2 * i + 1], f.y, a);
+            }
+          }
+          // the eight pieces of key t: lanes 8m .. 8m+7 of the warp
+          a += __shfl_xor_sync(0xffffffffu, a, 1);
+          a += __shfl_xor_sync(0xffffffffu, a, 2);
+          a += __shfl_xor_sync(0xffffffffu, a, 4);
+          if (t < nk) {
+            if (cc == 0) sc[t] = a;
+            mx = fmaxf(mx, a);
+          }
+        }
+      }
+      mx = warp_max(mx);
+      if (lane == 0) red[warp] = mx;
+      __syncthreads();
+      mx = red[0];
+#pragma unroll
+      for (int w = 1; w < DEC_WARPS; w++) mx = fmaxf(mx, red[w]);
+      __syncthreads();
+      float sum = 0.f;
+      for (int t = threadIdx.x; t < nk; t += DEC_THREADS) {
+        const float e = expf(sc[t] - mx);
+        sc[t] = e;
+        sum += e;
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) red[warp] = sum;
+      cp_async_wait_all();
+      __syncthreads();
+      float lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < DEC_WARPS; w++) lsum += red[w];
+      // out[d] = sum_t p_t v_t[d]: thread (s, d) takes keys s, s + 8, ...; the
+      // eight partial rows are then added in s order
+      {
+        const int d = threadIdx.x & 63, sl = threadIdx.x >> 6;
+        float acc = 0.f;
+        for (int t = sl; t < nk; t += DEC_THREADS / 64) acc = fmaf(sc[t], __bfloat162float(vs[t * 64 + d]), acc);
+        part[sl * 64 + d] = acc;
+      }
+      __syncthreads();
+      if (threadIdx.x < 64) {
+        float o = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < DEC_THREADS / 64; sl++) o += part[sl * 64 + threadIdx.x];
+        p.att[(size_t)b * C + hh * 64 + threadIdx.x] = __float2bfloat16_rn(o / lsum);
+      }
+      __syncthreads();
+    }
+    for (int bh = cta; hd != 64 && bh < B * p.H; bh += ncta) {
       const int b = bh / p.H, hh = bh % p.H;
       const bf16* base = cache + (size_t)b * p.Tmax * C3 + hh * hd;
       float* q = reinterpret_cast<float*>(xs);  // hd floats
@@ -238,11 +360,27 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
       for (int t = threadIdx.x; t <= p.pos; t += DEC_THREADS) {
         const bf16* kp = base + (size_t)t * C3 + C;
         float a = 0.f;
-        for (int d = 0; d < hd; d += 8) {
-          float kv[8];
-          ld16_cg(kp + d, kv);
+        if (hd == 64) {  // the GPT-2 head size: the key's eight 16-byte loads all in flight at once
+          uint4 kw[8];
 #pragma unroll
-          for (int e = 0; e < 8; e++) a = fmaf(q[d + e], kv[e], a);
+          for (int u = 0; u < 8; u++) kw[u] = __ldcg(reinterpret_cast<const uint4*>(kp) + u);
+#pragma unroll
+          for (int u = 0; u < 8; u++) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kw[u]);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+              const float2 f = __bfloat1622float2(h2[i]);
+              a = fmaf(q[8 * u + 2 * i], f.x, a);
+              a = fmaf(q[8 * u + 2 * i + 1], f.y, a);
+            }
+          }
+        } else {
+          for (int d = 0; d < hd; d += 8) {
+            float kv[8];
+            ld16_cg(kp + d, kv);
+#pragma unroll
+            for (int e = 0; e < 8; e++) a = fmaf(q[d + e], kv[e], a);
+          }
         }
         a *= p.scale;
         sc[t] = a;
@@ -311,7 +449,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
       int n0, n1;
       range(C, n0, n1);
       const bf16* bias = p.apb + (size_t)l * C;
-      dot_columns<NB>(xs, p.apw + (size_t)l * C * C, C, n0, n1, B, [&](int b, int n, float v) {
+      dot_columns<NB>(xs, p.apw + (size_t)l * C * C, C, n0, n1, B, red_dot, [&](int b, int n, float v) {
         const float pr = __bfloat162float(__float2bfloat16_rn(v + __bfloat162float(bias[n])));
         xn[(size_t)b * C + n] = __float2bfloat16_rn(ldcg_bf16(x + (size_t)b * C + n) + pr);
       });
@@ -325,7 +463,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
       int n0, n1;
       range(4 * C, n0, n1);
       const bf16* bias = p.fcb + (size_t)l * 4 * C;
-      dot_columns<NB>(xs, p.fcw + (size_t)l * 4 * C * C, C, n0, n1, B, [&](int b, int n, float v) {
+      dot_columns<NB>(xs, p.fcw + (size_t)l * 4 * C * C, C, n0, n1, B, red_dot, [&](int b, int n, float v) {
         // the pre-activation is rounded to bf16 first, as the training forward stores it
         const float pre = __bfloat162float(__float2bfloat16_rn(v + __bfloat162float(bias[n])));
         p.h[(size_t)b * 4 * C + n] = __float2bfloat16_rn(gelu_fwd(pre));
@@ -340,7 +478,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
       int n0, n1;
       range(C, n0, n1);
       const bf16* bias = p.fpb + (size_t)l * C;
-      dot_columns<NB>(xs, p.fpw + (size_t)l * 4 * C * C, 4 * C, n0, n1, B, [&](int b, int n, float v) {
+      dot_columns<NB>(xs, p.fpw + (size_t)l * 4 * C * C, 4 * C, n0, n1, B, red_dot, [&](int b, int n, float v) {
         const float pr = __bfloat162float(__float2bfloat16_rn(v + __bfloat162float(bias[n])));
         xn[(size_t)b * C + n] = __float2bfloat16_rn(ldcg_bf16(x + (size_t)b * C + n) + pr);
       });
@@ -352,7 +490,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1) decode_layers_kernel(DecodePar
 
 template <int NB>
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, int sms) {
-  const size_t smem = (size_t)NB * 4 * p.C * sizeof(bf16) + (size_t)p.Tmax * sizeof(float) +
+  const size_t smem = decode_region0(NB, p.C, p.Tmax) + (size_t)p.Tmax * sizeof(float) +
                       (size_t)DEC_THREADS * 8 * sizeof(float);
   static_assert(NB <= DEC_MAXB, "one partial sum per sequence in each lane");
   cudaError_t e = kernel_smem_attr(decode_layers_kernel<NB>, (int)smem);
@@ -379,8 +517,7 @@ static int decode_nb(int B) {
   return nb;
 }
 static size_t decode_layers_smem_bytes(int B, int C, int Tmax) {
-  return (size_t)decode_nb(B) * 4 * C * sizeof(bf16) + (size_t)Tmax * sizeof(float) +
-         (size_t)DEC_THREADS * 8 * sizeof(float);
+  return decode_region0(decode_nb(B), C, Tmax) + (size_t)Tmax * sizeof(float) + (size_t)DEC_THREADS * 8 * sizeof(float);
 }
 
 bool decode_layers_supported(int B, int C, int H, int Tmax) {

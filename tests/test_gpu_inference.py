@@ -23,6 +23,7 @@ pytestmark = pytest.mark.gpu
 
 TINY = dict(L=2, C=64, H=4, V=512, Vp=512, maxT=64, B=4, T=64)
 SMALL_BF16 = dict(L=2, C=128, H=2, V=1000, Vp=1024, maxT=256, B=4, T=256)
+LONG_BF16 = dict(L=1, C=128, H=2, V=1000, Vp=1024, maxT=1024, B=2, T=1024)
 
 
 @pytest.fixture(scope="module")
@@ -53,9 +54,11 @@ def _check_logits(prec, got, want, V):
     assert np.all(got[:, V:] == got[:, V:])  # finite
 
 
-@pytest.mark.parametrize("prec,n", [(0, 1), (0, 10), (1, 100), (1, 128)])
+@pytest.mark.parametrize("prec,n", [(0, 1), (0, 10), (1, 100), (1, 128), (1, 600)])
 def test_kv_cache_decode_matches_full_forward(g, prec, n):
-    cfgd = TINY if prec == 0 else SMALL_BF16
+    """n = 600 (bf16): the decode step's attention over 601-606 cached keys,
+    several batches of keys per thread with a ragged last one."""
+    cfgd = TINY if prec == 0 else (LONG_BF16 if n > 256 else SMALL_BF16)
     m, ref = _model(g, cfgd, prec)
     B, T, V = cfgd["B"], cfgd["T"], cfgd["V"]
     toks, _ = zipf_tokens(B, T, V, 77)
