@@ -804,9 +804,10 @@ __global__ void __launch_bounds__(256, NV <= 4 ? 2 : 1) layernorm_backward_kerne
 }
 
 // bf16 rows of at most 1024 columns: one CTA of LNBP_WARPS warps per SM, each
-// warp owning a contiguous range of rpw rows and keeping the next row's dy
-// and x in flight (registers) while it computes the current one; the
-// incoming dres of a row is fetched before that row's reductions.  Same
+// warp owning a contiguous range of rpw rows and keeping the next row's dy,
+// x, mean, rstd and (bf16, up to 768 columns) incoming residual gradient in
+// flight (registers) while it computes the current one; a wider or fp32
+// incoming residual gradient is fetched before the row's reductions.  Same
 // arithmetic, per-warp shared-memory accumulators and partial layout
 // (partial[block][3][C]) as layernorm_backward_kernel.
 constexpr int LNBP_WARPS = 16;
@@ -864,8 +865,11 @@ __device__ __forceinline__ void unpack_bf16x8_2(const uint4& v, float2 (&f)[4]) 
 }
 // The per-warp column sums live in shared memory as [3][C] (dw, db, new
 // residual gradient), each lane updating its own 8 columns with two 16-byte
-// read-modify-writes per array, so the slices are in the layout of the
-// partial buffer.  All arithmetic on packed fp32 pairs.
+// read-modify-writes per array, laid out so that those of a warp hit
+// consecutive addresses (acc_slot; with the columns in order, lanes 32 bytes
+// apart made every update an 8-way bank conflict, which cost more than the
+// rest of the kernel); the CTA's sum over its warps goes out in column order.
+// All arithmetic on packed fp32 pairs.
 template <typename RT, int NV>
 __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_kernel(
     RT* rout, const RT* rin, bf16* __restrict__ rcopy, float* __restrict__ rf32, const bf16* __restrict__ dy,
@@ -877,6 +881,11 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nvec = C / N;
   float* acc = lnb_sh + (size_t)warp * 3 * C;
+  // columns 8 vi + 4 h .. + 3 of array a at acc + a C + h C/2 + 4 vi: a warp's
+  // 16-byte updates of one half fall on consecutive addresses (no bank conflicts)
+  auto acc_slot = [&](int a, int h, int vi) {
+    return reinterpret_cast<float4*>(acc + (size_t)a * C + (size_t)h * (C / 2) + 4 * vi);
+  };
   if (partial)
     for (int c = 4 * lane; c < 3 * C; c += 128) *reinterpret_cast<float4*>(acc + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   uint4 wv[NV];
@@ -886,16 +895,34 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
   const int r0 = (blockIdx.x * LNBP_WARPS + warp) * rpw;
   const int r1 = min(rows, r0 + rpw);
   uint4 ndy[NV], nx[NV];
-  if (r0 < r1) lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)r0 * C, lane, nvec);
+  float nmu = 0.f, nrs = 0.f;  // the next row's statistics, fetched with its dy and x
+  // a bf16 incoming residual gradient is fetched a row ahead as well
+  constexpr bool PRE_DIN = sizeof(RT) == 2 && NV < 4;
+  uint4 ndin[PRE_DIN ? NV : 1];
+  auto fetch_next = [&](int rr) {
+    lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)rr * C, lane, nvec);
+    nmu = mean[rr];
+    nrs = rstd[rr];
+    if constexpr (PRE_DIN) {
+#pragma unroll
+      for (int i = 0; i < NV; i++) {
+        const int vi = lane + i * 32;
+        ndin[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (rin && vi < nvec) ndin[i] = __ldcs(reinterpret_cast<const uint4*>(rin + (size_t)rr * C) + vi);
+      }
+    }
+  };
+  if (r0 < r1) fetch_next(r0);
   for (int row = r0; row < r1; row++) {
-    uint4 cdy[NV], cx[NV];
+    uint4 cdy[NV], cx[NV], cdin[PRE_DIN ? NV : 1];
 #pragma unroll
     for (int i = 0; i < NV; i++) {
       cdy[i] = ndy[i];
       cx[i] = nx[i];
+      if constexpr (PRE_DIN) cdin[i] = ndin[i];
     }
-    if (row + 1 < r1) lnbp_fetch<NV>(ndy, nx, dy, x, (size_t)(row + 1) * C, lane, nvec);
-    const float mu = mean[row], rs = rstd[row];
+    const float mu = nmu, rs = nrs;
+    if (row + 1 < r1) fetch_next(row + 1);
     const float2 rs2 = make_float2(rs, rs), nmr = make_float2(-mu * rs, -mu * rs);
     // the incoming residual gradient: fetched with the row, or (the widest
     // rows, to keep registers free) after the first pass
@@ -903,10 +930,14 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
     auto load_din = [&]() {
 #pragma unroll
       for (int i = 0; i < NV; i++) {
-        const int vi = lane + i * 32;
+        if constexpr (PRE_DIN) {
+          unpack_bf16x8(cdin[i], din[i]);
+        } else {
+          const int vi = lane + i * 32;
 #pragma unroll
-        for (int k = 0; k < N; k++) din[i][k] = 0.f;
-        if (rin && vi < nvec) ld8(rin + (size_t)row * C + vi * N, din[i]);
+          for (int k = 0; k < N; k++) din[i][k] = 0.f;
+          if (rin && vi < nvec) ld8(rin + (size_t)row * C + vi * N, din[i]);
+        }
       }
     };
     if constexpr (NV < 4) load_din();
@@ -928,17 +959,17 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
           s2 = f2_fma(dn, xh[k], s2);
         }
         if (partial) {
-          float4* aw = reinterpret_cast<float4*>(acc + vi * N);
-          float4* ab = reinterpret_cast<float4*>(acc + C + vi * N);
 #pragma unroll
           for (int h = 0; h < 2; h++) {
-            float4 a = aw[h], b = ab[h];
+            float4* aw = acc_slot(0, h, vi);
+            float4* ab = acc_slot(1, h, vi);
+            float4 a = *aw, b = *ab;
             const float2 lo = f2_fma(dv[2 * h], xh[2 * h], make_float2(a.x, a.y));
             const float2 hi = f2_fma(dv[2 * h + 1], xh[2 * h + 1], make_float2(a.z, a.w));
             const float2 blo = f2_add(dv[2 * h], make_float2(b.x, b.y));
             const float2 bhi = f2_add(dv[2 * h + 1], make_float2(b.z, b.w));
-            aw[h] = make_float4(lo.x, lo.y, hi.x, hi.y);
-            ab[h] = make_float4(blo.x, blo.y, bhi.x, bhi.y);
+            *aw = make_float4(lo.x, lo.y, hi.x, hi.y);
+            *ab = make_float4(blo.x, blo.y, bhi.x, bhi.y);
           }
         }
       }
@@ -969,13 +1000,13 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
         if (rcopy) st16(rcopy + (size_t)row * C + vi * N, o);
         if (rf32) st8(rf32 + (size_t)row * C + vi * N, o);
         if (partial && want_rsum) {
-          float4* ar = reinterpret_cast<float4*>(acc + 2 * C + vi * N);
 #pragma unroll
           for (int h = 0; h < 2; h++) {
-            const float4 a = ar[h];
+            float4* ar = acc_slot(2, h, vi);
+            const float4 a = *ar;
             const float2 lo = f2_add(make_float2(o[4 * h], o[4 * h + 1]), make_float2(a.x, a.y));
             const float2 hi = f2_add(make_float2(o[4 * h + 2], o[4 * h + 3]), make_float2(a.z, a.w));
-            ar[h] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            *ar = make_float4(lo.x, lo.y, hi.x, hi.y);
           }
         }
       }
@@ -992,7 +1023,9 @@ __global__ void __launch_bounds__(32 * LNBP_WARPS, 1) layernorm_backward_pipe_ke
       const float4 u = *reinterpret_cast<const float4*>(lnb_sh + (size_t)q * 3 * C + idx);
       t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
     }
-    *reinterpret_cast<float4*>(dst + idx) = t;
+    // back to the partial buffer's column order (see acc_slot)
+    const int a = idx / C, f = idx % C, h = f / (C / 2), vi = (f % (C / 2)) / 4;
+    *reinterpret_cast<float4*>(dst + (size_t)a * C + 8 * vi + 4 * h) = t;
   }
 }
 
