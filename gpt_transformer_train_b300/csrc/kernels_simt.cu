@@ -582,6 +582,7 @@ cudaError_t layernorm_apply(T* y, const T* r, const float* mean, const float* rs
 // every gradient below is bitwise repeatable.
 // ============================================================================
 constexpr int RED_ROWS = 64;  // rows per chunk
+constexpr int CS_ROWS = 512;  // rows per chunk of the column sums (a multiple of RED_ROWS)
 int reduce_chunks(int rows) {
   int c = (int)cdiv(rows, RED_ROWS);
   return c < 1 ? 1 : c;
@@ -1122,7 +1123,8 @@ cudaError_t layernorm_backward(float* dres, T* dres_c, const T* dy, const T* x, 
 // ============================================================================
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__ partial, const T* __restrict__ X,
-                                                             int rows, int cols, long long ldx, long long sX) {
+                                                             int rows, int cols, long long ldx, long long sX,
+                                                             int chunk_rows) {
   pdl_enter();
   X += blockIdx.z * sX;  // batch item z: its own matrix and partial rows
   partial += (size_t)blockIdx.z * gridDim.y * cols;
@@ -1135,7 +1137,7 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(float* __restrict__
   float acc[1][N];
 #pragma unroll
   for (int k = 0; k < N; k++) acc[0][k] = 0.f;
-  const int r0 = blockIdx.y * RED_ROWS, r1 = min(rows, r0 + RED_ROWS);
+  const int r0 = blockIdx.y * chunk_rows, r1 = min(rows, r0 + chunk_rows);
   if (vi < nvec) {
     // rows warp, warp+8, ... in order; four loads in flight, added in that order
     int r = r0 + warp;
@@ -1172,10 +1174,13 @@ cudaError_t colsum(float* out, const T* X, int rows, int cols, long long ldx, fl
                    int nbatch, long long sOut, long long sX, int accumulate) {
   constexpr int N = VecN<T>::n;
   if (cols % N || ldx % N || nbatch < 1 || nbatch > 65535) return cudaErrorInvalidValue;
-  const int nch = reduce_chunks(rows);
+  // chunks of CS_ROWS rows (a block's fixed setup and its ordered warp combine
+  // are paid once per 512 rows, not per 64; at most reduce_chunks(rows) chunks,
+  // which the partial buffer is sized for)
+  const int nch = std::max(1, (int)cdiv(rows, CS_ROWS));
   dim3 grid((unsigned)cdiv(cols / N, 32), nch, nbatch);
   launch_k(colsum_partial_kernel<T>, dim3(grid), dim3(256), 32 * N * sizeof(float), st, partial, X, rows, cols, ldx,
-           sX);
+           sX, (int)CS_ROWS);
   cudaError_t e = launch_status(1);
   if (e != cudaSuccess) return e;
   return reduce_partials(out, nullptr, nullptr, partial, nch, cols, 1, st, nbatch, sOut, 0, accumulate);

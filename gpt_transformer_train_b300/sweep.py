@@ -10,7 +10,7 @@ against the measured peaks (HBM copy GB/s, bf16 burst TFLOP/s).
   python -m gpt_transformer_train_b300.sweep [--kernel NAME ...] [--reps N] [--warmup N]
 
 Kernel names: ln_fwd ln_bwd ln_bwd_f32res gelu_fwd gelu_bwd softmax_ce adamw encoder_fwd
-encoder_bwd attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096},
+encoder_bwd colsum_fc colsum_qkv (one layer's bias gradient) attn_fwd_T{256,1024,4096} attn_bwd_T{256,1024,4096},
 gemm_<layer>_{fwd,dgrad,wgrad} for layer in qkv attproj fc fcproj classifier,
 gemmepi_fc_gelu, gemmepi_fcproj_gelubwd, gemmepi_attproj_rowdot and
 gemmepi_classifier_stats (the fused epilogues as the step uses them),
@@ -99,6 +99,11 @@ def make_case(name, ops):
         m, v = torch.zeros(NPARAM, device="cuda"), torch.zeros(NPARAM, device="cuda")
         pb = torch.empty(NPARAM, device="cuda", dtype=BF)
         return (lambda: ops.gpt2_op_adamw(p, g, m, v, pb, 6e-4, 0.9, 0.95, 1e-8, 0.1, 1), 30 * NPARAM, "B")
+    if name.startswith("colsum_"):  # a bias gradient: column sums of one layer's output gradient
+        cols = {"colsum_fc": 4 * C, "colsum_qkv": 3 * C}[name]
+        X = randn((BT, cols), 22)
+        out = torch.zeros(cols, device="cuda")
+        return (lambda: ops.gpt2_op_colsum(out, X, BT, cols, cols), BT * cols * 2 + cols * 4, "B")
     if name == "encoder_fwd":
         tok = torch.randint(0, V, (BT,), generator=torch.Generator().manual_seed(15), dtype=torch.int32).cuda()
         wte, wpe = randn((VP, C), 16), randn((1024, C), 17)
@@ -195,7 +200,8 @@ def make_case(name, ops):
     raise SystemExit(f"unknown kernel {name}")
 
 
-ALL = (["ln_fwd", "ln_bwd", "gelu_fwd", "gelu_bwd", "softmax_ce", "adamw", "encoder_fwd", "encoder_bwd"] +
+ALL = (["ln_fwd", "ln_bwd", "gelu_fwd", "gelu_bwd", "softmax_ce", "adamw", "encoder_fwd", "encoder_bwd",
+        "colsum_fc", "colsum_qkv"] +
        [f"attn_{d}_T{t}" for d in ("fwd", "bwd") for t in (256, 1024, 4096)] +
        [f"gemm_{l}_{k}" for l in GEMM_LAYERS for k in ("fwd", "dgrad", "wgrad")] +
        ["gemmepi_fc_gelu", "gemmepi_fcproj_gelubwd", "gemmepi_attproj_rowdot", "gemmepi_classifier_stats",
